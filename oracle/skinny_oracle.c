@@ -1,0 +1,98 @@
+/*
+ * skinny_oracle.c -- the CPU oracle for the skinny BF16 GEMM.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * bench's CPU-baseline / reference leg may load this code.  The product path
+ * (the CUDA library under latency_skinny_bf16_gb300/) never calls it, links it
+ * or shares code with it; there is no CPU fallback.
+ *
+ * What it computes.  The pages describe the low-latency router GEMM
+ * ("[Perf][Feat] Add generic cuteDSL LL BF16 router (GEMM)", vllm PR #42562
+ * report, section "Implementation breakdown" items 1-2 and the
+ * _ll_bf16_dotprod.py / _ll_bf16_splitk.py snippets) and the decode-time
+ * bf16_skinny_gemm projections ("GLM-5.2 Blackwell decode optimizations",
+ * vllm PR #48597, section "Implementation breakdown" item 3): for token m and
+ * output column (expert / projection row) n,
+ *
+ *     Y[m][n] = sum_k  float(X[m][k]) * float(W[n][k])
+ *
+ * with X [M,K] and W [N,K] in bf16, the products and the accumulator in a
+ * wider type (the pages: fp32 acc_dtype, fp32 out_dtype).  That is exactly a
+ * matrix product Y = X . W^T.  The oracle writes the definition out with no
+ * blocking, fusion or reordering: decode each bf16 input exactly, multiply in
+ * fp64 (exact: two 8-bit significands give at most 16 bits), and add the
+ * products in ascending k in fp64.
+ *
+ * Companion output A[m][n] = sum_k |x*w| feeds the elementwise tolerance
+ * |y - y_ref| <= 1e-5 * A + 1e-6 that the parity tests apply.
+ *
+ * Plain C99, host compiler only, no CUDA header.
+ */
+#include <stdint.h>
+#include <string.h>
+#include <math.h>
+
+/* bfloat16 is the upper half of an IEEE-754 binary32: sign, 8 exponent bits
+ * (bias 127), 7 stored significand bits.  Decoding is exact: place the 16 bits
+ * in the high half of a binary32 word and reinterpret; the binary32 value
+ * widens to binary64 exactly. */
+double skinny_oracle_bf16_to_f64(uint16_t bits)
+{
+    uint32_t word = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &word, sizeof f);
+    return (double)f;
+}
+
+/* Y[m*ldy + n] = sum_{k<K} x(m,k) * w(n,k) in fp64, ascending k.
+ * A (may be NULL) receives sum_{k<K} |x(m,k) * w(n,k)| at A[m*lda + n].
+ * X is [M rows, ldx stride], W is [N rows, ldw stride]; both bf16 bit
+ * patterns.  K == 0 gives Y = 0 (the empty sum).  Entries of Y outside
+ * m<M, n<N are never touched. */
+void skinny_oracle_gemm(const uint16_t *X, int64_t ldx,
+                        const uint16_t *W, int64_t ldw,
+                        double *Y, int64_t ldy,
+                        double *A, int64_t lda,
+                        int M, int N, int K)
+{
+    for (int m = 0; m < M; ++m) {
+        const uint16_t *xrow = X + (int64_t)m * ldx;
+        for (int n = 0; n < N; ++n) {
+            const uint16_t *wrow = W + (int64_t)n * ldw;
+            double sum = 0.0;
+            double abs_sum = 0.0;
+            for (int k = 0; k < K; ++k) {
+                double prod = skinny_oracle_bf16_to_f64(xrow[k]) *
+                              skinny_oracle_bf16_to_f64(wrow[k]);
+                sum += prod;
+                abs_sum += fabs(prod);
+            }
+            Y[(int64_t)m * ldy + n] = sum;
+            if (A) A[(int64_t)m * lda + n] = abs_sum;
+        }
+    }
+}
+
+/* The same definition evaluated only at `count` sampled output positions
+ * (rows[i], cols[i]); used to check full-size launches without computing all
+ * of Y.  y[i] and a[i] receive the value and the absolute-product sum. */
+void skinny_oracle_gemm_points(const uint16_t *X, int64_t ldx,
+                               const uint16_t *W, int64_t ldw,
+                               int K, const int32_t *rows, const int32_t *cols,
+                               int count, double *y, double *a)
+{
+    for (int i = 0; i < count; ++i) {
+        const uint16_t *xrow = X + (int64_t)rows[i] * ldx;
+        const uint16_t *wrow = W + (int64_t)cols[i] * ldw;
+        double sum = 0.0;
+        double abs_sum = 0.0;
+        for (int k = 0; k < K; ++k) {
+            double prod = skinny_oracle_bf16_to_f64(xrow[k]) *
+                          skinny_oracle_bf16_to_f64(wrow[k]);
+            sum += prod;
+            abs_sum += fabs(prod);
+        }
+        y[i] = sum;
+        if (a) a[i] = abs_sum;
+    }
+}

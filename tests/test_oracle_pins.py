@@ -1,0 +1,401 @@
+"""Pins for the CPU oracle: results that do not come from the oracle itself.
+
+Each test checks the oracle against something the pages or the mathematics fix:
+hand-worked golden values (``tests/golden/``), exact rational brute force on
+tiny inputs, closed forms (one-hot rows, identity weights, K = 1), invariants
+(power-of-two scaling, additivity, row independence, zero-padding of K,
+strides), special values, and a float64 library matmul.  The last test plants
+mistakes in a copy of the oracle's C source and checks that the pins catch
+every one of them.
+"""
+import math
+import os
+import random
+import struct
+import subprocess
+import tempfile
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import skinny_inputs as si
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def exact_bits(value: float) -> int:
+    """bf16 bits of a value that bf16 represents exactly (asserts so)."""
+    (word,) = struct.unpack("<I", struct.pack("<f", float(value)))
+    assert word & 0xFFFF == 0, f"{value!r} is not exactly representable in bf16"
+    return word >> 16
+
+
+def bits_to_fraction(bits: int) -> Fraction:
+    """Exact rational value of a finite bf16 pattern, from the format definition."""
+    sign = -1 if bits & 0x8000 else 1
+    exp = (bits >> 7) & 0xFF
+    man = bits & 0x7F
+    assert exp != 0xFF
+    if exp == 0:
+        return sign * Fraction(man, 128) * Fraction(1, 2 ** 126)
+    return sign * (1 + Fraction(man, 128)) * (Fraction(2) ** (exp - 127))
+
+
+def random_grid_bits(rng: random.Random, n: int, emin: int = -4, emax: int = 4) -> np.ndarray:
+    """bf16 values s * (1 + j/128) * 2^e with e in [emin, emax] (or zero)."""
+    out = np.empty(n, np.uint16)
+    for i in range(n):
+        if rng.random() < 0.05:
+            out[i] = 0
+            continue
+        s = rng.randrange(2)
+        e = rng.randint(emin, emax)
+        j = rng.randrange(128)
+        out[i] = (s << 15) | ((e + 127) << 7) | j
+    return out
+
+
+def exact_gemm(X, W, M, N, K):
+    Xq = [[bits_to_fraction(int(X[m * K + k])) for k in range(K)] for m in range(M)]
+    Wq = [[bits_to_fraction(int(W[n * K + k])) for k in range(K)] for n in range(N)]
+    Y = [[sum((Xq[m][k] * Wq[n][k] for k in range(K)), Fraction(0)) for n in range(N)]
+         for m in range(M)]
+    A = [[sum((abs(Xq[m][k] * Wq[n][k]) for k in range(K)), Fraction(0)) for n in range(N)]
+         for m in range(M)]
+    return Y, A
+
+
+def parse_worked_examples(path):
+    examples = []
+    cur = None
+    with open(path) as f:
+        for raw in f:
+            line = raw.split("#", 1)[0].strip()
+            if not line:
+                continue
+            head, *rest = line.split(None, 1)
+            if head == "begin":
+                cur = {"name": rest[0]}
+            elif head == "end":
+                examples.append(cur)
+                cur = None
+            elif head in ("M", "N", "K"):
+                cur[head] = int(rest[0])
+            else:
+                rows = [[float(t) for t in r.split()] for r in rest[0].split(";")]
+                cur[head] = rows
+    return examples
+
+
+# ----------------------------------------------------------------------------- golden
+
+def test_bf16_decode_golden():
+    n = 0
+    with open(os.path.join(GOLDEN, "bf16_decode.txt")) as f:
+        for raw in f:
+            line = raw.split("#", 1)[0].strip()
+            if not line:
+                continue
+            hx, val = line.split()
+            bits = int(hx, 16)
+            got = oracle.bf16_to_f64(bits)
+            want = float(val)
+            if math.isnan(want):
+                assert math.isnan(got), hx
+            else:
+                assert got == want, (hx, got, want)
+                assert math.copysign(1.0, got) == math.copysign(1.0, want), hx
+            n += 1
+    assert n >= 15
+
+
+@pytest.mark.parametrize("ex", parse_worked_examples(os.path.join(GOLDEN, "worked_examples.txt")),
+                         ids=lambda e: e["name"])
+def test_worked_examples_golden(ex):
+    M, N, K = ex["M"], ex["N"], ex["K"]
+    X = np.array([exact_bits(v) for row in ex["X"] for v in row], np.uint16)
+    W = np.array([exact_bits(v) for row in ex["W"] for v in row], np.uint16)
+    assert X.size == M * K and W.size == N * K
+    Y, A = oracle.gemm(X, W, M, N, K)
+    assert Y.tolist() == ex["Y"]
+    assert A.tolist() == ex["A"]
+
+
+# ----------------------------------------------------------------------------- brute force
+
+@pytest.mark.parametrize("seed", range(40))
+def test_bruteforce_exact_on_tiny_grid_inputs(seed):
+    """Tiny shapes, values on a bounded exponent grid: every partial sum is a
+    multiple of 2^-22 below 2^16, so fp64 is exact in any order and the oracle
+    must equal the rational brute force exactly."""
+    rng = random.Random(seed)
+    M, N = rng.randint(1, 4), rng.randint(1, 4)
+    K = rng.randint(1, 4) if seed < 20 else rng.randint(5, 64)
+    X = random_grid_bits(rng, M * K)
+    W = random_grid_bits(rng, N * K)
+    Y, A = oracle.gemm(X, W, M, N, K)
+    Ye, Ae = exact_gemm(X, W, M, N, K)
+    for m in range(M):
+        for n in range(N):
+            assert Fraction(Y[m, n]) == Ye[m][n], (m, n)
+            assert Fraction(A[m, n]) == Ae[m][n], (m, n)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_bruteforce_within_fp64_bound_on_wide_range(seed):
+    """Unrestricted bf16 magnitudes (outlier workload recipe): the oracle is the
+    exact sum up to fp64 recursive-summation error, |err| <= K * 2^-53 * A."""
+    case = si.Case("bf", M=3, N=3, K=48, seed=1000 + seed, x_dist="normal",
+                   w_dist="normal", outliers=True)
+    X, W = si.make_inputs(case)
+    Y, A = oracle.gemm(X, W, 3, 3, 48)
+    Ye, Ae = exact_gemm(X.reshape(-1), W.reshape(-1), 3, 3, 48)
+    for m in range(3):
+        for n in range(3):
+            err = abs(Fraction(Y[m, n]) - Ye[m][n])
+            assert err <= Fraction(48) * Fraction(1, 2 ** 53) * Ae[m][n]
+            assert abs(Fraction(A[m, n]) - Ae[m][n]) <= Fraction(48) * Fraction(1, 2 ** 53) * Ae[m][n]
+
+
+# ----------------------------------------------------------------------------- closed forms
+
+def test_one_hot_rows_reproduce_weight_columns():
+    case = si.Case("oh", M=1, N=37, K=29, seed=7)
+    _, W = si.make_inputs(case)
+    K, N = 29, 37
+    for k in (0, 1, 13, 28):
+        X = np.zeros(K, np.uint16)
+        X[k] = exact_bits(1.0)
+        Y, _ = oracle.gemm(X, W, 1, N, K)
+        for n in range(N):
+            assert Y[0, n] == oracle.bf16_to_f64(int(W[n, k]))
+
+
+def test_identity_weight_reproduces_x():
+    K = 23
+    case = si.Case("id", M=5, N=K, K=K, seed=8)
+    X, _ = si.make_inputs(case)
+    W = np.zeros((K, K), np.uint16)
+    for i in range(K):
+        W[i, i] = exact_bits(1.0)
+    Y, _ = oracle.gemm(X, W, 5, K, K)
+    for m in range(5):
+        for k in range(K):
+            assert Y[m, k] == oracle.bf16_to_f64(int(X[m, k]))
+
+
+def test_k_equals_one_is_a_single_product():
+    case = si.Case("k1", M=4, N=9, K=1, seed=9)
+    X, W = si.make_inputs(case)
+    Y, A = oracle.gemm(X, W, 4, 9, 1)
+    for m in range(4):
+        for n in range(9):
+            p = Fraction(oracle.bf16_to_f64(int(X[m, 0]))) * Fraction(oracle.bf16_to_f64(int(W[n, 0])))
+            assert Fraction(Y[m, n]) == p
+            assert Fraction(A[m, n]) == abs(p)
+
+
+# ----------------------------------------------------------------------------- invariants
+
+def _scale_bits_pow2(bits: np.ndarray, j: int) -> np.ndarray:
+    """Multiply normal bf16 values by 2^j by moving the exponent field."""
+    b = bits.astype(np.int32)
+    exp = (b >> 7) & 0xFF
+    nz = exp != 0
+    assert np.all((exp[nz] + j > 0) & (exp[nz] + j < 255))
+    out = np.where(nz, b + (j << 7), b)
+    return out.astype(np.uint16)
+
+
+def test_power_of_two_scaling_is_exact():
+    case = si.Case("sc", M=3, N=11, K=300, seed=10)
+    X, W = si.make_inputs(case)
+    X = np.where(((X >> 7) & 0xFF) == 0, np.uint16(0), X).astype(np.uint16)
+    Y, _ = oracle.gemm(X, W, 3, 11, 300)
+    for j in (-5, 3, 17):
+        Ys, _ = oracle.gemm(_scale_bits_pow2(X, j), W, 3, 11, 300)
+        assert np.array_equal(Ys, Y * (2.0 ** j))
+
+
+def test_additivity():
+    """X1 + X2 representable (small integers): Y(X1+X2) = Y(X1) + Y(X2) up to fp64 rounding."""
+    rng = np.random.default_rng(11)
+    M, N, K = 3, 17, 200
+    x1 = rng.integers(-64, 65, size=(M, K))
+    x2 = rng.integers(-64, 65, size=(M, K))
+    X1 = np.array([exact_bits(v) for v in x1.reshape(-1)], np.uint16)
+    X2 = np.array([exact_bits(v) for v in x2.reshape(-1)], np.uint16)
+    X12 = np.array([exact_bits(v) for v in (x1 + x2).reshape(-1)], np.uint16)
+    _, W = si.make_inputs(si.Case("ad", M=1, N=N, K=K, seed=12))
+    Y1, A1 = oracle.gemm(X1, W, M, N, K)
+    Y2, A2 = oracle.gemm(X2, W, M, N, K)
+    Y12, _ = oracle.gemm(X12, W, M, N, K)
+    bound = 3 * K * 2.0 ** -53 * (A1 + A2)
+    assert np.all(np.abs(Y12 - (Y1 + Y2)) <= bound)
+
+
+def test_row_independence_bit_exact():
+    case = si.Case("ri", M=6, N=40, K=513, seed=13)
+    X, W = si.make_inputs(case)
+    Y, _ = oracle.gemm(X, W, 6, 40, 513)
+    for m in range(6):
+        Ym, _ = oracle.gemm(X[m:m + 1], W, 1, 40, 513)
+        assert np.array_equal(Ym[0], Y[m])
+
+
+def test_zero_padding_of_k_is_bit_exact():
+    case = si.Case("zp", M=4, N=21, K=333, seed=14)
+    X, W = si.make_inputs(case)
+    Y, A = oracle.gemm(X, W, 4, 21, 333)
+    for p in (1, 7, 64):
+        Xp = np.concatenate([X, np.zeros((4, p), np.uint16)], axis=1)
+        Wp = np.concatenate([W, np.zeros((21, p), np.uint16)], axis=1)
+        Yp, Ap = oracle.gemm(Xp, Wp, 4, 21, 333 + p)
+        assert np.array_equal(Yp, Y) and np.array_equal(Ap, A)
+
+
+def test_strides_match_compact_and_leave_gaps():
+    case = si.Case("st", M=5, N=13, K=77, seed=15)
+    X, W = si.make_inputs(case)
+    Y, A = oracle.gemm(X, W, 5, 13, 77)
+    ldx, ldw, ldy = 77 + 5, 77 + 3, 13 + 9
+    Xs = si.embed_rows(X, ldx, fill=0x7FC0)   # NaN in the gaps: must never be read
+    Ws = si.embed_rows(W, ldw, fill=0x7FC0)
+    sentinel = np.full((5, ldy), -12345.0)
+    Ys, As = oracle.gemm(Xs, Ws, 5, 13, 77, ldx=ldx, ldw=ldw, ldy=ldy, Y_init=sentinel)
+    assert np.array_equal(Ys[:, :13], Y)
+    assert np.array_equal(As[:, :13], A)
+    assert np.all(Ys[:, 13:] == -12345.0)
+
+
+def test_abs_companion_is_abs_gemm():
+    case = si.Case("ab", M=3, N=19, K=250, seed=16)
+    X, W = si.make_inputs(case)
+    Y, A = oracle.gemm(X, W, 3, 19, 250)
+    Yabs, _ = oracle.gemm(X & np.uint16(0x7FFF), W & np.uint16(0x7FFF), 3, 19, 250)
+    assert np.array_equal(A, Yabs)
+    assert np.all(np.abs(Y) <= A)
+
+
+def test_matches_float64_library_matmul():
+    case = si.Case("mm", M=16, N=64, K=1000, seed=17)
+    X, W = si.make_inputs(case)
+    Xd = (X.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    Wd = (W.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ref = Xd @ Wd.T
+    Y, A = oracle.gemm(X, W, 16, 64, 1000)
+    assert np.all(np.abs(Y - ref) <= 2 * 1000 * 2.0 ** -53 * A)
+
+
+def test_special_values_propagate():
+    inf, nan = exact_bits(float("inf")), 0x7FC0
+    one, zero, two = exact_bits(1.0), exact_bits(0.0), exact_bits(2.0)
+    X = np.array([inf, one, nan, two], np.uint16)          # M=2, K=2
+    W = np.array([one, one, zero, one, one, zero], np.uint16)  # N=3, K=2
+    Y, _ = oracle.gemm(X, W, 2, 3, 2)
+    assert Y[0, 0] == float("inf")        # inf*1 + 1*1
+    assert math.isnan(Y[0, 1])            # inf*0 -> NaN
+    assert Y[0, 2] == float("inf")        # inf*1 + 1*0
+    assert all(math.isnan(v) for v in Y[1])  # NaN row
+
+
+def test_degenerate_sizes():
+    X = np.zeros(4, np.uint16)
+    W = np.zeros(4, np.uint16)
+    Y, _ = oracle.gemm(X, W, 0, 4, 1)
+    assert Y.shape == (0, 4)
+    Y, _ = oracle.gemm(X, W, 2, 0, 2, ldy=3, Y_init=np.full((2, 3), 5.0))
+    assert np.all(Y == 5.0)
+    Y, A = oracle.gemm(X, W, 2, 2, 0)
+    assert np.all(Y == 0.0) and np.all(A == 0.0)
+
+
+def test_points_match_full():
+    case = si.Case("pt", M=7, N=50, K=900, seed=18)
+    X, W = si.make_inputs(case)
+    Y, A = oracle.gemm(X, W, 7, 50, 900)
+    rng = np.random.default_rng(0)
+    rows = rng.integers(0, 7, 40)
+    cols = rng.integers(0, 50, 40)
+    y, a = oracle.gemm_points(X, W, 900, rows, cols)
+    assert np.array_equal(y, Y[rows, cols]) and np.array_equal(a, A[rows, cols])
+
+
+# ----------------------------------------------------------------------------- planted mistakes
+
+def _pins_pass(lib) -> bool:
+    """A compact subset of the pins above, run against a given oracle build."""
+    try:
+        for ex in parse_worked_examples(os.path.join(GOLDEN, "worked_examples.txt")):
+            M, N, K = ex["M"], ex["N"], ex["K"]
+            X = np.array([exact_bits(v) for row in ex["X"] for v in row], np.uint16)
+            W = np.array([exact_bits(v) for row in ex["W"] for v in row], np.uint16)
+            Y, A = oracle.gemm(X, W, M, N, K, lib=lib)
+            if Y.tolist() != ex["Y"] or A.tolist() != ex["A"]:
+                return False
+        with open(os.path.join(GOLDEN, "bf16_decode.txt")) as f:
+            for raw in f:
+                line = raw.split("#", 1)[0].strip()
+                if not line:
+                    continue
+                hx, val = line.split()
+                got, want = oracle.bf16_to_f64(int(hx, 16), lib=lib), float(val)
+                if not (math.isnan(got) and math.isnan(want)) and got != want:
+                    return False
+        rng = random.Random(5)
+        for _ in range(5):
+            M, N, K = rng.randint(1, 4), rng.randint(1, 4), rng.randint(1, 40)
+            X, W = random_grid_bits(rng, M * K), random_grid_bits(rng, N * K)
+            Y, _ = oracle.gemm(X, W, M, N, K, lib=lib)
+            Ye, _ = exact_gemm(X, W, M, N, K)
+            if any(Fraction(Y[m, n]) != Ye[m][n] for m in range(M) for n in range(N)):
+                return False
+        case = si.Case("pm", M=3, N=7, K=30, seed=3)
+        X, W = si.make_inputs(case)
+        ldx, ldw, ldy = 33, 31, 9
+        Ys, _ = oracle.gemm(si.embed_rows(X, ldx), si.embed_rows(W, ldw), 3, 7, 30,
+                            ldx=ldx, ldw=ldw, ldy=ldy, Y_init=np.zeros((3, ldy)), lib=lib)
+        Yc, _ = oracle.gemm(X, W, 3, 7, 30, lib=lib)
+        if not np.array_equal(Ys[:, :7], Yc) or np.any(Ys[:, 7:] != 0):
+            return False
+        return True
+    except Exception:
+        return False
+
+
+MUTATIONS = [
+    ("drop last k", "for (int k = 0; k < K; ++k) {\n                double prod = skinny_oracle_bf16_to_f64(xrow[k])",
+     "for (int k = 0; k < K - 1; ++k) {\n                double prod = skinny_oracle_bf16_to_f64(xrow[k])"),
+    ("transposed W index", "const uint16_t *wrow = W + (int64_t)n * ldw;\n            double sum",
+     "const uint16_t *wrow = W + (int64_t)n;\n            double sum"),
+    ("sign flip", "sum += prod;\n                abs_sum", "sum -= prod;\n                abs_sum"),
+    ("fp32 accumulator", "double sum = 0.0;\n            double abs_sum = 0.0;\n            for (int k = 0; k < K; ++k) {\n                double prod",
+     "float sum = 0.0f;\n            double abs_sum = 0.0;\n            for (int k = 0; k < K; ++k) {\n                double prod"),
+    ("wrong decode shift", "((uint32_t)bits) << 16", "((uint32_t)bits) << 15"),
+    ("x stride ignored", "const uint16_t *xrow = X + (int64_t)m * ldx;\n        for (int n",
+     "const uint16_t *xrow = X + (int64_t)m * K;\n        for (int n"),
+    ("y stride ignored", "Y[(int64_t)m * ldy + n] = sum;", "Y[(int64_t)m * N + n] = sum;"),
+]
+
+
+def test_planted_mistakes_are_caught():
+    """Every planted mistake in a copy of the oracle source fails the pins, and
+    the unmodified source passes them."""
+    with open(oracle.SOURCE_PATH) as f:
+        src = f.read()
+    with tempfile.TemporaryDirectory() as td:
+        clean_so = os.path.join(td, "clean.so")
+        oracle.build(src=oracle.SOURCE_PATH, out=clean_so)
+        assert _pins_pass(oracle.load(clean_so))
+        for name, old, new in MUTATIONS:
+            assert src.count(old) == 1, f"mutation anchor not unique: {name}"
+            path = os.path.join(td, "mut.c")
+            with open(path, "w") as f:
+                f.write(src.replace(old, new))
+            so = os.path.join(td, f"mut_{abs(hash(name))}.so")
+            oracle.build(src=path, out=so)
+            assert not _pins_pass(oracle.load(so)), f"planted mistake not caught: {name}"
