@@ -1,0 +1,533 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 skinny BF16 GEMM (Y[M,N] = X[M,K] . W[N,K]^T, fp32 out).
+
+One *step* is one pass of the whole hot path over one batch of the workload:
+every call of the workload (default ``dotprod``: M in {1,2,3,4} x (K,N) in
+{(7168,256),(7168,384),(2880,128)}, 12 calls), each through the C ABI.
+
+Timing rules followed here:
+* W is a weight resident in HBM; every step reads a different replica of the
+  whole workload's W / X / Y, and the replicas together exceed 2x the L2 size,
+  so every call reads W from HBM (L2-cold without a flush kernel).
+* a step is replayed from a CUDA graph captured from the public C-ABI calls
+  (as a decode step is); W untimed warm-up steps, then exactly K timed steps
+  bracketed by a barrier and cuda synchronize, timed with CUDA events on the
+  launching stream; the max over ranks is reported.
+* per-launch durations for the roofline come from CUDA-event pairs around each
+  call in a second pass over the same rotating replicas.
+* clocks are sampled with nvidia-smi while the GPU is under load.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+(test infrastructure, single thread) on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import skinny_inputs as si  # noqa: E402
+
+METRIC = "µs/call and achieved HBM GB/s (% of roofline) for bf16 skinny GEMM, M=1–16"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD_DESC = {
+    "router_small": "router GEMM M=1, K=7168, N=256",
+    "dotprod": "dot-product regime: M in {1,2,3,4} x (K,N) in {(7168,256),(7168,384),(2880,128)}, 12 calls",
+    "splitk": "split-K regime: M in {5,8,12,16} x (K,N) in {(7168,256),(7168,384),(4096,256)}, 12 calls",
+    "projection": "decode projections: M in {1,2,3,8,16} x (N,K) in {(2112,7168),(24576,1536),(7168,14336)}, "
+                  "ldy=N+64, 15 calls",
+}
+KERNEL_SOURCES = ["api.cu", "dotprod.cu", "splitk.cu", "common.cuh", "internal.h", "tuning_table.inc"]
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="dotprod")
+    p.add_argument("--pdl", type=int, choices=[0, 1], default=1)
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget (s)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--per-shape", action="store_true", help="also time each call shape on its own")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def aggregate(elapsed_s: float, units_local: float, group=None):
+    """Max elapsed time and summed work over ranks (no data-path collective:
+    the GEMM replicas are independent; this only reduces two scalars)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_s, units_local
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units_local], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ peaks, clocks, traffic
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+            if key in d and d[key]:
+                return float(d[key]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, no measured peak file)"
+
+
+def kernel_sources_digest() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "latency_skinny_bf16_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(family: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{family}_{workload}.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_sources_sha256_16") != kernel_sources_digest():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        return self.summary()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ the GPU workload
+
+class Replica:
+    """Device buffers for one copy of the whole workload."""
+
+    def __init__(self, cases, host_inputs, torch, src=None):
+        self.x, self.w, self.y = [], [], []
+        for j, (c, (X, W)) in enumerate(zip(cases, host_inputs)):
+            if src is None:
+                x = torch.from_numpy(X.reshape(-1).view(np.int16).copy()).cuda()
+                w = torch.from_numpy(W.reshape(-1).view(np.int16).copy()).cuda()
+            else:
+                x, w = src.x[j].clone(), src.w[j].clone()
+            self.x.append(x)
+            self.w.append(w)
+            self.y.append(torch.zeros(c.M * c.ly, dtype=torch.float32, device="cuda"))
+
+
+def launch_step(sk, cases, rep, stream_handle, counter=None):
+    for c, x, w, y in zip(cases, rep.x, rep.w, rep.y):
+        st = sk.skinny_gemm_bf16(x.data_ptr(), c.lx, w.data_ptr(), c.lw, y.data_ptr(), c.ly, c.M, c.N, c.K,
+                                 stream_handle)
+        if st != sk.SKINNY_OK:
+            raise sk.SkinnyError(st, c.name)
+        if counter is not None:
+            counter[0] += 1
+
+
+def run_native(args):
+    import torch
+    import torch.distributed as dist
+    import latency_skinny_bf16_gb300 as sk
+
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    st = sk.skinny_init(local)
+    if st != sk.SKINNY_OK:
+        raise sk.SkinnyError(st, "skinny_init")
+    sk.skinny_set_option(sk.SKINNY_OPT_PDL, args.pdl)
+
+    cases = si.workload(args.workload)
+    host_inputs = [si.make_inputs(c) for c in cases]
+    step_bytes = sum(c.algorithmic_bytes for c in cases)
+    step_w_bytes = sum(2 * c.N * c.K for c in cases)
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    n_rep = max(1, math.ceil(2 * l2 / step_w_bytes))
+    reps = [Replica(cases, host_inputs, torch)]
+    for _ in range(n_rep - 1):
+        reps.append(Replica(cases, host_inputs, torch, src=reps[0]))
+    pool_mb = n_rep * step_w_bytes / 1e6
+    plans = []
+    for c, x, w, y in zip(cases, reps[0].x, reps[0].w, reps[0].y):
+        p = sk.skinny_query_plan(x.data_ptr(), c.lx, w.data_ptr(), c.lw, y.data_ptr(), c.ly, c.M, c.N, c.K)
+        plans.append(p)
+
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    # eager warm-up (first launches, module load), then capture one graph per replica
+    with torch.cuda.stream(stream):
+        for r in reps:
+            launch_step(sk, cases, r, sh)
+    torch.cuda.synchronize()
+    graphs = []
+    for r in reps:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            launch_step(sk, cases, r, sh)
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local) if not args.no_clocks else None
+    if clocks:
+        clocks.start()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % n_rep].replay()
+        # keep the GPU loaded ~1.5 s so the clock samples see it under load
+        t_end = time.time() + 1.5
+        i = 0
+        while time.time() < t_end:
+            for _ in range(50):
+                graphs[i % n_rep].replay()
+                i += 1
+            stream.synchronize()
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly `steps` graph replays, L2-cold (rotating replicas)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[i % n_rep].replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    clock_summary = clocks.stop() if clocks else None
+    launches = args.steps * len(cases)
+
+    # ---- L2-warm: same replica every step
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            graphs[0].replay()
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        warm_steps = max(50, min(args.steps, 2000))
+        w0.record(stream)
+        for _ in range(warm_steps):
+            graphs[0].replay()
+        w1.record(stream)
+    torch.cuda.synchronize()
+    warm_us_per_call = w0.elapsed_time(w1) * 1e3 / (warm_steps * len(cases))
+
+    # ---- per-launch durations (CUDA-event pairs around each call, same rotation)
+    per_launch = [[] for _ in cases]
+    n_launch_steps = max(4, min(args.steps, 200))
+    chunk = max(1, 150 // len(cases))
+    done = 0
+    while done < n_launch_steps:
+        k = min(chunk, n_launch_steps - done)
+        evs = []
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(50_000_000)      # let the host queue every launch before the GPU reaches them
+            for s_ in range(k):
+                r = reps[(done + s_) % n_rep]
+                for j, c in enumerate(cases):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    st = sk.skinny_gemm_bf16(r.x[j].data_ptr(), c.lx, r.w[j].data_ptr(), c.lw, r.y[j].data_ptr(),
+                                             c.ly, c.M, c.N, c.K, sh)
+                    b.record(stream)
+                    if st != sk.SKINNY_OK:
+                        raise sk.SkinnyError(st, c.name)
+                    evs.append((j, a, b))
+        torch.cuda.synchronize()
+        for j, a, b in evs:
+            per_launch[j].append(a.elapsed_time(b) * 1e3)   # us
+        done += k
+
+    # ---- e2e: host -> device X, the calls, device -> host Y, per step, through the C ABI
+    h2d = sum(2 * c.M * c.K for c in cases)
+    d2h = sum(4 * c.M * c.N for c in cases)
+    x_host = torch.empty(h2d // 2, dtype=torch.int16).pin_memory()
+    y_host = torch.empty(sum(c.M * c.ly for c in cases), dtype=torch.float32).pin_memory()
+    off = 0
+    for c, (X, _) in zip(cases, host_inputs):
+        x_host[off:off + c.M * c.K] = torch.from_numpy(X.reshape(-1).view(np.int16).copy())
+        off += c.M * c.K
+    x_dev = torch.empty_like(x_host, device="cuda")
+    y_dev = torch.empty(y_host.numel(), dtype=torch.float32, device="cuda")
+    e2e_graphs = []
+    for r in reps:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            x_dev.copy_(x_host, non_blocking=True)
+            xo = yo = 0
+            for c, w in zip(cases, r.w):
+                st = sk.skinny_gemm_bf16(x_dev.data_ptr() + 2 * xo, c.K, w.data_ptr(), c.lw,
+                                         y_dev.data_ptr() + 4 * yo, c.ly, c.M, c.N, c.K, sh)
+                if st != sk.SKINNY_OK:
+                    raise sk.SkinnyError(st, c.name)
+                xo += c.M * c.K
+                yo += c.M * c.ly
+            y_host.copy_(y_dev, non_blocking=True)
+        e2e_graphs.append(g)
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            e2e_graphs[i % n_rep].replay()
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            e2e_graphs[i % n_rep].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_elapsed = e0.elapsed_time(e1) / 1e3
+    barrier()
+    # correctness spot check of the e2e output against the device-only path
+    ref_y = torch.cat([y.view(-1) for y in reps[(args.steps - 1) % n_rep].y]).cpu()
+    if not torch.equal(ref_y, y_host):
+        raise RuntimeError("e2e output differs from the device-resident output")
+
+    elapsed_max, units = aggregate(elapsed, float(step_bytes * args.steps))
+    e2e_max, _ = aggregate(e2e_elapsed, 0.0)
+    return dict(cases=cases, plans=plans, elapsed=elapsed_max, units=units, launches=launches,
+                warm_us_per_call=warm_us_per_call, per_launch=per_launch, clocks=clock_summary,
+                e2e_elapsed=e2e_max, h2d=h2d, d2h=d2h, pool_mb=pool_mb, n_rep=n_rep, l2=l2,
+                step_bytes=step_bytes, world=world, rank=rank)
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def oracle_step_sample(cases, seconds: float, max_steps: int | None = None):
+    """Time the oracle (test infrastructure) on whole steps of the workload,
+    column-sampled when one step would exceed ~`seconds`/4."""
+    import oracle
+    inputs = [si.make_inputs(c) for c in cases]
+    full_macs = sum(c.M * c.N * c.K for c in cases)
+    # probe: one call of the smallest case
+    t0 = time.perf_counter()
+    c0 = min(cases, key=lambda c: c.M * c.N * c.K)
+    oracle.gemm(inputs[cases.index(c0)][0], inputs[cases.index(c0)][1], c0.M, c0.N, c0.K)
+    rate = max(c0.M * c0.N * c0.K / max(time.perf_counter() - t0, 1e-6), 1e6)   # MAC/s
+    frac = min(1.0, (seconds / 4) * rate / full_macs)
+    bytes_done = 0.0
+    steps = 0
+    t0 = time.perf_counter()
+    while True:
+        for c, (X, W) in zip(cases, inputs):
+            n = max(1, int(round(c.N * frac)))
+            oracle.gemm(X, W[:n], c.M, n, c.K)
+            bytes_done += 2 * n * c.K + 2 * c.M * c.K + 4 * c.M * n
+        steps += 1
+        el = time.perf_counter() - t0
+        if (max_steps is not None and steps >= max_steps) or (max_steps is None and el >= seconds):
+            break
+    sample = (f"{steps} step(s) of the whole workload, each call on the first {frac:.1%} of its N columns "
+              f"(all of M and K), single thread" if frac < 1 else
+              f"{steps} whole step(s) of the workload, single thread")
+    return bytes_done / el, el / steps, sample
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    cases = si.workload(args.workload)
+    step_bytes = sum(c.algorithmic_bytes for c in cases)
+    # untimed warm-up steps, then exactly `steps` timed steps, each a bounded sample
+    budget = min(120.0, max(5.0, 0.2 * args.steps))
+    per_step_budget = budget / max(args.steps, 1)
+    if args.warmup:
+        oracle_step_sample(cases, per_step_budget, max_steps=args.warmup)
+    gbs, s_per_step, sample = oracle_step_sample(cases, per_step_budget * 4, max_steps=args.steps)
+    us_per_call = s_per_step / len(cases) * 1e6
+    value = gbs / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s_per_step * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "us_per_call": round(us_per_call, 2),
+        "config": {"workload": WORKLOAD_DESC[args.workload], "calls_per_step": len(cases),
+                   "parallelism": "single host thread"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return line
+
+
+# ------------------------------------------------------------------ main
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+        return 0
+    r = run_native(args)
+    if r["rank"] != 0:
+        return 0
+    cases = r["cases"]
+    n = r["world"]
+    step_s = r["elapsed"] / args.steps
+    value_gbs = r["units"] / r["elapsed"] / 1e9
+    us_per_call = step_s / len(cases) * 1e6
+    peak, peak_src = hbm_peak()
+
+    # dominant kernel family by total per-launch time
+    fam_time, fam_bytes, fam_n = {}, {}, {}
+    per_shape = []
+    for c, p, d in zip(cases, r["plans"], r["per_launch"]):
+        fam = "dotprod" if p["backend"] == 1 else "splitk"
+        med = statistics.median(d)
+        fam_time[fam] = fam_time.get(fam, 0.0) + sum(d)
+        fam_bytes[fam] = fam_bytes.get(fam, 0.0) + c.algorithmic_bytes * len(d)
+        fam_n[fam] = fam_n.get(fam, 0) + len(d)
+        per_shape.append({"M": c.M, "N": c.N, "K": c.K, "kernel": fam, "consumer": p["consumer"],
+                          "split_k": p["split_k"], "block_n": p["block_n"],
+                          "us_median": round(med, 3), "us_p10": round(float(np.percentile(d, 10)), 3),
+                          "us_p90": round(float(np.percentile(d, 90)), 3),
+                          "gbs_median": round(c.algorithmic_bytes / med / 1e3, 1)})
+    dom = max(fam_time, key=fam_time.get)
+    total_t = sum(fam_time.values())
+    achieved = fam_bytes[dom] / (fam_time[dom] * 1e-6) / 1e9
+    traffic = committed_traffic(dom, args.workload)
+    roofline = {"bound": "hbm", "kernel": f"skinny_{dom}_kernel", "achieved": round(achieved, 1),
+                "peak": round(peak, 1), "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_source": peak_src,
+                "traffic": traffic, "time_share": round(fam_time[dom] / total_t, 3),
+                "avg_launch_us": round(fam_time[dom] / fam_n[dom], 3),
+                "algorithmic_bytes_per_launch": round(fam_bytes[dom] / fam_n[dom])}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        gbs, s_step, sample = oracle_step_sample(cases, args.cpu_seconds)
+        cpu = {"value": round(gbs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample}
+
+    e2e_gbs = r["step_bytes"] * args.steps * n / r["e2e_elapsed"] / 1e9
+    line = {
+        "metric": METRIC, "value": round(value_gbs, 2), "unit": "GB/s", "n_gpus": n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "calls_per_step": len(cases),
+                   "l2": f"cold: {r['n_rep']} rotating replicas of every W ({r['pool_mb']:.0f} MB > 2x L2 "
+                         f"{r['l2'] / 1e6:.0f} MB)",
+                   "graph": "each step replayed from a CUDA graph of the C-ABI calls",
+                   "pdl": args.pdl, "parallelism": f"replicas x{n}" if n > 1 else "single GPU"},
+        "us_per_call": round(us_per_call, 3),
+        "us_per_call_l2_warm": round(r["warm_us_per_call"], 3),
+        "pct_of_roofline_step": round(value_gbs / n / peak, 4),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"],
+                "us_per_call": round(r["e2e_elapsed"] / args.steps / len(cases) * 1e6, 3),
+                "note": "W resident (weights); X copied in and Y copied out every step, inside the graph"},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+        "per_shape": per_shape,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,171 @@
+/*
+ * skinny_gemm.h -- C ABI of the GB300 (sm_103a) low-latency skinny BF16 GEMM.
+ *
+ *     Y[m][n] = sum_k  X[m][k] * W[n][k]      0 <= m < M <= 16,  0 <= n < N
+ *
+ * X is [M, K] bf16, W is [N, K] bf16 (a weight, e.g. the MoE router's
+ * [experts, hidden] matrix or a decode projection's [out, in] matrix), both
+ * row-major with row strides ldx / ldw in elements; Y is [M, N] fp32, row
+ * stride ldy >= N (strided output, the gaps n >= N are never written).
+ * Products and sums are fp32 (fused multiply-add, round to nearest); the
+ * output is fp32.
+ *
+ * Operation defined by: "[Perf][Feat] Add generic cuteDSL LL BF16 router
+ * (GEMM)" (vllm PR #42562 report), section "Implementation breakdown"
+ * items 1-4 (dot-product kernel for small M, cluster split-K kernel for larger
+ * M, a (M, K, N) dispatcher, the M <= 16 bf16-only router tier) and the
+ * review notes on alignment and dtype guards; and "GLM-5.2 Blackwell decode
+ * optimizations" (vllm PR #48597), section "Implementation breakdown" item 3
+ * (bf16_skinny_gemm for the decode projections, strided output) and item 2
+ * (programmatic dependent launch).
+ *
+ * bf16 values are passed as their 16-bit patterns (uint16_t) so this header
+ * needs no CUDA header.  Streams are passed as `void*` holding a cudaStream_t
+ * (NULL = the legacy default stream).
+ *
+ * Ownership: the caller owns X, W and Y (device memory, e.g. allocated by
+ * PyTorch).  The library allocates nothing per call, never synchronises in
+ * skinny_gemm_bf16, and keeps only small per-device state created by
+ * skinny_init (or by the first call on a device).
+ *
+ * Thread safety: calls may be made concurrently from several host threads.
+ * Options (skinny_set_option) are process-wide.
+ */
+#ifndef SKINNY_GEMM_H_
+#define SKINNY_GEMM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SKINNY_MAX_M 16
+
+/* Exported from libskinny_gemm.so (built with hidden default visibility). */
+#if defined(__GNUC__)
+#define SKINNY_API __attribute__((visibility("default")))
+#else
+#define SKINNY_API
+#endif
+
+typedef enum {
+    SKINNY_OK = 0,
+    SKINNY_ERR_INVALID_VALUE = 1,   /* negative size, ld too small, NULL with work to do, Y overlaps X or W */
+    SKINNY_ERR_UNSUPPORTED = 2,     /* M > 16, or a forced plan that cannot run this shape */
+    SKINNY_ERR_MISALIGNED = 3,      /* X or W not 2-byte aligned, Y not 4-byte aligned */
+    SKINNY_ERR_LAUNCH = 4,          /* the CUDA launch failed (cudaGetLastError after the launch) */
+    SKINNY_ERR_DEVICE_TIMEOUT = 5,  /* a bounded wait inside a kernel gave up (see skinny_get_device_status) */
+    SKINNY_ERR_NO_DEVICE = 6        /* no usable CUDA device / the device is not sm_103 */
+} skinny_status_t;
+
+typedef enum {
+    SKINNY_BACKEND_AUTO = 0,
+    SKINNY_BACKEND_DOTPROD = 1,     /* one CTA per block of output columns, whole K */
+    SKINNY_BACKEND_SPLITK = 2       /* K split over the CTAs of a thread-block cluster */
+} skinny_backend_t;
+
+typedef enum {
+    SKINNY_CONSUMER_AUTO = 0,
+    SKINNY_CONSUMER_FMA = 1,        /* CUDA-core fp32 fused multiply-add */
+    SKINNY_CONSUMER_MMA = 2         /* mma.sync m16n8k16 bf16 -> fp32, W on the MMA's M side */
+} skinny_consumer_t;
+
+/* The launch a call would make.  Filled by skinny_query_plan / skinny_plan_for. */
+typedef struct {
+    int backend;       /* skinny_backend_t actually used */
+    int consumer;      /* skinny_consumer_t actually used (split-K only; dot-product is FMA) */
+    int vec_elems;     /* W load width in bf16 elements: 8 (128-bit), 4, 2 or 1 */
+    int block_n;       /* output columns (rows of W) per CTA tile */
+    int split_k;       /* CTAs per cluster along K (1 = no cluster) */
+    int stages;        /* shared-memory ring depth (split-K) */
+    int k_chunk;       /* dot-product: K elements of X staged in shared memory at a time;
+                          split-K: K elements per CTA (the cluster rank's slice) */
+    int grid_x;        /* grid dimensions launched */
+    int grid_y;
+    int threads;       /* threads per CTA */
+    int smem_bytes;    /* dynamic shared memory per CTA */
+    int pdl;           /* 1 if launched with programmatic dependent launch */
+    int tuned;         /* 1 if the plan came from the measured tuning table */
+} skinny_plan_t;
+
+typedef enum {
+    SKINNY_OPT_PDL = 1,              /* 0/1: programmatic dependent launch (default: env SKINNY_PDL, else 0) */
+    SKINNY_OPT_FORCE_BACKEND = 2,    /* skinny_backend_t; AUTO = dispatcher (tests / tuning only) */
+    SKINNY_OPT_FORCE_CONSUMER = 3,   /* skinny_consumer_t for split-K; AUTO = dispatcher */
+    SKINNY_OPT_FORCE_SPLIT_K = 4,    /* 0 = dispatcher, 1..8 = cluster size */
+    SKINNY_OPT_FORCE_BLOCK_N = 5,    /* 0 = dispatcher; dot-product 1/2/4/8, split-K 16/64 */
+    SKINNY_OPT_FORCE_STAGES = 6,     /* 0 = dispatcher, 2..8 */
+    SKINNY_OPT_WAIT_TIMEOUT_US = 7,  /* budget of each bounded wait in a kernel, microseconds
+                                        (default 500000).  0 makes every such wait give up at once,
+                                        which exercises the timeout path without any real hang */
+    SKINNY_OPT_LOG = 8               /* 1: print the plan chosen for each new call shape to stderr
+                                        (default: env SKINNY_LOG) */
+} skinny_option_t;
+
+/*
+ * Y = X . W^T on `stream` (asynchronous; no host synchronisation, no
+ * allocation, so it can be captured in a CUDA graph).
+ *
+ *   X      device pointer, bf16 [M, K], row stride ldx >= K (elements), 2-byte aligned
+ *   W      device pointer, bf16 [N, K], row stride ldw >= K (elements), 2-byte aligned
+ *   Y      device pointer, fp32 [M, N], row stride ldy >= N (elements), 4-byte aligned;
+ *          must not overlap X or W.  Only Y[m*ldy + n], m < M, n < N, is written.
+ *   M      1..16 tokens (0 is a no-op); N, K >= 0.  K == 0 writes zeros (the empty sum).
+ *
+ * 16-byte alignment is not required: the dispatcher picks the widest W load
+ * that the base pointer and ldw allow (see skinny_plan_t.vec_elems).
+ *
+ * With PDL on, W is read before the kernel waits for the preceding kernel in
+ * the stream (W is a weight); X is read and Y written only after that wait.
+ * So W must not be written by the kernel launched just before on the stream.
+ *
+ * Returns SKINNY_OK once the launch is queued; every argument error is
+ * detected on the host before anything is launched.  Errors inside a kernel
+ * (a bounded wait that gave up) are recorded in a per-device status word read
+ * by skinny_get_device_status.
+ */
+SKINNY_API skinny_status_t skinny_gemm_bf16(const uint16_t *X, int ldx,
+                                 const uint16_t *W, int ldw,
+                                 float *Y, int ldy,
+                                 int M, int N, int K, void *stream);
+
+/* Optional: prepare `device` (query it, check it is sm_103, set kernel
+ * attributes, find the status word).  The first call on a device does the
+ * same; calling this first keeps that work out of a CUDA-graph capture.
+ * Leaves the current device unchanged. */
+SKINNY_API skinny_status_t skinny_init(int device);
+
+/* The plan skinny_gemm_bf16 would launch for these arguments on the current
+ * device (after the same argument checks).  Host only, no launch. */
+SKINNY_API skinny_status_t skinny_query_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
+                                  const float *Y, int ldy, int M, int N, int K,
+                                  skinny_plan_t *plan);
+
+/* The dispatcher as a pure function of the arguments and an SM count: no
+ * CUDA call at all (usable without a GPU).  Honours the force options. */
+SKINNY_API skinny_status_t skinny_plan_for(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
+                                const float *Y, int ldy, int M, int N, int K,
+                                int num_sms, skinny_plan_t *plan);
+
+SKINNY_API skinny_status_t skinny_set_option(int option, int value);
+SKINNY_API skinny_status_t skinny_get_option(int option, int *value);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word: *code = 0 if no kernel reported an error since the last read, else a
+ * value whose low 8 bits are a skinny_status_t (SKINNY_ERR_DEVICE_TIMEOUT)
+ * and whose upper bits say which wait gave up (1 = consumer full-slot wait,
+ * 2 = producer empty-slot wait, 3 = drain wait).  Test and diagnostic use. */
+SKINNY_API skinny_status_t skinny_get_device_status(void *stream, int *code);
+
+/* Static string for a status code (never NULL). */
+SKINNY_API const char *skinny_status_string(skinny_status_t status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+SKINNY_API int skinny_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKINNY_GEMM_H_ */

@@ -1,0 +1,243 @@
+"""GB300-native low-latency skinny BF16 GEMM, ``Y[M,N] = X[M,K] . W[N,K]^T``.
+
+bf16 inputs, fp32 multiply-add, fp32 output, M = 1..16 (decode-sized), as used
+for the MoE router logits and the small-batch decode projections.
+
+This module is a thin ctypes binding over ``libskinny_gemm.so`` (the C ABI in
+``include/skinny_gemm.h``): the functions below carry the C names and only
+marshal arguments.  Every step of the GEMM runs in the library's sm_103a
+kernels; there is no CPU or library fallback, and importing the binding
+raises if the compiled library is missing.  PyTorch is used only by the
+tensor convenience wrapper :func:`gemm` (device memory and streams).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+__all__ = [
+    "SkinnyError", "load_library", "library_path",
+    "skinny_gemm_bf16", "skinny_init", "skinny_query_plan", "skinny_plan_for",
+    "skinny_set_option", "skinny_get_option", "skinny_get_device_status",
+    "skinny_status_string", "skinny_version", "gemm", "options",
+]
+
+# ---- constants mirrored from include/skinny_gemm.h
+SKINNY_MAX_M = 16
+SKINNY_OK = 0
+SKINNY_ERR_INVALID_VALUE = 1
+SKINNY_ERR_UNSUPPORTED = 2
+SKINNY_ERR_MISALIGNED = 3
+SKINNY_ERR_LAUNCH = 4
+SKINNY_ERR_DEVICE_TIMEOUT = 5
+SKINNY_ERR_NO_DEVICE = 6
+
+SKINNY_BACKEND_AUTO = 0
+SKINNY_BACKEND_DOTPROD = 1
+SKINNY_BACKEND_SPLITK = 2
+SKINNY_CONSUMER_AUTO = 0
+SKINNY_CONSUMER_FMA = 1
+SKINNY_CONSUMER_MMA = 2
+
+SKINNY_OPT_PDL = 1
+SKINNY_OPT_FORCE_BACKEND = 2
+SKINNY_OPT_FORCE_CONSUMER = 3
+SKINNY_OPT_FORCE_SPLIT_K = 4
+SKINNY_OPT_FORCE_BLOCK_N = 5
+SKINNY_OPT_FORCE_STAGES = 6
+SKINNY_OPT_WAIT_TIMEOUT_US = 7
+SKINNY_OPT_LOG = 8
+
+EXPORTED_SYMBOLS = (
+    "skinny_gemm_bf16", "skinny_init", "skinny_query_plan", "skinny_plan_for",
+    "skinny_set_option", "skinny_get_option", "skinny_get_device_status",
+    "skinny_status_string", "skinny_version",
+)
+
+
+class SkinnyError(RuntimeError):
+    """A non-zero skinny_status_t."""
+
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        super().__init__(f"{what}: {skinny_status_string(status)} ({status})" if what else
+                         f"{skinny_status_string(status)} ({status})")
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "backend", "consumer", "vec_elems", "block_n", "split_k", "stages", "k_chunk",
+        "grid_x", "grid_y", "threads", "smem_bytes", "pdl", "tuned")]
+
+    def as_dict(self) -> dict:
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    lib.skinny_gemm_bf16.argtypes = [vp, i, vp, i, vp, i, i, i, i, vp]
+    lib.skinny_gemm_bf16.restype = i
+    lib.skinny_init.argtypes = [i]
+    lib.skinny_init.restype = i
+    lib.skinny_query_plan.argtypes = [vp, i, vp, i, vp, i, i, i, i, ctypes.POINTER(_Plan)]
+    lib.skinny_query_plan.restype = i
+    lib.skinny_plan_for.argtypes = [vp, i, vp, i, vp, i, i, i, i, i, ctypes.POINTER(_Plan)]
+    lib.skinny_plan_for.restype = i
+    lib.skinny_set_option.argtypes = [i, i]
+    lib.skinny_set_option.restype = i
+    lib.skinny_get_option.argtypes = [i, ctypes.POINTER(i)]
+    lib.skinny_get_option.restype = i
+    lib.skinny_get_device_status.argtypes = [vp, ctypes.POINTER(i)]
+    lib.skinny_get_device_status.restype = i
+    lib.skinny_status_string.argtypes = [i]
+    lib.skinny_status_string.restype = ctypes.c_char_p
+    lib.skinny_version.argtypes = []
+    lib.skinny_version.restype = i
+    return lib
+
+
+def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
+    """The loaded ``libskinny_gemm.so``.  Raises if it has not been built
+    (``__graft_entry__.build()`` or ``python -m latency_skinny_bf16_gb300._build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                if not build_if_missing:
+                    raise ImportError(f"{path} is missing: build the CUDA library first "
+                                      "(python -c 'import __graft_entry__ as g; g.build()')")
+                _build.build()
+            _lib = _bind(ctypes.CDLL(path))
+        return _lib
+
+
+# ---------------------------------------------------------------- C-named wrappers (raw pointers)
+
+def skinny_gemm_bf16(X: int, ldx: int, W: int, ldw: int, Y: int, ldy: int,
+                     M: int, N: int, K: int, stream: int = 0) -> int:
+    """Raw C call: device pointers as ints; returns the skinny_status_t."""
+    return load_library().skinny_gemm_bf16(X, ldx, W, ldw, Y, ldy, M, N, K, stream)
+
+
+def skinny_init(device: int = 0) -> int:
+    return load_library().skinny_init(device)
+
+
+def skinny_query_plan(X: int, ldx: int, W: int, ldw: int, Y: int, ldy: int,
+                      M: int, N: int, K: int) -> dict:
+    p = _Plan()
+    st = load_library().skinny_query_plan(X, ldx, W, ldw, Y, ldy, M, N, K, ctypes.byref(p))
+    if st != SKINNY_OK:
+        raise SkinnyError(st, "skinny_query_plan")
+    return p.as_dict()
+
+
+def skinny_plan_for(X: int, ldx: int, W: int, ldw: int, Y: int, ldy: int,
+                    M: int, N: int, K: int, num_sms: int) -> dict:
+    p = _Plan()
+    st = load_library().skinny_plan_for(X, ldx, W, ldw, Y, ldy, M, N, K, num_sms, ctypes.byref(p))
+    if st != SKINNY_OK:
+        raise SkinnyError(st, "skinny_plan_for")
+    return p.as_dict()
+
+
+def skinny_set_option(option: int, value: int) -> None:
+    st = load_library().skinny_set_option(option, int(value))
+    if st != SKINNY_OK:
+        raise SkinnyError(st, f"skinny_set_option({option}, {value})")
+
+
+def skinny_get_option(option: int) -> int:
+    v = ctypes.c_int(0)
+    st = load_library().skinny_get_option(option, ctypes.byref(v))
+    if st != SKINNY_OK:
+        raise SkinnyError(st, f"skinny_get_option({option})")
+    return v.value
+
+
+def skinny_get_device_status(stream: int = 0) -> int:
+    """Synchronise ``stream``, read and clear the device status word."""
+    v = ctypes.c_int(0)
+    st = load_library().skinny_get_device_status(stream, ctypes.byref(v))
+    if st != SKINNY_OK:
+        raise SkinnyError(st, "skinny_get_device_status")
+    return v.value
+
+
+def skinny_status_string(status: int) -> str:
+    return load_library().skinny_status_string(int(status)).decode()
+
+
+def skinny_version() -> int:
+    return load_library().skinny_version()
+
+
+class options:
+    """Context manager that sets library options and restores them on exit."""
+
+    def __init__(self, **kw):
+        names = {"pdl": SKINNY_OPT_PDL, "backend": SKINNY_OPT_FORCE_BACKEND,
+                 "consumer": SKINNY_OPT_FORCE_CONSUMER, "split_k": SKINNY_OPT_FORCE_SPLIT_K,
+                 "block_n": SKINNY_OPT_FORCE_BLOCK_N, "stages": SKINNY_OPT_FORCE_STAGES,
+                 "wait_timeout_us": SKINNY_OPT_WAIT_TIMEOUT_US, "log": SKINNY_OPT_LOG}
+        self._set = [(names[k], int(v)) for k, v in kw.items()]
+        self._old = []
+
+    def __enter__(self):
+        for opt, v in self._set:
+            self._old.append((opt, skinny_get_option(opt)))
+            skinny_set_option(opt, v)
+        return self
+
+    def __exit__(self, *exc):
+        for opt, v in reversed(self._old):
+            skinny_set_option(opt, v)
+        self._old.clear()
+        return False
+
+
+# ---------------------------------------------------------------- tensor convenience
+
+def gemm(x, w, out=None, stream=None):
+    """``out[:M, :N] = x . w^T`` for CUDA tensors: x bf16 [M, K], w bf16 [N, K]
+    (unit stride along K), out fp32 [M, N] (any row stride >= N, unit column
+    stride).  Runs on ``stream`` (default: torch's current stream)."""
+    import torch
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+        raise TypeError("x and w must be bfloat16")
+    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError(f"shape mismatch: x {tuple(x.shape)}, w {tuple(w.shape)}")
+    if not (x.is_cuda and w.is_cuda):
+        raise ValueError("x and w must be CUDA tensors")
+    M, K = x.shape
+    N = w.shape[0]
+    if (K > 1 and (x.stride(1) != 1 or w.stride(1) != 1)):
+        raise ValueError("x and w need unit stride along K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if out.dtype != torch.float32 or out.dim() != 2 or tuple(out.shape) != (M, N):
+        raise ValueError("out must be fp32 [M, N]")
+    if N > 1 and out.stride(1) != 1:
+        raise ValueError("out needs unit column stride")
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    ldx = x.stride(0) if M > 1 else max(K, 1)
+    ldw = w.stride(0) if N > 1 else max(K, 1)
+    ldy = out.stride(0) if M > 1 else max(N, 1)
+    st = skinny_gemm_bf16(x.data_ptr(), ldx, w.data_ptr(), ldw, out.data_ptr(), ldy, M, N, K, s)
+    if st != SKINNY_OK:
+        raise SkinnyError(st, "skinny_gemm_bf16")
+    return out

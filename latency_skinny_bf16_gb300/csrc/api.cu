@@ -1,0 +1,431 @@
+// api.cu -- the C ABI of libskinny_gemm.so: argument checks, per-device set-up,
+// the (M, K, N) dispatcher with its measured tuning table, options, and the
+// device status word.
+//
+// Dispatch follows "[Perf][Feat] Add generic cuteDSL LL BF16 router (GEMM)",
+// section "Key source snippets" (ll_bf16.py: LLBf16Gemm.dispatch picks the
+// dot-product kernel when M is at most a per-(K, N) tuned maximum or K < 2048,
+// otherwise split-K with a per-(K, N, M) tuned (split_k, num_stages)), and the
+// review notes there (bf16-only, M <= 16, no over-strong alignment
+// assumption).  Here the tuning table is measured on GB300 and compiled in, and
+// every plan is checked against what the kernels support before launch.
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <set>
+#include <tuple>
+
+#include "internal.h"
+
+namespace skinny {
+namespace {
+
+// ------------------------------------------------------------------ device status word
+__device__ int g_status_word;
+
+__global__ void zero_fill_kernel(float *Y, int64_t ldy, int M, int N) {
+    const int64_t total = (int64_t)M * N;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = i / N, n = i - m * N;
+        Y[m * ldy + n] = 0.f;
+    }
+}
+
+// ------------------------------------------------------------------ options
+std::atomic<int> g_opt_pdl{-1};            // -1: not yet read from the environment
+std::atomic<int> g_opt_force_backend{0};
+std::atomic<int> g_opt_force_consumer{0};
+std::atomic<int> g_opt_force_split_k{0};
+std::atomic<int> g_opt_force_block_n{0};
+std::atomic<int> g_opt_force_stages{0};
+std::atomic<int> g_opt_wait_us{500000};
+std::atomic<int> g_opt_log{-1};
+
+int env_flag(const char *name) {
+    const char *v = std::getenv(name);
+    return (v && v[0] && std::strcmp(v, "0") != 0) ? 1 : 0;
+}
+int opt_pdl() {
+    int v = g_opt_pdl.load();
+    if (v < 0) { v = env_flag("SKINNY_PDL"); g_opt_pdl.store(v); }
+    return v;
+}
+int opt_log() {
+    int v = g_opt_log.load();
+    if (v < 0) { v = env_flag("SKINNY_LOG"); g_opt_log.store(v); }
+    return v;
+}
+
+// ------------------------------------------------------------------ per-device state
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+    std::once_flag once;
+    skinny_status_t status = SKINNY_ERR_NO_DEVICE;
+    int num_sms = 0;
+    int *status_word = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+
+skinny_status_t init_device_current(DeviceState &d, int device) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return SKINNY_ERR_NO_DEVICE;
+    if (major != 10 || minor != 3) return SKINNY_ERR_NO_DEVICE;   // built for sm_103a only
+    if (dotprod_prepare() != cudaSuccess || splitk_prepare() != cudaSuccess) return SKINNY_ERR_LAUNCH;
+    void *sym = nullptr;
+    if (cudaGetSymbolAddress(&sym, g_status_word) != cudaSuccess) return SKINNY_ERR_LAUNCH;
+    d.num_sms = sms;
+    d.status_word = static_cast<int *>(sym);
+    return SKINNY_OK;
+}
+
+// Runs the set-up once per device, with that device current.
+skinny_status_t ensure_device(int device) {
+    if (device < 0 || device >= kMaxDevices) return SKINNY_ERR_NO_DEVICE;
+    DeviceState &d = g_dev[device];
+    std::call_once(d.once, [&] {
+        int prev = -1;
+        if (cudaGetDevice(&prev) != cudaSuccess) { d.status = SKINNY_ERR_NO_DEVICE; return; }
+        if (prev != device && cudaSetDevice(device) != cudaSuccess) { d.status = SKINNY_ERR_NO_DEVICE; return; }
+        d.status = init_device_current(d, device);
+        if (prev != device) cudaSetDevice(prev);
+    });
+    return d.status;
+}
+
+skinny_status_t current_device(int *device) {
+    if (cudaGetDevice(device) != cudaSuccess) return SKINNY_ERR_NO_DEVICE;
+    return ensure_device(*device);
+}
+
+// ------------------------------------------------------------------ argument checks
+bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+// Host-only validation; no CUDA call.  *noop is set when there is nothing to launch.
+skinny_status_t validate(const uint16_t *X, int ldx, const uint16_t *W, int ldw, const float *Y, int ldy,
+                         int M, int N, int K, bool *noop) {
+    *noop = false;
+    if (M < 0 || N < 0 || K < 0) return SKINNY_ERR_INVALID_VALUE;
+    if (M > SKINNY_MAX_M) return SKINNY_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) { *noop = true; return SKINNY_OK; }
+    if (Y == nullptr || ldy < N) return SKINNY_ERR_INVALID_VALUE;
+    if (reinterpret_cast<uintptr_t>(Y) & 3) return SKINNY_ERR_MISALIGNED;
+    if (K == 0) return SKINNY_OK;
+    if (X == nullptr || W == nullptr || ldx < K || ldw < K) return SKINNY_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(X) & 1) || (reinterpret_cast<uintptr_t>(W) & 1)) return SKINNY_ERR_MISALIGNED;
+    const uintptr_t y0 = reinterpret_cast<uintptr_t>(Y);
+    const uintptr_t y1 = y0 + (uintptr_t)(((int64_t)(M - 1) * ldy + N) * 4);
+    const uintptr_t x0 = reinterpret_cast<uintptr_t>(X);
+    const uintptr_t x1 = x0 + (uintptr_t)(((int64_t)(M - 1) * ldx + K) * 2);
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(W);
+    const uintptr_t w1 = w0 + (uintptr_t)(((int64_t)(N - 1) * ldw + K) * 2);
+    if (ranges_overlap(y0, y1, x0, x1) || ranges_overlap(y0, y1, w0, w1)) return SKINNY_ERR_INVALID_VALUE;
+    return SKINNY_OK;
+}
+
+// ------------------------------------------------------------------ dispatcher
+struct TunedEntry {
+    int K, N, m_lo, m_hi;
+    int backend, consumer, split_k, block_n, stages;
+};
+const TunedEntry kTuned[] = {
+#include "tuning_table.inc"
+    {0, 0, 0, 0, 0, 0, 0, 0, 0}};
+
+const TunedEntry *lookup_tuned(int M, int N, int K) {
+    for (const TunedEntry &e : kTuned)
+        if (e.K == K && e.N == N && M >= e.m_lo && M <= e.m_hi) return &e;
+    return nullptr;
+}
+
+int widest_vec(const uint16_t *W, int ldw) {
+    const uintptr_t w = reinterpret_cast<uintptr_t>(W);
+    if ((w & 15) == 0 && (ldw & 7) == 0) return 8;
+    if ((w & 7) == 0 && (ldw & 3) == 0) return 4;
+    if ((w & 3) == 0 && (ldw & 1) == 0) return 2;
+    return 1;
+}
+
+int pow2_floor(int v) { int p = 1; while (p * 2 <= v) p *= 2; return p; }
+
+constexpr int kDotXBudget = 96 * 1024;     // X bytes staged per dot-product CTA
+constexpr int kSplitXBudget = 160 * 1024;  // X slice bytes per split-K CTA
+
+bool plan_dotprod(int M, int N, int K, int vec, int force_bn, int num_sms, skinny_plan_t *p) {
+    int bn = force_bn;
+    if (bn == 0) {
+        bn = (vec == 8) ? pow2_floor(N / (2 * num_sms) > 0 ? N / (2 * num_sms) : 1) : 1;
+        if (bn > 8) bn = 8;
+    }
+    if (!dotprod_supported(M, vec, bn)) return false;
+    // Whole K when it fits; otherwise chunks of a multiple of 8 * 128 elements,
+    // so every K vector lands on the same thread whatever M is (each thread's
+    // summation order, hence the result, is independent of M and of chunking).
+    const int k8 = (K + 7) & ~7;
+    int kc = (kDotXBudget / (2 * M)) & ~7;
+    if (kc >= k8) {
+        kc = k8;
+    } else {
+        kc = (kc / (8 * kDotThreads)) * (8 * kDotThreads);
+        if (kc < 8 * kDotThreads) kc = 8 * kDotThreads;
+    }
+    p->backend = SKINNY_BACKEND_DOTPROD;
+    p->consumer = SKINNY_CONSUMER_FMA;
+    p->vec_elems = vec;
+    p->block_n = bn;
+    p->split_k = 1;
+    p->stages = 0;
+    p->k_chunk = kc;
+    p->grid_x = (N + bn - 1) / bn;
+    p->grid_y = 1;
+    p->threads = kDotThreads;
+    p->smem_bytes = dotprod_smem_bytes(M, bn, kc);
+    return p->smem_bytes <= kMaxDynSmem;
+}
+
+bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int force_stages, int num_sms,
+                 skinny_plan_t *p) {
+    if (vec != 8 || K % 8 != 0 || K < 8) return false;
+    if (consumer == SKINNY_CONSUMER_MMA && K % 16 != 0) return false;
+    if (!splitk_supported(M, consumer, 16)) return false;
+    const int tiles = (N + 15) / 16;
+    if (tiles > 65535) return false;
+    int S = force_s;
+    if (S == 0) {
+        S = num_sms / tiles;
+        const int max_by_k = (K + kSplitBK - 1) / kSplitBK;
+        if (S > max_by_k) S = max_by_k;
+        if (S > kSplitMaxCluster) S = kSplitMaxCluster;
+        if (S < 1) S = 1;
+    }
+    if (S < 1 || S > kSplitMaxCluster) return false;
+    for (;; ++S) {
+        if (S > kSplitMaxCluster) return false;
+        const int ks = ((K + S - 1) / S + 15) & ~15;
+        const int xrows = consumer == SKINNY_CONSUMER_MMA ? (M <= 8 ? 8 : 16) : M;
+        const int xbytes = xrows * (((ks * 2 + 127) & ~127) + 16);
+        if (xbytes <= kSplitXBudget || force_s) {
+            const int nchunks = (ks + kSplitBK - 1) / kSplitBK;
+            int stages = force_stages ? force_stages : (nchunks < 4 ? (nchunks < 1 ? 1 : nchunks) : 4);
+            if (stages < 1 || stages > kSplitMaxStages) return false;
+            p->backend = SKINNY_BACKEND_SPLITK;
+            p->consumer = consumer;
+            p->vec_elems = 8;
+            p->block_n = 16;
+            p->split_k = S;
+            p->stages = stages;
+            p->k_chunk = ks;
+            p->grid_x = S;
+            p->grid_y = tiles;
+            p->threads = kSplitThreads;
+            p->smem_bytes = splitk_smem_bytes(M, consumer, 16, stages, ks, S);
+            return p->smem_bytes <= kMaxDynSmem;
+        }
+    }
+}
+
+skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int num_sms, skinny_plan_t *p) {
+    std::memset(p, 0, sizeof(*p));
+    if (num_sms < 1) return SKINNY_ERR_INVALID_VALUE;
+    const int vec = widest_vec(W, ldw);
+    const int fb = g_opt_force_backend.load(), fc = g_opt_force_consumer.load();
+    const int fs = g_opt_force_split_k.load(), fbn = g_opt_force_block_n.load();
+    const int fst = g_opt_force_stages.load();
+    const bool splitk_ok = vec == 8 && K % 8 == 0;
+    const bool mma_ok = splitk_ok && K % 16 == 0;
+    const int pdl = opt_pdl();
+
+    int backend = fb, consumer = fc, split = fs, bn = fbn, stages = fst;
+    int tuned = 0;
+    if (backend == SKINNY_BACKEND_AUTO) {
+        const TunedEntry *e = lookup_tuned(M, N, K);
+        if (e && (e->backend == SKINNY_BACKEND_DOTPROD || splitk_ok) &&
+            (e->consumer != SKINNY_CONSUMER_MMA || mma_ok)) {
+            backend = e->backend;
+            if (consumer == SKINNY_CONSUMER_AUTO) consumer = e->consumer;
+            if (!split) split = e->split_k;
+            if (!bn) bn = e->block_n;
+            if (!stages) stages = e->stages;
+            tuned = 1;
+        } else {
+            // default rule: dot-product for small M or short K, else split-K
+            backend = (M <= 4 || K < 2048 || !splitk_ok) ? SKINNY_BACKEND_DOTPROD : SKINNY_BACKEND_SPLITK;
+        }
+    }
+    bool ok;
+    if (backend == SKINNY_BACKEND_DOTPROD) {
+        if (fc == SKINNY_CONSUMER_MMA) return SKINNY_ERR_UNSUPPORTED;
+        if (vec != 8 && bn > 1 && fbn) return SKINNY_ERR_UNSUPPORTED;
+        ok = plan_dotprod(M, N, K, vec, vec == 8 ? bn : 1, num_sms, p);
+    } else if (backend == SKINNY_BACKEND_SPLITK) {
+        if (consumer == SKINNY_CONSUMER_AUTO) consumer = (M > 4 && mma_ok) ? SKINNY_CONSUMER_MMA : SKINNY_CONSUMER_FMA;
+        if (bn != 0 && bn != 16) return SKINNY_ERR_UNSUPPORTED;
+        ok = plan_splitk(M, N, K, vec, consumer, split, stages, num_sms, p);
+        if (!ok && fb == SKINNY_BACKEND_AUTO) {
+            // a tuned split-K entry that these pointers / strides cannot use
+            ok = plan_dotprod(M, N, K, vec, 0, num_sms, p);
+            tuned = 0;
+        }
+    } else {
+        return SKINNY_ERR_INVALID_VALUE;
+    }
+    if (!ok) return SKINNY_ERR_UNSUPPORTED;
+    p->pdl = pdl;
+    p->tuned = tuned;
+    return SKINNY_OK;
+}
+
+void log_plan(int M, int N, int K, int ldw, const skinny_plan_t &p) {
+    static std::mutex mu;
+    static std::set<std::tuple<int, int, int, int, int>> seen;
+    std::lock_guard<std::mutex> g(mu);
+    if (!seen.insert({M, N, K, ldw, p.pdl}).second) return;
+    std::fprintf(stderr,
+                 "[skinny] M=%d N=%d K=%d ldw=%d -> %s consumer=%d vec=%d block_n=%d split_k=%d stages=%d "
+                 "k_chunk=%d grid=%dx%d smem=%d pdl=%d tuned=%d\n",
+                 M, N, K, ldw, p.backend == SKINNY_BACKEND_DOTPROD ? "dotprod" : "splitk", p.consumer,
+                 p.vec_elems, p.block_n, p.split_k, p.stages, p.k_chunk, p.grid_x, p.grid_y, p.smem_bytes,
+                 p.pdl, p.tuned);
+}
+
+}  // namespace
+}  // namespace skinny
+
+using namespace skinny;
+
+extern "C" {
+
+skinny_status_t skinny_gemm_bf16(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
+                                 float *Y, int ldy, int M, int N, int K, void *stream) {
+    bool noop = false;
+    skinny_status_t st = validate(X, ldx, W, ldw, Y, ldy, M, N, K, &noop);
+    if (st != SKINNY_OK || noop) return st;
+    int device = 0;
+    st = current_device(&device);
+    if (st != SKINNY_OK) return st;
+    DeviceState &d = g_dev[device];
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        const int64_t total = (int64_t)M * N;
+        int blocks = (int)((total + 255) / 256);
+        if (blocks > 4 * d.num_sms) blocks = 4 * d.num_sms;
+        zero_fill_kernel<<<blocks, 256, 0, s>>>(Y, ldy, M, N);
+        return cudaPeekAtLastError() == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
+    }
+    skinny_plan_t plan;
+    st = make_plan(W, ldw, M, N, K, d.num_sms, &plan);
+    if (st != SKINNY_OK) return st;
+    if (opt_log()) log_plan(M, N, K, ldw, plan);
+    GemmArgs a{X, ldx, W, ldw, Y, ldy, M, N, K};
+    LaunchCtx c{s, plan.pdl != 0, d.status_word, (uint64_t)g_opt_wait_us.load() * 1000ull};
+    cudaError_t e = (plan.backend == SKINNY_BACKEND_DOTPROD) ? launch_dotprod(a, plan, c) : launch_splitk(a, plan, c);
+    return e == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
+}
+
+skinny_status_t skinny_init(int device) { return ensure_device(device); }
+
+skinny_status_t skinny_query_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw, const float *Y, int ldy,
+                                  int M, int N, int K, skinny_plan_t *plan) {
+    if (!plan) return SKINNY_ERR_INVALID_VALUE;
+    bool noop = false;
+    skinny_status_t st = validate(X, ldx, W, ldw, Y, ldy, M, N, K, &noop);
+    if (st != SKINNY_OK) return st;
+    int device = 0;
+    st = current_device(&device);
+    if (st != SKINNY_OK) return st;
+    if (noop || K == 0) { std::memset(plan, 0, sizeof(*plan)); return SKINNY_OK; }
+    return make_plan(W, ldw, M, N, K, g_dev[device].num_sms, plan);
+}
+
+skinny_status_t skinny_plan_for(const uint16_t *X, int ldx, const uint16_t *W, int ldw, const float *Y, int ldy,
+                                int M, int N, int K, int num_sms, skinny_plan_t *plan) {
+    if (!plan) return SKINNY_ERR_INVALID_VALUE;
+    bool noop = false;
+    skinny_status_t st = validate(X, ldx, W, ldw, Y, ldy, M, N, K, &noop);
+    if (st != SKINNY_OK) return st;
+    if (noop || K == 0) { std::memset(plan, 0, sizeof(*plan)); return SKINNY_OK; }
+    return make_plan(W, ldw, M, N, K, num_sms, plan);
+}
+
+skinny_status_t skinny_set_option(int option, int value) {
+    switch (option) {
+        case SKINNY_OPT_PDL:
+            if (value != 0 && value != 1) return SKINNY_ERR_INVALID_VALUE;
+            g_opt_pdl.store(value); return SKINNY_OK;
+        case SKINNY_OPT_FORCE_BACKEND:
+            if (value < 0 || value > 2) return SKINNY_ERR_INVALID_VALUE;
+            g_opt_force_backend.store(value); return SKINNY_OK;
+        case SKINNY_OPT_FORCE_CONSUMER:
+            if (value < 0 || value > 2) return SKINNY_ERR_INVALID_VALUE;
+            g_opt_force_consumer.store(value); return SKINNY_OK;
+        case SKINNY_OPT_FORCE_SPLIT_K:
+            if (value < 0 || value > kSplitMaxCluster) return SKINNY_ERR_INVALID_VALUE;
+            g_opt_force_split_k.store(value); return SKINNY_OK;
+        case SKINNY_OPT_FORCE_BLOCK_N:
+            if (!(value == 0 || value == 1 || value == 2 || value == 4 || value == 8 || value == 16))
+                return SKINNY_ERR_INVALID_VALUE;
+            g_opt_force_block_n.store(value); return SKINNY_OK;
+        case SKINNY_OPT_FORCE_STAGES:
+            if (value < 0 || value > kSplitMaxStages) return SKINNY_ERR_INVALID_VALUE;
+            g_opt_force_stages.store(value); return SKINNY_OK;
+        case SKINNY_OPT_WAIT_TIMEOUT_US:
+            if (value < 0) return SKINNY_ERR_INVALID_VALUE;
+            g_opt_wait_us.store(value); return SKINNY_OK;
+        case SKINNY_OPT_LOG:
+            if (value != 0 && value != 1) return SKINNY_ERR_INVALID_VALUE;
+            g_opt_log.store(value); return SKINNY_OK;
+        default:
+            return SKINNY_ERR_INVALID_VALUE;
+    }
+}
+
+skinny_status_t skinny_get_option(int option, int *value) {
+    if (!value) return SKINNY_ERR_INVALID_VALUE;
+    switch (option) {
+        case SKINNY_OPT_PDL: *value = opt_pdl(); return SKINNY_OK;
+        case SKINNY_OPT_FORCE_BACKEND: *value = g_opt_force_backend.load(); return SKINNY_OK;
+        case SKINNY_OPT_FORCE_CONSUMER: *value = g_opt_force_consumer.load(); return SKINNY_OK;
+        case SKINNY_OPT_FORCE_SPLIT_K: *value = g_opt_force_split_k.load(); return SKINNY_OK;
+        case SKINNY_OPT_FORCE_BLOCK_N: *value = g_opt_force_block_n.load(); return SKINNY_OK;
+        case SKINNY_OPT_FORCE_STAGES: *value = g_opt_force_stages.load(); return SKINNY_OK;
+        case SKINNY_OPT_WAIT_TIMEOUT_US: *value = g_opt_wait_us.load(); return SKINNY_OK;
+        case SKINNY_OPT_LOG: *value = opt_log(); return SKINNY_OK;
+        default: return SKINNY_ERR_INVALID_VALUE;
+    }
+}
+
+skinny_status_t skinny_get_device_status(void *stream, int *code) {
+    if (!code) return SKINNY_ERR_INVALID_VALUE;
+    int device = 0;
+    skinny_status_t st = current_device(&device);
+    if (st != SKINNY_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SKINNY_ERR_LAUNCH;
+    int v = 0;
+    const int zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return SKINNY_ERR_LAUNCH;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return SKINNY_ERR_LAUNCH;
+    *code = v;
+    return SKINNY_OK;
+}
+
+const char *skinny_status_string(skinny_status_t s) {
+    switch (s) {
+        case SKINNY_OK: return "SKINNY_OK";
+        case SKINNY_ERR_INVALID_VALUE: return "SKINNY_ERR_INVALID_VALUE";
+        case SKINNY_ERR_UNSUPPORTED: return "SKINNY_ERR_UNSUPPORTED";
+        case SKINNY_ERR_MISALIGNED: return "SKINNY_ERR_MISALIGNED";
+        case SKINNY_ERR_LAUNCH: return "SKINNY_ERR_LAUNCH";
+        case SKINNY_ERR_DEVICE_TIMEOUT: return "SKINNY_ERR_DEVICE_TIMEOUT";
+        case SKINNY_ERR_NO_DEVICE: return "SKINNY_ERR_NO_DEVICE";
+        default: return "SKINNY_ERR_UNKNOWN";
+    }
+}
+
+int skinny_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// internal.h -- host-side declarations shared by the translation units of
+// libskinny_gemm.so.  Nothing here is part of the public C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "skinny_gemm.h"
+
+namespace skinny {
+
+struct GemmArgs {
+    const uint16_t *X;
+    int64_t ldx;
+    const uint16_t *W;
+    int64_t ldw;
+    float *Y;
+    int64_t ldy;
+    int M, N, K;
+};
+
+struct LaunchCtx {
+    cudaStream_t stream;
+    bool pdl;            // programmatic dependent launch attribute
+    int *status;         // device status word (error reports from bounded waits)
+    uint64_t budget_ns;  // budget of each bounded wait; 0 = give up at once (test hook)
+};
+
+// ---- dot-product backend (dotprod.cu)
+constexpr int kDotThreads = 128;
+int dotprod_smem_bytes(int M, int block_n, int k_chunk);
+bool dotprod_supported(int M, int vec_elems, int block_n);
+cudaError_t dotprod_prepare();   // per-device kernel attributes
+cudaError_t launch_dotprod(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
+
+// ---- cluster split-K backend (splitk.cu)
+constexpr int kSplitConsumerWarps = 4;
+constexpr int kSplitThreads = (kSplitConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kSplitBK = 256;                                  // K elements per ring stage
+constexpr int kSplitMaxCluster = 8;
+constexpr int kSplitMaxStages = 8;
+int splitk_smem_bytes(int M, int consumer, int block_n, int stages, int k_slice, int split_k);
+bool splitk_supported(int M, int consumer, int block_n);
+cudaError_t splitk_prepare();
+cudaError_t launch_splitk(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
+
+// Per-CTA dynamic shared memory the dispatcher may plan for (B300: 232448
+// bytes opt-in per block; keep a margin for static shared memory).
+constexpr int kMaxDynSmem = 227 * 1024;
+
+}  // namespace skinny

@@ -1,0 +1,420 @@
+// splitk.cu -- the cluster split-K backend of the skinny BF16 GEMM.
+//
+// Design source: "[Perf][Feat] Add generic cuteDSL LL BF16 router (GEMM)",
+// section "Implementation breakdown" item 2 and the _ll_bf16_splitk.py
+// snippet (K partitioned over the CTAs of a thread-block cluster; DMA producer
+// warps and MMA consumer warps; a shared-memory pipeline of num_stages; the
+// partial sums reduced across the cluster through distributed shared memory
+// with st.shared::cluster), and the review notes on that page (the cluster
+// barrier must be the non-.aligned form because the producer warp takes
+// another branch).
+//
+// GB300 form.  A cluster of S <= 8 CTAs owns a tile of BN = 16 output columns
+// (rows of W); CTA `rank` owns the K slice [rank*KS, rank*KS + KS).
+//   * Warp 4 is the producer: one lane per W row issues a 1-D bulk async copy
+//     (cp.async.bulk, the TMA engine, no multicast) of the row's next BK = 256
+//     elements into a `stages`-deep shared-memory ring, completing on the
+//     stage's "full" mbarrier.  W is a weight, so with PDL these copies are
+//     issued before griddepcontrol.wait and overlap the preceding kernel.
+//   * Warps 0-3 are consumers.  After griddepcontrol.wait they stage the CTA's
+//     X slice in shared memory, then for each ring stage either
+//       FMA: warp w owns W rows 4w..4w+3, lane l the 8-element vector l of the
+//            chunk; fp32 fused multiply-add into acc[M][4], or
+//       MMA: mma.sync m16n8k16 with the 16 W rows on the MMA's M side and the
+//            tokens on its N side (8 or 16 tokens); ldmatrix feeds both
+//            operands from padded (conflict-free) rows; the warps split the
+//            chunk's 16-wide k steps, and each chunk's MMA sum is added into an
+//            fp32 register accumulator with a plain rounded add,
+//     and release the stage on its "empty" mbarrier.
+//   * The per-CTA partial [M][16] goes to its owner CTA (column c belongs to
+//     rank c % S) by st.shared::cluster into slot `rank`; after one
+//     barrier.cluster.arrive.release / wait.acquire every owner adds slots
+//     0..S-1 in that order and writes Y, so the result is bit-identical from
+//     run to run.
+// Every mbarrier wait is bounded (see mbar_wait_bounded); a wait that gives
+// up records an error in the device status word, waits (bounded) for its own
+// copies in flight, and the CTA still takes part in the cluster barrier.
+#include "common.cuh"
+#include "internal.h"
+
+namespace skinny {
+
+namespace {
+
+constexpr int kBN = 16;
+constexpr int kRowBytes = kSplitBK * 2 + 16;      // ring row stride: 528 = 16 (mod 128)
+constexpr int kStageBytes = kBN * kRowBytes;
+constexpr uint64_t kDrainBudgetNs = 200ull * 1000 * 1000;
+
+struct Layout {
+    int xrows, xrowb;
+    int ring, xs, red, slots, bars, ctrl, total;
+};
+
+__host__ __device__ inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline Layout make_layout(int MT, int consumer, int stages, int KS, int S) {
+    Layout L;
+    L.xrows = (consumer == SKINNY_CONSUMER_MMA) ? (MT <= 8 ? 8 : 16) : MT;
+    L.xrowb = round_up(KS * 2, 128) + 16;          // X row stride: 16 (mod 128)
+    int off = 0;
+    L.ring = off;  off += stages * kStageBytes;
+    L.xs = off;    off += L.xrows * L.xrowb;
+    off = round_up(off, 16);
+    L.red = off;   off += (consumer == SKINNY_CONSUMER_MMA) ? kSplitConsumerWarps * MT * kBN * 4 : 0;
+    L.slots = off; off += (S > 1) ? S * MT * kBN * 4 : 0;
+    off = round_up(off, 8);
+    L.bars = off;  off += 2 * stages * 8;
+    L.ctrl = off;  off += 16;
+    L.total = round_up(off, 128);
+    return L;
+}
+
+struct SplitParams {
+    const uint16_t *X; int64_t ldx;
+    const uint16_t *W; int64_t ldw;
+    float *Y; int64_t ldy;
+    int M, N, K;
+    int KS;            // K elements per rank (multiple of 16)
+    int stages;
+    int x_vec16;       // X rows 16-byte aligned (vector staging)
+    int *status;
+    uint64_t budget_ns;
+};
+
+// Bounded wait used when draining: also stops early once the producer has
+// given up before issuing the awaited chunk.
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, int g,
+                                           volatile int *abort_flag, volatile int *issued) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag && *issued <= g) return false;   // never issued: nothing in flight
+        if (globaltimer_ns() - t0 > kDrainBudgetNs) return false;
+    }
+}
+
+template <int MT, int CONS>
+__global__ void __launch_bounds__(kSplitThreads)
+splitk_kernel(const SplitParams p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int S = gridDim.x;
+    const Layout L = make_layout(MT, CONS, p.stages, p.KS, S);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rank = (S > 1) ? (int)cluster_ctarank() : 0;
+    const int n0 = blockIdx.y * kBN;
+    const int rows = min(kBN, p.N - n0);
+    const int kbeg = rank * p.KS;
+    const int klen = max(0, min(p.K, kbeg + p.KS) - kbeg);
+    const int nchunks = (klen + kSplitBK - 1) / kSplitBK;
+    const int stages = p.stages;
+
+    const uint32_t ring = smem_u32(smem + L.ring);
+    const uint32_t full0 = smem_u32(smem + L.bars);
+    const uint32_t empty0 = full0 + 8 * stages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.ctrl);
+    volatile int *issued = abort_flag + 1;
+
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kSplitConsumerWarps);
+        }
+        *abort_flag = 0;
+        *issued = 0;
+        fence_mbarrier_init_cluster();
+    }
+    __syncthreads();
+    // Cluster phase 1 (split arrive / wait): a peer's shared memory may be
+    // written through DSMEM only once that peer has started.
+    if (S > 1) cluster_arrive_relaxed();
+
+    if (warp == kSplitConsumerWarps) {
+        // ============================ producer warp ============================
+        const uint16_t *wbase = p.W + (int64_t)n0 * p.ldw + kbeg;
+        for (int g = 0; g < nchunks; ++g) {
+            const int s = g % stages;
+            if (g >= stages) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_bounded(empty0 + 8 * s, ((g / stages) - 1) & 1, p.budget_ns);
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                if (!ok) {
+                    if (lane == 0) {
+                        report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitProducerEmpty);
+                        *abort_flag = 1;
+                    }
+                    break;
+                }
+            }
+            const int len = min(kSplitBK, klen - g * kSplitBK);
+            const uint32_t full = full0 + 8 * s;
+            if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(rows * len * 2));
+            __syncwarp();
+            for (int r = lane; r < rows; r += 32)
+                bulk_copy_g2s(ring + s * kStageBytes + r * kRowBytes,
+                              wbase + (int64_t)r * p.ldw + g * kSplitBK, (uint32_t)(len * 2), full);
+            __syncwarp();
+            if (lane == 0) *issued = g + 1;
+        }
+        griddep_launch_dependents();
+        if (S > 1) cluster_wait();
+    } else {
+        // ============================ consumer warps ============================
+        griddep_wait();   // X may come from the preceding kernel
+        // ---- stage X[0:M, kbeg:kbeg+klen] (rows of L.xrowb bytes)
+        uint8_t *xs = smem + L.xs;
+        if (p.x_vec16) {
+            const int nv = klen >> 3;
+#pragma unroll 4
+            for (int i = tid; i < p.M * nv; i += kSplitConsumerWarps * 32) {
+                const int m = i / nv, v = i - m * nv;
+                *reinterpret_cast<uint4 *>(xs + m * L.xrowb + v * 16) =
+                    ldg_v4(p.X + m * p.ldx + kbeg + 8 * v);
+            }
+        } else {
+#pragma unroll 4
+            for (int i = tid; i < p.M * klen; i += kSplitConsumerWarps * 32) {
+                const int m = i / klen, k = i - m * klen;
+                *reinterpret_cast<uint16_t *>(xs + m * L.xrowb + 2 * k) = ldg_u16(p.X + m * p.ldx + kbeg + k);
+            }
+        }
+        named_bar_sync(1, kSplitConsumerWarps * 32);
+        griddep_launch_dependents();
+
+        bool failed = false;
+        float part[MT][4];           // FMA: acc[m][r] for rows 4w+r.  MMA: fragment sums (see below)
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) part[m][r] = 0.f;
+        float macc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // MMA accumulators
+
+        for (int g = 0; g < nchunks; ++g) {
+            const int s = g % stages;
+            const uint32_t full = full0 + 8 * s;
+            const uint32_t par = (g / stages) & 1;
+            if (!failed) {
+                if (*abort_flag && *issued <= g) {
+                    failed = true;             // the producer gave up before this chunk
+                } else if (!mbar_wait_bounded(full, par, p.budget_ns)) {
+                    failed = true;
+                    if (lane == 0) report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitConsumerFull);
+                    if (!drain_wait(full, par, g, abort_flag, issued) && lane == 0)
+                        report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitDrain);
+                }
+            } else if (!(*abort_flag && *issued <= g)) {
+                // already failed: still wait (bounded) for this chunk's copies
+                // so nothing lands in shared memory after the CTA exits
+                if (!drain_wait(full, par, g, abort_flag, issued) && lane == 0)
+                    report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitDrain);
+            }
+            if (!failed) {
+                const int len = min(kSplitBK, klen - g * kSplitBK);
+                const uint32_t stage = ring + s * kStageBytes;
+                if constexpr (CONS == SKINNY_CONSUMER_FMA) {
+                    const int nv = len >> 3;
+                    if (lane < nv) {
+                        const int r0 = warp * 4;
+                        float w[4][8];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            uint4 v;
+                            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                                         : "r"(stage + (r0 + r) * kRowBytes + lane * 16));
+                            w[r][0] = bf16_lo(v.x); w[r][1] = bf16_hi(v.x);
+                            w[r][2] = bf16_lo(v.y); w[r][3] = bf16_hi(v.y);
+                            w[r][4] = bf16_lo(v.z); w[r][5] = bf16_hi(v.z);
+                            w[r][6] = bf16_lo(v.w); w[r][7] = bf16_hi(v.w);
+                        }
+                        const uint8_t *xcol = xs + (g * kSplitBK + lane * 8) * 2;
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(xcol + m * L.xrowb);
+                            float x[8];
+                            x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+                            x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+#pragma unroll
+                                for (int r = 0; r < 4; ++r) part[m][r] = fmaf(x[e], w[r][e], part[m][r]);
+                        }
+                    }
+                } else {
+                    // MMA: A = 16 W rows x 16 k (ldmatrix.x4), B = 16 k x 8|16 tokens.
+                    const int steps = len >> 4;
+                    float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    const uint32_t a_row = (lane & 7) + 8 * ((lane >> 3) & 1);
+                    const uint32_t a_addr0 = stage + a_row * kRowBytes + (lane >> 4) * 16;
+                    const uint32_t xs_u32 = smem_u32(xs);
+                    for (int j = warp; j < steps; j += kSplitConsumerWarps) {
+                        uint32_t a[4];
+                        ldmatrix_x4(a_addr0 + j * 32, a[0], a[1], a[2], a[3]);
+                        const int kx = g * kSplitBK + j * 16;
+                        if constexpr (MT <= 8) {
+                            const uint32_t tok = lane & 7, kh = (lane >> 3) & 1;
+                            uint32_t b0, b1;
+                            ldmatrix_x2(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1);
+                            mma_bf16_16816(d[0], a, b0, b1, d[0]);
+                        } else {
+                            const uint32_t tok = (lane & 7) + 8 * (lane >> 4), kh = (lane >> 3) & 1;
+                            uint32_t b0, b1, b2, b3;
+                            ldmatrix_x4(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1, b2, b3);
+                            mma_bf16_16816(d[0], a, b0, b1, d[0]);
+                            mma_bf16_16816(d[1], a, b2, b3, d[1]);
+                        }
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) macc[h][i] += d[h][i];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        }
+
+        // ---- per-CTA partial P[m][c] (c = tile column), then to its owner
+        if (S > 1) cluster_wait();   // every peer has started
+        const uint32_t slots = smem_u32(smem + L.slots);
+        auto emit = [&](int m, int c, float v) {
+            if (m >= p.M || c >= rows) return;
+            if (S == 1) {
+                p.Y[m * p.ldy + n0 + c] = v;
+            } else {
+                const uint32_t local = slots + (uint32_t)(((rank * MT + m) * kBN + c) * 4);
+                st_shared_cluster_f32(mapa_shared(local, (uint32_t)(c % S)), v);
+            }
+        };
+        if constexpr (CONS == SKINNY_CONSUMER_FMA) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    float v = part[m][r];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                    part[m][r] = v;
+                }
+            // every lane now holds all sums; lane l emits pairs l, l+32, ...
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    if (((m * 4 + r) & 31) == lane) emit(m, warp * 4 + r, part[m][r]);
+        } else {
+            // fragment: thread (g4 = lane/4, t4 = lane%4) holds rows g4, g4+8
+            // for tokens 2*t4, 2*t4+1 (+8 for the second MMA)
+            float *red = reinterpret_cast<float *>(smem + L.red);   // [warp][MT][16]
+            const int g4 = lane >> 2, t4 = lane & 3;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (h == 1 && MT <= 8) break;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int tok = 8 * h + 2 * t4 + (i & 1);
+                    const int row = g4 + 8 * (i >> 1);
+                    if (tok < MT) red[(warp * MT + tok) * kBN + row] = macc[h][i];
+                }
+            }
+            named_bar_sync(1, kSplitConsumerWarps * 32);
+            for (int i = tid; i < MT * kBN; i += kSplitConsumerWarps * 32) {
+                const int m = i / kBN, c = i - m * kBN;
+                float v = red[m * kBN + c];
+#pragma unroll
+                for (int w = 1; w < kSplitConsumerWarps; ++w) v += red[(w * MT + m) * kBN + c];
+                emit(m, c, v);
+            }
+        }
+    }
+
+    if (S > 1) {
+        // Cluster phase 2: every thread of every CTA arrives exactly once
+        // (non-.aligned forms, the branches above diverge by warp role).
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        const float *sl = reinterpret_cast<const float *>(smem + L.slots);
+        for (int i = tid; i < MT * kBN; i += kSplitThreads) {
+            const int m = i / kBN, c = i - m * kBN;
+            if (m < p.M && c < rows && (c % S) == rank) {
+                float v = sl[(0 * MT + m) * kBN + c];
+                for (int r = 1; r < S; ++r) v += sl[(r * MT + m) * kBN + c];
+                p.Y[m * p.ldy + n0 + c] = v;
+            }
+        }
+    }
+}
+
+using SplitKernel = void (*)(const SplitParams);
+
+template <int MT> constexpr SplitKernel fma_k() { return &splitk_kernel<MT, SKINNY_CONSUMER_FMA>; }
+
+const SplitKernel kFma[SKINNY_MAX_M] = {
+    fma_k<1>(), fma_k<2>(), fma_k<3>(), fma_k<4>(), fma_k<5>(), fma_k<6>(), fma_k<7>(), fma_k<8>(),
+    fma_k<9>(), fma_k<10>(), fma_k<11>(), fma_k<12>(), fma_k<13>(), fma_k<14>(), fma_k<15>(), fma_k<16>()};
+const SplitKernel kMma[2] = {&splitk_kernel<8, SKINNY_CONSUMER_MMA>, &splitk_kernel<16, SKINNY_CONSUMER_MMA>};
+
+int mt_for(int M, int consumer) {
+    return consumer == SKINNY_CONSUMER_MMA ? (M <= 8 ? 8 : 16) : M;
+}
+
+}  // namespace
+
+bool splitk_supported(int M, int consumer, int block_n) {
+    return M >= 1 && M <= SKINNY_MAX_M && block_n == kBN &&
+           (consumer == SKINNY_CONSUMER_FMA || consumer == SKINNY_CONSUMER_MMA);
+}
+
+int splitk_smem_bytes(int M, int consumer, int block_n, int stages, int k_slice, int split_k) {
+    (void)block_n;
+    return make_layout(mt_for(M, consumer), consumer, stages, k_slice, split_k).total;
+}
+
+cudaError_t splitk_prepare() {
+    for (int m = 0; m < SKINNY_MAX_M; ++m) {
+        cudaError_t e = cudaFuncSetAttribute(kFma[m], cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        if (e != cudaSuccess) return e;
+    }
+    for (int i = 0; i < 2; ++i) {
+        cudaError_t e = cudaFuncSetAttribute(kMma[i], cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_splitk(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCtx &c) {
+    if (!splitk_supported(a.M, pl.consumer, pl.block_n)) return cudaErrorInvalidValue;
+    SplitParams p;
+    p.X = a.X; p.ldx = a.ldx; p.W = a.W; p.ldw = a.ldw; p.Y = a.Y; p.ldy = a.ldy;
+    p.M = a.M; p.N = a.N; p.K = a.K;
+    p.KS = pl.k_chunk;
+    p.stages = pl.stages;
+    p.x_vec16 = ((reinterpret_cast<uintptr_t>(a.X) & 15) == 0 && (a.ldx & 7) == 0) ? 1 : 0;
+    p.status = c.status;
+    p.budget_ns = c.budget_ns;
+    SplitKernel fn = (pl.consumer == SKINNY_CONSUMER_MMA) ? kMma[a.M <= 8 ? 0 : 1] : kFma[a.M - 1];
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.grid_x, pl.grid_y, 1);
+    cfg.blockDim = dim3(kSplitThreads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem_bytes;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
+    ++n;
+    if (pl.split_k > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = pl.split_k;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+}  // namespace skinny

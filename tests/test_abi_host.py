@@ -1,0 +1,170 @@
+"""Host-side tests of the C ABI: no GPU needed, no kernel launched.
+
+The library must load and export every function that ``include/*.h``
+declares; every argument error must be reported on the host before any CUDA
+call; the dispatcher (``skinny_plan_for``) is a pure function of the shapes,
+pointers and the SM count.
+"""
+import glob
+import os
+import re
+
+import pytest
+
+import latency_skinny_bf16_gb300 as sk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+A16 = 0x7F0000000000        # fake, 16-byte aligned "device" addresses: never dereferenced
+B16 = 0x7F0010000000
+C16 = 0x7F0020000000
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        with open(h) as f:
+            src = f.read()
+        names += re.findall(r"SKINNY_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = sk.load_library()
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(sk.EXPORTED_SYMBOLS) <= set(names)
+    assert sk.skinny_version() >= 100
+
+
+def test_status_strings():
+    for code in range(7):
+        assert sk.skinny_status_string(code).startswith("SKINNY_")
+    assert sk.skinny_status_string(99) == "SKINNY_ERR_UNKNOWN"
+
+
+def call(X=A16, ldx=64, W=B16, ldw=64, Y=C16, ldy=32, M=4, N=32, K=64):
+    return sk.skinny_gemm_bf16(X, ldx, W, ldw, Y, ldy, M, N, K, 0)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(M=-1), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(N=-1), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(K=-1), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(M=17), sk.SKINNY_ERR_UNSUPPORTED),
+    (dict(M=64), sk.SKINNY_ERR_UNSUPPORTED),
+    (dict(M=0), sk.SKINNY_OK),
+    (dict(N=0), sk.SKINNY_OK),
+    (dict(M=0, X=0, W=0, Y=0), sk.SKINNY_OK),
+    (dict(ldx=63), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(ldw=10), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(ldy=31), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(X=0), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(W=0), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(Y=0), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(X=A16 + 1), sk.SKINNY_ERR_MISALIGNED),
+    (dict(W=B16 + 3), sk.SKINNY_ERR_MISALIGNED),
+    (dict(Y=C16 + 2), sk.SKINNY_ERR_MISALIGNED),
+    (dict(Y=A16 + 64), sk.SKINNY_ERR_INVALID_VALUE),      # Y overlaps X
+    (dict(Y=B16 + 2048), sk.SKINNY_ERR_INVALID_VALUE),    # Y overlaps W
+])
+def test_argument_errors_are_host_side(kw, expect):
+    assert call(**kw) == expect
+
+
+def test_k_zero_needs_only_y():
+    # K == 0: X and W are not read, so NULL is allowed; Y must still be valid
+    assert sk.skinny_plan_for(0, 0, 0, 0, C16, 32, 4, 32, 0, 152)["backend"] == 0
+    with pytest.raises(sk.SkinnyError):
+        sk.skinny_plan_for(0, 0, 0, 0, 0, 32, 4, 32, 0, 152)
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="checks the no-device answer")
+def test_valid_call_without_device_reports_no_device():
+    assert call() == sk.SKINNY_ERR_NO_DEVICE
+    assert sk.skinny_init(0) == sk.SKINNY_ERR_NO_DEVICE
+
+
+def plan(M, N, K, ldw=None, W=B16, num_sms=152, X=A16, ldx=None, Y=C16, ldy=None):
+    return sk.skinny_plan_for(X, ldx or K, W, ldw or K, Y, ldy or N, M, N, K, num_sms)
+
+
+def test_default_rule_dotprod_small_m_or_short_k():
+    for M in (1, 2, 3, 4):
+        assert plan(M, 256, 7168)["backend"] == sk.SKINNY_BACKEND_DOTPROD
+    assert plan(8, 256, 1024)["backend"] == sk.SKINNY_BACKEND_DOTPROD   # K < 2048
+
+
+def test_default_rule_splitk_larger_m():
+    for M in (5, 8, 12, 16):
+        p = plan(M, 256, 7168)
+        assert p["backend"] == sk.SKINNY_BACKEND_SPLITK
+        assert 1 <= p["split_k"] <= 8 and p["grid_x"] == p["split_k"]
+        assert p["grid_y"] == 16 and p["block_n"] == 16
+        assert p["smem_bytes"] <= 227 * 1024
+        assert p["split_k"] * p["k_chunk"] >= 7168 and p["k_chunk"] % 16 == 0
+
+
+def test_vector_width_follows_alignment():
+    assert plan(1, 256, 7168)["vec_elems"] == 8
+    assert plan(1, 256, 7168, W=B16 + 8)["vec_elems"] == 4
+    assert plan(1, 256, 7168, W=B16 + 4)["vec_elems"] == 2
+    assert plan(1, 256, 7168, W=B16 + 2)["vec_elems"] == 1
+    assert plan(1, 256, 7170)["vec_elems"] == 2       # ldw = K = 7170: rows 4-byte aligned
+    assert plan(1, 256, 7169)["vec_elems"] == 1       # odd ldw: rows 2-byte aligned
+    assert plan(1, 256, 2884)["vec_elems"] == 4
+
+
+def test_misaligned_weights_never_take_splitk():
+    for W, K in ((B16 + 2, 7168), (B16, 7169), (B16, 7172)):
+        assert plan(16, 256, K, W=W)["backend"] == sk.SKINNY_BACKEND_DOTPROD
+
+
+def test_dotprod_block_n_grows_with_n():
+    assert plan(1, 256, 7168)["block_n"] == 1
+    assert plan(1, 24576, 1536)["block_n"] == 8
+    p = plan(2, 2112, 7168)
+    assert p["grid_x"] * p["block_n"] >= 2112
+
+
+def test_x_chunking_for_large_m_times_k():
+    p = plan(16, 7168, 14336, ldy=7168 + 64)
+    if p["backend"] == sk.SKINNY_BACKEND_DOTPROD:
+        assert p["k_chunk"] < 14336
+    else:
+        assert p["split_k"] * p["k_chunk"] >= 14336
+    assert p["smem_bytes"] <= 227 * 1024
+
+
+def test_forced_options_and_restore():
+    with sk.options(backend=sk.SKINNY_BACKEND_SPLITK, consumer=sk.SKINNY_CONSUMER_FMA, split_k=4, stages=2):
+        p = plan(3, 256, 7168)
+        assert (p["backend"], p["consumer"], p["split_k"], p["stages"]) == (2, 1, 4, 2)
+        with pytest.raises(sk.SkinnyError):      # split-K cannot read misaligned W rows
+            plan(3, 256, 7169)
+    with sk.options(backend=sk.SKINNY_BACKEND_DOTPROD, block_n=4):
+        p = plan(16, 256, 7168)
+        assert (p["backend"], p["block_n"]) == (1, 4)
+    assert sk.skinny_get_option(sk.SKINNY_OPT_FORCE_BACKEND) == 0
+    assert sk.skinny_get_option(sk.SKINNY_OPT_FORCE_BLOCK_N) == 0
+    with sk.options(backend=sk.SKINNY_BACKEND_SPLITK, consumer=sk.SKINNY_CONSUMER_MMA):
+        with pytest.raises(sk.SkinnyError):      # MMA needs K % 16 == 0
+            plan(8, 256, 7176)
+
+
+@pytest.mark.parametrize("opt,bad", [(sk.SKINNY_OPT_PDL, 2), (sk.SKINNY_OPT_FORCE_BACKEND, 3),
+                                     (sk.SKINNY_OPT_FORCE_SPLIT_K, 9), (sk.SKINNY_OPT_FORCE_BLOCK_N, 3),
+                                     (sk.SKINNY_OPT_FORCE_STAGES, 9), (sk.SKINNY_OPT_WAIT_TIMEOUT_US, -1),
+                                     (99, 0)])
+def test_option_values_are_checked(opt, bad):
+    with pytest.raises(sk.SkinnyError):
+        sk.skinny_set_option(opt, bad)
+
+
+def test_every_workload_case_has_a_plan():
+    import skinny_inputs as si
+    for c in si.iter_all():
+        p = plan(c.M, c.N, c.K, ldy=c.ly)
+        assert p["smem_bytes"] <= 227 * 1024
+        assert p["grid_x"] >= 1 and p["grid_y"] >= 1
