@@ -64,7 +64,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget (s)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
-    p.add_argument("--per-shape", action="store_true", help="also time each call shape on its own")
+    p.add_argument("--profile-mode", action="store_true",
+                   help="short run for ncu: no clock soak, no CPU baseline, few extra passes")
     return p.parse_args(argv)
 
 
@@ -270,14 +271,14 @@ def run_native(args):
         graphs.append(g)
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(local) if not args.no_clocks else None
+    clocks = ClockSampler(local) if not (args.no_clocks or args.profile_mode) else None
     if clocks:
         clocks.start()
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             graphs[i % n_rep].replay()
         # keep the GPU loaded ~1.5 s so the clock samples see it under load
-        t_end = time.time() + 1.5
+        t_end = time.time() + (1.5 if clocks else 0.0)
         i = 0
         while time.time() < t_end:
             for _ in range(50):
@@ -306,7 +307,7 @@ def run_native(args):
         for _ in range(max(3, args.warmup)):
             graphs[0].replay()
         w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        warm_steps = max(50, min(args.steps, 2000))
+        warm_steps = 3 if args.profile_mode else max(50, min(args.steps, 2000))
         w0.record(stream)
         for _ in range(warm_steps):
             graphs[0].replay()
@@ -314,31 +315,37 @@ def run_native(args):
     torch.cuda.synchronize()
     warm_us_per_call = w0.elapsed_time(w1) * 1e3 / (warm_steps * len(cases))
 
-    # ---- per-launch durations (CUDA-event pairs around each call, same rotation)
-    per_launch = [[] for _ in cases]
-    n_launch_steps = max(4, min(args.steps, 200))
-    chunk = max(1, 150 // len(cases))
-    done = 0
-    while done < n_launch_steps:
-        k = min(chunk, n_launch_steps - done)
-        evs = []
+    # ---- per-launch durations: for each call shape, a CUDA graph of n_rep
+    # back-to-back launches over the rotating W replicas (L2-cold), PDL off so
+    # launches do not overlap; CUDA events around whole replays (the event
+    # clock is too coarse for a single few-microsecond launch).
+    per_launch = []
+    sk.skinny_set_option(sk.SKINNY_OPT_PDL, 0)
+    iters = 2 if args.profile_mode else 10
+    for j, c in enumerate(cases):
+        # enough copies of this call's W alone to exceed 2x L2
+        n_j = max(8, math.ceil(2 * l2 / (2 * c.N * c.K)))
+        ws = [reps[i % n_rep].w[j] if i < n_rep else reps[0].w[j].clone() for i in range(n_j)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i, w in enumerate(ws):
+                r = reps[i % n_rep]
+                st = sk.skinny_gemm_bf16(r.x[j].data_ptr(), c.lx, w.data_ptr(), c.lw, r.y[j].data_ptr(),
+                                         c.ly, c.M, c.N, c.K, sh)
+                if st != sk.SKINNY_OK:
+                    raise sk.SkinnyError(st, c.name)
         with torch.cuda.stream(stream):
-            torch.cuda._sleep(50_000_000)      # let the host queue every launch before the GPU reaches them
-            for s_ in range(k):
-                r = reps[(done + s_) % n_rep]
-                for j, c in enumerate(cases):
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    st = sk.skinny_gemm_bf16(r.x[j].data_ptr(), c.lx, r.w[j].data_ptr(), c.lw, r.y[j].data_ptr(),
-                                             c.ly, c.M, c.N, c.K, sh)
-                    b.record(stream)
-                    if st != sk.SKINNY_OK:
-                        raise sk.SkinnyError(st, c.name)
-                    evs.append((j, a, b))
+            g.replay()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            for _ in range(iters):
+                g.replay()
+            b_.record(stream)
         torch.cuda.synchronize()
-        for j, a, b in evs:
-            per_launch[j].append(a.elapsed_time(b) * 1e3)   # us
-        done += k
+        per_launch.append(a_.elapsed_time(b_) * 1e3 / (iters * n_j))   # us
+        del g, ws
+    sk.skinny_set_option(sk.SKINNY_OPT_PDL, args.pdl)
+    launches += 0  # the per-launch pass is outside the timed region
 
     # ---- e2e: host -> device X, the calls, device -> host Y, per step, through the C ABI
     h2d = sum(2 * c.M * c.K for c in cases)
@@ -474,17 +481,15 @@ def main(argv=None):
     # dominant kernel family by total per-launch time
     fam_time, fam_bytes, fam_n = {}, {}, {}
     per_shape = []
-    for c, p, d in zip(cases, r["plans"], r["per_launch"]):
+    for c, p, us in zip(cases, r["plans"], r["per_launch"]):
         fam = "dotprod" if p["backend"] == 1 else "splitk"
-        med = statistics.median(d)
-        fam_time[fam] = fam_time.get(fam, 0.0) + sum(d)
-        fam_bytes[fam] = fam_bytes.get(fam, 0.0) + c.algorithmic_bytes * len(d)
-        fam_n[fam] = fam_n.get(fam, 0) + len(d)
+        fam_time[fam] = fam_time.get(fam, 0.0) + us
+        fam_bytes[fam] = fam_bytes.get(fam, 0.0) + c.algorithmic_bytes
+        fam_n[fam] = fam_n.get(fam, 0) + 1
         per_shape.append({"M": c.M, "N": c.N, "K": c.K, "kernel": fam, "consumer": p["consumer"],
-                          "split_k": p["split_k"], "block_n": p["block_n"],
-                          "us_median": round(med, 3), "us_p10": round(float(np.percentile(d, 10)), 3),
-                          "us_p90": round(float(np.percentile(d, 90)), 3),
-                          "gbs_median": round(c.algorithmic_bytes / med / 1e3, 1)})
+                          "split_k": p["split_k"], "block_n": p["block_n"], "grid": [p["grid_x"], p["grid_y"]],
+                          "us_per_launch": round(us, 3), "gbs": round(c.algorithmic_bytes / us / 1e3, 1),
+                          "frac_of_peak": round(c.algorithmic_bytes / us / 1e3 / peak, 4)})
     dom = max(fam_time, key=fam_time.get)
     total_t = sum(fam_time.values())
     achieved = fam_bytes[dom] / (fam_time[dom] * 1e-6) / 1e9
@@ -493,11 +498,13 @@ def main(argv=None):
                 "peak": round(peak, 1), "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "peak_source": peak_src,
                 "traffic": traffic, "time_share": round(fam_time[dom] / total_t, 3),
+                "method": "per call shape: CUDA graph of back-to-back launches over rotating W copies (L2-cold), "
+                          "PDL off, CUDA events around the replays",
                 "avg_launch_us": round(fam_time[dom] / fam_n[dom], 3),
                 "algorithmic_bytes_per_launch": round(fam_bytes[dom] / fam_n[dom])}
 
     cpu = None
-    if not args.no_cpu_baseline:
+    if not (args.no_cpu_baseline or args.profile_mode):
         gbs, s_step, sample = oracle_step_sample(cases, args.cpu_seconds)
         cpu = {"value": round(gbs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample}
 

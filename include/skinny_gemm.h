@@ -81,8 +81,8 @@ typedef struct {
     int stages;        /* shared-memory ring depth (split-K) */
     int k_chunk;       /* dot-product: K elements of X staged in shared memory at a time;
                           split-K: K elements per CTA (the cluster rank's slice) */
-    int grid_x;        /* grid dimensions launched */
-    int grid_y;
+    int grid_x;        /* grid dimensions launched; split-K: grid_x = split_k CTAs per cluster, */
+    int grid_y;        /* grid_y = clusters, each looping over 16-row tiles tile = y, y + grid_y, ... */
     int threads;       /* threads per CTA */
     int smem_bytes;    /* dynamic shared memory per CTA */
     int pdl;           /* 1 if launched with programmatic dependent launch */
@@ -99,8 +99,10 @@ typedef enum {
     SKINNY_OPT_WAIT_TIMEOUT_US = 7,  /* budget of each bounded wait in a kernel, microseconds
                                         (default 500000).  0 makes every such wait give up at once,
                                         which exercises the timeout path without any real hang */
-    SKINNY_OPT_LOG = 8               /* 1: print the plan chosen for each new call shape to stderr
+    SKINNY_OPT_LOG = 8,              /* 1: print the plan chosen for each new call shape to stderr
                                         (default: env SKINNY_LOG) */
+    SKINNY_OPT_FORCE_CLUSTERS = 9    /* split-K: 0 = dispatcher, else the number of (persistent)
+                                        clusters, each looping over row tiles (tests / tuning only) */
 } skinny_option_t;
 
 /*

@@ -50,6 +50,7 @@ SKINNY_OPT_FORCE_BLOCK_N = 5
 SKINNY_OPT_FORCE_STAGES = 6
 SKINNY_OPT_WAIT_TIMEOUT_US = 7
 SKINNY_OPT_LOG = 8
+SKINNY_OPT_FORCE_CLUSTERS = 9
 
 EXPORTED_SYMBOLS = (
     "skinny_gemm_bf16", "skinny_init", "skinny_query_plan", "skinny_plan_for",
@@ -191,7 +192,8 @@ class options:
         names = {"pdl": SKINNY_OPT_PDL, "backend": SKINNY_OPT_FORCE_BACKEND,
                  "consumer": SKINNY_OPT_FORCE_CONSUMER, "split_k": SKINNY_OPT_FORCE_SPLIT_K,
                  "block_n": SKINNY_OPT_FORCE_BLOCK_N, "stages": SKINNY_OPT_FORCE_STAGES,
-                 "wait_timeout_us": SKINNY_OPT_WAIT_TIMEOUT_US, "log": SKINNY_OPT_LOG}
+                 "wait_timeout_us": SKINNY_OPT_WAIT_TIMEOUT_US, "log": SKINNY_OPT_LOG,
+                 "clusters": SKINNY_OPT_FORCE_CLUSTERS}
         self._set = [(names[k], int(v)) for k, v in kw.items()]
         self._old = []
 

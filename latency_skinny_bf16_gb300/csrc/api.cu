@@ -42,6 +42,7 @@ std::atomic<int> g_opt_force_split_k{0};
 std::atomic<int> g_opt_force_block_n{0};
 std::atomic<int> g_opt_force_stages{0};
 std::atomic<int> g_opt_wait_us{500000};
+std::atomic<int> g_opt_force_grid_y{0};
 std::atomic<int> g_opt_log{-1};
 
 int env_flag(const char *name) {
@@ -188,13 +189,12 @@ bool plan_dotprod(int M, int N, int K, int vec, int force_bn, int num_sms, skinn
     return p->smem_bytes <= kMaxDynSmem;
 }
 
-bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int force_stages, int num_sms,
-                 skinny_plan_t *p) {
+bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int force_stages, int force_c,
+                 int num_sms, skinny_plan_t *p) {
     if (vec != 8 || K % 8 != 0 || K < 8) return false;
     if (consumer == SKINNY_CONSUMER_MMA && K % 16 != 0) return false;
     if (!splitk_supported(M, consumer, 16)) return false;
     const int tiles = (N + 15) / 16;
-    if (tiles > 65535) return false;
     int S = force_s;
     if (S == 0) {
         S = num_sms / tiles;
@@ -209,23 +209,43 @@ bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int fo
         const int ks = ((K + S - 1) / S + 15) & ~15;
         const int xrows = consumer == SKINNY_CONSUMER_MMA ? (M <= 8 ? 8 : 16) : M;
         const int xbytes = xrows * (((ks * 2 + 127) & ~127) + 16);
-        if (xbytes <= kSplitXBudget || force_s) {
-            const int nchunks = (ks + kSplitBK - 1) / kSplitBK;
-            int stages = force_stages ? force_stages : (nchunks < 4 ? (nchunks < 1 ? 1 : nchunks) : 4);
-            if (stages < 1 || stages > kSplitMaxStages) return false;
-            p->backend = SKINNY_BACKEND_SPLITK;
-            p->consumer = consumer;
-            p->vec_elems = 8;
-            p->block_n = 16;
-            p->split_k = S;
-            p->stages = stages;
-            p->k_chunk = ks;
-            p->grid_x = S;
-            p->grid_y = tiles;
-            p->threads = kSplitThreads;
-            p->smem_bytes = splitk_smem_bytes(M, consumer, 16, stages, ks, S);
-            return p->smem_bytes <= kMaxDynSmem;
+        if (xbytes > kSplitXBudget && !force_s) continue;
+        const int nchunks = (ks + kSplitBK - 1) / kSplitBK;
+        int stages = force_stages ? force_stages : (nchunks < 4 ? (nchunks < 1 ? 1 : nchunks) : 4);
+        if (stages < 1 || stages > kSplitMaxStages) return false;
+        const int smem = splitk_smem_bytes(M, consumer, 16, stages, ks, S);
+        if (smem > kMaxDynSmem) return false;
+        // Persistent clusters: as many as can be resident (shared memory, and
+        // at most 3 CTAs of 160 threads per SM by registers), with the tiles
+        // spread evenly over them.
+        int per_sm = (228 * 1024) / (smem + 1024);
+        if (per_sm > 3) per_sm = 3;
+        if (per_sm < 1) per_sm = 1;
+        int cap = num_sms * per_sm / S;
+        if (cap < 1) cap = 1;
+        int C = force_c;
+        if (C == 0) {
+            if (tiles <= cap) {
+                C = tiles;
+            } else {
+                const int per = (tiles + cap - 1) / cap;
+                C = (tiles + per - 1) / per;
+            }
         }
+        if (C < 1 || C > 65535) return false;
+        if (C > tiles) C = tiles;
+        p->backend = SKINNY_BACKEND_SPLITK;
+        p->consumer = consumer;
+        p->vec_elems = 8;
+        p->block_n = 16;
+        p->split_k = S;
+        p->stages = stages;
+        p->k_chunk = ks;
+        p->grid_x = S;
+        p->grid_y = C;
+        p->threads = kSplitThreads;
+        p->smem_bytes = smem;
+        return true;
     }
 }
 
@@ -236,6 +256,7 @@ skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int n
     const int fb = g_opt_force_backend.load(), fc = g_opt_force_consumer.load();
     const int fs = g_opt_force_split_k.load(), fbn = g_opt_force_block_n.load();
     const int fst = g_opt_force_stages.load();
+    const int fgy = g_opt_force_grid_y.load();
     const bool splitk_ok = vec == 8 && K % 8 == 0;
     const bool mma_ok = splitk_ok && K % 16 == 0;
     const int pdl = opt_pdl();
@@ -265,7 +286,7 @@ skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int n
     } else if (backend == SKINNY_BACKEND_SPLITK) {
         if (consumer == SKINNY_CONSUMER_AUTO) consumer = (M > 4 && mma_ok) ? SKINNY_CONSUMER_MMA : SKINNY_CONSUMER_FMA;
         if (bn != 0 && bn != 16) return SKINNY_ERR_UNSUPPORTED;
-        ok = plan_splitk(M, N, K, vec, consumer, split, stages, num_sms, p);
+        ok = plan_splitk(M, N, K, vec, consumer, split, stages, fgy, num_sms, p);
         if (!ok && fb == SKINNY_BACKEND_AUTO) {
             // a tuned split-K entry that these pointers / strides cannot use
             ok = plan_dotprod(M, N, K, vec, 0, num_sms, p);
@@ -379,6 +400,9 @@ skinny_status_t skinny_set_option(int option, int value) {
         case SKINNY_OPT_LOG:
             if (value != 0 && value != 1) return SKINNY_ERR_INVALID_VALUE;
             g_opt_log.store(value); return SKINNY_OK;
+        case SKINNY_OPT_FORCE_CLUSTERS:
+            if (value < 0 || value > 65535) return SKINNY_ERR_INVALID_VALUE;
+            g_opt_force_grid_y.store(value); return SKINNY_OK;
         default:
             return SKINNY_ERR_INVALID_VALUE;
     }
@@ -395,6 +419,7 @@ skinny_status_t skinny_get_option(int option, int *value) {
         case SKINNY_OPT_FORCE_STAGES: *value = g_opt_force_stages.load(); return SKINNY_OK;
         case SKINNY_OPT_WAIT_TIMEOUT_US: *value = g_opt_wait_us.load(); return SKINNY_OK;
         case SKINNY_OPT_LOG: *value = opt_log(); return SKINNY_OK;
+        case SKINNY_OPT_FORCE_CLUSTERS: *value = g_opt_force_grid_y.load(); return SKINNY_OK;
         default: return SKINNY_ERR_INVALID_VALUE;
     }
 }

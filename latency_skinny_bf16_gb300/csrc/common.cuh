@@ -176,7 +176,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 
 // ------------------------------------------------------------------ device status word
 // Low 8 bits: skinny_status_t; bits 8..15: which wait gave up.
-enum : int { kWaitConsumerFull = 1, kWaitProducerEmpty = 2, kWaitDrain = 3 };
+enum : int { kWaitConsumerFull = 1, kWaitProducerEmpty = 2, kWaitDrain = 3, kWaitX = 4 };
 __device__ __forceinline__ void report_status(int *status, int code, int where) {
     if (status) atomicCAS(status, 0, code | (where << 8));
 }

@@ -18,8 +18,12 @@
 // in each warp and summed across the 4 warps in shared memory in a fixed
 // order, so a plan's result is bit-identical from run to run.
 //
-// With PDL the CTA warms L2 with its own W rows (W is a weight, never written
-// by the preceding kernel), then waits on griddepcontrol before reading X.
+// With PDL the CTA warms L2 with its own W rows and puts its first batch of W
+// loads in flight (W is a weight, never written by the preceding kernel), then
+// waits on griddepcontrol before reading X.  X rows that are 16-byte aligned
+// arrive by bulk async copies (the TMA engine, one per row, all in flight at
+// once) completing on an mbarrier whose wait is bounded; otherwise threads
+// stage X with ordinary L2 loads.
 #include "common.cuh"
 #include "internal.h"
 
@@ -102,7 +106,7 @@ __global__ void __launch_bounds__(kDotThreads)
 dotprod_kernel(const uint16_t *__restrict__ X, int64_t ldx,
                const uint16_t *__restrict__ W, int64_t ldw,
                float *__restrict__ Y, int64_t ldy,
-               int N, int K, int kc, int x_vec16)
+               int N, int K, int kc, int x_vec16, int *status, uint64_t budget_ns)
 {
     // Loads in flight per thread per step: U vectors of each of the BN rows.
     constexpr int U = (BN >= 8) ? 1 : 8 / BN;
@@ -110,8 +114,15 @@ dotprod_kernel(const uint16_t *__restrict__ X, int64_t ldx,
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);                       // [MT][kc]
     float *red = reinterpret_cast<float *>(smem_raw + ((MT * kc * 2 + 15) & ~15));  // [kWarps][MT][BN]
 
+    __shared__ __align__(8) uint64_t xbar_storage;   // X chunk copies complete here
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n0 = blockIdx.x * BN;
+    const uint32_t xbar = smem_u32(&xbar_storage);
+    if (tid == 0) {
+        mbar_init(xbar, 1);
+        fence_mbarrier_init_cluster();
+    }
+    __syncthreads();
 
     const uint16_t *wrow[BN];
 #pragma unroll
@@ -161,27 +172,36 @@ dotprod_kernel(const uint16_t *__restrict__ X, int64_t ldx,
             __syncthreads();            // every thread is done with the previous chunk of X
             load_batch(k0, nvec, tid);  // first W batch of this chunk, before staging X
         }
-        // ---- stage X[0:M, k0:k0+klen] in shared memory
-        if (x_vec16) {
-            const int nv = klen >> 3;
-#pragma unroll 4
-            for (int i = tid; i < MT * nv; i += kDotThreads) {
-                const int m = i / nv, v = i - m * nv;
-                *reinterpret_cast<uint4 *>(xs + m * kc + 8 * v) = ldg_v4(X + m * ldx + k0 + 8 * v);
+        // ---- stage X[0:M, k0:k0+klen] in shared memory: when X rows are
+        // 16-byte aligned, one bulk async copy per row (the TMA engine) for
+        // the whole multiple-of-8 part, the last klen % 8 elements by hand
+        const int kb = x_vec16 ? (klen & ~7) : 0;
+        if (x_vec16 && warp == 0) {
+            if (lane == 0) {
+                fence_proxy_async_smem();   // the previous chunk was read by ordinary loads
+                mbar_arrive_expect_tx(xbar, (uint32_t)(MT * kb * 2));
             }
-            const int rem = klen - 8 * nv;
+            __syncwarp();
+            if (kb > 0 && lane < MT)
+                bulk_copy_g2s(smem_u32(xs + lane * kc), X + lane * ldx + k0, (uint32_t)(kb * 2), xbar);
+        }
+        {
+            const int rem = klen - kb;
+#pragma unroll 4
             for (int i = tid; i < MT * rem; i += kDotThreads) {
-                const int m = i / rem, k = 8 * nv + (i - m * rem);
-                xs[m * kc + k] = ldg_u16(X + m * ldx + k0 + k);
-            }
-        } else {
-#pragma unroll 4
-            for (int i = tid; i < MT * klen; i += kDotThreads) {
-                const int m = i / klen, k = i - m * klen;
+                const int m = i / rem, k = kb + (i - m * rem);
                 xs[m * kc + k] = ldg_u16(X + m * ldx + k0 + k);
             }
         }
         __syncthreads();
+        if (x_vec16) {
+            const uint32_t par = (uint32_t)((k0 / kc) & 1);
+            if (!mbar_wait_bounded(xbar, par, budget_ns)) {
+                if (lane == 0) report_status(status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitX);
+                if (!mbar_wait_bounded(xbar, par, 200ull * 1000 * 1000) && lane == 0)
+                    report_status(status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitDrain);
+            }
+        }
 
         // ---- main part: VW-wide vectors, U per row in flight per batch
         for (int v0 = tid; v0 < nvec; v0 += U * kDotThreads) {
@@ -252,7 +272,7 @@ dotprod_kernel(const uint16_t *__restrict__ X, int64_t ldx,
 
 // ------------------------------------------------------------------ instantiation table
 using DotKernel = void (*)(const uint16_t *, int64_t, const uint16_t *, int64_t, float *, int64_t,
-                           int, int, int, int);
+                           int, int, int, int, int *, uint64_t);
 
 template <int MT, int VW, int BN> constexpr DotKernel kfn() { return &dotprod_kernel<MT, VW, BN>; }
 
@@ -289,8 +309,7 @@ int dotprod_smem_bytes(int M, int block_n, int k_chunk) {
 cudaError_t dotprod_prepare() {
     for (int m = 0; m < SKINNY_MAX_M; ++m)
         for (int v = 0; v < kDotVariants; ++v) {
-            cudaError_t e = cudaFuncSetAttribute(kTable[m][v], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 kMaxDynSmem);
+            cudaError_t e = set_max_dyn_smem(kTable[m][v]);
             if (e != cudaSuccess) return e;
         }
     return cudaSuccess;
@@ -312,7 +331,8 @@ cudaError_t launch_dotprod(const GemmArgs &a, const skinny_plan_t &p, const Laun
     attr[0].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fn, a.X, a.ldx, a.W, a.ldw, a.Y, a.ldy, a.N, a.K, p.k_chunk, x_vec16);
+    return cudaLaunchKernelEx(&cfg, fn, a.X, a.ldx, a.W, a.ldw, a.Y, a.ldy, a.N, a.K, p.k_chunk, x_vec16, c.status,
+                              c.budget_ns);
 }
 
 }  // namespace skinny

@@ -44,8 +44,22 @@ bool splitk_supported(int M, int consumer, int block_n);
 cudaError_t splitk_prepare();
 cudaError_t launch_splitk(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
 
-// Per-CTA dynamic shared memory the dispatcher may plan for (B300: 232448
-// bytes opt-in per block; keep a margin for static shared memory).
-constexpr int kMaxDynSmem = 227 * 1024;
+// Per-CTA dynamic shared memory the dispatcher may plan for (GB300: 232448
+// bytes opt-in per block, less a margin for the kernels' static shared memory).
+constexpr int kMaxDynSmem = 227 * 1024 - 1024;
+
+// Allow `fn` the device's opt-in shared memory per block, less its static part.
+template <typename F>
+inline cudaError_t set_max_dyn_smem(F *fn) {
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncAttributes fa;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(fn));
+    if (e != cudaSuccess) return e;
+    const int limit = optin - (int)fa.sharedSizeBytes;
+    return cudaFuncSetAttribute(reinterpret_cast<const void *>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                limit < kMaxDynSmem ? limit : kMaxDynSmem);
+}
 
 }  // namespace skinny

@@ -9,15 +9,18 @@
 // barrier must be the non-.aligned form because the producer warp takes
 // another branch).
 //
-// GB300 form.  A cluster of S <= 8 CTAs owns a tile of BN = 16 output columns
-// (rows of W); CTA `rank` owns the K slice [rank*KS, rank*KS + KS).
+// GB300 form.  The grid is S x C: clusters of S <= 8 CTAs along K, C clusters
+// along N.  Each cluster loops over 16-row tiles of W (output columns)
+// tile = y, y + C, ... (persistent when there are more tiles than clusters);
+// CTA `rank` owns the K slice [rank*KS, rank*KS + KS) of every tile.
 //   * Warp 4 is the producer: one lane per W row issues a 1-D bulk async copy
 //     (cp.async.bulk, the TMA engine, no multicast) of the row's next BK = 256
 //     elements into a `stages`-deep shared-memory ring, completing on the
-//     stage's "full" mbarrier.  W is a weight, so with PDL these copies are
-//     issued before griddepcontrol.wait and overlap the preceding kernel.
+//     stage's "full" mbarrier; it streams straight across tile boundaries.
+//     W is a weight, so with PDL these copies are issued before
+//     griddepcontrol.wait and overlap the preceding kernel.
 //   * Warps 0-3 are consumers.  After griddepcontrol.wait they stage the CTA's
-//     X slice in shared memory, then for each ring stage either
+//     X slice in shared memory once, then for each ring stage either
 //       FMA: warp w owns W rows 4w..4w+3, lane l the 8-element vector l of the
 //            chunk; fp32 fused multiply-add into acc[M][4], or
 //       MMA: mma.sync m16n8k16 with the 16 W rows on the MMA's M side and the
@@ -26,14 +29,15 @@
 //            chunk's 16-wide k steps, and each chunk's MMA sum is added into an
 //            fp32 register accumulator with a plain rounded add,
 //     and release the stage on its "empty" mbarrier.
-//   * The per-CTA partial [M][16] goes to its owner CTA (column c belongs to
-//     rank c % S) by st.shared::cluster into slot `rank`; after one
+//   * The per-CTA partial [M][16] of a tile goes to its owner CTA (column c
+//     belongs to rank c % S) by st.shared::cluster into slot `rank` of the
+//     tile's slot buffer (two buffers, alternating by tile); after one
 //     barrier.cluster.arrive.release / wait.acquire every owner adds slots
 //     0..S-1 in that order and writes Y, so the result is bit-identical from
-//     run to run.
+//     run to run.  With S = 1 the partial is the result and goes to Y directly.
 // Every mbarrier wait is bounded (see mbar_wait_bounded); a wait that gives
 // up records an error in the device status word, waits (bounded) for its own
-// copies in flight, and the CTA still takes part in the cluster barrier.
+// copies in flight, and the CTA still takes part in every cluster barrier.
 #include "common.cuh"
 #include "internal.h"
 
@@ -62,9 +66,9 @@ __host__ __device__ inline Layout make_layout(int MT, int consumer, int stages, 
     L.xs = off;    off += L.xrows * L.xrowb;
     off = round_up(off, 16);
     L.red = off;   off += (consumer == SKINNY_CONSUMER_MMA) ? kSplitConsumerWarps * MT * kBN * 4 : 0;
-    L.slots = off; off += (S > 1) ? S * MT * kBN * 4 : 0;
+    L.slots = off; off += (S > 1) ? 2 * S * MT * kBN * 4 : 0;   // double-buffered by tile
     off = round_up(off, 8);
-    L.bars = off;  off += 2 * stages * 8;
+    L.bars = off;  off += 2 * stages * 8 + 8;      // full[stages], empty[stages], x_full
     L.ctrl = off;  off += 16;
     L.total = round_up(off, 128);
     return L;
@@ -99,12 +103,13 @@ __global__ void __launch_bounds__(kSplitThreads)
 splitk_kernel(const SplitParams p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const int S = gridDim.x;
+    const int S = gridDim.x;                       // CTAs per cluster along K
+    const int C = gridDim.y;                       // clusters, persistent over row tiles
+    const int T = (p.N + kBN - 1) / kBN;           // row tiles of 16
+    const int my_tiles = ((int)blockIdx.y < T) ? (T - 1 - (int)blockIdx.y) / C + 1 : 0;
     const Layout L = make_layout(MT, CONS, p.stages, p.KS, S);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rank = (S > 1) ? (int)cluster_ctarank() : 0;
-    const int n0 = blockIdx.y * kBN;
-    const int rows = min(kBN, p.N - n0);
     const int kbeg = rank * p.KS;
     const int klen = max(0, min(p.K, kbeg + p.KS) - kbeg);
     const int nchunks = (klen + kSplitBK - 1) / kSplitBK;
@@ -113,6 +118,9 @@ splitk_kernel(const SplitParams p)
     const uint32_t ring = smem_u32(smem + L.ring);
     const uint32_t full0 = smem_u32(smem + L.bars);
     const uint32_t empty0 = full0 + 8 * stages;
+    const uint32_t xfull = empty0 + 8 * stages;
+    // X slice by bulk copies when its rows are 16-byte aligned (klen % 8 == 0 always holds here)
+    const bool bulk_x = p.x_vec16 && klen > 0 && my_tiles > 0;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.ctrl);
     volatile int *issued = abort_flag + 1;
 
@@ -121,50 +129,91 @@ splitk_kernel(const SplitParams p)
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, kSplitConsumerWarps);
         }
+        mbar_init(xfull, 1);
         *abort_flag = 0;
         *issued = 0;
         fence_mbarrier_init_cluster();
     }
     __syncthreads();
-    // Cluster phase 1 (split arrive / wait): a peer's shared memory may be
-    // written through DSMEM only once that peer has started.
+    // Cluster barrier phases (S > 1), each one split into arrive / wait and
+    // executed by every thread of every CTA exactly once:
+    //   phase 0      every CTA of the cluster has started (its shared memory
+    //                may be written through DSMEM from then on);
+    //   phase i + 1  every CTA has written its partials of tile i into the
+    //                owners' slot buffer (i & 1) and has read its own slots of
+    //                tile i - 1, so buffer (i + 1) & 1 is free again.
     if (S > 1) cluster_arrive_relaxed();
 
     if (warp == kSplitConsumerWarps) {
         // ============================ producer warp ============================
-        const uint16_t *wbase = p.W + (int64_t)n0 * p.ldw + kbeg;
-        for (int g = 0; g < nchunks; ++g) {
-            const int s = g % stages;
-            if (g >= stages) {
-                bool ok = true;
-                if (lane == 0) ok = mbar_wait_bounded(empty0 + 8 * s, ((g / stages) - 1) & 1, p.budget_ns);
-                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                if (!ok) {
-                    if (lane == 0) {
-                        report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitProducerEmpty);
-                        *abort_flag = 1;
+        // Streams (tile, chunk) pieces through the ring across tile boundaries.
+        bool aborted = false;
+        bool x_done = !bulk_x;
+        // X is the preceding kernel's output: wait for it (PDL) only after the
+        // first ring fill of W is in flight, then one bulk copy per X row.
+        auto issue_x = [&]() {
+            griddep_wait();
+            if (lane == 0) mbar_arrive_expect_tx(xfull, (uint32_t)(p.M * klen * 2));
+            __syncwarp();
+            if (lane < p.M)
+                bulk_copy_g2s(smem_u32(smem + L.xs) + lane * L.xrowb, p.X + lane * p.ldx + kbeg,
+                              (uint32_t)(klen * 2), xfull);
+            x_done = true;
+        };
+        int g = 0;
+        for (int i = 0; i < my_tiles; ++i) {
+            const int n0 = ((int)blockIdx.y + i * C) * kBN;
+            const int rows = min(kBN, p.N - n0);
+            const uint16_t *wbase = p.W + (int64_t)n0 * p.ldw + kbeg;
+            for (int c = 0; c < nchunks; ++c, ++g) {
+                if (!x_done && g == stages) issue_x();
+                if (aborted) continue;
+                const int s = g % stages;
+                if (g >= stages) {
+                    bool ok = true;
+                    if (lane == 0) ok = mbar_wait_bounded(empty0 + 8 * s, ((g / stages) - 1) & 1, p.budget_ns);
+                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                    if (!ok) {
+                        if (lane == 0) {
+                            report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitProducerEmpty);
+                            *abort_flag = 1;
+                        }
+                        aborted = true;
+                        continue;
                     }
-                    break;
                 }
+                const int len = min(kSplitBK, klen - c * kSplitBK);
+                const uint32_t full = full0 + 8 * s;
+                if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(rows * len * 2));
+                __syncwarp();
+                for (int r = lane; r < rows; r += 32)
+                    bulk_copy_g2s(ring + s * kStageBytes + r * kRowBytes,
+                                  wbase + (int64_t)r * p.ldw + c * kSplitBK, (uint32_t)(len * 2), full);
+                __syncwarp();
+                if (lane == 0) *issued = g + 1;
             }
-            const int len = min(kSplitBK, klen - g * kSplitBK);
-            const uint32_t full = full0 + 8 * s;
-            if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(rows * len * 2));
-            __syncwarp();
-            for (int r = lane; r < rows; r += 32)
-                bulk_copy_g2s(ring + s * kStageBytes + r * kRowBytes,
-                              wbase + (int64_t)r * p.ldw + g * kSplitBK, (uint32_t)(len * 2), full);
-            __syncwarp();
-            if (lane == 0) *issued = g + 1;
+            if (i == 0) griddep_launch_dependents();
+            if (S > 1) {
+                cluster_wait();             // phase i
+                cluster_arrive_relaxed();   // phase i + 1 (the producer writes no slots)
+            }
         }
-        griddep_launch_dependents();
-        if (S > 1) cluster_wait();
+        if (!x_done) issue_x();
+        if (my_tiles == 0) griddep_launch_dependents();
+        if (S > 1) cluster_wait();          // phase my_tiles
     } else {
         // ============================ consumer warps ============================
-        griddep_wait();   // X may come from the preceding kernel
-        // ---- stage X[0:M, kbeg:kbeg+klen] (rows of L.xrowb bytes)
+        griddep_wait();   // X may come from the preceding kernel; Y may still be read by it
+        // ---- X[0:M, kbeg:kbeg+klen] in shared memory once (rows of L.xrowb bytes):
+        // bulk copies from the producer, else staged here
         uint8_t *xs = smem + L.xs;
-        if (p.x_vec16) {
+        if (bulk_x) {
+            if (!mbar_wait_bounded(xfull, 0, p.budget_ns)) {
+                if (lane == 0) report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitX);
+                if (!mbar_wait_bounded(xfull, 0, kDrainBudgetNs) && lane == 0)
+                    report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitDrain);
+            }
+        } else if (p.x_vec16) {
             const int nv = klen >> 3;
 #pragma unroll 4
             for (int i = tid; i < p.M * nv; i += kSplitConsumerWarps * 32) {
@@ -181,166 +230,172 @@ splitk_kernel(const SplitParams p)
         }
         named_bar_sync(1, kSplitConsumerWarps * 32);
         griddep_launch_dependents();
+        if (S > 1) cluster_wait();          // phase 0: every peer has started
 
+        const uint32_t xs_u32 = smem_u32(xs);
+        const uint32_t slots = smem_u32(smem + L.slots);
+        float *red = reinterpret_cast<float *>(smem + L.red);   // MMA: [warp][MT][16]
         bool failed = false;
-        float part[MT][4];           // FMA: acc[m][r] for rows 4w+r.  MMA: fragment sums (see below)
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) part[m][r] = 0.f;
-        float macc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // MMA accumulators
+        int g = 0;
+        for (int i = 0; i < my_tiles; ++i) {
+            const int n0 = ((int)blockIdx.y + i * C) * kBN;
+            const int rows = min(kBN, p.N - n0);
+            const uint32_t slot_buf = slots + (uint32_t)((i & 1) * S * MT * kBN * 4);
 
-        for (int g = 0; g < nchunks; ++g) {
-            const int s = g % stages;
-            const uint32_t full = full0 + 8 * s;
-            const uint32_t par = (g / stages) & 1;
-            if (!failed) {
-                if (*abort_flag && *issued <= g) {
-                    failed = true;             // the producer gave up before this chunk
-                } else if (!mbar_wait_bounded(full, par, p.budget_ns)) {
-                    failed = true;
-                    if (lane == 0) report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitConsumerFull);
+            float part[MT][4];        // FMA: acc[m][r] for W rows 4*warp + r
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) part[m][r] = 0.f;
+            float macc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // MMA accumulators
+
+            for (int c = 0; c < nchunks; ++c, ++g) {
+                const int s = g % stages;
+                const uint32_t full = full0 + 8 * s;
+                const uint32_t par = (g / stages) & 1;
+                if (!failed) {
+                    if (*abort_flag && *issued <= g) {
+                        failed = true;             // the producer gave up before this chunk
+                    } else if (!mbar_wait_bounded(full, par, p.budget_ns)) {
+                        failed = true;
+                        if (lane == 0) report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitConsumerFull);
+                        if (!drain_wait(full, par, g, abort_flag, issued) && lane == 0)
+                            report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitDrain);
+                    }
+                } else if (!(*abort_flag && *issued <= g)) {
+                    // already failed: still wait (bounded) for this chunk's copies
+                    // so nothing lands in shared memory after the CTA exits
                     if (!drain_wait(full, par, g, abort_flag, issued) && lane == 0)
                         report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitDrain);
                 }
-            } else if (!(*abort_flag && *issued <= g)) {
-                // already failed: still wait (bounded) for this chunk's copies
-                // so nothing lands in shared memory after the CTA exits
-                if (!drain_wait(full, par, g, abort_flag, issued) && lane == 0)
-                    report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitDrain);
-            }
-            if (!failed) {
-                const int len = min(kSplitBK, klen - g * kSplitBK);
-                const uint32_t stage = ring + s * kStageBytes;
-                if constexpr (CONS == SKINNY_CONSUMER_FMA) {
-                    const int nv = len >> 3;
-                    if (lane < nv) {
-                        const int r0 = warp * 4;
-                        float w[4][8];
+                if (!failed) {
+                    const int len = min(kSplitBK, klen - c * kSplitBK);
+                    const uint32_t stage = ring + s * kStageBytes;
+                    if constexpr (CONS == SKINNY_CONSUMER_FMA) {
+                        const int nv = len >> 3;
+                        if (lane < nv) {
+                            const int r0 = warp * 4;
+                            float w[4][8];
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            uint4 v;
-                            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                                         : "r"(stage + (r0 + r) * kRowBytes + lane * 16));
-                            w[r][0] = bf16_lo(v.x); w[r][1] = bf16_hi(v.x);
-                            w[r][2] = bf16_lo(v.y); w[r][3] = bf16_hi(v.y);
-                            w[r][4] = bf16_lo(v.z); w[r][5] = bf16_hi(v.z);
-                            w[r][6] = bf16_lo(v.w); w[r][7] = bf16_hi(v.w);
+                            for (int r = 0; r < 4; ++r) {
+                                uint4 v;
+                                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                                             : "r"(stage + (r0 + r) * kRowBytes + lane * 16));
+                                w[r][0] = bf16_lo(v.x); w[r][1] = bf16_hi(v.x);
+                                w[r][2] = bf16_lo(v.y); w[r][3] = bf16_hi(v.y);
+                                w[r][4] = bf16_lo(v.z); w[r][5] = bf16_hi(v.z);
+                                w[r][6] = bf16_lo(v.w); w[r][7] = bf16_hi(v.w);
+                            }
+                            const uint8_t *xcol = xs + (c * kSplitBK + lane * 8) * 2;
+#pragma unroll
+                            for (int m = 0; m < MT; ++m) {
+                                const uint4 v = *reinterpret_cast<const uint4 *>(xcol + m * L.xrowb);
+                                float x[8];
+                                x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+                                x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+#pragma unroll
+                                    for (int r = 0; r < 4; ++r) part[m][r] = fmaf(x[e], w[r][e], part[m][r]);
+                            }
                         }
-                        const uint8_t *xcol = xs + (g * kSplitBK + lane * 8) * 2;
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            const uint4 v = *reinterpret_cast<const uint4 *>(xcol + m * L.xrowb);
-                            float x[8];
-                            x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
-                            x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-#pragma unroll
-                                for (int r = 0; r < 4; ++r) part[m][r] = fmaf(x[e], w[r][e], part[m][r]);
+                    } else {
+                        // MMA: A = 16 W rows x 16 k (ldmatrix.x4), B = 16 k x 8|16 tokens.
+                        const int steps = len >> 4;
+                        float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                        const uint32_t a_row = (lane & 7) + 8 * ((lane >> 3) & 1);
+                        const uint32_t a_addr0 = stage + a_row * kRowBytes + (lane >> 4) * 16;
+                        for (int j = warp; j < steps; j += kSplitConsumerWarps) {
+                            uint32_t a[4];
+                            ldmatrix_x4(a_addr0 + j * 32, a[0], a[1], a[2], a[3]);
+                            const int kx = c * kSplitBK + j * 16;
+                            if constexpr (MT <= 8) {
+                                const uint32_t tok = lane & 7, kh = (lane >> 3) & 1;
+                                uint32_t b0, b1;
+                                ldmatrix_x2(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1);
+                                mma_bf16_16816(d[0], a, b0, b1, d[0]);
+                            } else {
+                                const uint32_t tok = (lane & 7) + 8 * (lane >> 4), kh = (lane >> 3) & 1;
+                                uint32_t b0, b1, b2, b3;
+                                ldmatrix_x4(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1, b2, b3);
+                                mma_bf16_16816(d[0], a, b0, b1, d[0]);
+                                mma_bf16_16816(d[1], a, b2, b3, d[1]);
+                            }
                         }
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) macc[h][q] += d[h][q];
                     }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * s);
+            }
+
+            // ---- the CTA's partial P[m][c] of this tile, to Y (S == 1) or to its owner
+            auto emit = [&](int m, int c, float v) {
+                if (m >= p.M || c >= rows) return;
+                if (S == 1) {
+                    p.Y[m * p.ldy + n0 + c] = v;
                 } else {
-                    // MMA: A = 16 W rows x 16 k (ldmatrix.x4), B = 16 k x 8|16 tokens.
-                    const int steps = len >> 4;
-                    float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    const uint32_t a_row = (lane & 7) + 8 * ((lane >> 3) & 1);
-                    const uint32_t a_addr0 = stage + a_row * kRowBytes + (lane >> 4) * 16;
-                    const uint32_t xs_u32 = smem_u32(xs);
-                    for (int j = warp; j < steps; j += kSplitConsumerWarps) {
-                        uint32_t a[4];
-                        ldmatrix_x4(a_addr0 + j * 32, a[0], a[1], a[2], a[3]);
-                        const int kx = g * kSplitBK + j * 16;
-                        if constexpr (MT <= 8) {
-                            const uint32_t tok = lane & 7, kh = (lane >> 3) & 1;
-                            uint32_t b0, b1;
-                            ldmatrix_x2(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1);
-                            mma_bf16_16816(d[0], a, b0, b1, d[0]);
-                        } else {
-                            const uint32_t tok = (lane & 7) + 8 * (lane >> 4), kh = (lane >> 3) & 1;
-                            uint32_t b0, b1, b2, b3;
-                            ldmatrix_x4(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1, b2, b3);
-                            mma_bf16_16816(d[0], a, b0, b1, d[0]);
-                            mma_bf16_16816(d[1], a, b2, b3, d[1]);
-                        }
+                    const uint32_t local = slot_buf + (uint32_t)(((rank * MT + m) * kBN + c) * 4);
+                    st_shared_cluster_f32(mapa_shared(local, (uint32_t)(c % S)), v);
+                }
+            };
+            if constexpr (CONS == SKINNY_CONSUMER_FMA) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        float v = part[m][r];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                        part[m][r] = v;
                     }
+                // every lane now holds all sums; lane l emits pairs l, l+32, ...
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
+                for (int m = 0; m < MT; ++m)
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) macc[h][i] += d[h][i];
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * s);
-        }
-
-        // ---- per-CTA partial P[m][c] (c = tile column), then to its owner
-        if (S > 1) cluster_wait();   // every peer has started
-        const uint32_t slots = smem_u32(smem + L.slots);
-        auto emit = [&](int m, int c, float v) {
-            if (m >= p.M || c >= rows) return;
-            if (S == 1) {
-                p.Y[m * p.ldy + n0 + c] = v;
+                    for (int r = 0; r < 4; ++r)
+                        if (((m * 4 + r) & 31) == lane) emit(m, warp * 4 + r, part[m][r]);
             } else {
-                const uint32_t local = slots + (uint32_t)(((rank * MT + m) * kBN + c) * 4);
-                st_shared_cluster_f32(mapa_shared(local, (uint32_t)(c % S)), v);
-            }
-        };
-        if constexpr (CONS == SKINNY_CONSUMER_FMA) {
+                // fragment: thread (g4 = lane/4, t4 = lane%4) holds rows g4, g4+8
+                // for tokens 2*t4, 2*t4+1 (+8 for the second MMA)
+                const int g4 = lane >> 2, t4 = lane & 3;
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && MT <= 8) break;
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    float v = part[m][r];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-                    part[m][r] = v;
+                    for (int q = 0; q < 4; ++q) {
+                        const int tok = 8 * h + 2 * t4 + (q & 1);
+                        const int row = g4 + 8 * (q >> 1);
+                        if (tok < MT) red[(warp * MT + tok) * kBN + row] = macc[h][q];
+                    }
                 }
-            // every lane now holds all sums; lane l emits pairs l, l+32, ...
+                named_bar_sync(1, kSplitConsumerWarps * 32);
+                for (int e = tid; e < MT * kBN; e += kSplitConsumerWarps * 32) {
+                    const int m = e / kBN, c = e - m * kBN;
+                    float v = red[m * kBN + c];
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    if (((m * 4 + r) & 31) == lane) emit(m, warp * 4 + r, part[m][r]);
-        } else {
-            // fragment: thread (g4 = lane/4, t4 = lane%4) holds rows g4, g4+8
-            // for tokens 2*t4, 2*t4+1 (+8 for the second MMA)
-            float *red = reinterpret_cast<float *>(smem + L.red);   // [warp][MT][16]
-            const int g4 = lane >> 2, t4 = lane & 3;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if (h == 1 && MT <= 8) break;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int tok = 8 * h + 2 * t4 + (i & 1);
-                    const int row = g4 + 8 * (i >> 1);
-                    if (tok < MT) red[(warp * MT + tok) * kBN + row] = macc[h][i];
+                    for (int w = 1; w < kSplitConsumerWarps; ++w) v += red[(w * MT + m) * kBN + c];
+                    emit(m, c, v);
                 }
+                named_bar_sync(1, kSplitConsumerWarps * 32);   // red is reused by the next tile
             }
-            named_bar_sync(1, kSplitConsumerWarps * 32);
-            for (int i = tid; i < MT * kBN; i += kSplitConsumerWarps * 32) {
-                const int m = i / kBN, c = i - m * kBN;
-                float v = red[m * kBN + c];
-#pragma unroll
-                for (int w = 1; w < kSplitConsumerWarps; ++w) v += red[(w * MT + m) * kBN + c];
-                emit(m, c, v);
-            }
-        }
-    }
 
-    if (S > 1) {
-        // Cluster phase 2: every thread of every CTA arrives exactly once
-        // (non-.aligned forms, the branches above diverge by warp role).
-        cluster_arrive_release();
-        cluster_wait_acquire();
-        const float *sl = reinterpret_cast<const float *>(smem + L.slots);
-        for (int i = tid; i < MT * kBN; i += kSplitThreads) {
-            const int m = i / kBN, c = i - m * kBN;
-            if (m < p.M && c < rows && (c % S) == rank) {
-                float v = sl[(0 * MT + m) * kBN + c];
-                for (int r = 1; r < S; ++r) v += sl[(r * MT + m) * kBN + c];
-                p.Y[m * p.ldy + n0 + c] = v;
+            if (S > 1) {
+                cluster_arrive_release();   // phase i + 1: partials of tile i are in the owners' slots
+                cluster_wait_acquire();
+                const float *sl = reinterpret_cast<const float *>(smem + L.slots) + (i & 1) * S * MT * kBN;
+                for (int e = tid; e < MT * kBN; e += kSplitConsumerWarps * 32) {
+                    const int m = e / kBN, c = e - m * kBN;
+                    if (m < p.M && c < rows && (c % S) == rank) {
+                        float v = sl[(0 * MT + m) * kBN + c];
+                        for (int r = 1; r < S; ++r) v += sl[(r * MT + m) * kBN + c];
+                        p.Y[m * p.ldy + n0 + c] = v;
+                    }
+                }
             }
         }
     }
@@ -373,11 +428,11 @@ int splitk_smem_bytes(int M, int consumer, int block_n, int stages, int k_slice,
 
 cudaError_t splitk_prepare() {
     for (int m = 0; m < SKINNY_MAX_M; ++m) {
-        cudaError_t e = cudaFuncSetAttribute(kFma[m], cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        cudaError_t e = set_max_dyn_smem(kFma[m]);
         if (e != cudaSuccess) return e;
     }
     for (int i = 0; i < 2; ++i) {
-        cudaError_t e = cudaFuncSetAttribute(kMma[i], cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        cudaError_t e = set_max_dyn_smem(kMma[i]);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

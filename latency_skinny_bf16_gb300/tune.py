@@ -1,0 +1,148 @@
+"""Measure every supported plan per (K, N, M) and write the dispatcher's table.
+
+For one call shape, each candidate plan (dot-product with each block_n, split-K
+with each consumer / cluster size / ring depth) is forced through the library
+options and timed L2-cold: a CUDA graph of R back-to-back calls over R distinct
+copies of W (together more than 2x the L2 size) is replayed, and the time per
+call is taken from CUDA events on the launching stream.  The fastest plan of
+each shape becomes one line of ``csrc/tuning_table.inc``; consecutive M with
+the same winner are merged into one range.
+
+    python -m latency_skinny_bf16_gb300.tune --shapes 7168x256,7168x384 --out table.inc
+
+Shapes are KxN.  Needs a GPU; run it on the machine the table is for.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import sys
+
+import numpy as np
+import torch
+
+import latency_skinny_bf16_gb300 as sk
+
+DEFAULT_SHAPES = ["7168x256", "7168x384", "2880x128", "4096x256", "7168x2112", "1536x24576", "14336x7168"]
+
+
+def candidates(M: int, K: int):
+    out = []
+    for bn in (1, 2, 4, 8):
+        out.append(dict(backend=1, block_n=bn, consumer=0, split_k=0, stages=0))
+    for cons in (1, 2):
+        if cons == 2 and K % 16:
+            continue
+        for s in (1, 2, 4, 8):
+            for stages in (2, 4, 8):
+                out.append(dict(backend=2, consumer=cons, split_k=s, stages=stages, block_n=0))
+    return out
+
+
+def time_plan(M, N, K, xs, ws, ys, stream, iters=20):
+    """us per call: a graph of len(ws) calls over distinct W copies, replayed `iters` times."""
+    sh = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        for x, w, y in zip(xs, ws, ys):
+            st = sk.skinny_gemm_bf16(x.data_ptr(), K, w.data_ptr(), K, y.data_ptr(), N, M, N, K, sh)
+            if st != sk.SKINNY_OK:
+                return None
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for x, w, y in zip(xs, ws, ys):
+            sk.skinny_gemm_bf16(x.data_ptr(), K, w.data_ptr(), K, y.data_ptr(), N, M, N, K, sh)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (iters * len(ws))
+
+
+def tune_shape(K, N, m_values, l2_bytes, pdl, log):
+    rng = torch.Generator().manual_seed(K * 7919 + N)
+    w_bytes = 2 * N * K
+    reps = max(4, math.ceil(2 * l2_bytes / w_bytes))
+    reps = min(reps, 512)
+    w0 = (torch.randn(N, K, generator=rng) * 0.02).to(torch.bfloat16).cuda()
+    ws = [w0.clone() for _ in range(reps)]
+    stream = torch.cuda.Stream()
+    rows = []
+    for M in m_values:
+        x = torch.randn(M, K, generator=rng).to(torch.bfloat16).cuda()
+        xs = [x] * reps
+        ys = [torch.empty(M, N, device="cuda") for _ in range(reps)]
+        best = None
+        results = []
+        for c in candidates(M, K):
+            with sk.options(pdl=pdl, **c):
+                try:
+                    us = time_plan(M, N, K, xs, ws, ys, stream)
+                except sk.SkinnyError:
+                    us = None
+            if us is None:
+                continue
+            results.append((us, c))
+            if best is None or us < best[0]:
+                best = (us, c)
+        results.sort(key=lambda t: t[0])
+        log.write(json.dumps({"K": K, "N": N, "M": M, "best_us": round(best[0], 3), "best": best[1],
+                              "top5": [(round(u, 3), c) for u, c in results[:5]]}) + "\n")
+        log.flush()
+        rows.append((M, best[1], best[0]))
+        del ys
+    del ws
+    torch.cuda.empty_cache()
+    return rows
+
+
+def merge_rows(K, N, rows):
+    """Consecutive M with identical winning plans -> one table line."""
+    lines = []
+    i = 0
+    while i < len(rows):
+        j = i
+        while j + 1 < len(rows) and rows[j + 1][1] == rows[i][1] and rows[j + 1][0] == rows[j][0] + 1:
+            j += 1
+        c = rows[i][1]
+        lines.append((K, N, rows[i][0], rows[j][0], c["backend"], c["consumer"], c["split_k"], c["block_n"],
+                      c["stages"], [round(r[2], 2) for r in rows[i:j + 1]]))
+        i = j + 1
+    return lines
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--shapes", default=",".join(DEFAULT_SHAPES))
+    ap.add_argument("--m", default="1-16")
+    ap.add_argument("--pdl", type=int, default=1)
+    ap.add_argument("--out", default="-")
+    ap.add_argument("--log", default=None)
+    a = ap.parse_args(argv)
+    lo, hi = (int(v) for v in a.m.split("-")) if "-" in a.m else (int(a.m), int(a.m))
+    m_values = list(range(lo, hi + 1))
+    assert sk.skinny_init(0) == sk.SKINNY_OK
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    log = open(a.log, "a") if a.log else sys.stderr
+    out_lines = []
+    for shp in a.shapes.split(","):
+        K, N = (int(v) for v in shp.lower().split("x"))
+        rows = tune_shape(K, N, m_values, l2, a.pdl, log)
+        for (k, n, mlo, mhi, be, co, sp, bn, st, us) in merge_rows(K, N, rows):
+            out_lines.append(f"{{{k}, {n}, {mlo}, {mhi}, {be}, {co}, {sp}, {bn}, {st}}},  // us/call {us}")
+    text = "\n".join(out_lines) + "\n"
+    if a.out == "-":
+        sys.stdout.write(text)
+    else:
+        with open(a.out, "w") as f:
+            f.write(text)
+
+
+if __name__ == "__main__":
+    main()
