@@ -64,6 +64,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget (s)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--only", default=None, help="comma list of case indices of the workload to keep (profiling)")
     p.add_argument("--profile-mode", action="store_true",
                    help="short run for ncu: no clock soak, no CPU baseline, few extra passes")
     return p.parse_args(argv)
@@ -201,6 +202,13 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ the GPU workload
 
+def select_cases(args):
+    cases = si.workload(args.workload)
+    if args.only:
+        cases = [cases[int(i)] for i in args.only.split(",")]
+    return cases
+
+
 class Replica:
     """Device buffers for one copy of the whole workload."""
 
@@ -241,7 +249,7 @@ def run_native(args):
         raise sk.SkinnyError(st, "skinny_init")
     sk.skinny_set_option(sk.SKINNY_OPT_PDL, args.pdl)
 
-    cases = si.workload(args.workload)
+    cases = select_cases(args)
     host_inputs = [si.make_inputs(c) for c in cases]
     step_bytes = sum(c.algorithmic_bytes for c in cases)
     step_w_bytes = sum(2 * c.N * c.K for c in cases)
@@ -437,7 +445,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return None
-    cases = si.workload(args.workload)
+    cases = select_cases(args)
     step_bytes = sum(c.algorithmic_bytes for c in cases)
     # untimed warm-up steps, then exactly `steps` timed steps, each a bounded sample
     budget = min(120.0, max(5.0, 0.2 * args.steps))

@@ -79,6 +79,7 @@ typedef struct {
     int block_n;       /* output columns (rows of W) per CTA tile */
     int split_k;       /* CTAs per cluster along K (1 = no cluster) */
     int stages;        /* shared-memory ring depth (split-K) */
+    int stage_k;       /* split-K: K elements of each W row per ring stage (64..2048, multiple of 64) */
     int k_chunk;       /* dot-product: K elements of X staged in shared memory at a time;
                           split-K: K elements per CTA (the cluster rank's slice) */
     int grid_x;        /* grid dimensions launched; split-K: grid_x = split_k CTAs per cluster, */
@@ -95,14 +96,16 @@ typedef enum {
     SKINNY_OPT_FORCE_CONSUMER = 3,   /* skinny_consumer_t for split-K; AUTO = dispatcher */
     SKINNY_OPT_FORCE_SPLIT_K = 4,    /* 0 = dispatcher, 1..8 = cluster size */
     SKINNY_OPT_FORCE_BLOCK_N = 5,    /* 0 = dispatcher; dot-product 1/2/4/8, split-K 16/64 */
-    SKINNY_OPT_FORCE_STAGES = 6,     /* 0 = dispatcher, 2..8 */
+    SKINNY_OPT_FORCE_STAGES = 6,     /* 0 = dispatcher, 1..16 */
     SKINNY_OPT_WAIT_TIMEOUT_US = 7,  /* budget of each bounded wait in a kernel, microseconds
                                         (default 500000).  0 makes every such wait give up at once,
                                         which exercises the timeout path without any real hang */
     SKINNY_OPT_LOG = 8,              /* 1: print the plan chosen for each new call shape to stderr
                                         (default: env SKINNY_LOG) */
-    SKINNY_OPT_FORCE_CLUSTERS = 9    /* split-K: 0 = dispatcher, else the number of (persistent)
+    SKINNY_OPT_FORCE_CLUSTERS = 9,   /* split-K: 0 = dispatcher, else the number of (persistent)
                                         clusters, each looping over row tiles (tests / tuning only) */
+    SKINNY_OPT_FORCE_STAGE_K = 10    /* split-K: 0 = dispatcher, else K elements per ring stage
+                                        (64..2048, multiple of 64; tests / tuning only) */
 } skinny_option_t;
 
 /*

@@ -51,6 +51,7 @@ SKINNY_OPT_FORCE_STAGES = 6
 SKINNY_OPT_WAIT_TIMEOUT_US = 7
 SKINNY_OPT_LOG = 8
 SKINNY_OPT_FORCE_CLUSTERS = 9
+SKINNY_OPT_FORCE_STAGE_K = 10
 
 EXPORTED_SYMBOLS = (
     "skinny_gemm_bf16", "skinny_init", "skinny_query_plan", "skinny_plan_for",
@@ -70,7 +71,7 @@ class SkinnyError(RuntimeError):
 
 class _Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
-        "backend", "consumer", "vec_elems", "block_n", "split_k", "stages", "k_chunk",
+        "backend", "consumer", "vec_elems", "block_n", "split_k", "stages", "stage_k", "k_chunk",
         "grid_x", "grid_y", "threads", "smem_bytes", "pdl", "tuned")]
 
     def as_dict(self) -> dict:
@@ -193,7 +194,7 @@ class options:
                  "consumer": SKINNY_OPT_FORCE_CONSUMER, "split_k": SKINNY_OPT_FORCE_SPLIT_K,
                  "block_n": SKINNY_OPT_FORCE_BLOCK_N, "stages": SKINNY_OPT_FORCE_STAGES,
                  "wait_timeout_us": SKINNY_OPT_WAIT_TIMEOUT_US, "log": SKINNY_OPT_LOG,
-                 "clusters": SKINNY_OPT_FORCE_CLUSTERS}
+                 "clusters": SKINNY_OPT_FORCE_CLUSTERS, "stage_k": SKINNY_OPT_FORCE_STAGE_K}
         self._set = [(names[k], int(v)) for k, v in kw.items()]
         self._old = []
 

@@ -43,6 +43,7 @@ std::atomic<int> g_opt_force_block_n{0};
 std::atomic<int> g_opt_force_stages{0};
 std::atomic<int> g_opt_wait_us{500000};
 std::atomic<int> g_opt_force_grid_y{0};
+std::atomic<int> g_opt_force_stage_k{0};
 std::atomic<int> g_opt_log{-1};
 
 int env_flag(const char *name) {
@@ -190,7 +191,7 @@ bool plan_dotprod(int M, int N, int K, int vec, int force_bn, int num_sms, skinn
 }
 
 bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int force_stages, int force_c,
-                 int num_sms, skinny_plan_t *p) {
+                 int force_bk, int num_sms, skinny_plan_t *p) {
     if (vec != 8 || K % 8 != 0 || K < 8) return false;
     if (consumer == SKINNY_CONSUMER_MMA && K % 16 != 0) return false;
     if (!splitk_supported(M, consumer, 16)) return false;
@@ -210,10 +211,25 @@ bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int fo
         const int xrows = consumer == SKINNY_CONSUMER_MMA ? (M <= 8 ? 8 : 16) : M;
         const int xbytes = xrows * (((ks * 2 + 127) & ~127) + 16);
         if (xbytes > kSplitXBudget && !force_s) continue;
-        const int nchunks = (ks + kSplitBK - 1) / kSplitBK;
-        int stages = force_stages ? force_stages : (nchunks < 4 ? (nchunks < 1 ? 1 : nchunks) : 4);
+        // Ring chunk: 256 K elements when the whole slice fits a ring of up to 8
+        // such stages (one shot: every W byte requested at kernel start);
+        // otherwise stream 1024-element (2 KB per W row) chunks, which keeps each
+        // row's reads contiguous in DRAM.
+        int bk = force_bk;
+        if (bk == 0) bk = ((ks + kSplitBK - 1) / kSplitBK <= 8) ? kSplitBK : kSplitStreamBK;
+        if (bk < 64 || bk > kSplitMaxBK || bk % 64) return false;
+        const int nchunks = (ks + bk - 1) / bk;
+        int stages = force_stages;
+        if (stages == 0) {
+            if (nchunks <= 8) {
+                stages = nchunks < 1 ? 1 : nchunks;
+            } else {
+                stages = kSplitMaxStages;
+                while (stages > 2 && splitk_smem_bytes(M, consumer, 16, stages, ks, S, bk) > kMaxDynSmem) --stages;
+            }
+        }
         if (stages < 1 || stages > kSplitMaxStages) return false;
-        const int smem = splitk_smem_bytes(M, consumer, 16, stages, ks, S);
+        const int smem = splitk_smem_bytes(M, consumer, 16, stages, ks, S, bk);
         if (smem > kMaxDynSmem) return false;
         // Persistent clusters: as many as can be resident (shared memory, and
         // at most 3 CTAs of 160 threads per SM by registers), with the tiles
@@ -240,6 +256,7 @@ bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int fo
         p->block_n = 16;
         p->split_k = S;
         p->stages = stages;
+        p->stage_k = bk;
         p->k_chunk = ks;
         p->grid_x = S;
         p->grid_y = C;
@@ -286,7 +303,7 @@ skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int n
     } else if (backend == SKINNY_BACKEND_SPLITK) {
         if (consumer == SKINNY_CONSUMER_AUTO) consumer = (M > 4 && mma_ok) ? SKINNY_CONSUMER_MMA : SKINNY_CONSUMER_FMA;
         if (bn != 0 && bn != 16) return SKINNY_ERR_UNSUPPORTED;
-        ok = plan_splitk(M, N, K, vec, consumer, split, stages, fgy, num_sms, p);
+        ok = plan_splitk(M, N, K, vec, consumer, split, stages, fgy, g_opt_force_stage_k.load(), num_sms, p);
         if (!ok && fb == SKINNY_BACKEND_AUTO) {
             // a tuned split-K entry that these pointers / strides cannot use
             ok = plan_dotprod(M, N, K, vec, 0, num_sms, p);
@@ -307,10 +324,10 @@ void log_plan(int M, int N, int K, int ldw, const skinny_plan_t &p) {
     std::lock_guard<std::mutex> g(mu);
     if (!seen.insert({M, N, K, ldw, p.pdl}).second) return;
     std::fprintf(stderr,
-                 "[skinny] M=%d N=%d K=%d ldw=%d -> %s consumer=%d vec=%d block_n=%d split_k=%d stages=%d "
+                 "[skinny] M=%d N=%d K=%d ldw=%d -> %s consumer=%d vec=%d block_n=%d split_k=%d stages=%d stage_k=%d "
                  "k_chunk=%d grid=%dx%d smem=%d pdl=%d tuned=%d\n",
                  M, N, K, ldw, p.backend == SKINNY_BACKEND_DOTPROD ? "dotprod" : "splitk", p.consumer,
-                 p.vec_elems, p.block_n, p.split_k, p.stages, p.k_chunk, p.grid_x, p.grid_y, p.smem_bytes,
+                 p.vec_elems, p.block_n, p.split_k, p.stages, p.stage_k, p.k_chunk, p.grid_x, p.grid_y, p.smem_bytes,
                  p.pdl, p.tuned);
 }
 
@@ -403,6 +420,9 @@ skinny_status_t skinny_set_option(int option, int value) {
         case SKINNY_OPT_FORCE_CLUSTERS:
             if (value < 0 || value > 65535) return SKINNY_ERR_INVALID_VALUE;
             g_opt_force_grid_y.store(value); return SKINNY_OK;
+        case SKINNY_OPT_FORCE_STAGE_K:
+            if (value < 0 || value > kSplitMaxBK || value % 64) return SKINNY_ERR_INVALID_VALUE;
+            g_opt_force_stage_k.store(value); return SKINNY_OK;
         default:
             return SKINNY_ERR_INVALID_VALUE;
     }
@@ -420,6 +440,7 @@ skinny_status_t skinny_get_option(int option, int *value) {
         case SKINNY_OPT_WAIT_TIMEOUT_US: *value = g_opt_wait_us.load(); return SKINNY_OK;
         case SKINNY_OPT_LOG: *value = opt_log(); return SKINNY_OK;
         case SKINNY_OPT_FORCE_CLUSTERS: *value = g_opt_force_grid_y.load(); return SKINNY_OK;
+        case SKINNY_OPT_FORCE_STAGE_K: *value = g_opt_force_stage_k.load(); return SKINNY_OK;
         default: return SKINNY_ERR_INVALID_VALUE;
     }
 }

@@ -147,8 +147,9 @@ dotprod_kernel(const uint16_t *__restrict__ X, int64_t ldx,
         for (int r = 0; r < BN; ++r) acc[m][r] = 0.f;
 
     // Batch b of a chunk: vectors v = tid + (b*U + u) * T, u < U, predicated.
-    RawW<VW> raw[U][BN];
-    auto load_batch = [&](int k0, int nvec, int v0) {
+    // Two register buffers: batch b+1 is in flight while batch b is consumed.
+    RawW<VW> rawA[U][BN], rawB[U][BN];
+    auto load_batch = [&](RawW<VW> (&raw)[U][BN], int k0, int nvec, int v0) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int v = v0 + u * kDotThreads;
@@ -158,9 +159,16 @@ dotprod_kernel(const uint16_t *__restrict__ X, int64_t ldx,
             }
         }
     };
+    auto fma_batch = [&](const RawW<VW> (&raw)[U][BN], int nvec, int v0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + u * kDotThreads;
+            if (v < nvec) fma_vec<MT, VW, BN>(acc, xs, kc, v * VW, raw[u]);
+        }
+    };
     {
         const int klen0 = min(kc, K);
-        load_batch(0, klen0 / VW, tid);
+        load_batch(rawA, 0, klen0 / VW, tid);
     }
     griddep_wait();
     griddep_launch_dependents();
@@ -170,7 +178,7 @@ dotprod_kernel(const uint16_t *__restrict__ X, int64_t ldx,
         const int nvec = klen / VW;
         if (k0 > 0) {
             __syncthreads();            // every thread is done with the previous chunk of X
-            load_batch(k0, nvec, tid);  // first W batch of this chunk, before staging X
+            load_batch(rawA, k0, nvec, tid);  // first W batch of this chunk, before staging X
         }
         // ---- stage X[0:M, k0:k0+klen] in shared memory: when X rows are
         // 16-byte aligned, one bulk async copy per row (the TMA engine) for
@@ -203,13 +211,20 @@ dotprod_kernel(const uint16_t *__restrict__ X, int64_t ldx,
             }
         }
 
-        // ---- main part: VW-wide vectors, U per row in flight per batch
-        for (int v0 = tid; v0 < nvec; v0 += U * kDotThreads) {
-            if (v0 != tid) load_batch(k0, nvec, v0);
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int v = v0 + u * kDotThreads;
-                if (v < nvec) fma_vec<MT, VW, BN>(acc, xs, kc, v * VW, raw[u]);
+        // ---- main part: VW-wide vectors, U per row per batch, two batches in flight
+        constexpr int kStep = U * kDotThreads;
+        if constexpr (MT * BN <= 32) {
+            for (int v0 = tid; v0 < nvec; v0 += 2 * kStep) {
+                if (v0 + kStep < nvec) load_batch(rawB, k0, nvec, v0 + kStep);
+                fma_batch(rawA, nvec, v0);
+                if (v0 + 2 * kStep < nvec) load_batch(rawA, k0, nvec, v0 + 2 * kStep);
+                if (v0 + kStep < nvec) fma_batch(rawB, nvec, v0 + kStep);
+            }
+        } else {
+            // many accumulators: one register buffer (no spills)
+            for (int v0 = tid; v0 < nvec; v0 += kStep) {
+                if (v0 != tid) load_batch(rawA, k0, nvec, v0);
+                fma_batch(rawA, nvec, v0);
             }
         }
 

@@ -36,10 +36,12 @@ cudaError_t launch_dotprod(const GemmArgs &a, const skinny_plan_t &p, const Laun
 // ---- cluster split-K backend (splitk.cu)
 constexpr int kSplitConsumerWarps = 4;
 constexpr int kSplitThreads = (kSplitConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kSplitBK = 256;                                  // K elements per ring stage
+constexpr int kSplitBK = 256;        // default K elements per ring stage (one-shot slices)
+constexpr int kSplitStreamBK = 1024; // K elements per ring stage when streaming (2 KB per W row)
+constexpr int kSplitMaxBK = 2048;
 constexpr int kSplitMaxCluster = 8;
-constexpr int kSplitMaxStages = 8;
-int splitk_smem_bytes(int M, int consumer, int block_n, int stages, int k_slice, int split_k);
+constexpr int kSplitMaxStages = 16;
+int splitk_smem_bytes(int M, int consumer, int block_n, int stages, int k_slice, int split_k, int stage_k);
 bool splitk_supported(int M, int consumer, int block_n);
 cudaError_t splitk_prepare();
 cudaError_t launch_splitk(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);

@@ -46,8 +46,10 @@ namespace skinny {
 namespace {
 
 constexpr int kBN = 16;
-constexpr int kRowBytes = kSplitBK * 2 + 16;      // ring row stride: 528 = 16 (mod 128)
-constexpr int kStageBytes = kBN * kRowBytes;
+// Ring rows hold `bk` K elements (bk a multiple of 64) plus 16 bytes of pad, so
+// the row stride is 16 (mod 128) bytes and ldmatrix / 128-bit shared loads of
+// 8 consecutive rows hit 8 different bank groups.
+__host__ __device__ inline int ring_row_bytes(int bk) { return bk * 2 + 16; }
 constexpr uint64_t kDrainBudgetNs = 200ull * 1000 * 1000;
 
 struct Layout {
@@ -57,12 +59,12 @@ struct Layout {
 
 __host__ __device__ inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline Layout make_layout(int MT, int consumer, int stages, int KS, int S) {
+__host__ __device__ inline Layout make_layout(int MT, int consumer, int stages, int KS, int S, int bk) {
     Layout L;
     L.xrows = (consumer == SKINNY_CONSUMER_MMA) ? (MT <= 8 ? 8 : 16) : MT;
     L.xrowb = round_up(KS * 2, 128) + 16;          // X row stride: 16 (mod 128)
     int off = 0;
-    L.ring = off;  off += stages * kStageBytes;
+    L.ring = off;  off += stages * kBN * ring_row_bytes(bk);
     L.xs = off;    off += L.xrows * L.xrowb;
     off = round_up(off, 16);
     L.red = off;   off += (consumer == SKINNY_CONSUMER_MMA) ? kSplitConsumerWarps * MT * kBN * 4 : 0;
@@ -80,6 +82,7 @@ struct SplitParams {
     float *Y; int64_t ldy;
     int M, N, K;
     int KS;            // K elements per rank (multiple of 16)
+    int bk;            // K elements per ring stage (multiple of 64, <= 2048)
     int stages;
     int x_vec16;       // X rows 16-byte aligned (vector staging)
     int *status;
@@ -107,12 +110,15 @@ splitk_kernel(const SplitParams p)
     const int C = gridDim.y;                       // clusters, persistent over row tiles
     const int T = (p.N + kBN - 1) / kBN;           // row tiles of 16
     const int my_tiles = ((int)blockIdx.y < T) ? (T - 1 - (int)blockIdx.y) / C + 1 : 0;
-    const Layout L = make_layout(MT, CONS, p.stages, p.KS, S);
+    const Layout L = make_layout(MT, CONS, p.stages, p.KS, S, p.bk);
+    const int bk = p.bk;
+    const int row_bytes = ring_row_bytes(bk);
+    const int stage_bytes = kBN * row_bytes;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rank = (S > 1) ? (int)cluster_ctarank() : 0;
     const int kbeg = rank * p.KS;
     const int klen = max(0, min(p.K, kbeg + p.KS) - kbeg);
-    const int nchunks = (klen + kSplitBK - 1) / kSplitBK;
+    const int nchunks = (klen + bk - 1) / bk;
     const int stages = p.stages;
 
     const uint32_t ring = smem_u32(smem + L.ring);
@@ -182,16 +188,19 @@ splitk_kernel(const SplitParams p)
                         continue;
                     }
                 }
-                const int len = min(kSplitBK, klen - c * kSplitBK);
+                const int len = min(bk, klen - c * bk);
                 const uint32_t full = full0 + 8 * s;
                 if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(rows * len * 2));
                 __syncwarp();
                 for (int r = lane; r < rows; r += 32)
-                    bulk_copy_g2s(ring + s * kStageBytes + r * kRowBytes,
-                                  wbase + (int64_t)r * p.ldw + c * kSplitBK, (uint32_t)(len * 2), full);
+                    bulk_copy_g2s(ring + s * stage_bytes + r * row_bytes,
+                                  wbase + (int64_t)r * p.ldw + c * bk, (uint32_t)(len * 2), full);
                 __syncwarp();
                 if (lane == 0) *issued = g + 1;
             }
+            // X must be in flight before the producer first waits on a cluster
+            // phase: that phase needs the consumers, and they need X.
+            if (!x_done) issue_x();
             if (i == 0) griddep_launch_dependents();
             if (S > 1) {
                 cluster_wait();             // phase i
@@ -269,25 +278,25 @@ splitk_kernel(const SplitParams p)
                         report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitDrain);
                 }
                 if (!failed) {
-                    const int len = min(kSplitBK, klen - c * kSplitBK);
-                    const uint32_t stage = ring + s * kStageBytes;
+                    const int len = min(bk, klen - c * bk);
+                    const uint32_t stage = ring + s * stage_bytes;
                     if constexpr (CONS == SKINNY_CONSUMER_FMA) {
                         const int nv = len >> 3;
-                        if (lane < nv) {
-                            const int r0 = warp * 4;
+                        const int r0 = warp * 4;
+                        for (int j = lane; j < nv; j += 32) {
                             float w[4][8];
 #pragma unroll
                             for (int r = 0; r < 4; ++r) {
                                 uint4 v;
                                 asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                                              : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                                             : "r"(stage + (r0 + r) * kRowBytes + lane * 16));
+                                             : "r"(stage + (r0 + r) * row_bytes + j * 16));
                                 w[r][0] = bf16_lo(v.x); w[r][1] = bf16_hi(v.x);
                                 w[r][2] = bf16_lo(v.y); w[r][3] = bf16_hi(v.y);
                                 w[r][4] = bf16_lo(v.z); w[r][5] = bf16_hi(v.z);
                                 w[r][6] = bf16_lo(v.w); w[r][7] = bf16_hi(v.w);
                             }
-                            const uint8_t *xcol = xs + (c * kSplitBK + lane * 8) * 2;
+                            const uint8_t *xcol = xs + (c * bk + j * 8) * 2;
 #pragma unroll
                             for (int m = 0; m < MT; ++m) {
                                 const uint4 v = *reinterpret_cast<const uint4 *>(xcol + m * L.xrowb);
@@ -302,31 +311,39 @@ splitk_kernel(const SplitParams p)
                         }
                     } else {
                         // MMA: A = 16 W rows x 16 k (ldmatrix.x4), B = 16 k x 8|16 tokens.
+                        // The MMA sum is moved into the fp32 accumulator (a rounded
+                        // add) after at most 4 k16 steps.
                         const int steps = len >> 4;
-                        float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                         const uint32_t a_row = (lane & 7) + 8 * ((lane >> 3) & 1);
-                        const uint32_t a_addr0 = stage + a_row * kRowBytes + (lane >> 4) * 16;
-                        for (int j = warp; j < steps; j += kSplitConsumerWarps) {
-                            uint32_t a[4];
-                            ldmatrix_x4(a_addr0 + j * 32, a[0], a[1], a[2], a[3]);
-                            const int kx = c * kSplitBK + j * 16;
-                            if constexpr (MT <= 8) {
-                                const uint32_t tok = lane & 7, kh = (lane >> 3) & 1;
-                                uint32_t b0, b1;
-                                ldmatrix_x2(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1);
-                                mma_bf16_16816(d[0], a, b0, b1, d[0]);
-                            } else {
-                                const uint32_t tok = (lane & 7) + 8 * (lane >> 4), kh = (lane >> 3) & 1;
-                                uint32_t b0, b1, b2, b3;
-                                ldmatrix_x4(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1, b2, b3);
-                                mma_bf16_16816(d[0], a, b0, b1, d[0]);
-                                mma_bf16_16816(d[1], a, b2, b3, d[1]);
+                        const uint32_t a_addr0 = stage + a_row * row_bytes + (lane >> 4) * 16;
+                        for (int j0 = warp; j0 < steps; j0 += 4 * kSplitConsumerWarps) {
+                            float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const int j = j0 + q * kSplitConsumerWarps;
+                                if (j < steps) {
+                                    uint32_t a[4];
+                                    ldmatrix_x4(a_addr0 + j * 32, a[0], a[1], a[2], a[3]);
+                                    const int kx = c * bk + j * 16;
+                                    if constexpr (MT <= 8) {
+                                        const uint32_t tok = lane & 7, kh = (lane >> 3) & 1;
+                                        uint32_t b0, b1;
+                                        ldmatrix_x2(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1);
+                                        mma_bf16_16816(d[0], a, b0, b1, d[0]);
+                                    } else {
+                                        const uint32_t tok = (lane & 7) + 8 * (lane >> 4), kh = (lane >> 3) & 1;
+                                        uint32_t b0, b1, b2, b3;
+                                        ldmatrix_x4(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1, b2, b3);
+                                        mma_bf16_16816(d[0], a, b0, b1, d[0]);
+                                        mma_bf16_16816(d[1], a, b2, b3, d[1]);
+                                    }
+                                }
                             }
+#pragma unroll
+                            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) macc[h][q] += d[h][q];
                         }
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) macc[h][q] += d[h][q];
                     }
                 }
                 __syncwarp();
@@ -421,9 +438,9 @@ bool splitk_supported(int M, int consumer, int block_n) {
            (consumer == SKINNY_CONSUMER_FMA || consumer == SKINNY_CONSUMER_MMA);
 }
 
-int splitk_smem_bytes(int M, int consumer, int block_n, int stages, int k_slice, int split_k) {
+int splitk_smem_bytes(int M, int consumer, int block_n, int stages, int k_slice, int split_k, int bk) {
     (void)block_n;
-    return make_layout(mt_for(M, consumer), consumer, stages, k_slice, split_k).total;
+    return make_layout(mt_for(M, consumer), consumer, stages, k_slice, split_k, bk).total;
 }
 
 cudaError_t splitk_prepare() {
@@ -440,10 +457,12 @@ cudaError_t splitk_prepare() {
 
 cudaError_t launch_splitk(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCtx &c) {
     if (!splitk_supported(a.M, pl.consumer, pl.block_n)) return cudaErrorInvalidValue;
+    if (pl.stage_k < 64 || pl.stage_k > kSplitMaxBK || pl.stage_k % 64) return cudaErrorInvalidValue;
     SplitParams p;
     p.X = a.X; p.ldx = a.ldx; p.W = a.W; p.ldw = a.ldw; p.Y = a.Y; p.ldy = a.ldy;
     p.M = a.M; p.N = a.N; p.K = a.K;
     p.KS = pl.k_chunk;
+    p.bk = pl.stage_k;
     p.stages = pl.stages;
     p.x_vec16 = ((reinterpret_cast<uintptr_t>(a.X) & 15) == 0 && (a.ldx & 7) == 0) ? 1 : 0;
     p.status = c.status;

@@ -18,6 +18,7 @@ import argparse
 import json
 import math
 import sys
+import time
 
 import numpy as np
 import torch
@@ -34,13 +35,13 @@ def candidates(M: int, K: int):
     for cons in (1, 2):
         if cons == 2 and K % 16:
             continue
-        for s in (1, 2, 4, 8):
-            for stages in (2, 4, 8):
+        for s in (1, 2, 4, 6, 8):
+            for stages in (0, 4, 16):      # 0: the dispatcher's ring depth for this shape
                 out.append(dict(backend=2, consumer=cons, split_k=s, stages=stages, block_n=0))
     return out
 
 
-def time_plan(M, N, K, xs, ws, ys, stream, iters=20):
+def time_plan(M, N, K, xs, ws, ys, stream, iters=10):
     """us per call: a graph of len(ws) calls over distinct W copies, replayed `iters` times."""
     sh = stream.cuda_stream
     with torch.cuda.stream(stream):
@@ -50,9 +51,11 @@ def time_plan(M, N, K, xs, ws, ys, stream, iters=20):
                 return None
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
+    with torch.cuda.stream(stream):
+        g.capture_begin()
         for x, w, y in zip(xs, ws, ys):
             sk.skinny_gemm_bf16(x.data_ptr(), K, w.data_ptr(), K, y.data_ptr(), N, M, N, K, sh)
+        g.capture_end()
     with torch.cuda.stream(stream):
         for _ in range(3):
             g.replay()
@@ -81,12 +84,17 @@ def tune_shape(K, N, m_values, l2_bytes, pdl, log):
         best = None
         results = []
         for c in candidates(M, K):
+            t0 = time.perf_counter()
             with sk.options(pdl=pdl, **c):
                 try:
                     us = time_plan(M, N, K, xs, ws, ys, stream)
                 except sk.SkinnyError:
                     us = None
-            if us is None:
+            wall = time.perf_counter() - t0
+            status = sk.skinny_get_device_status()
+            log.write(json.dumps({"K": K, "N": N, "M": M, "cand": c, "us": us, "wall_s": round(wall, 3),
+                                  "status": status}) + "\n")
+            if us is None or status != 0:
                 continue
             results.append((us, c))
             if best is None or us < best[0]:
@@ -102,16 +110,19 @@ def tune_shape(K, N, m_values, l2_bytes, pdl, log):
     return rows
 
 
-def merge_rows(K, N, rows):
-    """Consecutive M with identical winning plans -> one table line."""
+def merge_rows(K, N, rows, m_max=16):
+    """Winners of consecutive tuned M values (in order) that agree -> one table
+    line; each line's M range reaches up to the next line's first M, so the
+    lines cover every M from the first tuned one to m_max."""
     lines = []
     i = 0
     while i < len(rows):
         j = i
-        while j + 1 < len(rows) and rows[j + 1][1] == rows[i][1] and rows[j + 1][0] == rows[j][0] + 1:
+        while j + 1 < len(rows) and rows[j + 1][1] == rows[i][1]:
             j += 1
         c = rows[i][1]
-        lines.append((K, N, rows[i][0], rows[j][0], c["backend"], c["consumer"], c["split_k"], c["block_n"],
+        m_hi = rows[j + 1][0] - 1 if j + 1 < len(rows) else m_max
+        lines.append((K, N, rows[i][0], m_hi, c["backend"], c["consumer"], c["split_k"], c["block_n"],
                       c["stages"], [round(r[2], 2) for r in rows[i:j + 1]]))
         i = j + 1
     return lines
@@ -120,20 +131,25 @@ def merge_rows(K, N, rows):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--shapes", default=",".join(DEFAULT_SHAPES))
-    ap.add_argument("--m", default="1-16")
+    ap.add_argument("--m", default="1-16", help="M values for the router shapes (a-b range or list)")
+    ap.add_argument("--m-large", default="1,2,3,4,6,8,12,16", help="M values for shapes with W > 16 MB")
     ap.add_argument("--pdl", type=int, default=1)
     ap.add_argument("--out", default="-")
     ap.add_argument("--log", default=None)
     a = ap.parse_args(argv)
-    lo, hi = (int(v) for v in a.m.split("-")) if "-" in a.m else (int(a.m), int(a.m))
-    m_values = list(range(lo, hi + 1))
+    def parse_m(spec):
+        if "-" in spec:
+            lo, hi = (int(v) for v in spec.split("-"))
+            return list(range(lo, hi + 1))
+        return [int(v) for v in spec.split(",")]
+    m_small, m_large = parse_m(a.m), parse_m(a.m_large)
     assert sk.skinny_init(0) == sk.SKINNY_OK
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     log = open(a.log, "a") if a.log else sys.stderr
     out_lines = []
     for shp in a.shapes.split(","):
         K, N = (int(v) for v in shp.lower().split("x"))
-        rows = tune_shape(K, N, m_values, l2, a.pdl, log)
+        rows = tune_shape(K, N, m_large if 2 * N * K > 16e6 else m_small, l2, a.pdl, log)
         for (k, n, mlo, mhi, be, co, sp, bn, st, us) in merge_rows(K, N, rows):
             out_lines.append(f"{{{k}, {n}, {mlo}, {mhi}, {be}, {co}, {sp}, {bn}, {st}}},  // us/call {us}")
     text = "\n".join(out_lines) + "\n"

@@ -155,7 +155,7 @@ def test_forced_options_and_restore():
 
 @pytest.mark.parametrize("opt,bad", [(sk.SKINNY_OPT_PDL, 2), (sk.SKINNY_OPT_FORCE_BACKEND, 3),
                                      (sk.SKINNY_OPT_FORCE_SPLIT_K, 9), (sk.SKINNY_OPT_FORCE_BLOCK_N, 3),
-                                     (sk.SKINNY_OPT_FORCE_STAGES, 9), (sk.SKINNY_OPT_WAIT_TIMEOUT_US, -1),
+                                     (sk.SKINNY_OPT_FORCE_STAGES, 17), (sk.SKINNY_OPT_WAIT_TIMEOUT_US, -1),
                                      (99, 0)])
 def test_option_values_are_checked(opt, bad):
     with pytest.raises(sk.SkinnyError):
@@ -168,3 +168,31 @@ def test_every_workload_case_has_a_plan():
         p = plan(c.M, c.N, c.K, ldy=c.ly)
         assert p["smem_bytes"] <= 227 * 1024
         assert p["grid_x"] >= 1 and p["grid_y"] >= 1
+
+
+def _table_entries():
+    path = os.path.join(ROOT, "latency_skinny_bf16_gb300", "csrc", "tuning_table.inc")
+    out = []
+    with open(path) as f:
+        for line in f:
+            line = line.split("//", 1)[0].strip()
+            if line.startswith("{"):
+                vals = [int(v) for v in line.strip("{},").split(",")]
+                out.append(vals)
+    return out
+
+
+def test_every_tuned_entry_is_a_supported_plan_and_is_used():
+    for K, N, m_lo, m_hi, be, co, s, bn, st in _table_entries():
+        assert 1 <= m_lo <= m_hi <= 16
+        for M in range(m_lo, m_hi + 1):
+            p = plan(M, N, K)
+            assert p["tuned"] == 1, (K, N, M)
+            assert p["backend"] == be
+            if be == sk.SKINNY_BACKEND_SPLITK:
+                assert (p["consumer"], p["split_k"]) == (co, s)
+                if st:
+                    assert p["stages"] == st
+            else:
+                assert p["block_n"] == bn
+            assert p["smem_bytes"] <= 227 * 1024

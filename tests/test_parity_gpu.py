@@ -114,6 +114,7 @@ def test_every_variant(case):
             assert st == sk.SKINNY_OK, (v, sk.skinny_status_string(st))
             check_parity(b.y_mat(), yref, A, f"{case.name} {v}")
             assert b.canary_ok(), v
+            assert sk.skinny_get_device_status() == 0, v     # no bounded wait gave up
             ran += 1
     assert ran >= len(_variants(case)) // 2
 
@@ -317,8 +318,10 @@ def test_tensor_wrapper():
 
 
 @pytest.mark.parametrize("cons", [sk.SKINNY_CONSUMER_FMA, sk.SKINNY_CONSUMER_MMA])
-@pytest.mark.parametrize("split,clusters,stages", [(1, 3, 2), (1, 7, 8), (2, 5, 4), (4, 2, 3), (8, 3, 2)])
-def test_persistent_clusters(cons, split, clusters, stages):
+@pytest.mark.parametrize("split,clusters,stages,stage_k", [
+    (1, 3, 2, 0), (1, 7, 8, 0), (2, 5, 4, 0), (4, 2, 3, 0), (8, 3, 2, 0), (8, 2, 16, 0), (4, 3, 16, 0),
+    (1, 2, 16, 0), (1, 3, 4, 1024), (2, 5, 3, 512), (8, 2, 2, 64), (1, 4, 2, 2048), (4, 3, 5, 192)])
+def test_persistent_clusters(cons, split, clusters, stages, stage_k):
     """Clusters that loop over several 16-row tiles (tile = y, y + C, ...): the
     ring streams across tile boundaries and the DSMEM slots alternate between
     two buffers, one cluster-barrier phase per tile."""
@@ -326,10 +329,12 @@ def test_persistent_clusters(cons, split, clusters, stages):
     X, W = si.make_inputs(case)
     yref, A = reference(case, X, W)
     with sk.options(backend=sk.SKINNY_BACKEND_SPLITK, consumer=cons, split_k=split, clusters=clusters,
-                    stages=stages):
+                    stages=stages, stage_k=stage_k):
         b = Buffers(case, X, W, ldy=case.N + 9)
         p = b.plan()
         assert (p["grid_x"], p["grid_y"]) == (split, clusters)
+        if stage_k:
+            assert p["stage_k"] == stage_k
         first = None
         for _ in range(3):
             assert b.run() == sk.SKINNY_OK
