@@ -196,3 +196,16 @@ def test_every_tuned_entry_is_a_supported_plan_and_is_used():
             else:
                 assert p["block_n"] == bn
             assert p["smem_bytes"] <= 227 * 1024
+
+
+def test_forced_gpu_test_plans_fit_on_gb300():
+    """Every forced persistent split-K configuration the GPU tests run plans on a
+    152-SM GB300 (so a GPU run never spends its time on a refused plan)."""
+    import test_parity_gpu as tp
+    for cons in (sk.SKINNY_CONSUMER_FMA, sk.SKINNY_CONSUMER_MMA):
+        for split, clusters, stages, stage_k in tp.PERSISTENT_CFGS:
+            c = tp.persistent_case(cons, split)
+            with sk.options(backend=sk.SKINNY_BACKEND_SPLITK, consumer=cons, split_k=split, clusters=clusters,
+                            stages=stages, stage_k=stage_k):
+                p = plan(c.M, c.N, c.K, ldy=c.N + 9)
+            assert (p["grid_x"], p["grid_y"]) == (split, clusters)

@@ -317,21 +317,32 @@ def test_tensor_wrapper():
         sk.gemm(torch.zeros(17, 2048, dtype=torch.bfloat16, device="cuda"), w)
 
 
+PERSISTENT_CFGS = [  # (split_k, clusters, stages, stage_k)
+    (1, 3, 2, 0), (1, 7, 8, 256), (2, 5, 4, 0), (4, 2, 3, 0), (8, 3, 2, 0), (8, 2, 16, 0), (4, 3, 16, 0),
+    (1, 2, 10, 256), (1, 3, 2, 1024), (2, 5, 3, 512), (8, 2, 2, 64), (2, 4, 2, 2048), (4, 3, 5, 192)]
+
+
+def persistent_case(cons, split):
+    return si.Case("pers", M=11 if cons == sk.SKINNY_CONSUMER_MMA else 6, N=16 * 13 + 5, K=4096, seed=900 + split)
+
+
 @pytest.mark.parametrize("cons", [sk.SKINNY_CONSUMER_FMA, sk.SKINNY_CONSUMER_MMA])
-@pytest.mark.parametrize("split,clusters,stages,stage_k", [
-    (1, 3, 2, 0), (1, 7, 8, 0), (2, 5, 4, 0), (4, 2, 3, 0), (8, 3, 2, 0), (8, 2, 16, 0), (4, 3, 16, 0),
-    (1, 2, 16, 0), (1, 3, 4, 1024), (2, 5, 3, 512), (8, 2, 2, 64), (1, 4, 2, 2048), (4, 3, 5, 192)])
+@pytest.mark.parametrize("split,clusters,stages,stage_k", PERSISTENT_CFGS)
 def test_persistent_clusters(cons, split, clusters, stages, stage_k):
     """Clusters that loop over several 16-row tiles (tile = y, y + C, ...): the
     ring streams across tile boundaries and the DSMEM slots alternate between
     two buffers, one cluster-barrier phase per tile."""
-    case = si.Case("pers", M=11 if cons == sk.SKINNY_CONSUMER_MMA else 6, N=16 * 13 + 5, K=4096, seed=900 + split)
+    case = persistent_case(cons, split)
     X, W = si.make_inputs(case)
     yref, A = reference(case, X, W)
     with sk.options(backend=sk.SKINNY_BACKEND_SPLITK, consumer=cons, split_k=split, clusters=clusters,
                     stages=stages, stage_k=stage_k):
         b = Buffers(case, X, W, ldy=case.N + 9)
-        p = b.plan()
+        try:
+            p = b.plan()
+        except sk.SkinnyError as e:      # a forced plan that does not fit shared memory
+            assert e.status == sk.SKINNY_ERR_UNSUPPORTED and b.run() == sk.SKINNY_ERR_UNSUPPORTED
+            pytest.skip("forced plan does not fit shared memory")
         assert (p["grid_x"], p["grid_y"]) == (split, clusters)
         if stage_k:
             assert p["stage_k"] == stage_k
