@@ -50,7 +50,7 @@ WORKLOAD_DESC = {
     "projection": "decode projections: M in {1,2,3,8,16} x (N,K) in {(2112,7168),(24576,1536),(7168,14336)}, "
                   "ldy=N+64, 15 calls",
 }
-KERNEL_SOURCES = ["api.cu", "dotprod.cu", "splitk.cu", "common.cuh", "internal.h", "tuning_table.inc"]
+KERNEL_SOURCES = ["api.cu", "dotprod.cu", "dotmma.cu", "splitk.cu", "common.cuh", "internal.h", "tuning_table.inc"]
 
 
 def parse_args(argv=None):
@@ -490,7 +490,7 @@ def main(argv=None):
     fam_time, fam_bytes, fam_n = {}, {}, {}
     per_shape = []
     for c, p, us in zip(cases, r["plans"], r["per_launch"]):
-        fam = "dotprod" if p["backend"] == 1 else "splitk"
+        fam = ("dotmma" if p["consumer"] == 2 else "dotprod") if p["backend"] == 1 else "splitk"
         fam_time[fam] = fam_time.get(fam, 0.0) + us
         fam_bytes[fam] = fam_bytes.get(fam, 0.0) + c.algorithmic_bytes
         fam_n[fam] = fam_n.get(fam, 0) + 1

@@ -68,13 +68,14 @@ typedef enum {
 typedef enum {
     SKINNY_CONSUMER_AUTO = 0,
     SKINNY_CONSUMER_FMA = 1,        /* CUDA-core fp32 fused multiply-add */
-    SKINNY_CONSUMER_MMA = 2         /* mma.sync m16n8k16 bf16 -> fp32, W on the MMA's M side */
+    SKINNY_CONSUMER_MMA = 2         /* mma.sync m16n8k16 bf16 -> fp32, W on the MMA's M side
+                                       (split-K, or the dot-product layout with block_n 16/32/64) */
 } skinny_consumer_t;
 
 /* The launch a call would make.  Filled by skinny_query_plan / skinny_plan_for. */
 typedef struct {
     int backend;       /* skinny_backend_t actually used */
-    int consumer;      /* skinny_consumer_t actually used (split-K only; dot-product is FMA) */
+    int consumer;      /* skinny_consumer_t actually used (FMA or MMA, for either backend) */
     int vec_elems;     /* W load width in bf16 elements: 8 (128-bit), 4, 2 or 1 */
     int block_n;       /* output columns (rows of W) per CTA tile */
     int split_k;       /* CTAs per cluster along K (1 = no cluster) */
@@ -95,7 +96,7 @@ typedef enum {
     SKINNY_OPT_FORCE_BACKEND = 2,    /* skinny_backend_t; AUTO = dispatcher (tests / tuning only) */
     SKINNY_OPT_FORCE_CONSUMER = 3,   /* skinny_consumer_t for split-K; AUTO = dispatcher */
     SKINNY_OPT_FORCE_SPLIT_K = 4,    /* 0 = dispatcher, 1..8 = cluster size */
-    SKINNY_OPT_FORCE_BLOCK_N = 5,    /* 0 = dispatcher; dot-product 1/2/4/8, split-K 16/64 */
+    SKINNY_OPT_FORCE_BLOCK_N = 5,    /* 0 = dispatcher; dot-product FMA 1/2/4/8, MMA 16/32/64; split-K 16 */
     SKINNY_OPT_FORCE_STAGES = 6,     /* 0 = dispatcher, 1..16 */
     SKINNY_OPT_WAIT_TIMEOUT_US = 7,  /* budget of each bounded wait in a kernel, microseconds
                                         (default 500000).  0 makes every such wait give up at once,

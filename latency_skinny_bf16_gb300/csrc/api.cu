@@ -78,7 +78,8 @@ skinny_status_t init_device_current(DeviceState &d, int device) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         return SKINNY_ERR_NO_DEVICE;
     if (major != 10 || minor != 3) return SKINNY_ERR_NO_DEVICE;   // built for sm_103a only
-    if (dotprod_prepare() != cudaSuccess || splitk_prepare() != cudaSuccess) return SKINNY_ERR_LAUNCH;
+    if (dotprod_prepare() != cudaSuccess || dotmma_prepare() != cudaSuccess || splitk_prepare() != cudaSuccess)
+        return SKINNY_ERR_LAUNCH;
     void *sym = nullptr;
     if (cudaGetSymbolAddress(&sym, g_status_word) != cudaSuccess) return SKINNY_ERR_LAUNCH;
     d.num_sms = sms;
@@ -157,6 +158,7 @@ int pow2_floor(int v) { int p = 1; while (p * 2 <= v) p *= 2; return p; }
 
 constexpr int kDotXBudget = 96 * 1024;     // X bytes staged per dot-product CTA
 constexpr int kSplitXBudget = 160 * 1024;  // X slice bytes per split-K CTA
+constexpr int kMmaXBudget = 64 * 1024;     // X bytes staged per tensor-core dot-product CTA (3 CTAs / SM)
 
 bool plan_dotprod(int M, int N, int K, int vec, int force_bn, int num_sms, skinny_plan_t *p) {
     int bn = force_bn;
@@ -187,6 +189,35 @@ bool plan_dotprod(int M, int N, int K, int vec, int force_bn, int num_sms, skinn
     p->grid_y = 1;
     p->threads = kDotThreads;
     p->smem_bytes = dotprod_smem_bytes(M, bn, kc);
+    return p->smem_bytes <= kMaxDynSmem;
+}
+
+// Dot-product layout with mma.sync arithmetic: block_n = 16 * row tiles.
+bool plan_dotmma(int M, int N, int K, int vec, int force_bn, int num_sms, skinny_plan_t *p) {
+    if (vec != 8 || K % 32 != 0 || K < 32) return false;
+    int bn = force_bn;
+    if (bn == 0) {
+        // enough CTAs for every SM, fewer X re-reads when N is large
+        bn = 16;
+        while (bn < 64 && (N + 2 * bn - 1) / (2 * bn) >= 2 * num_sms) bn *= 2;
+    }
+    if (!dotmma_supported(M, bn)) return false;
+    const int MT = M <= 8 ? 8 : 16;
+    int kc = (kMmaXBudget / (2 * MT)) & ~31;
+    if (kc >= K) kc = K;
+    if (kc < 32) kc = 32;
+    p->backend = SKINNY_BACKEND_DOTPROD;
+    p->consumer = SKINNY_CONSUMER_MMA;
+    p->vec_elems = 8;
+    p->block_n = bn;
+    p->split_k = 1;
+    p->stages = 0;
+    p->stage_k = 0;
+    p->k_chunk = kc;
+    p->grid_x = (N + bn - 1) / bn;
+    p->grid_y = 1;
+    p->threads = kDotThreads;
+    p->smem_bytes = dotmma_smem_bytes(M, bn, kc);
     return p->smem_bytes <= kMaxDynSmem;
 }
 
@@ -221,12 +252,8 @@ bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int fo
         const int nchunks = (ks + bk - 1) / bk;
         int stages = force_stages;
         if (stages == 0) {
-            if (nchunks <= 8) {
-                stages = nchunks < 1 ? 1 : nchunks;
-            } else {
-                stages = kSplitMaxStages;
-                while (stages > 2 && splitk_smem_bytes(M, consumer, 16, stages, ks, S, bk) > kMaxDynSmem) --stages;
-            }
+            stages = nchunks <= 8 ? (nchunks < 1 ? 1 : nchunks) : kSplitMaxStages;
+            while (stages > 2 && splitk_smem_bytes(M, consumer, 16, stages, ks, S, bk) > kMaxDynSmem) --stages;
         }
         if (stages < 1 || stages > kSplitMaxStages) return false;
         const int smem = splitk_smem_bytes(M, consumer, 16, stages, ks, S, bk);
@@ -280,24 +307,38 @@ skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int n
 
     int backend = fb, consumer = fc, split = fs, bn = fbn, stages = fst;
     int tuned = 0;
+    const bool dotmma_ok = splitk_ok && K % 32 == 0;
     if (backend == SKINNY_BACKEND_AUTO) {
         const TunedEntry *e = lookup_tuned(M, N, K);
-        if (e && (e->backend == SKINNY_BACKEND_DOTPROD || splitk_ok) &&
-            (e->consumer != SKINNY_CONSUMER_MMA || mma_ok)) {
+        const bool entry_ok =
+            e && ((e->backend == SKINNY_BACKEND_DOTPROD && e->consumer != SKINNY_CONSUMER_MMA) ||
+                  (e->backend == SKINNY_BACKEND_DOTPROD && e->consumer == SKINNY_CONSUMER_MMA && dotmma_ok) ||
+                  (e->backend == SKINNY_BACKEND_SPLITK && splitk_ok &&
+                   (e->consumer != SKINNY_CONSUMER_MMA || mma_ok)));
+        if (entry_ok) {
             backend = e->backend;
             if (consumer == SKINNY_CONSUMER_AUTO) consumer = e->consumer;
             if (!split) split = e->split_k;
             if (!bn) bn = e->block_n;
             if (!stages) stages = e->stages;
             tuned = 1;
+        } else if (dotmma_ok && M >= 4 && 2.0 * N * K >= 16e6) {
+            // default rule, bandwidth-bound weights (>= 16 MB): tensor-core dot-product
+            backend = SKINNY_BACKEND_DOTPROD;
+            if (consumer == SKINNY_CONSUMER_AUTO) consumer = SKINNY_CONSUMER_MMA;
         } else {
             // default rule: dot-product for small M or short K, else split-K
             backend = (M <= 4 || K < 2048 || !splitk_ok) ? SKINNY_BACKEND_DOTPROD : SKINNY_BACKEND_SPLITK;
         }
     }
     bool ok;
-    if (backend == SKINNY_BACKEND_DOTPROD) {
-        if (fc == SKINNY_CONSUMER_MMA) return SKINNY_ERR_UNSUPPORTED;
+    if (backend == SKINNY_BACKEND_DOTPROD && consumer == SKINNY_CONSUMER_MMA) {
+        ok = plan_dotmma(M, N, K, vec, bn, num_sms, p);
+        if (!ok && fb == SKINNY_BACKEND_AUTO && fc == SKINNY_CONSUMER_AUTO) {
+            ok = plan_dotprod(M, N, K, vec, 0, num_sms, p);
+            tuned = 0;
+        }
+    } else if (backend == SKINNY_BACKEND_DOTPROD) {
         if (vec != 8 && bn > 1 && fbn) return SKINNY_ERR_UNSUPPORTED;
         ok = plan_dotprod(M, N, K, vec, vec == 8 ? bn : 1, num_sms, p);
     } else if (backend == SKINNY_BACKEND_SPLITK) {
@@ -361,7 +402,11 @@ skinny_status_t skinny_gemm_bf16(const uint16_t *X, int ldx, const uint16_t *W, 
     if (opt_log()) log_plan(M, N, K, ldw, plan);
     GemmArgs a{X, ldx, W, ldw, Y, ldy, M, N, K};
     LaunchCtx c{s, plan.pdl != 0, d.status_word, (uint64_t)g_opt_wait_us.load() * 1000ull};
-    cudaError_t e = (plan.backend == SKINNY_BACKEND_DOTPROD) ? launch_dotprod(a, plan, c) : launch_splitk(a, plan, c);
+    cudaError_t e;
+    if (plan.backend == SKINNY_BACKEND_DOTPROD)
+        e = plan.consumer == SKINNY_CONSUMER_MMA ? launch_dotmma(a, plan, c) : launch_dotprod(a, plan, c);
+    else
+        e = launch_splitk(a, plan, c);
     return e == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
 }
 
@@ -405,7 +450,8 @@ skinny_status_t skinny_set_option(int option, int value) {
             if (value < 0 || value > kSplitMaxCluster) return SKINNY_ERR_INVALID_VALUE;
             g_opt_force_split_k.store(value); return SKINNY_OK;
         case SKINNY_OPT_FORCE_BLOCK_N:
-            if (!(value == 0 || value == 1 || value == 2 || value == 4 || value == 8 || value == 16))
+            if (!(value == 0 || value == 1 || value == 2 || value == 4 || value == 8 || value == 16 ||
+                  value == 32 || value == 64))
                 return SKINNY_ERR_INVALID_VALUE;
             g_opt_force_block_n.store(value); return SKINNY_OK;
         case SKINNY_OPT_FORCE_STAGES:

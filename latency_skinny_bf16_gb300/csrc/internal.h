@@ -33,6 +33,12 @@ bool dotprod_supported(int M, int vec_elems, int block_n);
 cudaError_t dotprod_prepare();   // per-device kernel attributes
 cudaError_t launch_dotprod(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
 
+// ---- dot-product backend with mma.sync arithmetic (dotmma.cu): block_n 16/32/64
+int dotmma_smem_bytes(int M, int block_n, int k_chunk);
+bool dotmma_supported(int M, int block_n);
+cudaError_t dotmma_prepare();
+cudaError_t launch_dotmma(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
+
 // ---- cluster split-K backend (splitk.cu)
 constexpr int kSplitConsumerWarps = 4;
 constexpr int kSplitThreads = (kSplitConsumerWarps + 1) * 32;  // + one producer warp

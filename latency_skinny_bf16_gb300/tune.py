@@ -32,6 +32,9 @@ def candidates(M: int, K: int):
     out = []
     for bn in (1, 2, 4, 8):
         out.append(dict(backend=1, block_n=bn, consumer=0, split_k=0, stages=0))
+    if K % 32 == 0:
+        for bn in (16, 32, 64):
+            out.append(dict(backend=1, block_n=bn, consumer=2, split_k=0, stages=0))
     for cons in (1, 2):
         if cons == 2 and K % 16:
             continue

@@ -209,3 +209,12 @@ def test_forced_gpu_test_plans_fit_on_gb300():
                             stages=stages, stage_k=stage_k):
                 p = plan(c.M, c.N, c.K, ldy=c.N + 9)
             assert (p["grid_x"], p["grid_y"]) == (split, clusters)
+
+
+def test_projection_shapes_at_large_m_take_a_fitting_splitk_plan():
+    # a one-shot ring that would not fit shared memory is shortened, not dropped
+    for (N, K) in ((7168, 14336), (2112, 7168)):
+        for M in (5, 8, 16):
+            with sk.options(backend=sk.SKINNY_BACKEND_SPLITK):
+                p = plan(M, N, K, ldy=N + 64)
+            assert p["backend"] == sk.SKINNY_BACKEND_SPLITK and p["smem_bytes"] <= 227 * 1024
