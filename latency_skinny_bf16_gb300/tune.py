@@ -121,10 +121,18 @@ def merge_rows(K, N, rows, m_max=16):
     i = 0
     while i < len(rows):
         j = i
-        while j + 1 < len(rows) and rows[j + 1][1] == rows[i][1]:
+        # M <= 8 and M > 8 use different kernels (8- vs 16-token MMA tiles,
+        # different X footprints), so a line never crosses that boundary
+        while (j + 1 < len(rows) and rows[j + 1][1] == rows[i][1]
+               and (rows[j + 1][0] <= 8) == (rows[i][0] <= 8)):
             j += 1
         c = rows[i][1]
-        m_hi = rows[j + 1][0] - 1 if j + 1 < len(rows) else m_max
+        if j + 1 < len(rows):
+            m_hi = rows[j + 1][0] - 1
+            if rows[i][0] <= 8 < rows[j + 1][0]:
+                m_hi = min(m_hi, 8)
+        else:
+            m_hi = m_max
         lines.append((K, N, rows[i][0], m_hi, c["backend"], c["consumer"], c["split_k"], c["block_n"],
                       c["stages"], [round(r[2], 2) for r in rows[i:j + 1]]))
         i = j + 1
@@ -135,7 +143,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--shapes", default=",".join(DEFAULT_SHAPES))
     ap.add_argument("--m", default="1-16", help="M values for the router shapes (a-b range or list)")
-    ap.add_argument("--m-large", default="1,2,3,4,6,8,12,16", help="M values for shapes with W > 16 MB")
+    ap.add_argument("--m-large", default="1,2,3,4,6,8,9,12,16", help="M values for shapes with W > 16 MB")
     ap.add_argument("--pdl", type=int, default=1)
     ap.add_argument("--out", default="-")
     ap.add_argument("--log", default=None)

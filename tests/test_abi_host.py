@@ -90,20 +90,22 @@ def plan(M, N, K, ldw=None, W=B16, num_sms=152, X=A16, ldx=None, Y=C16, ldy=None
     return sk.skinny_plan_for(X, ldx or K, W, ldw or K, Y, ldy or N, M, N, K, num_sms)
 
 
+# shapes below are not in the tuning table, so they exercise the default rule
 def test_default_rule_dotprod_small_m_or_short_k():
     for M in (1, 2, 3, 4):
-        assert plan(M, 256, 7168)["backend"] == sk.SKINNY_BACKEND_DOTPROD
+        assert plan(M, 320, 7168)["backend"] == sk.SKINNY_BACKEND_DOTPROD
+        assert plan(M, 320, 7168)["tuned"] == 0
     assert plan(8, 256, 1024)["backend"] == sk.SKINNY_BACKEND_DOTPROD   # K < 2048
 
 
 def test_default_rule_splitk_larger_m():
     for M in (5, 8, 12, 16):
-        p = plan(M, 256, 7168)
+        p = plan(M, 256, 7200)
         assert p["backend"] == sk.SKINNY_BACKEND_SPLITK
         assert 1 <= p["split_k"] <= 8 and p["grid_x"] == p["split_k"]
         assert p["grid_y"] == 16 and p["block_n"] == 16
         assert p["smem_bytes"] <= 227 * 1024
-        assert p["split_k"] * p["k_chunk"] >= 7168 and p["k_chunk"] % 16 == 0
+        assert p["split_k"] * p["k_chunk"] >= 7200 and p["k_chunk"] % 16 == 0
 
 
 def test_vector_width_follows_alignment():
@@ -122,8 +124,14 @@ def test_misaligned_weights_never_take_splitk():
 
 
 def test_dotprod_block_n_grows_with_n():
-    assert plan(1, 256, 7168)["block_n"] == 1
-    assert plan(1, 24576, 1536)["block_n"] == 8
+    assert plan(1, 256, 7200)["block_n"] == 1
+    assert plan(1, 24576, 1504)["block_n"] == 8
+
+
+def test_default_rule_tensor_core_dotprod_for_large_weights():
+    p = plan(8, 8192, 4096)          # 64 MB of W, not tuned
+    assert (p["backend"], p["consumer"]) == (sk.SKINNY_BACKEND_DOTPROD, sk.SKINNY_CONSUMER_MMA)
+    assert p["block_n"] in (16, 32, 64) and p["grid_x"] * p["block_n"] >= 8192
     p = plan(2, 2112, 7168)
     assert p["grid_x"] * p["block_n"] >= 2112
 

@@ -20,3 +20,10 @@ def test_merge_rows_merges_consecutive_equal_winners():
     # ranges cover 1..16: a gap (M=6 not tuned) goes to the line before it
     assert [(l[2], l[3], l[4]) for l in lines] == [(1, 1, 1), (2, 4, 2), (5, 6, 1), (7, 16, 2)]
     assert lines[1][9] == [3.5, 3.6, 3.7]
+
+
+def test_merge_rows_never_crosses_the_8_token_boundary():
+    a = dict(backend=2, consumer=2, split_k=1, stages=0, block_n=0)
+    rows = [(3, a, 8.7), (8, a, 9.1), (12, a, 13.0), (16, a, 13.6)]
+    lines = tune.merge_rows(7168, 2112, rows)
+    assert [(l[2], l[3]) for l in lines] == [(3, 8), (12, 16)]   # M 9..11 left to the default rule
