@@ -50,7 +50,8 @@ WORKLOAD_DESC = {
     "projection": "decode projections: M in {1,2,3,8,16} x (N,K) in {(2112,7168),(24576,1536),(7168,14336)}, "
                   "ldy=N+64, 15 calls",
 }
-KERNEL_SOURCES = ["api.cu", "dotprod.cu", "dotmma.cu", "splitk.cu", "common.cuh", "internal.h", "tuning_table.inc"]
+# the device code: DRAM traffic measured by ncu stays valid while these are unchanged
+KERNEL_SOURCES = ["dotprod.cu", "dotmma.cu", "splitk.cu", "common.cuh", "internal.h"]
 
 
 def parse_args(argv=None):

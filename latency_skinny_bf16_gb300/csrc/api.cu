@@ -134,11 +134,11 @@ skinny_status_t validate(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
 // ------------------------------------------------------------------ dispatcher
 struct TunedEntry {
     int K, N, m_lo, m_hi;
-    int backend, consumer, split_k, block_n, stages;
+    int backend, consumer, split_k, block_n, stages, stage_k;
 };
 const TunedEntry kTuned[] = {
 #include "tuning_table.inc"
-    {0, 0, 0, 0, 0, 0, 0, 0, 0}};
+    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0}};
 
 const TunedEntry *lookup_tuned(int M, int N, int K) {
     for (const TunedEntry &e : kTuned)
@@ -242,12 +242,21 @@ bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int fo
         const int xrows = consumer == SKINNY_CONSUMER_MMA ? (M <= 8 ? 8 : 16) : M;
         const int xbytes = xrows * (((ks * 2 + 127) & ~127) + 16);
         if (xbytes > kSplitXBudget && !force_s) continue;
-        // Ring chunk: 256 K elements when the whole slice fits a ring of up to 8
-        // such stages (one shot: every W byte requested at kernel start);
-        // otherwise stream 1024-element (2 KB per W row) chunks, which keeps each
-        // row's reads contiguous in DRAM.
+        // Ring chunk: 256 K elements when the whole slice of a single tile fits a
+        // ring of up to 8 such stages (one shot: every W byte requested at kernel
+        // start); when streaming (persistent clusters or long slices) chunks of
+        // up to 1024 elements (2 KB per W row) keep each row's reads contiguous
+        // in DRAM.
         int bk = force_bk;
-        if (bk == 0) bk = ((ks + kSplitBK - 1) / kSplitBK <= 8) ? kSplitBK : kSplitStreamBK;
+        if (bk == 0) {
+            const bool persistent = (long long)tiles * S > 2LL * num_sms;
+            if (!persistent && (ks + kSplitBK - 1) / kSplitBK <= 8) {
+                bk = kSplitBK;
+            } else {
+                bk = ((ks + 63) / 64) * 64;       // whole slice per stage when it is short
+                if (bk > kSplitStreamBK) bk = kSplitStreamBK;
+            }
+        }
         if (bk < 64 || bk > kSplitMaxBK || bk % 64) return false;
         const int nchunks = (ks + bk - 1) / bk;
         int stages = force_stages;
@@ -305,7 +314,7 @@ skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int n
     const bool mma_ok = splitk_ok && K % 16 == 0;
     const int pdl = opt_pdl();
 
-    int backend = fb, consumer = fc, split = fs, bn = fbn, stages = fst;
+    int backend = fb, consumer = fc, split = fs, bn = fbn, stages = fst, stage_k = g_opt_force_stage_k.load();
     int tuned = 0;
     const bool dotmma_ok = splitk_ok && K % 32 == 0;
     if (backend == SKINNY_BACKEND_AUTO) {
@@ -321,6 +330,7 @@ skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int n
             if (!split) split = e->split_k;
             if (!bn) bn = e->block_n;
             if (!stages) stages = e->stages;
+            if (!stage_k) stage_k = e->stage_k;
             tuned = 1;
         } else if (dotmma_ok && M >= 4 && 2.0 * N * K >= 16e6) {
             // default rule, bandwidth-bound weights (>= 16 MB): tensor-core dot-product
@@ -344,7 +354,7 @@ skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int n
     } else if (backend == SKINNY_BACKEND_SPLITK) {
         if (consumer == SKINNY_CONSUMER_AUTO) consumer = (M > 4 && mma_ok) ? SKINNY_CONSUMER_MMA : SKINNY_CONSUMER_FMA;
         if (bn != 0 && bn != 16) return SKINNY_ERR_UNSUPPORTED;
-        ok = plan_splitk(M, N, K, vec, consumer, split, stages, fgy, g_opt_force_stage_k.load(), num_sms, p);
+        ok = plan_splitk(M, N, K, vec, consumer, split, stages, fgy, stage_k, num_sms, p);
         if (!ok && fb == SKINNY_BACKEND_AUTO) {
             // a tuned split-K entry that these pointers / strides cannot use
             ok = plan_dotprod(M, N, K, vec, 0, num_sms, p);

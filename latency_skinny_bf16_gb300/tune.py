@@ -1,12 +1,15 @@
 """Measure every supported plan per (K, N, M) and write the dispatcher's table.
 
-For one call shape, each candidate plan (dot-product with each block_n, split-K
-with each consumer / cluster size / ring depth) is forced through the library
-options and timed L2-cold: a CUDA graph of R back-to-back calls over R distinct
-copies of W (together more than 2x the L2 size) is replayed, and the time per
-call is taken from CUDA events on the launching stream.  The fastest plan of
-each shape becomes one line of ``csrc/tuning_table.inc``; consecutive M with
-the same winner are merged into one range.
+For one call shape, each candidate plan (dot-product with FMA or MMA and each
+block_n, split-K with each consumer / cluster size / ring depth / ring chunk)
+is forced through the library options and timed L2-cold: a CUDA graph of R
+back-to-back calls over R distinct copies of W (together more than 2x the L2
+size) is replayed, and the time per call is taken from CUDA events on the
+launching stream.  Each candidate is timed twice: with programmatic dependent
+launch (consecutive identical calls overlap) and without (each call runs on its
+own, as when its neighbours in a decode step are other kernels); the score is
+the mean of the two.  The best-scoring plan of each shape becomes one line of
+``csrc/tuning_table.inc``; consecutive M with the same winner are merged.
 
     python -m latency_skinny_bf16_gb300.tune --shapes 7168x256,7168x384 --out table.inc
 
@@ -28,19 +31,25 @@ import latency_skinny_bf16_gb300 as sk
 DEFAULT_SHAPES = ["7168x256", "7168x384", "2880x128", "4096x256", "7168x2112", "1536x24576", "14336x7168"]
 
 
-def candidates(M: int, K: int):
+def candidates(M: int, K: int, N: int = 0):
     out = []
     for bn in (1, 2, 4, 8):
-        out.append(dict(backend=1, block_n=bn, consumer=0, split_k=0, stages=0))
+        out.append(dict(backend=1, block_n=bn, consumer=0, split_k=0, stages=0, stage_k=0))
     if K % 32 == 0:
         for bn in (16, 32, 64):
-            out.append(dict(backend=1, block_n=bn, consumer=2, split_k=0, stages=0))
+            out.append(dict(backend=1, block_n=bn, consumer=2, split_k=0, stages=0, stage_k=0))
+    big = 2 * N * K > 16e6
     for cons in (1, 2):
         if cons == 2 and K % 16:
             continue
-        for s in (1, 2, 4, 6, 8):
-            for stages in (0, 4, 16):      # 0: the dispatcher's ring depth for this shape
-                out.append(dict(backend=2, consumer=cons, split_k=s, stages=stages, block_n=0))
+        if big:
+            for s in (1, 2, 4, 8):
+                for bk in (0, 512, 2048):      # 0: the dispatcher's ring chunk for this shape
+                    out.append(dict(backend=2, consumer=cons, split_k=s, stages=0, block_n=0, stage_k=bk))
+        else:
+            for s in (2, 4, 6, 8):
+                for stages in (0, 4):          # 0: the dispatcher's ring depth for this shape
+                    out.append(dict(backend=2, consumer=cons, split_k=s, stages=stages, block_n=0, stage_k=0))
     return out
 
 
@@ -86,17 +95,22 @@ def tune_shape(K, N, m_values, l2_bytes, pdl, log):
         ys = [torch.empty(M, N, device="cuda") for _ in range(reps)]
         best = None
         results = []
-        for c in candidates(M, K):
+        for c in candidates(M, K, N):
             t0 = time.perf_counter()
-            with sk.options(pdl=pdl, **c):
+            with sk.options(pdl=1, **c):
                 try:
-                    us = time_plan(M, N, K, xs, ws, ys, stream)
+                    us_pdl = time_plan(M, N, K, xs, ws, ys, stream)
                 except sk.SkinnyError:
-                    us = None
+                    us_pdl = None
+            us_iso = None
+            if us_pdl is not None:
+                with sk.options(pdl=0, **c):
+                    us_iso = time_plan(M, N, K, xs, ws, ys, stream)
+            us = None if (us_pdl is None or us_iso is None) else 0.5 * (us_pdl + us_iso)
             wall = time.perf_counter() - t0
             status = sk.skinny_get_device_status()
-            log.write(json.dumps({"K": K, "N": N, "M": M, "cand": c, "us": us, "wall_s": round(wall, 3),
-                                  "status": status}) + "\n")
+            log.write(json.dumps({"K": K, "N": N, "M": M, "cand": c, "us": us, "us_pdl": us_pdl, "us_iso": us_iso,
+                                  "wall_s": round(wall, 3), "status": status}) + "\n")
             if us is None or status != 0:
                 continue
             results.append((us, c))
@@ -134,7 +148,7 @@ def merge_rows(K, N, rows, m_max=16):
         else:
             m_hi = m_max
         lines.append((K, N, rows[i][0], m_hi, c["backend"], c["consumer"], c["split_k"], c["block_n"],
-                      c["stages"], [round(r[2], 2) for r in rows[i:j + 1]]))
+                      c["stages"], c.get("stage_k", 0), [round(r[2], 2) for r in rows[i:j + 1]]))
         i = j + 1
     return lines
 
@@ -144,7 +158,6 @@ def main(argv=None):
     ap.add_argument("--shapes", default=",".join(DEFAULT_SHAPES))
     ap.add_argument("--m", default="1-16", help="M values for the router shapes (a-b range or list)")
     ap.add_argument("--m-large", default="1,2,3,4,6,8,9,12,16", help="M values for shapes with W > 16 MB")
-    ap.add_argument("--pdl", type=int, default=1)
     ap.add_argument("--out", default="-")
     ap.add_argument("--log", default=None)
     a = ap.parse_args(argv)
@@ -160,9 +173,9 @@ def main(argv=None):
     out_lines = []
     for shp in a.shapes.split(","):
         K, N = (int(v) for v in shp.lower().split("x"))
-        rows = tune_shape(K, N, m_large if 2 * N * K > 16e6 else m_small, l2, a.pdl, log)
-        for (k, n, mlo, mhi, be, co, sp, bn, st, us) in merge_rows(K, N, rows):
-            out_lines.append(f"{{{k}, {n}, {mlo}, {mhi}, {be}, {co}, {sp}, {bn}, {st}}},  // us/call {us}")
+        rows = tune_shape(K, N, m_large if 2 * N * K > 16e6 else m_small, l2, None, log)
+        for (k, n, mlo, mhi, be, co, sp, bn, st, bk, us) in merge_rows(K, N, rows):
+            out_lines.append(f"{{{k}, {n}, {mlo}, {mhi}, {be}, {co}, {sp}, {bn}, {st}, {bk}}},  // us/call {us}")
     text = "\n".join(out_lines) + "\n"
     if a.out == "-":
         sys.stdout.write(text)

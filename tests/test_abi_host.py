@@ -191,7 +191,7 @@ def _table_entries():
 
 
 def test_every_tuned_entry_is_a_supported_plan_and_is_used():
-    for K, N, m_lo, m_hi, be, co, s, bn, st in _table_entries():
+    for K, N, m_lo, m_hi, be, co, s, bn, st, bk in _table_entries():
         assert 1 <= m_lo <= m_hi <= 16
         for M in range(m_lo, m_hi + 1):
             p = plan(M, N, K)
@@ -201,8 +201,10 @@ def test_every_tuned_entry_is_a_supported_plan_and_is_used():
                 assert (p["consumer"], p["split_k"]) == (co, s)
                 if st:
                     assert p["stages"] == st
+                if bk:
+                    assert p["stage_k"] == bk
             else:
-                assert p["block_n"] == bn
+                assert p["block_n"] == bn and p["consumer"] == (co if co else sk.SKINNY_CONSUMER_FMA)
             assert p["smem_bytes"] <= 227 * 1024
 
 

@@ -19,7 +19,7 @@ def test_merge_rows_merges_consecutive_equal_winners():
     lines = tune.merge_rows(7168, 256, rows)
     # ranges cover 1..16: a gap (M=6 not tuned) goes to the line before it
     assert [(l[2], l[3], l[4]) for l in lines] == [(1, 1, 1), (2, 4, 2), (5, 6, 1), (7, 16, 2)]
-    assert lines[1][9] == [3.5, 3.6, 3.7]
+    assert lines[1][10] == [3.5, 3.6, 3.7]
 
 
 def test_merge_rows_never_crosses_the_8_token_boundary():
