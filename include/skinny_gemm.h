@@ -136,6 +136,24 @@ SKINNY_API skinny_status_t skinny_gemm_bf16(const uint16_t *X, int ldx,
                                  float *Y, int ldy,
                                  int M, int N, int K, void *stream);
 
+/*
+ * As skinny_gemm_bf16, but Y is bf16 (uint16_t bit patterns, 2-byte aligned,
+ * row stride ldy >= N): each output is the same fp32 result the fp32 entry
+ * point computes with the same plan, rounded once to the nearest bf16 (ties to
+ * even).  The inputs, plans, checks and errors are those of skinny_gemm_bf16
+ * (Y misaligned = not 2-byte aligned; the overlap check uses 2-byte elements).
+ *
+ * Defined by: "[Perf][Feat] Add generic cuteDSL LL BF16 router (GEMM)",
+ * section "Review highlights" (the output type is hard-coded to Float32, noted
+ * there as a limitation to lift), and "GLM-5.2 Blackwell decode optimizations",
+ * Implementation breakdown item 3 (bf16 decode projections, whose consumers
+ * take bf16 activations).
+ */
+SKINNY_API skinny_status_t skinny_gemm_bf16_bf16out(const uint16_t *X, int ldx,
+                                         const uint16_t *W, int ldw,
+                                         uint16_t *Y, int ldy,
+                                         int M, int N, int K, void *stream);
+
 /* Optional: prepare `device` (query it, check it is sm_103, set kernel
  * attributes, find the status word).  The first call on a device does the
  * same; calling this first keeps that work out of a CUDA-graph capture.

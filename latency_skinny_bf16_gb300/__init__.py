@@ -20,7 +20,7 @@ from . import _build
 
 __all__ = [
     "SkinnyError", "load_library", "library_path",
-    "skinny_gemm_bf16", "skinny_init", "skinny_query_plan", "skinny_plan_for",
+    "skinny_gemm_bf16", "skinny_gemm_bf16_bf16out", "skinny_init", "skinny_query_plan", "skinny_plan_for",
     "skinny_set_option", "skinny_get_option", "skinny_get_device_status",
     "skinny_status_string", "skinny_version", "gemm", "options",
 ]
@@ -54,7 +54,7 @@ SKINNY_OPT_FORCE_CLUSTERS = 9
 SKINNY_OPT_FORCE_STAGE_K = 10
 
 EXPORTED_SYMBOLS = (
-    "skinny_gemm_bf16", "skinny_init", "skinny_query_plan", "skinny_plan_for",
+    "skinny_gemm_bf16", "skinny_gemm_bf16_bf16out", "skinny_init", "skinny_query_plan", "skinny_plan_for",
     "skinny_set_option", "skinny_get_option", "skinny_get_device_status",
     "skinny_status_string", "skinny_version",
 )
@@ -90,6 +90,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     vp, i = ctypes.c_void_p, ctypes.c_int
     lib.skinny_gemm_bf16.argtypes = [vp, i, vp, i, vp, i, i, i, i, vp]
     lib.skinny_gemm_bf16.restype = i
+    lib.skinny_gemm_bf16_bf16out.argtypes = [vp, i, vp, i, vp, i, i, i, i, vp]
+    lib.skinny_gemm_bf16_bf16out.restype = i
     lib.skinny_init.argtypes = [i]
     lib.skinny_init.restype = i
     lib.skinny_query_plan.argtypes = [vp, i, vp, i, vp, i, i, i, i, ctypes.POINTER(_Plan)]
@@ -131,6 +133,12 @@ def skinny_gemm_bf16(X: int, ldx: int, W: int, ldw: int, Y: int, ldy: int,
                      M: int, N: int, K: int, stream: int = 0) -> int:
     """Raw C call: device pointers as ints; returns the skinny_status_t."""
     return load_library().skinny_gemm_bf16(X, ldx, W, ldw, Y, ldy, M, N, K, stream)
+
+
+def skinny_gemm_bf16_bf16out(X: int, ldx: int, W: int, ldw: int, Y: int, ldy: int,
+                             M: int, N: int, K: int, stream: int = 0) -> int:
+    """Raw C call with a bf16 Y (bit patterns); returns the skinny_status_t."""
+    return load_library().skinny_gemm_bf16_bf16out(X, ldx, W, ldw, Y, ldy, M, N, K, stream)
 
 
 def skinny_init(device: int = 0) -> int:
@@ -215,8 +223,8 @@ class options:
 
 def gemm(x, w, out=None, stream=None):
     """``out[:M, :N] = x . w^T`` for CUDA tensors: x bf16 [M, K], w bf16 [N, K]
-    (unit stride along K), out fp32 [M, N] (any row stride >= N, unit column
-    stride).  Runs on ``stream`` (default: torch's current stream)."""
+    (unit stride along K), out fp32 or bf16 [M, N] (any row stride >= N, unit
+    column stride; bf16 is the fp32 result rounded to nearest-even).  Runs on ``stream`` (default: torch's current stream)."""
     import torch
     if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
         raise TypeError("x and w must be bfloat16")
@@ -230,8 +238,8 @@ def gemm(x, w, out=None, stream=None):
         raise ValueError("x and w need unit stride along K")
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    if out.dtype != torch.float32 or out.dim() != 2 or tuple(out.shape) != (M, N):
-        raise ValueError("out must be fp32 [M, N]")
+    if out.dtype not in (torch.float32, torch.bfloat16) or out.dim() != 2 or tuple(out.shape) != (M, N):
+        raise ValueError("out must be fp32 or bf16 [M, N]")
     if N > 1 and out.stride(1) != 1:
         raise ValueError("out needs unit column stride")
     if stream is None:
@@ -240,7 +248,8 @@ def gemm(x, w, out=None, stream=None):
     ldx = x.stride(0) if M > 1 else max(K, 1)
     ldw = w.stride(0) if N > 1 else max(K, 1)
     ldy = out.stride(0) if M > 1 else max(N, 1)
-    st = skinny_gemm_bf16(x.data_ptr(), ldx, w.data_ptr(), ldw, out.data_ptr(), ldy, M, N, K, s)
+    call = skinny_gemm_bf16 if out.dtype == torch.float32 else skinny_gemm_bf16_bf16out
+    st = call(x.data_ptr(), ldx, w.data_ptr(), ldw, out.data_ptr(), ldy, M, N, K, s)
     if st != SKINNY_OK:
         raise SkinnyError(st, "skinny_gemm_bf16")
     return out

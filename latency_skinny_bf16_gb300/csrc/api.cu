@@ -25,12 +25,14 @@ namespace {
 // ------------------------------------------------------------------ device status word
 __device__ int g_status_word;
 
-__global__ void zero_fill_kernel(float *Y, int64_t ldy, int M, int N) {
+// K == 0: Y is the empty sum, +0 (fp32 or bf16 bits).
+__global__ void zero_fill_kernel(void *Y, int64_t ldy, int M, int N, int out_bf16) {
     const int64_t total = (int64_t)M * N;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t m = i / N, n = i - m * N;
-        Y[m * ldy + n] = 0.f;
+        if (out_bf16) static_cast<uint16_t *>(Y)[m * ldy + n] = 0;
+        else static_cast<float *>(Y)[m * ldy + n] = 0.f;
     }
 }
 
@@ -110,19 +112,20 @@ skinny_status_t current_device(int *device) {
 bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
 
 // Host-only validation; no CUDA call.  *noop is set when there is nothing to launch.
-skinny_status_t validate(const uint16_t *X, int ldx, const uint16_t *W, int ldw, const float *Y, int ldy,
-                         int M, int N, int K, bool *noop) {
+// y_bytes: size of one Y element (4 for fp32, 2 for bf16).
+skinny_status_t validate(const uint16_t *X, int ldx, const uint16_t *W, int ldw, const void *Y, int ldy,
+                         int M, int N, int K, bool *noop, int y_bytes = 4) {
     *noop = false;
     if (M < 0 || N < 0 || K < 0) return SKINNY_ERR_INVALID_VALUE;
     if (M > SKINNY_MAX_M) return SKINNY_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) { *noop = true; return SKINNY_OK; }
     if (Y == nullptr || ldy < N) return SKINNY_ERR_INVALID_VALUE;
-    if (reinterpret_cast<uintptr_t>(Y) & 3) return SKINNY_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(Y) & (uintptr_t)(y_bytes - 1)) return SKINNY_ERR_MISALIGNED;
     if (K == 0) return SKINNY_OK;
     if (X == nullptr || W == nullptr || ldx < K || ldw < K) return SKINNY_ERR_INVALID_VALUE;
     if ((reinterpret_cast<uintptr_t>(X) & 1) || (reinterpret_cast<uintptr_t>(W) & 1)) return SKINNY_ERR_MISALIGNED;
     const uintptr_t y0 = reinterpret_cast<uintptr_t>(Y);
-    const uintptr_t y1 = y0 + (uintptr_t)(((int64_t)(M - 1) * ldy + N) * 4);
+    const uintptr_t y1 = y0 + (uintptr_t)(((int64_t)(M - 1) * ldy + N) * y_bytes);
     const uintptr_t x0 = reinterpret_cast<uintptr_t>(X);
     const uintptr_t x1 = x0 + (uintptr_t)(((int64_t)(M - 1) * ldx + K) * 2);
     const uintptr_t w0 = reinterpret_cast<uintptr_t>(W);
@@ -242,27 +245,26 @@ bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int fo
         const int xrows = consumer == SKINNY_CONSUMER_MMA ? (M <= 8 ? 8 : 16) : M;
         const int xbytes = xrows * (((ks * 2 + 127) & ~127) + 16);
         if (xbytes > kSplitXBudget && !force_s) continue;
-        // Ring chunk: 256 K elements when the whole slice of a single tile fits a
-        // ring of up to 8 such stages (one shot: every W byte requested at kernel
-        // start); when streaming (persistent clusters or long slices) chunks of
-        // up to 1024 elements (2 KB per W row) keep each row's reads contiguous
-        // in DRAM.
-        int bk = force_bk;
-        if (bk == 0) {
-            const bool persistent = (long long)tiles * S > 2LL * num_sms;
-            if (!persistent && (ks + kSplitBK - 1) / kSplitBK <= 8) {
-                bk = kSplitBK;
-            } else {
-                bk = ((ks + 63) / 64) * 64;       // whole slice per stage when it is short
-                if (bk > kSplitStreamBK) bk = kSplitStreamBK;
-            }
-        }
+        // Ring chunk: each W row of a chunk is one bulk copy, and the copy
+        // engine's cost is per copy (~50 ns each on GB300, measured), so
+        // chunks are as long as possible: the whole slice (up to 2048 elements,
+        // 4 KB per row) in one stage when a cluster owns a single tile (one
+        // shot: every W byte requested at kernel start), and up to 2048-element
+        // chunks when persistent clusters stream many tiles.
+        int bk = force_bk ? force_bk : ((ks + 63) / 64) * 64;
+        if (!force_bk && bk > kSplitMaxBK) bk = kSplitMaxBK;
         if (bk < 64 || bk > kSplitMaxBK || bk % 64) return false;
-        const int nchunks = (ks + bk - 1) / bk;
-        int stages = force_stages;
-        if (stages == 0) {
-            stages = nchunks <= 8 ? (nchunks < 1 ? 1 : nchunks) : kSplitMaxStages;
-            while (stages > 2 && splitk_smem_bytes(M, consumer, 16, stages, ks, S, bk) > kMaxDynSmem) --stages;
+        int stages = 0;
+        for (;;) {
+            // one shot when the slice is at most 8 chunks, else the deepest ring
+            // that fits; if even 2 stages do not fit, halve the chunk
+            const int nchunks = (ks + bk - 1) / bk;
+            stages = force_stages ? force_stages : (nchunks <= 8 ? (nchunks < 1 ? 1 : nchunks) : kSplitMaxStages);
+            while (!force_stages && stages > 2 && splitk_smem_bytes(M, consumer, 16, stages, ks, S, bk) > kMaxDynSmem)
+                --stages;
+            if (splitk_smem_bytes(M, consumer, 16, stages, ks, S, bk) <= kMaxDynSmem) break;
+            if (force_bk || bk <= kSplitBK) break;
+            bk = ((bk / 2 + 63) / 64) * 64;
         }
         if (stages < 1 || stages > kSplitMaxStages) return false;
         const int smem = splitk_smem_bytes(M, consumer, 16, stages, ks, S, bk);
@@ -387,12 +389,13 @@ void log_plan(int M, int N, int K, int ldw, const skinny_plan_t &p) {
 
 using namespace skinny;
 
-extern "C" {
-
-skinny_status_t skinny_gemm_bf16(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
-                                 float *Y, int ldy, int M, int N, int K, void *stream) {
+namespace skinny {
+namespace {
+// One call: checks, plan, launch.  out_bf16 selects a bf16 Y (2-byte elements).
+skinny_status_t run_gemm(const uint16_t *X, int ldx, const uint16_t *W, int ldw, void *Y, int ldy,
+                         int M, int N, int K, void *stream, int out_bf16) {
     bool noop = false;
-    skinny_status_t st = validate(X, ldx, W, ldw, Y, ldy, M, N, K, &noop);
+    skinny_status_t st = validate(X, ldx, W, ldw, Y, ldy, M, N, K, &noop, out_bf16 ? 2 : 4);
     if (st != SKINNY_OK || noop) return st;
     int device = 0;
     st = current_device(&device);
@@ -403,14 +406,14 @@ skinny_status_t skinny_gemm_bf16(const uint16_t *X, int ldx, const uint16_t *W, 
         const int64_t total = (int64_t)M * N;
         int blocks = (int)((total + 255) / 256);
         if (blocks > 4 * d.num_sms) blocks = 4 * d.num_sms;
-        zero_fill_kernel<<<blocks, 256, 0, s>>>(Y, ldy, M, N);
+        zero_fill_kernel<<<blocks, 256, 0, s>>>(Y, ldy, M, N, out_bf16);
         return cudaPeekAtLastError() == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
     }
     skinny_plan_t plan;
     st = make_plan(W, ldw, M, N, K, d.num_sms, &plan);
     if (st != SKINNY_OK) return st;
     if (opt_log()) log_plan(M, N, K, ldw, plan);
-    GemmArgs a{X, ldx, W, ldw, Y, ldy, M, N, K};
+    GemmArgs a{X, ldx, W, ldw, Y, ldy, M, N, K, out_bf16};
     LaunchCtx c{s, plan.pdl != 0, d.status_word, (uint64_t)g_opt_wait_us.load() * 1000ull};
     cudaError_t e;
     if (plan.backend == SKINNY_BACKEND_DOTPROD)
@@ -418,6 +421,20 @@ skinny_status_t skinny_gemm_bf16(const uint16_t *X, int ldx, const uint16_t *W, 
     else
         e = launch_splitk(a, plan, c);
     return e == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
+}
+}  // namespace
+}  // namespace skinny
+
+extern "C" {
+
+skinny_status_t skinny_gemm_bf16(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
+                                 float *Y, int ldy, int M, int N, int K, void *stream) {
+    return run_gemm(X, ldx, W, ldw, Y, ldy, M, N, K, stream, 0);
+}
+
+skinny_status_t skinny_gemm_bf16_bf16out(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
+                                         uint16_t *Y, int ldy, int M, int N, int K, void *stream) {
+    return run_gemm(X, ldx, W, ldw, Y, ldy, M, N, K, stream, 1);
 }
 
 skinny_status_t skinny_init(int device) { return ensure_device(device); }

@@ -17,6 +17,19 @@ __device__ __forceinline__ float bf16_lo(uint32_t pair) { return __uint_as_float
 __device__ __forceinline__ float bf16_hi(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16_one(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
 
+// ------------------------------------------------------------------ output store
+// Y is fp32, or bf16 when out_bf16: the fp32 result rounded once to the
+// nearest bf16 (ties to even) by the hardware conversion.
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
+    unsigned short r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ void store_y(void *Y, int out_bf16, int64_t idx, float v) {
+    if (out_bf16) static_cast<uint16_t *>(Y)[idx] = f32_to_bf16_rn(v);
+    else static_cast<float *>(Y)[idx] = v;
+}
+
 // ------------------------------------------------------------------ global loads
 // W is streamed exactly once per call: read-only path, no L1 allocation.
 __device__ __forceinline__ uint4 ldg_stream_v4(const void *p) {

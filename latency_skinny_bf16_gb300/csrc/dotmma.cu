@@ -48,8 +48,8 @@ template <int MT, int RT>
 __global__ void __launch_bounds__(kDotThreads)
 dotmma_kernel(const uint16_t *__restrict__ X, int64_t ldx,
               const uint16_t *__restrict__ W, int64_t ldw,
-              float *__restrict__ Y, int64_t ldy,
-              int M, int N, int K, int kc, int x_vec16, int *status, uint64_t budget_ns)
+              void *__restrict__ Y, int64_t ldy,
+              int M, int N, int K, int kc, int x_vec16, int *status, uint64_t budget_ns, int out_bf16)
 {
     constexpr int P = kWarps / RT;    // K parts per row tile
     constexpr int NT = MT / 8;        // n8 token tiles
@@ -184,13 +184,13 @@ dotmma_kernel(const uint16_t *__restrict__ X, int64_t ldx,
             float v = red[((tl * P + 0) * 16 + row) * MT + m];
 #pragma unroll
             for (int pp = 1; pp < P; ++pp) v += red[((tl * P + pp) * 16 + row) * MT + m];
-            Y[m * ldy + n] = v;
+            store_y(Y, out_bf16, m * ldy + n, v);
         }
     }
 }
 
-using MmaKernel = void (*)(const uint16_t *, int64_t, const uint16_t *, int64_t, float *, int64_t,
-                           int, int, int, int, int, int *, uint64_t);
+using MmaKernel = void (*)(const uint16_t *, int64_t, const uint16_t *, int64_t, void *, int64_t,
+                           int, int, int, int, int, int *, uint64_t, int);
 
 const MmaKernel kTable[2][3] = {
     {&dotmma_kernel<8, 1>, &dotmma_kernel<8, 2>, &dotmma_kernel<8, 4>},
@@ -235,7 +235,7 @@ cudaError_t launch_dotmma(const GemmArgs &a, const skinny_plan_t &p, const Launc
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fn, a.X, a.ldx, a.W, a.ldw, a.Y, a.ldy, a.M, a.N, a.K, p.k_chunk, x_vec16,
-                              c.status, c.budget_ns);
+                              c.status, c.budget_ns, a.out_bf16);
 }
 
 }  // namespace skinny

@@ -105,8 +105,8 @@ template <int MT, int VW, int BN>
 __global__ void __launch_bounds__(kDotThreads)
 dotprod_kernel(const uint16_t *__restrict__ X, int64_t ldx,
                const uint16_t *__restrict__ W, int64_t ldw,
-               float *__restrict__ Y, int64_t ldy,
-               int N, int K, int kc, int x_vec16, int *status, uint64_t budget_ns)
+               void *__restrict__ Y, int64_t ldy,
+               int N, int K, int kc, int x_vec16, int *status, uint64_t budget_ns, int out_bf16)
 {
     // Loads in flight per thread per step: U vectors of each of the BN rows.
     constexpr int U = (BN >= 8) ? 1 : 8 / BN;
@@ -280,14 +280,14 @@ dotprod_kernel(const uint16_t *__restrict__ X, int64_t ldx,
             float s = red[m * BN + r];
 #pragma unroll
             for (int w = 1; w < kWarps; ++w) s += red[(w * MT + m) * BN + r];
-            Y[m * ldy + n] = s;
+            store_y(Y, out_bf16, m * ldy + n, s);
         }
     }
 }
 
 // ------------------------------------------------------------------ instantiation table
-using DotKernel = void (*)(const uint16_t *, int64_t, const uint16_t *, int64_t, float *, int64_t,
-                           int, int, int, int, int *, uint64_t);
+using DotKernel = void (*)(const uint16_t *, int64_t, const uint16_t *, int64_t, void *, int64_t,
+                           int, int, int, int, int *, uint64_t, int);
 
 template <int MT, int VW, int BN> constexpr DotKernel kfn() { return &dotprod_kernel<MT, VW, BN>; }
 
@@ -347,7 +347,7 @@ cudaError_t launch_dotprod(const GemmArgs &a, const skinny_plan_t &p, const Laun
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fn, a.X, a.ldx, a.W, a.ldw, a.Y, a.ldy, a.N, a.K, p.k_chunk, x_vec16, c.status,
-                              c.budget_ns);
+                              c.budget_ns, a.out_bf16);
 }
 
 }  // namespace skinny

@@ -14,9 +14,10 @@ struct GemmArgs {
     int64_t ldx;
     const uint16_t *W;
     int64_t ldw;
-    float *Y;
+    void *Y;             // fp32, or bf16 bits when out_bf16
     int64_t ldy;
     int M, N, K;
+    int out_bf16;
 };
 
 struct LaunchCtx {

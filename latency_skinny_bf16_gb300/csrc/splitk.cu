@@ -79,7 +79,7 @@ __host__ __device__ inline Layout make_layout(int MT, int consumer, int stages, 
 struct SplitParams {
     const uint16_t *X; int64_t ldx;
     const uint16_t *W; int64_t ldw;
-    float *Y; int64_t ldy;
+    void *Y; int64_t ldy;   // fp32, or bf16 bits when out_bf16
     int M, N, K;
     int KS;            // K elements per rank (multiple of 16)
     int bk;            // K elements per ring stage (multiple of 64, <= 2048)
@@ -87,6 +87,7 @@ struct SplitParams {
     int x_vec16;       // X rows 16-byte aligned (vector staging)
     int *status;
     uint64_t budget_ns;
+    int out_bf16;
 };
 
 // Bounded wait used when draining: also stops early once the producer has
@@ -354,7 +355,7 @@ splitk_kernel(const SplitParams p)
             auto emit = [&](int m, int c, float v) {
                 if (m >= p.M || c >= rows) return;
                 if (S == 1) {
-                    p.Y[m * p.ldy + n0 + c] = v;
+                    store_y(p.Y, p.out_bf16, m * p.ldy + n0 + c, v);
                 } else {
                     const uint32_t local = slot_buf + (uint32_t)(((rank * MT + m) * kBN + c) * 4);
                     st_shared_cluster_f32(mapa_shared(local, (uint32_t)(c % S)), v);
@@ -410,7 +411,7 @@ splitk_kernel(const SplitParams p)
                     if (m < p.M && c < rows && (c % S) == rank) {
                         float v = sl[(0 * MT + m) * kBN + c];
                         for (int r = 1; r < S; ++r) v += sl[(r * MT + m) * kBN + c];
-                        p.Y[m * p.ldy + n0 + c] = v;
+                        store_y(p.Y, p.out_bf16, m * p.ldy + n0 + c, v);
                     }
                 }
             }
@@ -467,6 +468,7 @@ cudaError_t launch_splitk(const GemmArgs &a, const skinny_plan_t &pl, const Laun
     p.x_vec16 = ((reinterpret_cast<uintptr_t>(a.X) & 15) == 0 && (a.ldx & 7) == 0) ? 1 : 0;
     p.status = c.status;
     p.budget_ns = c.budget_ns;
+    p.out_bf16 = a.out_bf16;
     SplitKernel fn = (pl.consumer == SKINNY_CONSUMER_MMA) ? kMma[a.M <= 8 ? 0 : 1] : kFma[a.M - 1];
 
     cudaLaunchConfig_t cfg = {};

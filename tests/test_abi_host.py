@@ -228,3 +228,24 @@ def test_projection_shapes_at_large_m_take_a_fitting_splitk_plan():
             with sk.options(backend=sk.SKINNY_BACKEND_SPLITK):
                 p = plan(M, N, K, ldy=N + 64)
             assert p["backend"] == sk.SKINNY_BACKEND_SPLITK and p["smem_bytes"] <= 227 * 1024
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(Y=C16 + 1), sk.SKINNY_ERR_MISALIGNED),      # bf16 Y: 2-byte alignment
+    (dict(Y=B16 + 1024), sk.SKINNY_ERR_INVALID_VALUE),  # overlaps W (2-byte elements)
+    (dict(M=17), sk.SKINNY_ERR_UNSUPPORTED),
+    (dict(ldy=31), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(M=0), sk.SKINNY_OK),
+])
+def test_bf16_output_argument_errors(kw, expect):
+    args = dict(X=A16, ldx=64, W=B16, ldw=64, Y=C16, ldy=32, M=4, N=32, K=64)
+    args.update(kw)
+    assert sk.skinny_gemm_bf16_bf16out(args["X"], args["ldx"], args["W"], args["ldw"], args["Y"], args["ldy"],
+                                       args["M"], args["N"], args["K"], 0) == expect
+
+
+def test_bf16_output_two_byte_aligned_y_passes_the_checks():
+    # C16 + 2 is misaligned for fp32 Y but fine for bf16 Y
+    assert call(Y=C16 + 2) == sk.SKINNY_ERR_MISALIGNED
+    st = sk.skinny_gemm_bf16_bf16out(A16, 64, B16, 64, C16 + 2, 32, 4, 32, 64, 0)
+    assert st in (sk.SKINNY_OK, sk.SKINNY_ERR_NO_DEVICE)

@@ -375,3 +375,62 @@ def test_persistent_clusters(cons, split, clusters, stages, stage_k):
                 assert np.array_equal(y.view(np.uint32), first.view(np.uint32))
         assert b.canary_ok()
     assert sk.skinny_get_device_status() == 0
+
+
+# ---------------------------------------------------------------- bf16 output
+
+def _bf16_round(y32: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 round-to-nearest-even by PyTorch's conversion, as bit patterns."""
+    return torch.from_numpy(np.ascontiguousarray(y32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+BF16_SHAPES = [si.Case("b_router", M=4, N=256, K=7168, seed=1101),
+               si.Case("b_ragged", M=9, N=37, K=2880, seed=1102),
+               si.Case("b_odd", M=3, N=50, K=1001, seed=1103, x_dist="normal", w_dist="normal", outliers=True)]
+
+
+@pytest.mark.parametrize("case", BF16_SHAPES, ids=_ids(BF16_SHAPES))
+def test_bf16_output_every_variant(case):
+    """bf16 Y is the fp32 result of the same plan rounded once to nearest-even:
+    bit-exact against the fp32 entry point's output rounded by PyTorch, and
+    within the fp32 bound plus one bf16 ulp of the oracle.  Gaps untouched."""
+    X, W = si.make_inputs(case)
+    yref, A = reference(case, X, W)
+    ldy = case.N + 5
+    for v in _variants(case):
+        with sk.options(**v):
+            b = Buffers(case, X, W, ldy=ldy)
+            st = b.run()
+            if st == sk.SKINNY_ERR_UNSUPPORTED:
+                continue
+            assert st == sk.SKINNY_OK
+            y32 = b.y_mat().copy()
+            yb = torch.full((case.M * ldy + 16,), 0x7FC1, dtype=torch.int16, device="cuda")   # canary: a NaN pattern
+            st = sk.skinny_gemm_bf16_bf16out(b.x_ptr, b.ldx, b.w_ptr, b.ldw, yb.data_ptr(), ldy, case.M, case.N,
+                                             case.K, 0)
+            assert st == sk.SKINNY_OK, v
+            torch.cuda.synchronize()
+            ybits = yb.cpu().numpy().view(np.uint16)
+            body = ybits[: case.M * ldy].reshape(case.M, ldy)
+            assert np.array_equal(body[:, : case.N], _bf16_round(y32)), v
+            assert np.all(body[:, case.N:] == 0x7FC1) and np.all(ybits[case.M * ldy:] == 0x7FC1), v
+            yv = (body[:, : case.N].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            fin = np.isfinite(yref)
+            err = np.abs(yv[fin] - yref[fin])
+            assert np.all(err <= 1e-5 * A[fin] + 1e-6 + 2.0 ** -8 * np.abs(yref[fin])), v
+    assert sk.skinny_get_device_status() == 0
+
+
+def test_bf16_output_k_zero_and_wrapper():
+    yb = torch.full((3, 9), 7.0, dtype=torch.bfloat16, device="cuda")
+    assert sk.skinny_gemm_bf16_bf16out(0, 0, 0, 0, yb.data_ptr(), 9, 3, 8, 0, 0) == sk.SKINNY_OK
+    torch.cuda.synchronize()
+    assert torch.all(yb[:, :8] == 0) and torch.all(yb[:, 8] == 7.0)
+    case = si.Case("bw", M=6, N=300, K=2048, seed=1104)
+    X, W = si.make_inputs(case)
+    x = torch.from_numpy(X.view(np.int16)).cuda().view(torch.bfloat16)
+    w = torch.from_numpy(W.view(np.int16)).cuda().view(torch.bfloat16)
+    out32 = sk.gemm(x, w)
+    out16 = sk.gemm(x, w, out=torch.empty(6, 300, dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(out16, out32.to(torch.bfloat16))
