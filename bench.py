@@ -49,6 +49,8 @@ WORKLOAD_DESC = {
     "splitk": "split-K regime: M in {5,8,12,16} x (K,N) in {(7168,256),(7168,384),(4096,256)}, 12 calls",
     "projection": "decode projections: M in {1,2,3,8,16} x (N,K) in {(2112,7168),(24576,1536),(7168,14336)}, "
                   "ldy=N+64, 15 calls",
+    "midm": "medium-M decode regime (split-K MMA): M in {17,24,32,40,64} x (K,N) in {(7168,256),(4096,384)}, "
+            "M in {17,32,64} x (N,K) in {(2112,7168),(24576,1536)}, M in {17,32} x (7168,14336), 18 calls",
 }
 # the device code: DRAM traffic measured by ncu stays valid while these are unchanged
 KERNEL_SOURCES = ["dotprod.cu", "dotmma.cu", "splitk.cu", "common.cuh", "internal.h"]
@@ -366,7 +368,8 @@ def run_native(args):
         x_host[off:off + c.M * c.K] = torch.from_numpy(X.reshape(-1).view(np.int16).copy())
         off += c.M * c.K
     x_dev = torch.empty_like(x_host, device="cuda")
-    y_dev = torch.empty(y_host.numel(), dtype=torch.float32, device="cuda")
+    # zeros like the replicas' Y, so the never-written gaps of a strided Y compare equal
+    y_dev = torch.zeros(y_host.numel(), dtype=torch.float32, device="cuda")
     e2e_graphs = []
     for r in reps:
         g = torch.cuda.CUDAGraph()

@@ -1,7 +1,7 @@
 /*
  * skinny_gemm.h -- C ABI of the GB300 (sm_103a) low-latency skinny BF16 GEMM.
  *
- *     Y[m][n] = sum_k  X[m][k] * W[n][k]      0 <= m < M <= 16,  0 <= n < N
+ *     Y[m][n] = sum_k  X[m][k] * W[n][k]      0 <= m < M <= 64,  0 <= n < N
  *
  * X is [M, K] bf16, W is [N, K] bf16 (a weight, e.g. the MoE router's
  * [experts, hidden] matrix or a decode projection's [out, in] matrix), both
@@ -18,6 +18,17 @@
  * optimizations" (vllm PR #48597), section "Implementation breakdown" item 3
  * (bf16_skinny_gemm for the decode projections, strided output) and item 2
  * (programmatic dependent launch).
+ *
+ * Token range.  M = 1..16 is the router tier of the first page; every
+ * backend takes it.  M = 17..64 is the medium-M regime that the second page
+ * (item 3) hands to a separate fused GEMM before falling back to cuBLAS; here
+ * it runs on the cluster split-K backend with the mma.sync consumer only
+ * (the tokens become 2 or 4 groups of 16 on the MMA's N side), so it needs
+ * K % 16 == 0, 16-byte aligned W rows (W and ldw), and a per-CTA X slice
+ * (tokens rounded up to 32 or 64, x K / split_k x 2 bytes, split_k <= 8) of
+ * at most 160 KB that fits in shared memory beside the W ring: at 64 tokens
+ * K = 7168 runs, K = 14336 does not.  Other M > 16 shapes return
+ * SKINNY_ERR_UNSUPPORTED.
  *
  * bf16 values are passed as their 16-bit patterns (uint16_t) so this header
  * needs no CUDA header.  Streams are passed as `void*` holding a cudaStream_t
@@ -40,7 +51,7 @@
 extern "C" {
 #endif
 
-#define SKINNY_MAX_M 16
+#define SKINNY_MAX_M 64
 
 /* Exported from libskinny_gemm.so (built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -52,7 +63,8 @@ extern "C" {
 typedef enum {
     SKINNY_OK = 0,
     SKINNY_ERR_INVALID_VALUE = 1,   /* negative size, ld too small, NULL with work to do, Y overlaps X or W */
-    SKINNY_ERR_UNSUPPORTED = 2,     /* M > 16, or a forced plan that cannot run this shape */
+    SKINNY_ERR_UNSUPPORTED = 2,     /* M > 64; M > 16 on a shape the split-K MMA path cannot
+                                       take; or a forced plan that cannot run this shape */
     SKINNY_ERR_MISALIGNED = 3,      /* X or W not 2-byte aligned, Y not 4-byte aligned */
     SKINNY_ERR_LAUNCH = 4,          /* the CUDA launch failed (cudaGetLastError after the launch) */
     SKINNY_ERR_DEVICE_TIMEOUT = 5,  /* a bounded wait inside a kernel gave up (see skinny_get_device_status) */
@@ -117,7 +129,8 @@ typedef enum {
  *   W      device pointer, bf16 [N, K], row stride ldw >= K (elements), 2-byte aligned
  *   Y      device pointer, fp32 [M, N], row stride ldy >= N (elements), 4-byte aligned;
  *          must not overlap X or W.  Only Y[m*ldy + n], m < M, n < N, is written.
- *   M      1..16 tokens (0 is a no-op); N, K >= 0.  K == 0 writes zeros (the empty sum).
+ *   M      1..64 tokens (0 is a no-op; 17..64 only on the shapes listed under "Token
+ *          range" above); N, K >= 0.  K == 0 writes zeros (the empty sum).
  *
  * 16-byte alignment is not required: the dispatcher picks the widest W load
  * that the base pointer and ldw allow (see skinny_plan_t.vec_elems).

@@ -1,7 +1,8 @@
 """GB300-native low-latency skinny BF16 GEMM, ``Y[M,N] = X[M,K] . W[N,K]^T``.
 
-bf16 inputs, fp32 multiply-add, fp32 output, M = 1..16 (decode-sized), as used
-for the MoE router logits and the small-batch decode projections.
+bf16 inputs, fp32 multiply-add, fp32 (or bf16) output, M = 1..16 (decode-sized)
+on every kernel and M = 17..64 on the cluster split-K tensor-core kernel, as
+used for the MoE router logits and the small-batch decode projections.
 
 This module is a thin ctypes binding over ``libskinny_gemm.so`` (the C ABI in
 ``include/skinny_gemm.h``): the functions below carry the C names and only
@@ -26,7 +27,7 @@ __all__ = [
 ]
 
 # ---- constants mirrored from include/skinny_gemm.h
-SKINNY_MAX_M = 16
+SKINNY_MAX_M = 64
 SKINNY_OK = 0
 SKINNY_ERR_INVALID_VALUE = 1
 SKINNY_ERR_UNSUPPORTED = 2

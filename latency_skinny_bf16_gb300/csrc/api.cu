@@ -242,7 +242,7 @@ bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int fo
     for (;; ++S) {
         if (S > kSplitMaxCluster) return false;
         const int ks = ((K + S - 1) / S + 15) & ~15;
-        const int xrows = consumer == SKINNY_CONSUMER_MMA ? (M <= 8 ? 8 : 16) : M;
+        const int xrows = consumer == SKINNY_CONSUMER_MMA ? splitk_mma_tokens(M) : M;
         const int xbytes = xrows * (((ks * 2 + 127) & ~127) + 16);
         if (xbytes > kSplitXBudget && !force_s) continue;
         // Ring chunk: each W row of a chunk is one bulk copy, and the copy
@@ -277,8 +277,13 @@ bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int fo
         if (per_sm < 1) per_sm = 1;
         int cap = num_sms * per_sm / S;
         if (cap < 1) cap = 1;
+        // 32 / 64 tokens keep one partial-sum buffer: one tile per cluster
+        const bool one_tile = S > 1 && consumer == SKINNY_CONSUMER_MMA && splitk_mma_tokens(M) >= 32;
+        if (one_tile && force_c && force_c < tiles) return false;
         int C = force_c;
-        if (C == 0) {
+        if (one_tile) {
+            C = tiles;
+        } else if (C == 0) {
             if (tiles <= cap) {
                 C = tiles;
             } else {
@@ -319,6 +324,23 @@ skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int n
     int backend = fb, consumer = fc, split = fs, bn = fbn, stages = fst, stage_k = g_opt_force_stage_k.load();
     int tuned = 0;
     const bool dotmma_ok = splitk_ok && K % 32 == 0;
+    // 17..64 tokens: only the split-K backend with the MMA consumer
+    const bool mid_m = M > kMaxMSmall;
+    if (mid_m) {
+        if (!mma_ok) return SKINNY_ERR_UNSUPPORTED;
+        if ((fb != SKINNY_BACKEND_AUTO && fb != SKINNY_BACKEND_SPLITK) ||
+            (fc != SKINNY_CONSUMER_AUTO && fc != SKINNY_CONSUMER_MMA))
+            return SKINNY_ERR_UNSUPPORTED;
+        backend = SKINNY_BACKEND_SPLITK;
+        consumer = SKINNY_CONSUMER_MMA;
+        const TunedEntry *e = (fb == SKINNY_BACKEND_AUTO) ? lookup_tuned(M, N, K) : nullptr;
+        if (e && e->backend == SKINNY_BACKEND_SPLITK && e->consumer == SKINNY_CONSUMER_MMA) {
+            if (!split) split = e->split_k;
+            if (!stages) stages = e->stages;
+            if (!stage_k) stage_k = e->stage_k;
+            tuned = 1;
+        }
+    }
     if (backend == SKINNY_BACKEND_AUTO) {
         const TunedEntry *e = lookup_tuned(M, N, K);
         const bool entry_ok =
@@ -357,7 +379,12 @@ skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int n
         if (consumer == SKINNY_CONSUMER_AUTO) consumer = (M > 4 && mma_ok) ? SKINNY_CONSUMER_MMA : SKINNY_CONSUMER_FMA;
         if (bn != 0 && bn != 16) return SKINNY_ERR_UNSUPPORTED;
         ok = plan_splitk(M, N, K, vec, consumer, split, stages, fgy, stage_k, num_sms, p);
-        if (!ok && fb == SKINNY_BACKEND_AUTO) {
+        if (!ok && mid_m && tuned) {
+            // a tuned entry these pointers / strides cannot use: the default split-K plan
+            ok = plan_splitk(M, N, K, vec, consumer, fs, fst, fgy, g_opt_force_stage_k.load(), num_sms, p);
+            tuned = 0;
+        }
+        if (!ok && fb == SKINNY_BACKEND_AUTO && !mid_m) {
             // a tuned split-K entry that these pointers / strides cannot use
             ok = plan_dotprod(M, N, K, vec, 0, num_sms, p);
             tuned = 0;

@@ -202,7 +202,7 @@ int rt_index(int block_n) {
 
 }  // namespace
 
-bool dotmma_supported(int M, int block_n) { return M >= 1 && M <= SKINNY_MAX_M && rt_index(block_n) >= 0; }
+bool dotmma_supported(int M, int block_n) { return M >= 1 && M <= kMaxMSmall && rt_index(block_n) >= 0; }
 
 int dotmma_smem_bytes(int M, int block_n, int k_chunk) {
     (void)block_n;
@@ -221,7 +221,7 @@ cudaError_t dotmma_prepare() {
 
 cudaError_t launch_dotmma(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c) {
     const int ri = rt_index(p.block_n);
-    if (ri < 0 || a.M < 1 || a.M > SKINNY_MAX_M || a.K % 32 != 0 || p.k_chunk % 32 != 0) return cudaErrorInvalidValue;
+    if (ri < 0 || a.M < 1 || a.M > kMaxMSmall || a.K % 32 != 0 || p.k_chunk % 32 != 0) return cudaErrorInvalidValue;
     MmaKernel fn = kTable[a.M <= 8 ? 0 : 1][ri];
     const int x_vec16 = ((reinterpret_cast<uintptr_t>(a.X) & 15) == 0 && (a.ldx & 7) == 0) ? 1 : 0;
     cudaLaunchConfig_t cfg = {};

@@ -299,7 +299,7 @@ template <int MT> struct Row {
         kfn<MT, 4, 1>(), kfn<MT, 2, 1>(), kfn<MT, 1, 1>()};
 };
 
-const DotKernel *kTable[SKINNY_MAX_M] = {
+const DotKernel *kTable[kMaxMSmall] = {
     Row<1>::k, Row<2>::k, Row<3>::k, Row<4>::k, Row<5>::k, Row<6>::k, Row<7>::k, Row<8>::k,
     Row<9>::k, Row<10>::k, Row<11>::k, Row<12>::k, Row<13>::k, Row<14>::k, Row<15>::k, Row<16>::k};
 
@@ -314,7 +314,7 @@ int variant_index(int vec_elems, int block_n) {
 }  // namespace
 
 bool dotprod_supported(int M, int vec_elems, int block_n) {
-    return M >= 1 && M <= SKINNY_MAX_M && variant_index(vec_elems, block_n) >= 0;
+    return M >= 1 && M <= kMaxMSmall && variant_index(vec_elems, block_n) >= 0;
 }
 
 int dotprod_smem_bytes(int M, int block_n, int k_chunk) {
@@ -322,7 +322,7 @@ int dotprod_smem_bytes(int M, int block_n, int k_chunk) {
 }
 
 cudaError_t dotprod_prepare() {
-    for (int m = 0; m < SKINNY_MAX_M; ++m)
+    for (int m = 0; m < kMaxMSmall; ++m)
         for (int v = 0; v < kDotVariants; ++v) {
             cudaError_t e = set_max_dyn_smem(kTable[m][v]);
             if (e != cudaSuccess) return e;
@@ -332,7 +332,7 @@ cudaError_t dotprod_prepare() {
 
 cudaError_t launch_dotprod(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c) {
     const int vi = variant_index(p.vec_elems, p.block_n);
-    if (vi < 0 || a.M < 1 || a.M > SKINNY_MAX_M) return cudaErrorInvalidValue;
+    if (vi < 0 || a.M < 1 || a.M > kMaxMSmall) return cudaErrorInvalidValue;
     DotKernel fn = kTable[a.M - 1][vi];
     const int x_vec16 = ((reinterpret_cast<uintptr_t>(a.X) & 15) == 0 && (a.ldx & 7) == 0) ? 1 : 0;
 

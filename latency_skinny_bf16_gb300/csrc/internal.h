@@ -9,6 +9,12 @@
 
 namespace skinny {
 
+// Token counts: every kernel takes M <= 16; the cluster split-K kernel with
+// the MMA consumer also takes 17..64 (the SKINNY_MAX_M of the C ABI).
+constexpr int kMaxMSmall = 16;
+constexpr int kMaxMSplitMma = SKINNY_MAX_M;
+int splitk_mma_tokens(int M);   // MMA token bucket: 8, 16, 32 or 64
+
 struct GemmArgs {
     const uint16_t *X;
     int64_t ldx;

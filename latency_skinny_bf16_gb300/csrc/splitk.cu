@@ -24,7 +24,8 @@
 //       FMA: warp w owns W rows 4w..4w+3, lane l the 8-element vector l of the
 //            chunk; fp32 fused multiply-add into acc[M][4], or
 //       MMA: mma.sync m16n8k16 with the 16 W rows on the MMA's M side and the
-//            tokens on its N side (8 or 16 tokens); ldmatrix feeds both
+//            tokens on its N side (8, 16, 32 or 64 tokens: each A fragment
+//            serves every 8-token group); ldmatrix feeds both
 //            operands from padded (conflict-free) rows; the warps split the
 //            chunk's 16-wide k steps, and each chunk's MMA sum is added into an
 //            fp32 register accumulator with a plain rounded add,
@@ -59,16 +60,21 @@ struct Layout {
 
 __host__ __device__ inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
+// Partial-sum slot buffers per CTA: two, alternating by tile, so persistent
+// clusters can loop over tiles; one for 32 / 64 tokens, whose plans are never
+// persistent (each cluster owns one tile), to keep shared memory in bounds.
+__host__ __device__ constexpr int slot_buffers(int MT) { return MT >= 32 ? 1 : 2; }
+
 __host__ __device__ inline Layout make_layout(int MT, int consumer, int stages, int KS, int S, int bk) {
     Layout L;
-    L.xrows = (consumer == SKINNY_CONSUMER_MMA) ? (MT <= 8 ? 8 : 16) : MT;
+    L.xrows = MT;   // MMA: MT is the token bucket 8 / 16 / 32 / 64, FMA: M
     L.xrowb = round_up(KS * 2, 128) + 16;          // X row stride: 16 (mod 128)
     int off = 0;
     L.ring = off;  off += stages * kBN * ring_row_bytes(bk);
     L.xs = off;    off += L.xrows * L.xrowb;
     off = round_up(off, 16);
     L.red = off;   off += (consumer == SKINNY_CONSUMER_MMA) ? kSplitConsumerWarps * MT * kBN * 4 : 0;
-    L.slots = off; off += (S > 1) ? 2 * S * MT * kBN * 4 : 0;   // double-buffered by tile
+    L.slots = off; off += (S > 1) ? slot_buffers(MT) * S * MT * kBN * 4 : 0;   // alternating by tile
     off = round_up(off, 8);
     L.bars = off;  off += 2 * stages * 8 + 8;      // full[stages], empty[stages], x_full
     L.ctrl = off;  off += 16;
@@ -148,7 +154,8 @@ splitk_kernel(const SplitParams p)
     //                may be written through DSMEM from then on);
     //   phase i + 1  every CTA has written its partials of tile i into the
     //                owners' slot buffer (i & 1) and has read its own slots of
-    //                tile i - 1, so buffer (i + 1) & 1 is free again.
+    //                tile i - 1, so buffer (i + 1) & 1 is free again (32 / 64
+    //                tokens: one buffer, and a cluster owns at most one tile).
     if (S > 1) cluster_arrive_relaxed();
 
     if (warp == kSplitConsumerWarps) {
@@ -162,8 +169,8 @@ splitk_kernel(const SplitParams p)
             griddep_wait();
             if (lane == 0) mbar_arrive_expect_tx(xfull, (uint32_t)(p.M * klen * 2));
             __syncwarp();
-            if (lane < p.M)
-                bulk_copy_g2s(smem_u32(smem + L.xs) + lane * L.xrowb, p.X + lane * p.ldx + kbeg,
+            for (int r = lane; r < p.M; r += 32)
+                bulk_copy_g2s(smem_u32(smem + L.xs) + r * L.xrowb, p.X + r * p.ldx + kbeg,
                               (uint32_t)(klen * 2), xfull);
             x_done = true;
         };
@@ -250,14 +257,21 @@ splitk_kernel(const SplitParams p)
         for (int i = 0; i < my_tiles; ++i) {
             const int n0 = ((int)blockIdx.y + i * C) * kBN;
             const int rows = min(kBN, p.N - n0);
-            const uint32_t slot_buf = slots + (uint32_t)((i & 1) * S * MT * kBN * 4);
+            const int sbuf = (slot_buffers(MT) == 2) ? (i & 1) : 0;
+            const uint32_t slot_buf = slots + (uint32_t)(sbuf * S * MT * kBN * 4);
 
-            float part[MT][4];        // FMA: acc[m][r] for W rows 4*warp + r
+            constexpr int PM = (CONS == SKINNY_CONSUMER_FMA) ? MT : 1;
+            constexpr int NT = (CONS == SKINNY_CONSUMER_MMA) ? MT / 8 : 1;   // n8 token tiles
+            float part[PM][4];        // FMA: acc[m][r] for W rows 4*warp + r
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
+            for (int m = 0; m < PM; ++m)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) part[m][r] = 0.f;
-            float macc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // MMA accumulators
+            float macc[NT][4];        // MMA accumulators, one n8 token tile each
+#pragma unroll
+            for (int h = 0; h < NT; ++h)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) macc[h][q] = 0.f;
 
             for (int c = 0; c < nchunks; ++c, ++g) {
                 const int s = g % stages;
@@ -311,14 +325,18 @@ splitk_kernel(const SplitParams p)
                             }
                         }
                     } else {
-                        // MMA: A = 16 W rows x 16 k (ldmatrix.x4), B = 16 k x 8|16 tokens.
+                        // MMA: A = 16 W rows x 16 k (ldmatrix.x4), B = 16 k x MT tokens.
                         // The MMA sum is moved into the fp32 accumulator (a rounded
                         // add) after at most 4 k16 steps.
                         const int steps = len >> 4;
                         const uint32_t a_row = (lane & 7) + 8 * ((lane >> 3) & 1);
                         const uint32_t a_addr0 = stage + a_row * row_bytes + (lane >> 4) * 16;
                         for (int j0 = warp; j0 < steps; j0 += 4 * kSplitConsumerWarps) {
-                            float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                            float d[NT][4];
+#pragma unroll
+                            for (int h = 0; h < NT; ++h)
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) d[h][q] = 0.f;
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
                                 const int j = j0 + q * kSplitConsumerWarps;
@@ -332,16 +350,21 @@ splitk_kernel(const SplitParams p)
                                         ldmatrix_x2(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1);
                                         mma_bf16_16816(d[0], a, b0, b1, d[0]);
                                     } else {
-                                        const uint32_t tok = (lane & 7) + 8 * (lane >> 4), kh = (lane >> 3) & 1;
-                                        uint32_t b0, b1, b2, b3;
-                                        ldmatrix_x4(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1, b2, b3);
-                                        mma_bf16_16816(d[0], a, b0, b1, d[0]);
-                                        mma_bf16_16816(d[1], a, b2, b3, d[1]);
+                                        // 16 tokens per ldmatrix.x4; the A fragment serves every group
+#pragma unroll
+                                        for (int h2 = 0; h2 < MT / 16; ++h2) {
+                                            const uint32_t tok = (lane & 7) + 8 * (lane >> 4) + 16 * h2,
+                                                           kh = (lane >> 3) & 1;
+                                            uint32_t b0, b1, b2, b3;
+                                            ldmatrix_x4(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1, b2, b3);
+                                            mma_bf16_16816(d[2 * h2], a, b0, b1, d[2 * h2]);
+                                            mma_bf16_16816(d[2 * h2 + 1], a, b2, b3, d[2 * h2 + 1]);
+                                        }
                                     }
                                 }
                             }
 #pragma unroll
-                            for (int h = 0; h < 2; ++h)
+                            for (int h = 0; h < NT; ++h)
 #pragma unroll
                                 for (int q = 0; q < 4; ++q) macc[h][q] += d[h][q];
                         }
@@ -382,8 +405,7 @@ splitk_kernel(const SplitParams p)
                 // for tokens 2*t4, 2*t4+1 (+8 for the second MMA)
                 const int g4 = lane >> 2, t4 = lane & 3;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (h == 1 && MT <= 8) break;
+                for (int h = 0; h < NT; ++h) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int tok = 8 * h + 2 * t4 + (q & 1);
@@ -405,7 +427,7 @@ splitk_kernel(const SplitParams p)
             if (S > 1) {
                 cluster_arrive_release();   // phase i + 1: partials of tile i are in the owners' slots
                 cluster_wait_acquire();
-                const float *sl = reinterpret_cast<const float *>(smem + L.slots) + (i & 1) * S * MT * kBN;
+                const float *sl = reinterpret_cast<const float *>(smem + L.slots) + sbuf * S * MT * kBN;
                 for (int e = tid; e < MT * kBN; e += kSplitConsumerWarps * 32) {
                     const int m = e / kBN, c = e - m * kBN;
                     if (m < p.M && c < rows && (c % S) == rank) {
@@ -423,20 +445,27 @@ using SplitKernel = void (*)(const SplitParams);
 
 template <int MT> constexpr SplitKernel fma_k() { return &splitk_kernel<MT, SKINNY_CONSUMER_FMA>; }
 
-const SplitKernel kFma[SKINNY_MAX_M] = {
+const SplitKernel kFma[kMaxMSmall] = {
     fma_k<1>(), fma_k<2>(), fma_k<3>(), fma_k<4>(), fma_k<5>(), fma_k<6>(), fma_k<7>(), fma_k<8>(),
     fma_k<9>(), fma_k<10>(), fma_k<11>(), fma_k<12>(), fma_k<13>(), fma_k<14>(), fma_k<15>(), fma_k<16>()};
-const SplitKernel kMma[2] = {&splitk_kernel<8, SKINNY_CONSUMER_MMA>, &splitk_kernel<16, SKINNY_CONSUMER_MMA>};
+const SplitKernel kMma[4] = {&splitk_kernel<8, SKINNY_CONSUMER_MMA>, &splitk_kernel<16, SKINNY_CONSUMER_MMA>,
+                             &splitk_kernel<32, SKINNY_CONSUMER_MMA>, &splitk_kernel<64, SKINNY_CONSUMER_MMA>};
 
-int mt_for(int M, int consumer) {
-    return consumer == SKINNY_CONSUMER_MMA ? (M <= 8 ? 8 : 16) : M;
-}
+int mma_index(int M) { return M <= 8 ? 0 : M <= 16 ? 1 : M <= 32 ? 2 : 3; }
+
+}  // namespace
+
+int splitk_mma_tokens(int M) { return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : 64; }
+
+namespace {
+int mt_for(int M, int consumer) { return consumer == SKINNY_CONSUMER_MMA ? splitk_mma_tokens(M) : M; }
 
 }  // namespace
 
 bool splitk_supported(int M, int consumer, int block_n) {
-    return M >= 1 && M <= SKINNY_MAX_M && block_n == kBN &&
-           (consumer == SKINNY_CONSUMER_FMA || consumer == SKINNY_CONSUMER_MMA);
+    return M >= 1 && block_n == kBN &&
+           ((consumer == SKINNY_CONSUMER_FMA && M <= kMaxMSmall) ||
+            (consumer == SKINNY_CONSUMER_MMA && M <= kMaxMSplitMma));
 }
 
 int splitk_smem_bytes(int M, int consumer, int block_n, int stages, int k_slice, int split_k, int bk) {
@@ -445,11 +474,11 @@ int splitk_smem_bytes(int M, int consumer, int block_n, int stages, int k_slice,
 }
 
 cudaError_t splitk_prepare() {
-    for (int m = 0; m < SKINNY_MAX_M; ++m) {
+    for (int m = 0; m < kMaxMSmall; ++m) {
         cudaError_t e = set_max_dyn_smem(kFma[m]);
         if (e != cudaSuccess) return e;
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
         cudaError_t e = set_max_dyn_smem(kMma[i]);
         if (e != cudaSuccess) return e;
     }
@@ -459,6 +488,10 @@ cudaError_t splitk_prepare() {
 cudaError_t launch_splitk(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCtx &c) {
     if (!splitk_supported(a.M, pl.consumer, pl.block_n)) return cudaErrorInvalidValue;
     if (pl.stage_k < 64 || pl.stage_k > kSplitMaxBK || pl.stage_k % 64) return cudaErrorInvalidValue;
+    // a single slot buffer (32 / 64 tokens) is only safe when no cluster loops over tiles
+    if (pl.split_k > 1 && pl.consumer == SKINNY_CONSUMER_MMA &&
+        slot_buffers(splitk_mma_tokens(a.M)) == 1 && pl.grid_y < (a.N + kBN - 1) / kBN)
+        return cudaErrorInvalidValue;
     SplitParams p;
     p.X = a.X; p.ldx = a.ldx; p.W = a.W; p.ldw = a.ldw; p.Y = a.Y; p.ldy = a.ldy;
     p.M = a.M; p.N = a.N; p.K = a.K;
@@ -469,7 +502,7 @@ cudaError_t launch_splitk(const GemmArgs &a, const skinny_plan_t &pl, const Laun
     p.status = c.status;
     p.budget_ns = c.budget_ns;
     p.out_bf16 = a.out_bf16;
-    SplitKernel fn = (pl.consumer == SKINNY_CONSUMER_MMA) ? kMma[a.M <= 8 ? 0 : 1] : kFma[a.M - 1];
+    SplitKernel fn = (pl.consumer == SKINNY_CONSUMER_MMA) ? kMma[mma_index(a.M)] : kFma[a.M - 1];
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.grid_x, pl.grid_y, 1);

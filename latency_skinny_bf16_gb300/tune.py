@@ -31,8 +31,22 @@ import latency_skinny_bf16_gb300 as sk
 DEFAULT_SHAPES = ["7168x256", "7168x384", "2880x128", "4096x256", "7168x2112", "1536x24576", "14336x7168"]
 
 
+def token_bucket(M: int) -> int:
+    """Kernels are instantiated per token bucket: 1..8, 9..16 (MMA tiles of 8 /
+    16 tokens), 17..32 and 33..64 (split-K MMA only)."""
+    return 8 if M <= 8 else 16 if M <= 16 else 32 if M <= 32 else 64
+
+
 def candidates(M: int, K: int, N: int = 0):
     out = []
+    if M > 16:
+        # 17..64 tokens: cluster split-K with the MMA consumer is the only path
+        if K % 16:
+            return out
+        for s in (2, 4, 6, 8):
+            for bk in (0, 512):           # 0: the dispatcher's ring chunk for this shape
+                out.append(dict(backend=2, consumer=2, split_k=s, stages=0, block_n=0, stage_k=bk))
+        return out
     for bn in (1, 2, 4, 8):
         out.append(dict(backend=1, block_n=bn, consumer=0, split_k=0, stages=0, stage_k=0))
     if K % 32 == 0:
@@ -116,6 +130,11 @@ def tune_shape(K, N, m_values, l2_bytes, pdl, log):
             results.append((us, c))
             if best is None or us < best[0]:
                 best = (us, c)
+        if best is None:
+            # no plan runs this M (e.g. the X slice of 64 tokens does not fit)
+            log.write(json.dumps({"K": K, "N": N, "M": M, "best_us": None}) + "\n")
+            del ys
+            continue
         results.sort(key=lambda t: t[0])
         log.write(json.dumps({"K": K, "N": N, "M": M, "best_us": round(best[0], 3), "best": best[1],
                               "top5": [(round(u, 3), c) for u, c in results[:5]]}) + "\n")
@@ -127,26 +146,25 @@ def tune_shape(K, N, m_values, l2_bytes, pdl, log):
     return rows
 
 
-def merge_rows(K, N, rows, m_max=16):
+def merge_rows(K, N, rows, m_max=64):
     """Winners of consecutive tuned M values (in order) that agree -> one table
     line; each line's M range reaches up to the next line's first M, so the
-    lines cover every M from the first tuned one to m_max."""
+    lines cover every M from the first tuned one to m_max.  A line never
+    crosses a token bucket (different kernels, different X footprints), and
+    the last line ends with its bucket: untuned buckets keep the default rule."""
     lines = []
     i = 0
     while i < len(rows):
         j = i
-        # M <= 8 and M > 8 use different kernels (8- vs 16-token MMA tiles,
-        # different X footprints), so a line never crosses that boundary
+        b = token_bucket(rows[i][0])
         while (j + 1 < len(rows) and rows[j + 1][1] == rows[i][1]
-               and (rows[j + 1][0] <= 8) == (rows[i][0] <= 8)):
+               and token_bucket(rows[j + 1][0]) == b):
             j += 1
         c = rows[i][1]
         if j + 1 < len(rows):
-            m_hi = rows[j + 1][0] - 1
-            if rows[i][0] <= 8 < rows[j + 1][0]:
-                m_hi = min(m_hi, 8)
+            m_hi = min(rows[j + 1][0] - 1, b)
         else:
-            m_hi = m_max
+            m_hi = min(m_max, b)
         lines.append((K, N, rows[i][0], m_hi, c["backend"], c["consumer"], c["split_k"], c["block_n"],
                       c["stages"], c.get("stage_k", 0), [round(r[2], 2) for r in rows[i:j + 1]]))
         i = j + 1
@@ -158,22 +176,25 @@ def main(argv=None):
     ap.add_argument("--shapes", default=",".join(DEFAULT_SHAPES))
     ap.add_argument("--m", default="1-16", help="M values for the router shapes (a-b range or list)")
     ap.add_argument("--m-large", default="1,2,3,4,6,8,9,12,16", help="M values for shapes with W > 16 MB")
+    ap.add_argument("--m-mid", default="17,24,32,33,48,64", help="M values 17..64 (split-K MMA), every shape")
     ap.add_argument("--out", default="-")
     ap.add_argument("--log", default=None)
     a = ap.parse_args(argv)
     def parse_m(spec):
+        if spec in ("", "none"):
+            return []
         if "-" in spec:
             lo, hi = (int(v) for v in spec.split("-"))
             return list(range(lo, hi + 1))
         return [int(v) for v in spec.split(",")]
-    m_small, m_large = parse_m(a.m), parse_m(a.m_large)
+    m_small, m_large, m_mid = parse_m(a.m), parse_m(a.m_large), parse_m(a.m_mid)
     assert sk.skinny_init(0) == sk.SKINNY_OK
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     log = open(a.log, "a") if a.log else sys.stderr
     out_lines = []
     for shp in a.shapes.split(","):
         K, N = (int(v) for v in shp.lower().split("x"))
-        rows = tune_shape(K, N, m_large if 2 * N * K > 16e6 else m_small, l2, None, log)
+        rows = tune_shape(K, N, (m_large if 2 * N * K > 16e6 else m_small) + m_mid, l2, None, log)
         for (k, n, mlo, mhi, be, co, sp, bn, st, bk, us) in merge_rows(K, N, rows):
             out_lines.append(f"{{{k}, {n}, {mlo}, {mhi}, {be}, {co}, {sp}, {bn}, {st}, {bk}}},  // us/call {us}")
     text = "\n".join(out_lines) + "\n"

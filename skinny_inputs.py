@@ -30,6 +30,15 @@ qkv_a / q_b / eh_proj style projection shapes):
                      ldy in [N, N+67], X and W ~N(0,1) with 1% x100 outliers;
                      case parameters from master seed 4.
 * ``pdl_chain``      64 back-to-back calls M=4, K=7168, N=256 (seed 5).
+* ``midm``           the medium-M decode regime, 17..64 tokens:
+                     M in {17,24,32,40,64} x (K,N) in {(7168,256),(4096,384)}
+                     (router distributions, seeds 401..410), then
+                     M in {17,32,64} x (N,K) in {(2112,7168),(24576,1536)} and
+                     M in {17,32} x (N,K) = (7168,14336) (projection
+                     distributions, ldy = N+64, seeds 421..428).
+* ``midm_edge``      40 random cases, M in [17,64], N in [1,1024],
+                     K = 16*[1,512] (the path needs K % 16 == 0), ldy in [N, N+67],
+                     X and W ~N(0,1) with 1% x100 outliers; master seed 6.
 """
 from __future__ import annotations
 
@@ -178,6 +187,36 @@ def edge_cases(count: int = 200, master_seed: int = 4) -> list[Case]:
     return out
 
 
+def midm_cases() -> list[Case]:
+    out = []
+    seed = 401
+    for (K, N) in ((7168, 256), (4096, 384)):
+        for M in (17, 24, 32, 40, 64):
+            out.append(Case(f"midm_M{M}_K{K}_N{N}", M=M, N=N, K=K, seed=seed))
+            seed += 1
+    seed = 421
+    for (N, K), ms in (((2112, 7168), (17, 32, 64)), ((24576, 1536), (17, 32, 64)), ((7168, 14336), (17, 32))):
+        for M in ms:
+            out.append(Case(f"midm_proj_M{M}_N{N}_K{K}", M=M, N=N, K=K, seed=seed,
+                            w_dist="uniform_isqrtk", ldy=N + 64))
+            seed += 1
+    return out
+
+
+def midm_edge_cases(count: int = 40, master_seed: int = 6) -> list[Case]:
+    rng = np.random.default_rng(master_seed)
+    out = []
+    for i in range(count):
+        M = int(rng.integers(17, 65))
+        N = int(rng.integers(1, 1025))
+        K = 16 * int(rng.integers(1, 513))
+        ldy = N + int(rng.integers(0, 68))
+        seed = int(rng.integers(0, 2**31 - 1))
+        out.append(Case(f"midm_edge{i:02d}_M{M}_N{N}_K{K}", M=M, N=N, K=K, seed=seed,
+                        x_dist="normal", w_dist="normal", outliers=True, ldy=ldy))
+    return out
+
+
 def pdl_chain_case() -> Case:
     return Case("pdl_chain_M4_K7168_N256", M=4, N=256, K=7168, seed=5)
 
@@ -188,6 +227,8 @@ WORKLOADS = {
     "splitk": splitk_cases,
     "projection": projection_cases,
     "edge": edge_cases,
+    "midm": midm_cases,
+    "midm_edge": midm_edge_cases,
 }
 
 

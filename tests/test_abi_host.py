@@ -52,8 +52,8 @@ def call(X=A16, ldx=64, W=B16, ldw=64, Y=C16, ldy=32, M=4, N=32, K=64):
     (dict(M=-1), sk.SKINNY_ERR_INVALID_VALUE),
     (dict(N=-1), sk.SKINNY_ERR_INVALID_VALUE),
     (dict(K=-1), sk.SKINNY_ERR_INVALID_VALUE),
-    (dict(M=17), sk.SKINNY_ERR_UNSUPPORTED),
-    (dict(M=64), sk.SKINNY_ERR_UNSUPPORTED),
+    (dict(M=65), sk.SKINNY_ERR_UNSUPPORTED),
+    (dict(M=1000), sk.SKINNY_ERR_UNSUPPORTED),
     (dict(M=0), sk.SKINNY_OK),
     (dict(N=0), sk.SKINNY_OK),
     (dict(M=0, X=0, W=0, Y=0), sk.SKINNY_OK),
@@ -192,7 +192,11 @@ def _table_entries():
 
 def test_every_tuned_entry_is_a_supported_plan_and_is_used():
     for K, N, m_lo, m_hi, be, co, s, bn, st, bk in _table_entries():
-        assert 1 <= m_lo <= m_hi <= 16
+        assert 1 <= m_lo <= m_hi <= 64
+        # a row never spans two kernels: 1..8 / 9..16 / 17..32 / 33..64 tokens
+        assert (m_lo <= 8) == (m_hi <= 8) and (m_lo <= 16) == (m_hi <= 16) and (m_lo <= 32) == (m_hi <= 32)
+        if m_hi > 16:
+            assert (be, co) == (sk.SKINNY_BACKEND_SPLITK, sk.SKINNY_CONSUMER_MMA)
         for M in range(m_lo, m_hi + 1):
             p = plan(M, N, K)
             assert p["tuned"] == 1, (K, N, M)
@@ -233,7 +237,7 @@ def test_projection_shapes_at_large_m_take_a_fitting_splitk_plan():
 @pytest.mark.parametrize("kw,expect", [
     (dict(Y=C16 + 1), sk.SKINNY_ERR_MISALIGNED),      # bf16 Y: 2-byte alignment
     (dict(Y=B16 + 1024), sk.SKINNY_ERR_INVALID_VALUE),  # overlaps W (2-byte elements)
-    (dict(M=17), sk.SKINNY_ERR_UNSUPPORTED),
+    (dict(M=65), sk.SKINNY_ERR_UNSUPPORTED),
     (dict(ldy=31), sk.SKINNY_ERR_INVALID_VALUE),
     (dict(M=0), sk.SKINNY_OK),
 ])
@@ -249,3 +253,52 @@ def test_bf16_output_two_byte_aligned_y_passes_the_checks():
     assert call(Y=C16 + 2) == sk.SKINNY_ERR_MISALIGNED
     st = sk.skinny_gemm_bf16_bf16out(A16, 64, B16, 64, C16 + 2, 32, 4, 32, 64, 0)
     assert st in (sk.SKINNY_OK, sk.SKINNY_ERR_NO_DEVICE)
+
+
+# ---------------------------------------------------------------- 17..64 tokens
+MID_M = (17, 24, 32, 33, 40, 48, 63, 64)
+
+
+def test_mid_m_takes_the_splitk_mma_path_one_tile_per_cluster():
+    for M in MID_M:
+        for (N, K) in ((256, 7168), (384, 7168), (2112, 7168), (1536, 4096)):
+            p = plan(M, N, K)
+            assert (p["backend"], p["consumer"]) == (sk.SKINNY_BACKEND_SPLITK, sk.SKINNY_CONSUMER_MMA), (M, N, K)
+            assert p["block_n"] == 16 and p["smem_bytes"] <= 227 * 1024
+            assert p["split_k"] * p["k_chunk"] >= K and p["k_chunk"] % 16 == 0
+            if p["split_k"] > 1:
+                # a single partial-sum buffer: no cluster loops over two tiles
+                assert p["grid_y"] == (N + 15) // 16
+
+
+def test_mid_m_unsupported_shapes_are_refused_on_the_host():
+    with pytest.raises(sk.SkinnyError) as e:
+        plan(64, 7168, 14336)                      # X slice does not fit shared memory
+    assert e.value.status == sk.SKINNY_ERR_UNSUPPORTED
+    for kw in (dict(K=7160), dict(K=7176, W=B16 + 8), dict(K=7169)):   # K % 16, W rows not 16-byte aligned
+        K = kw.pop("K")
+        with pytest.raises(sk.SkinnyError) as e:
+            plan(20, 256, K, **kw)
+        assert e.value.status == sk.SKINNY_ERR_UNSUPPORTED
+    for opts in (dict(backend=sk.SKINNY_BACKEND_DOTPROD), dict(consumer=sk.SKINNY_CONSUMER_FMA),
+                 dict(backend=sk.SKINNY_BACKEND_SPLITK, split_k=8, clusters=4)):
+        with sk.options(**opts):
+            with pytest.raises(sk.SkinnyError) as e:
+                plan(40, 256, 7168)
+            assert e.value.status == sk.SKINNY_ERR_UNSUPPORTED
+    # small M is unchanged by the mid-M rules
+    assert plan(16, 256, 7200)["backend"] == sk.SKINNY_BACKEND_SPLITK
+
+
+def test_mid_m_forced_split_sizes_plan():
+    for M in (17, 32, 64):
+        for S in (1, 2, 4, 8):
+            with sk.options(backend=sk.SKINNY_BACKEND_SPLITK, consumer=sk.SKINNY_CONSUMER_MMA, split_k=S):
+                try:
+                    p = plan(M, 256, 4096)
+                except sk.SkinnyError as e:
+                    # only a slice too long for shared memory may refuse
+                    # (32 tokens x 4096 x 2 B = 256 KB at S = 1; 64 tokens x 2048 x 2 B at S = 2)
+                    assert e.status == sk.SKINNY_ERR_UNSUPPORTED and (S == 1 or (M > 32 and S == 2))
+                    continue
+            assert p["split_k"] == S and p["smem_bytes"] <= 227 * 1024

@@ -59,6 +59,12 @@ def test_workload_tables():
                for c in e)
     assert any(c.K % 8 != 0 for c in e) and any(c.K % 2 == 1 for c in e)
     assert si.edge_cases() == e   # deterministic
+    m = si.workload("midm")
+    assert len(m) == 18 and all(17 <= c.M <= 64 for c in m) and {c.M for c in m} >= {17, 32, 64}
+    assert [c.seed for c in m] == list(range(401, 411)) + list(range(421, 429))
+    me = si.workload("midm_edge")
+    assert len(me) == 40 and si.midm_edge_cases() == me
+    assert all(17 <= c.M <= 64 and c.K % 16 == 0 and 16 <= c.K <= 8192 and c.N <= c.ly <= c.N + 67 for c in me)
 
 
 def test_embed_rows():

@@ -332,7 +332,7 @@ def test_tensor_wrapper():
     with pytest.raises(TypeError):
         sk.gemm(x.float(), w)
     with pytest.raises(sk.SkinnyError):
-        sk.gemm(torch.zeros(17, 2048, dtype=torch.bfloat16, device="cuda"), w)
+        sk.gemm(torch.zeros(65, 2048, dtype=torch.bfloat16, device="cuda"), w)   # M > 64
 
 
 PERSISTENT_CFGS = [  # (split_k, clusters, stages, stage_k)

@@ -17,8 +17,8 @@ def test_merge_rows_merges_consecutive_equal_winners():
     b = dict(backend=1, consumer=0, split_k=0, stages=0, block_n=1)
     rows = [(1, b, 3.0), (2, a, 3.5), (3, a, 3.6), (4, a, 3.7), (5, b, 4.0), (7, a, 4.1)]
     lines = tune.merge_rows(7168, 256, rows)
-    # ranges cover 1..16: a gap (M=6 not tuned) goes to the line before it
-    assert [(l[2], l[3], l[4]) for l in lines] == [(1, 1, 1), (2, 4, 2), (5, 6, 1), (7, 16, 2)]
+    # a gap (M=6 not tuned) goes to the line before it; the last line ends with its token bucket
+    assert [(l[2], l[3], l[4]) for l in lines] == [(1, 1, 1), (2, 4, 2), (5, 6, 1), (7, 8, 2)]
     assert lines[1][10] == [3.5, 3.6, 3.7]
 
 
@@ -27,3 +27,20 @@ def test_merge_rows_never_crosses_the_8_token_boundary():
     rows = [(3, a, 8.7), (8, a, 9.1), (12, a, 13.0), (16, a, 13.6)]
     lines = tune.merge_rows(7168, 2112, rows)
     assert [(l[2], l[3]) for l in lines] == [(3, 8), (12, 16)]   # M 9..11 left to the default rule
+
+
+def test_mid_m_candidates_are_splitk_mma_only():
+    c = tune.candidates(17, 7168, 256)
+    assert c and all((x["backend"], x["consumer"]) == (2, 2) for x in c)
+    assert tune.candidates(40, 7176, 256) == []      # K % 16 != 0: no path for 17..64 tokens
+    assert [tune.token_bucket(m) for m in (1, 8, 9, 16, 17, 32, 33, 64)] == [8, 8, 16, 16, 32, 32, 64, 64]
+
+
+def test_merge_rows_respects_every_token_bucket():
+    a = dict(backend=2, consumer=2, split_k=8, stages=0, block_n=0, stage_k=0)
+    rows = [(12, a, 5.0), (16, a, 5.1), (17, a, 6.0), (24, a, 6.1), (32, a, 6.3), (40, a, 7.0), (64, a, 8.0)]
+    lines = tune.merge_rows(7168, 256, rows)
+    assert [(l[2], l[3]) for l in lines] == [(12, 16), (17, 32), (40, 64)]   # 33..39 left to the default
+    # a shape whose 33..64 bucket does not run ends its last line at 32
+    lines = tune.merge_rows(14336, 7168, rows[:5])
+    assert [(l[2], l[3]) for l in lines] == [(12, 16), (17, 32)]
