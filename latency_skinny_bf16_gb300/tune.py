@@ -57,8 +57,8 @@ def candidates(M: int, K: int, N: int = 0):
         if cons == 2 and K % 16:
             continue
         if big:
-            for s in (1, 2, 4, 8):
-                for bk in (0, 512, 2048):      # 0: the dispatcher's ring chunk for this shape
+            for s in (1, 2, 3, 4, 6, 8):
+                for bk in (0, 1024, 2048):     # 0: the dispatcher's ring chunk for this shape
                     out.append(dict(backend=2, consumer=cons, split_k=s, stages=0, block_n=0, stage_k=bk))
         else:
             for s in (2, 4, 6, 8):
