@@ -53,7 +53,7 @@ WORKLOAD_DESC = {
             "M in {17,32,64} x (N,K) in {(2112,7168),(24576,1536)}, M in {17,32} x (7168,14336), 18 calls",
 }
 # the device code: DRAM traffic measured by ncu stays valid while these are unchanged
-KERNEL_SOURCES = ["dotprod.cu", "dotmma.cu", "splitk.cu", "common.cuh", "internal.h"]
+KERNEL_SOURCES = ["dotprod.cu", "dotmma.cu", "splitk.cu", "stream.cu", "common.cuh", "internal.h"]
 
 
 def parse_args(argv=None):
@@ -494,7 +494,8 @@ def main(argv=None):
     fam_time, fam_bytes, fam_n = {}, {}, {}
     per_shape = []
     for c, p, us in zip(cases, r["plans"], r["per_launch"]):
-        fam = ("dotmma" if p["consumer"] == 2 else "dotprod") if p["backend"] == 1 else "splitk"
+        fam = (("dotmma" if p["consumer"] == 2 else "dotprod") if p["backend"] == 1 else
+               "splitk" if p["backend"] == 2 else "stream")
         fam_time[fam] = fam_time.get(fam, 0.0) + us
         fam_bytes[fam] = fam_bytes.get(fam, 0.0) + c.algorithmic_bytes
         fam_n[fam] = fam_n.get(fam, 0) + 1

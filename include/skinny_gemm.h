@@ -25,9 +25,9 @@
  * it runs on the cluster split-K backend with the mma.sync consumer only
  * (the tokens become 2 or 4 groups of 16 on the MMA's N side), so it needs
  * K % 16 == 0, 16-byte aligned W rows (W and ldw), and a per-CTA X slice
- * (tokens rounded up to 32 or 64, x K / split_k x 2 bytes, split_k <= 8) of
- * at most 160 KB that fits in shared memory beside the W ring: at 64 tokens
- * K = 7168 runs, K = 14336 does not.  Other M > 16 shapes return
+ * (M x K / split_k x 2 bytes, split_k <= 8) of at most 160 KB that fits in
+ * shared memory beside the W ring: at 64 tokens K = 7168 runs, K = 14336
+ * does not.  Other M > 16 shapes return
  * SKINNY_ERR_UNSUPPORTED.
  *
  * bf16 values are passed as their 16-bit patterns (uint16_t) so this header
@@ -74,7 +74,10 @@ typedef enum {
 typedef enum {
     SKINNY_BACKEND_AUTO = 0,
     SKINNY_BACKEND_DOTPROD = 1,     /* one CTA per block of output columns, whole K */
-    SKINNY_BACKEND_SPLITK = 2       /* K split over the CTAs of a thread-block cluster */
+    SKINNY_BACKEND_SPLITK = 2,      /* K split over the CTAs of a thread-block cluster */
+    SKINNY_BACKEND_STREAM = 3       /* one CTA per SM, whole K per 16-row tile, K-outer: X and W
+                                       stream through one ring chunk by chunk (large weights;
+                                       needs 16-byte aligned X and W rows, K % 16 == 0, M <= 16) */
 } skinny_backend_t;
 
 typedef enum {

@@ -80,7 +80,8 @@ skinny_status_t init_device_current(DeviceState &d, int device) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         return SKINNY_ERR_NO_DEVICE;
     if (major != 10 || minor != 3) return SKINNY_ERR_NO_DEVICE;   // built for sm_103a only
-    if (dotprod_prepare() != cudaSuccess || dotmma_prepare() != cudaSuccess || splitk_prepare() != cudaSuccess)
+    if (dotprod_prepare() != cudaSuccess || dotmma_prepare() != cudaSuccess || splitk_prepare() != cudaSuccess ||
+        stream_prepare() != cudaSuccess)
         return SKINNY_ERR_LAUNCH;
     void *sym = nullptr;
     if (cudaGetSymbolAddress(&sym, g_status_word) != cudaSuccess) return SKINNY_ERR_LAUNCH;
@@ -242,8 +243,7 @@ bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int fo
     for (;; ++S) {
         if (S > kSplitMaxCluster) return false;
         const int ks = ((K + S - 1) / S + 15) & ~15;
-        const int xrows = consumer == SKINNY_CONSUMER_MMA ? splitk_mma_tokens(M) : M;
-        const int xbytes = xrows * (((ks * 2 + 127) & ~127) + 16);
+        const int xbytes = M * (((ks * 2 + 127) & ~127) + 16);   // the M token rows of X
         if (xbytes > kSplitXBudget && !force_s) continue;
         // Ring chunk: each W row of a chunk is one bulk copy, and the copy
         // engine's cost is per copy (~50 ns each on GB300, measured), so
@@ -309,7 +309,64 @@ bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int fo
     }
 }
 
-skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int num_sms, skinny_plan_t *p) {
+// K-outer streaming plan: one CTA per SM (at most kStreamMaxTiles tiles
+// each), the longest chunks up to 2048 elements that split K evenly, and the
+// deepest ring that fits (at least one chunk's X and W entries, plus one).
+bool plan_stream(int M, int N, int K, int vec, bool x_ok, int force_c, int force_stages, int force_bk,
+                 int num_sms, skinny_plan_t *p) {
+    if (vec != 8 || !x_ok || K % 16 != 0 || K < 16 || !stream_supported(M)) return false;
+    const int tiles = (N + 15) / 16;
+    int C = force_c ? force_c : (tiles < num_sms ? tiles : num_sms);
+    if (C > tiles) C = tiles;
+    if (C < 1 || C > 65535) return false;
+    int per = (tiles + C - 1) / C;
+    if (per > kStreamMaxTiles) {
+        if (force_c) return false;
+        C = (tiles + kStreamMaxTiles - 1) / kStreamMaxTiles;
+        per = (tiles + C - 1) / C;
+    }
+    auto deepest = [&](int bk_) {   // deepest ring that fits, at most kSplitMaxStages
+        int st = kSplitMaxStages;
+        while (st > 1 && stream_smem_bytes(M, st, bk_) > kMaxDynSmem) --st;
+        return st;
+    };
+    int bk = force_bk;
+    if (!bk) {
+        // K in equal chunks of at most 2048 elements; shorter chunks (more of
+        // them) until the ring holds two chunks' worth of entries, else one
+        int nch = (K + kSplitMaxBK - 1) / kSplitMaxBK;
+        int best = 0;
+        for (int tries = 0; tries < 6; ++tries, nch *= 2) {
+            const int cand = (((K + nch - 1) / nch) + 63) / 64 * 64;
+            if (cand < 64) break;
+            const int st = deepest(cand);
+            if (st >= per + 2) { bk = cand; break; }
+            if (!best && st >= per + 1) best = cand;
+        }
+        if (!bk) bk = best;
+    }
+    if (bk < 64 || bk > kSplitMaxBK || bk % 64) return false;
+    int stages = force_stages ? force_stages : deepest(bk);
+    if (stages < per + 1 || stages > kSplitMaxStages) return false;
+    const int smem = stream_smem_bytes(M, stages, bk);
+    if (smem > kMaxDynSmem) return false;
+    p->backend = SKINNY_BACKEND_STREAM;
+    p->consumer = SKINNY_CONSUMER_MMA;
+    p->vec_elems = 8;
+    p->block_n = 16;
+    p->split_k = 1;
+    p->stages = stages;
+    p->stage_k = bk;
+    p->k_chunk = K;
+    p->grid_x = C;
+    p->grid_y = 1;
+    p->threads = 160;
+    p->smem_bytes = smem;
+    return true;
+}
+
+skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw, int M, int N, int K, int num_sms,
+                          skinny_plan_t *p) {
     std::memset(p, 0, sizeof(*p));
     if (num_sms < 1) return SKINNY_ERR_INVALID_VALUE;
     const int vec = widest_vec(W, ldw);
@@ -319,6 +376,8 @@ skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int n
     const int fgy = g_opt_force_grid_y.load();
     const bool splitk_ok = vec == 8 && K % 8 == 0;
     const bool mma_ok = splitk_ok && K % 16 == 0;
+    const bool x_ok = (reinterpret_cast<uintptr_t>(X) & 15) == 0 && ldx % 8 == 0;
+    const bool stream_ok = mma_ok && x_ok && M <= kMaxMSmall;
     const int pdl = opt_pdl();
 
     int backend = fb, consumer = fc, split = fs, bn = fbn, stages = fst, stage_k = g_opt_force_stage_k.load();
@@ -347,7 +406,8 @@ skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int n
             e && ((e->backend == SKINNY_BACKEND_DOTPROD && e->consumer != SKINNY_CONSUMER_MMA) ||
                   (e->backend == SKINNY_BACKEND_DOTPROD && e->consumer == SKINNY_CONSUMER_MMA && dotmma_ok) ||
                   (e->backend == SKINNY_BACKEND_SPLITK && splitk_ok &&
-                   (e->consumer != SKINNY_CONSUMER_MMA || mma_ok)));
+                   (e->consumer != SKINNY_CONSUMER_MMA || mma_ok)) ||
+                  (e->backend == SKINNY_BACKEND_STREAM && stream_ok));
         if (entry_ok) {
             backend = e->backend;
             if (consumer == SKINNY_CONSUMER_AUTO) consumer = e->consumer;
@@ -356,6 +416,10 @@ skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int n
             if (!stages) stages = e->stages;
             if (!stage_k) stage_k = e->stage_k;
             tuned = 1;
+        } else if (stream_ok && M >= 12 && K >= 4096 && 2.0 * N * K >= 16e6) {
+            // default rule, bandwidth-bound weights (>= 16 MB), long K and many tokens:
+            // K-outer streaming (measured ahead of the other backends only there)
+            backend = SKINNY_BACKEND_STREAM;
         } else if (dotmma_ok && M >= 4 && 2.0 * N * K >= 16e6) {
             // default rule, bandwidth-bound weights (>= 16 MB): tensor-core dot-product
             backend = SKINNY_BACKEND_DOTPROD;
@@ -389,6 +453,16 @@ skinny_status_t make_plan(const uint16_t *W, int ldw, int M, int N, int K, int n
             ok = plan_dotprod(M, N, K, vec, 0, num_sms, p);
             tuned = 0;
         }
+    } else if (backend == SKINNY_BACKEND_STREAM) {
+        if ((fc != SKINNY_CONSUMER_AUTO && fc != SKINNY_CONSUMER_MMA) || (bn != 0 && bn != 16))
+            return SKINNY_ERR_UNSUPPORTED;
+        ok = plan_stream(M, N, K, vec, x_ok, fgy, stages, stage_k, num_sms, p);
+        if (!ok && fb == SKINNY_BACKEND_AUTO) {
+            // a tuned or default streaming plan these pointers / sizes cannot use
+            ok = (dotmma_ok && M >= 4 && plan_dotmma(M, N, K, vec, 0, num_sms, p)) ||
+                 plan_dotprod(M, N, K, vec, 0, num_sms, p);
+            tuned = 0;
+        }
     } else {
         return SKINNY_ERR_INVALID_VALUE;
     }
@@ -406,7 +480,9 @@ void log_plan(int M, int N, int K, int ldw, const skinny_plan_t &p) {
     std::fprintf(stderr,
                  "[skinny] M=%d N=%d K=%d ldw=%d -> %s consumer=%d vec=%d block_n=%d split_k=%d stages=%d stage_k=%d "
                  "k_chunk=%d grid=%dx%d smem=%d pdl=%d tuned=%d\n",
-                 M, N, K, ldw, p.backend == SKINNY_BACKEND_DOTPROD ? "dotprod" : "splitk", p.consumer,
+                 M, N, K, ldw,
+                 p.backend == SKINNY_BACKEND_DOTPROD ? "dotprod" : p.backend == SKINNY_BACKEND_SPLITK ? "splitk" : "stream",
+                 p.consumer,
                  p.vec_elems, p.block_n, p.split_k, p.stages, p.stage_k, p.k_chunk, p.grid_x, p.grid_y, p.smem_bytes,
                  p.pdl, p.tuned);
 }
@@ -437,7 +513,7 @@ skinny_status_t run_gemm(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
         return cudaPeekAtLastError() == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
     }
     skinny_plan_t plan;
-    st = make_plan(W, ldw, M, N, K, d.num_sms, &plan);
+    st = make_plan(X, ldx, W, ldw, M, N, K, d.num_sms, &plan);
     if (st != SKINNY_OK) return st;
     if (opt_log()) log_plan(M, N, K, ldw, plan);
     GemmArgs a{X, ldx, W, ldw, Y, ldy, M, N, K, out_bf16};
@@ -445,6 +521,8 @@ skinny_status_t run_gemm(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
     cudaError_t e;
     if (plan.backend == SKINNY_BACKEND_DOTPROD)
         e = plan.consumer == SKINNY_CONSUMER_MMA ? launch_dotmma(a, plan, c) : launch_dotprod(a, plan, c);
+    else if (plan.backend == SKINNY_BACKEND_STREAM)
+        e = launch_stream(a, plan, c);
     else
         e = launch_splitk(a, plan, c);
     return e == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
@@ -476,7 +554,7 @@ skinny_status_t skinny_query_plan(const uint16_t *X, int ldx, const uint16_t *W,
     st = current_device(&device);
     if (st != SKINNY_OK) return st;
     if (noop || K == 0) { std::memset(plan, 0, sizeof(*plan)); return SKINNY_OK; }
-    return make_plan(W, ldw, M, N, K, g_dev[device].num_sms, plan);
+    return make_plan(X, ldx, W, ldw, M, N, K, g_dev[device].num_sms, plan);
 }
 
 skinny_status_t skinny_plan_for(const uint16_t *X, int ldx, const uint16_t *W, int ldw, const float *Y, int ldy,
@@ -486,7 +564,7 @@ skinny_status_t skinny_plan_for(const uint16_t *X, int ldx, const uint16_t *W, i
     skinny_status_t st = validate(X, ldx, W, ldw, Y, ldy, M, N, K, &noop);
     if (st != SKINNY_OK) return st;
     if (noop || K == 0) { std::memset(plan, 0, sizeof(*plan)); return SKINNY_OK; }
-    return make_plan(W, ldw, M, N, K, num_sms, plan);
+    return make_plan(X, ldx, W, ldw, M, N, K, num_sms, plan);
 }
 
 skinny_status_t skinny_set_option(int option, int value) {
@@ -495,7 +573,7 @@ skinny_status_t skinny_set_option(int option, int value) {
             if (value != 0 && value != 1) return SKINNY_ERR_INVALID_VALUE;
             g_opt_pdl.store(value); return SKINNY_OK;
         case SKINNY_OPT_FORCE_BACKEND:
-            if (value < 0 || value > 2) return SKINNY_ERR_INVALID_VALUE;
+            if (value < 0 || value > 3) return SKINNY_ERR_INVALID_VALUE;
             g_opt_force_backend.store(value); return SKINNY_OK;
         case SKINNY_OPT_FORCE_CONSUMER:
             if (value < 0 || value > 2) return SKINNY_ERR_INVALID_VALUE;

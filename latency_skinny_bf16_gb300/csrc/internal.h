@@ -59,6 +59,14 @@ bool splitk_supported(int M, int consumer, int block_n);
 cudaError_t splitk_prepare();
 cudaError_t launch_splitk(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
 
+// ---- K-outer streaming backend (stream.cu): one CTA per SM, whole K per
+// 16-row tile, X streamed through the ring chunk by chunk
+constexpr int kStreamMaxTiles = 4;   // 16-row tiles per CTA (register accumulators)
+int stream_smem_bytes(int M, int stages, int stage_k);
+bool stream_supported(int M);
+cudaError_t stream_prepare();
+cudaError_t launch_stream(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
+
 // Per-CTA dynamic shared memory the dispatcher may plan for (GB300: 232448
 // bytes opt-in per block, less a margin for the kernels' static shared memory).
 constexpr int kMaxDynSmem = 227 * 1024 - 1024;

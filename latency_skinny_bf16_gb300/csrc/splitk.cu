@@ -65,9 +65,12 @@ __host__ __device__ inline int round_up(int v, int a) { return (v + a - 1) / a *
 // persistent (each cluster owns one tile), to keep shared memory in bounds.
 __host__ __device__ constexpr int slot_buffers(int MT) { return MT >= 32 ? 1 : 2; }
 
-__host__ __device__ inline Layout make_layout(int MT, int consumer, int stages, int KS, int S, int bk) {
+// X holds the M real token rows only: the MMA consumer's fragment loads for
+// tokens M..MT-1 (whose sums are dropped) read row 0 instead.
+__host__ __device__ inline Layout make_layout(int MT, int M, int consumer, int stages, int KS, int S, int bk) {
     Layout L;
-    L.xrows = MT;   // MMA: MT is the token bucket 8 / 16 / 32 / 64, FMA: M
+    (void)consumer;
+    L.xrows = M;
     L.xrowb = round_up(KS * 2, 128) + 16;          // X row stride: 16 (mod 128)
     int off = 0;
     L.ring = off;  off += stages * kBN * ring_row_bytes(bk);
@@ -117,7 +120,7 @@ splitk_kernel(const SplitParams p)
     const int C = gridDim.y;                       // clusters, persistent over row tiles
     const int T = (p.N + kBN - 1) / kBN;           // row tiles of 16
     const int my_tiles = ((int)blockIdx.y < T) ? (T - 1 - (int)blockIdx.y) / C + 1 : 0;
-    const Layout L = make_layout(MT, CONS, p.stages, p.KS, S, p.bk);
+    const Layout L = make_layout(MT, p.M, CONS, p.stages, p.KS, S, p.bk);
     const int bk = p.bk;
     const int row_bytes = ring_row_bytes(bk);
     const int stage_bytes = kBN * row_bytes;
@@ -327,10 +330,22 @@ splitk_kernel(const SplitParams p)
                     } else {
                         // MMA: A = 16 W rows x 16 k (ldmatrix.x4), B = 16 k x MT tokens.
                         // The MMA sum is moved into the fp32 accumulator (a rounded
-                        // add) after at most 4 k16 steps.
+                        // add) after at most 4 k16 steps.  (Issuing every fragment load
+                        // of the 4 steps first, into 4 independent MMA chains, measured
+                        // no faster on GB300: the consumer is not what bounds this kernel.)
+                        constexpr int GB = (MT <= 8) ? 1 : MT / 16;   // B fragments per step
                         const int steps = len >> 4;
                         const uint32_t a_row = (lane & 7) + 8 * ((lane >> 3) & 1);
                         const uint32_t a_addr0 = stage + a_row * row_bytes + (lane >> 4) * 16;
+                        const uint32_t kh = (lane >> 3) & 1;
+                        // byte offset of the X row this lane addresses in each B fragment
+                        // (tokens past M read row 0; their sums are dropped)
+                        uint32_t xrow[GB];
+#pragma unroll
+                        for (int h2 = 0; h2 < GB; ++h2) {
+                            const int tok = (MT <= 8) ? (lane & 7) : (lane & 7) + 8 * (lane >> 4) + 16 * h2;
+                            xrow[h2] = (uint32_t)((tok < p.M ? tok : 0) * L.xrowb);
+                        }
                         for (int j0 = warp; j0 < steps; j0 += 4 * kSplitConsumerWarps) {
                             float d[NT][4];
 #pragma unroll
@@ -345,18 +360,15 @@ splitk_kernel(const SplitParams p)
                                     ldmatrix_x4(a_addr0 + j * 32, a[0], a[1], a[2], a[3]);
                                     const int kx = c * bk + j * 16;
                                     if constexpr (MT <= 8) {
-                                        const uint32_t tok = lane & 7, kh = (lane >> 3) & 1;
                                         uint32_t b0, b1;
-                                        ldmatrix_x2(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1);
+                                        ldmatrix_x2(xs_u32 + xrow[0] + (kx + 8 * kh) * 2, b0, b1);
                                         mma_bf16_16816(d[0], a, b0, b1, d[0]);
                                     } else {
                                         // 16 tokens per ldmatrix.x4; the A fragment serves every group
 #pragma unroll
-                                        for (int h2 = 0; h2 < MT / 16; ++h2) {
-                                            const uint32_t tok = (lane & 7) + 8 * (lane >> 4) + 16 * h2,
-                                                           kh = (lane >> 3) & 1;
+                                        for (int h2 = 0; h2 < GB; ++h2) {
                                             uint32_t b0, b1, b2, b3;
-                                            ldmatrix_x4(xs_u32 + tok * L.xrowb + (kx + 8 * kh) * 2, b0, b1, b2, b3);
+                                            ldmatrix_x4(xs_u32 + xrow[h2] + (kx + 8 * kh) * 2, b0, b1, b2, b3);
                                             mma_bf16_16816(d[2 * h2], a, b0, b1, d[2 * h2]);
                                             mma_bf16_16816(d[2 * h2 + 1], a, b2, b3, d[2 * h2 + 1]);
                                         }
@@ -470,7 +482,7 @@ bool splitk_supported(int M, int consumer, int block_n) {
 
 int splitk_smem_bytes(int M, int consumer, int block_n, int stages, int k_slice, int split_k, int bk) {
     (void)block_n;
-    return make_layout(mt_for(M, consumer), consumer, stages, k_slice, split_k, bk).total;
+    return make_layout(mt_for(M, consumer), M, consumer, stages, k_slice, split_k, bk).total;
 }
 
 cudaError_t splitk_prepare() {

@@ -56,6 +56,10 @@ def candidates(M: int, K: int, N: int = 0):
     for cons in (1, 2):
         if cons == 2 and K % 16:
             continue
+        if big and cons == 2:
+            # K-outer streaming: whole K per tile, one CTA per SM
+            for bk in (0, 1024, 2048):
+                out.append(dict(backend=3, consumer=2, split_k=0, stages=0, block_n=0, stage_k=bk))
         if big:
             for s in (1, 2, 3, 4, 6, 8):
                 for bk in (0, 1024, 2048):     # 0: the dispatcher's ring chunk for this shape

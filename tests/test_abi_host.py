@@ -129,7 +129,7 @@ def test_dotprod_block_n_grows_with_n():
 
 
 def test_default_rule_tensor_core_dotprod_for_large_weights():
-    p = plan(8, 8192, 4096)          # 64 MB of W, not tuned
+    p = plan(8, 8192, 3072)          # 48 MB of W, not tuned, K < 4096 (longer K streams)
     assert (p["backend"], p["consumer"]) == (sk.SKINNY_BACKEND_DOTPROD, sk.SKINNY_CONSUMER_MMA)
     assert p["block_n"] in (16, 32, 64) and p["grid_x"] * p["block_n"] >= 8192
     p = plan(2, 2112, 7168)
@@ -161,7 +161,7 @@ def test_forced_options_and_restore():
             plan(8, 256, 7176)
 
 
-@pytest.mark.parametrize("opt,bad", [(sk.SKINNY_OPT_PDL, 2), (sk.SKINNY_OPT_FORCE_BACKEND, 3),
+@pytest.mark.parametrize("opt,bad", [(sk.SKINNY_OPT_PDL, 2), (sk.SKINNY_OPT_FORCE_BACKEND, 4),
                                      (sk.SKINNY_OPT_FORCE_SPLIT_K, 9), (sk.SKINNY_OPT_FORCE_BLOCK_N, 3),
                                      (sk.SKINNY_OPT_FORCE_STAGES, 17), (sk.SKINNY_OPT_WAIT_TIMEOUT_US, -1),
                                      (99, 0)])
@@ -302,3 +302,50 @@ def test_mid_m_forced_split_sizes_plan():
                     assert e.status == sk.SKINNY_ERR_UNSUPPORTED and (S == 1 or (M > 32 and S == 2))
                     continue
             assert p["split_k"] == S and p["smem_bytes"] <= 227 * 1024
+
+
+# ---------------------------------------------------------------- K-outer streaming backend
+def test_stream_default_rule_for_large_weights_with_long_k():
+    p = plan(16, 8192, 8192)                 # 128 MB of W, not tuned
+    assert (p["backend"], p["consumer"]) == (sk.SKINNY_BACKEND_STREAM, sk.SKINNY_CONSUMER_MMA)
+    tiles = 8192 // 16
+    assert p["grid_x"] == 152 and p["grid_y"] == 1 and p["split_k"] == 1
+    per = -(-tiles // p["grid_x"])
+    assert per <= 4 and p["stages"] >= per + 1 and p["smem_bytes"] <= 227 * 1024
+    assert p["stage_k"] % 64 == 0 and p["stage_k"] <= 2048 and p["k_chunk"] == 8192
+    # K split into equal chunks of at most 2048 elements
+    assert -(-8192 // p["stage_k"]) * p["stage_k"] - 8192 < 64
+
+
+def test_stream_needs_aligned_x_and_w_and_k16():
+    for kw in (dict(X=A16 + 2), dict(ldx=8200 + 1), dict(W=B16 + 8)):
+        p = plan(16, 8192, 8192, **kw)
+        assert p["backend"] != sk.SKINNY_BACKEND_STREAM
+    with sk.options(backend=sk.SKINNY_BACKEND_STREAM):
+        for kw in (dict(X=A16 + 2), dict(W=B16 + 8)):
+            with pytest.raises(sk.SkinnyError) as e:
+                plan(8, 8192, 8192, **kw)
+            assert e.value.status == sk.SKINNY_ERR_UNSUPPORTED
+        with pytest.raises(sk.SkinnyError):
+            plan(8, 256, 7176)               # K % 16 != 0
+        with pytest.raises(sk.SkinnyError):
+            plan(17, 256, 7168)              # M > 16
+        with sk.options(consumer=sk.SKINNY_CONSUMER_FMA):
+            with pytest.raises(sk.SkinnyError):
+                plan(8, 256, 7168)
+
+
+def test_stream_forced_shapes_plan():
+    # small weights, forced: clusters = CTAs, every CTA at most 4 tiles
+    with sk.options(backend=sk.SKINNY_BACKEND_STREAM, clusters=5):
+        p = plan(3, 16 * 13 + 5, 4096)
+        assert p["grid_x"] == 5 and p["stages"] >= 4
+    with sk.options(backend=sk.SKINNY_BACKEND_STREAM, clusters=2):
+        with pytest.raises(sk.SkinnyError):  # 14 tiles on 2 CTAs: 7 per CTA > 4
+            plan(3, 16 * 13 + 5, 4096)
+    with sk.options(backend=sk.SKINNY_BACKEND_STREAM, clusters=5, stages=3):
+        with pytest.raises(sk.SkinnyError):  # the ring must hold 3 tiles + X + 1
+            plan(3, 16 * 13 + 5, 4096)
+    with sk.options(backend=sk.SKINNY_BACKEND_STREAM, stage_k=64):
+        p = plan(16, 37, 1040)
+        assert p["stage_k"] == 64 and p["grid_x"] == 3
