@@ -175,6 +175,23 @@ def merge_rows(K, N, rows, m_max=64):
     return lines
 
 
+def plannable_range(K, N, m_lo, m_hi, c, num_sms):
+    """The largest m_hi' <= m_hi such that the winner's forced plan exists for
+    every M in m_lo..m_hi' (a plan measured at one M may not fit a larger M
+    of the same line, e.g. its X slice); M past it keep the default rule."""
+    x, w, y = 0x7F0000000000, 0x7F0010000000, 0x7F0020000000   # 16-byte aligned, never dereferenced
+    opts = {k: v for k, v in c.items() if k in ("backend", "consumer", "split_k", "block_n", "stages", "stage_k")}
+    last = m_lo - 1
+    for M in range(m_lo, m_hi + 1):
+        with sk.options(**opts):
+            try:
+                sk.skinny_plan_for(x, K, w, K, y, N, M, N, K, num_sms)
+            except sk.SkinnyError:
+                break
+        last = M
+    return last
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--shapes", default=",".join(DEFAULT_SHAPES))
@@ -199,8 +216,12 @@ def main(argv=None):
     for shp in a.shapes.split(","):
         K, N = (int(v) for v in shp.lower().split("x"))
         rows = tune_shape(K, N, (m_large if 2 * N * K > 16e6 else m_small) + m_mid, l2, None, log)
+        num_sms = torch.cuda.get_device_properties(0).multi_processor_count
         for (k, n, mlo, mhi, be, co, sp, bn, st, bk, us) in merge_rows(K, N, rows):
-            out_lines.append(f"{{{k}, {n}, {mlo}, {mhi}, {be}, {co}, {sp}, {bn}, {st}, {bk}}},  // us/call {us}")
+            c = dict(backend=be, consumer=co, split_k=sp, block_n=bn, stages=st, stage_k=bk)
+            mhi = plannable_range(K, N, mlo, mhi, c, num_sms)
+            if mhi >= mlo:
+                out_lines.append(f"{{{k}, {n}, {mlo}, {mhi}, {be}, {co}, {sp}, {bn}, {st}, {bk}}},  // us/call {us}")
     text = "\n".join(out_lines) + "\n"
     if a.out == "-":
         sys.stdout.write(text)

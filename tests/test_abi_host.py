@@ -207,6 +207,10 @@ def test_every_tuned_entry_is_a_supported_plan_and_is_used():
                     assert p["stages"] == st
                 if bk:
                     assert p["stage_k"] == bk
+            elif be == sk.SKINNY_BACKEND_STREAM:
+                assert (p["consumer"], p["block_n"], p["grid_y"]) == (sk.SKINNY_CONSUMER_MMA, 16, 1)
+                if bk:
+                    assert p["stage_k"] == bk
             else:
                 assert p["block_n"] == bn and p["consumer"] == (co if co else sk.SKINNY_CONSUMER_FMA)
             assert p["smem_bytes"] <= 227 * 1024
