@@ -15,6 +15,11 @@ Blackwell decode optimizations", "Implementation breakdown" item 3: the bf16
 A x B^T decode projections).  This module only compiles the C file with the
 host compiler and marshals numpy arrays.
 
+It also holds the router epilogue that consumes the router logits: a
+softmax over each token's N logits and its k largest entries
+(``router_topk``); the pages print no epilogue, so the oracle takes the
+plainest one (see ``skinny_oracle.c``).
+
 Every function here is pinned by ``tests/test_oracle_pins.py`` to results that
 do not come from the oracle itself (hand-worked values under
 ``tests/golden/``, exact rational brute force, one-hot / identity / linearity /
@@ -71,6 +76,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.skinny_oracle_gemm_points.argtypes = [u16p, i64, u16p, i64, ctypes.c_int,
                                               i32p, i32p, ctypes.c_int, f64p, f64p]
     lib.skinny_oracle_gemm_points.restype = None
+    f32p = ctypes.POINTER(ctypes.c_float)
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    lib.skinny_oracle_router_topk.argtypes = [f32p, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              f64p, i64, i32p, i64, u8p]
+    lib.skinny_oracle_router_topk.restype = None
     return lib
 
 
@@ -163,6 +173,31 @@ def gemm_points(X: np.ndarray, W: np.ndarray, K: int, rows, cols,
                                   K, r.ctypes.data_as(i32p), c.ctypes.data_as(i32p), r.size,
                                   y.ctypes.data_as(f64p), a.ctypes.data_as(f64p))
     return y, a
+
+
+def router_topk(logits: np.ndarray, k: int, renormalize: bool = False, lib: ctypes.CDLL | None = None):
+    """Softmax over each row of the float32 ``logits [M, N]`` and its ``k``
+    largest entries: returns ``(weights [M, k] fp64, ids [M, k] int32)``, ids in
+    descending order of the float32 logit, equal logits by ascending index
+    (the router epilogue in ``skinny_oracle.c``)."""
+    lib = lib or load()
+    L = np.ascontiguousarray(logits, dtype=np.float32)
+    if L.ndim != 2:
+        raise ValueError("logits must be [M, N]")
+    M, N = L.shape
+    if not 1 <= k <= N:
+        raise ValueError("need 1 <= k <= N")
+    w = np.empty((M, k), np.float64)
+    ids = np.empty((M, k), np.int32)
+    scratch = np.empty(N, np.uint8)
+    f32p = ctypes.POINTER(ctypes.c_float)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    lib.skinny_oracle_router_topk(L.ctypes.data_as(f32p), N, M, N, k, 1 if renormalize else 0,
+                                  w.ctypes.data_as(f64p), k, ids.ctypes.data_as(i32p), k,
+                                  scratch.ctypes.data_as(u8p))
+    return w, ids
 
 
 SOURCE_PATH = _SRC

@@ -96,3 +96,46 @@ void skinny_oracle_gemm_points(const uint16_t *X, int64_t ldx,
         if (a) a[i] = abs_sum;
     }
 }
+
+/* Router epilogue (the consumer of the router logits: "[Perf][Feat] Add
+ * generic cuteDSL LL BF16 router (GEMM)", section "Implementation breakdown"
+ * item 4, the MoE gate's forward; the pages print no epilogue, so this is the
+ * plainest one): for each token m, the softmax of its N logits and the k
+ * experts of largest probability.
+ *
+ *   p_n = exp(l_n - l_max) / sum_j exp(l_j - l_max)          (fp64)
+ *   ids  = the k indices of the largest logits, in descending order of the
+ *          logit as given (float32), equal logits by ascending index
+ *   weights[i] = p_{ids[i]}, or with renormalize != 0
+ *   weights[i] = p_{ids[i]} / sum_{i'<k} p_{ids[i']}
+ *
+ * Selection is made on the float32 logits exactly as given (the same values
+ * the GPU kernel compares), by k passes of "largest not yet chosen" over the
+ * row.  Rows must hold at least one finite logit; 1 <= k <= N. */
+void skinny_oracle_router_topk(const float *L, int64_t ldl, int M, int N, int k, int renormalize,
+                               double *weights, int64_t ldwt, int32_t *ids, int64_t ldid,
+                               unsigned char *taken /* N bytes of scratch */)
+{
+    for (int m = 0; m < M; ++m) {
+        const float *row = L + (int64_t)m * ldl;
+        float lmax = row[0];
+        for (int n = 1; n < N; ++n)
+            if (row[n] > lmax) lmax = row[n];
+        double denom = 0.0;
+        for (int n = 0; n < N; ++n) denom += exp((double)row[n] - (double)lmax);
+        memset(taken, 0, (size_t)N);
+        double chosen = 0.0;
+        for (int i = 0; i < k; ++i) {
+            int best = -1;
+            for (int n = 0; n < N; ++n)
+                if (!taken[n] && (best < 0 || row[n] > row[best])) best = n;
+            taken[best] = 1;
+            ids[(int64_t)m * ldid + i] = best;
+            const double pv = exp((double)row[best] - (double)lmax) / denom;
+            weights[(int64_t)m * ldwt + i] = pv;
+            chosen += pv;
+        }
+        if (renormalize)
+            for (int i = 0; i < k; ++i) weights[(int64_t)m * ldwt + i] /= chosen;
+    }
+}

@@ -399,3 +399,123 @@ def test_planted_mistakes_are_caught():
             so = os.path.join(td, f"mut_{abs(hash(name))}.so")
             oracle.build(src=path, out=so)
             assert not _pins_pass(oracle.load(so)), f"planted mistake not caught: {name}"
+
+
+# ---------------------------------------------------------------- router epilogue (softmax + top-k)
+
+def test_topk_uniform_logits_closed_form():
+    """N equal logits: every probability is 1/N, ties go to the lower index."""
+    for N, k in ((8, 3), (256, 8), (5, 5)):
+        w, ids = oracle.router_topk(np.full((2, N), 0.75, np.float32), k)
+        assert ids.tolist() == [list(range(k))] * 2
+        assert np.allclose(w, 1.0 / N, rtol=1e-15, atol=0)
+        wr, _ = oracle.router_topk(np.full((1, N), -3.0, np.float32), k, renormalize=True)
+        assert np.allclose(wr, 1.0 / k, rtol=1e-15, atol=0)
+
+
+def test_topk_two_level_logits_closed_form():
+    """s logits at c and N - s at c - ln(t): the high ones each carry 1 / (s + (N - s) / t)."""
+    N, s, t = 64, 5, 4.0
+    L = np.zeros((1, N), np.float32)
+    hi = [3, 17, 18, 40, 63]
+    L[0, :] = np.float32(2.0 - math.log(t))
+    L[0, hi] = 2.0
+    w, ids = oracle.router_topk(L, s)
+    assert ids[0].tolist() == hi
+    lo = float(np.float32(2.0 - math.log(t)))
+    expected = 1.0 / (s + (N - s) * math.exp(lo - 2.0))
+    assert np.allclose(w, expected, rtol=1e-14, atol=0)
+
+
+def test_topk_matches_stable_argsort_and_library_softmax():
+    """Selection equals numpy's stable sort of the negated logits (ties by
+    index); probabilities equal scipy's softmax."""
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(31)
+    for N, k in ((256, 8), (384, 8), (37, 37), (1000, 1), (16, 4)):
+        L = rng.standard_normal((6, N)).astype(np.float32)
+        L[0, 5] = L[0, 7] = L[0, 9] = L[0].max() + 1     # a three-way tie at the top
+        L[1, ::3] = np.float32(0.25)                       # many ties in the middle
+        for renorm in (False, True):
+            w, ids = oracle.router_topk(L, k, renormalize=renorm)
+            ref_ids = np.argsort(-L, axis=1, kind="stable")[:, :k]
+            assert np.array_equal(ids, ref_ids)
+            p = special.softmax(L.astype(np.float64), axis=1)
+            ref_w = np.take_along_axis(p, ref_ids, axis=1)
+            if renorm:
+                ref_w = ref_w / ref_w.sum(axis=1, keepdims=True)
+            assert np.allclose(w, ref_w, rtol=1e-13, atol=1e-300)
+
+
+def test_topk_invariants():
+    rng = np.random.default_rng(32)
+    # multiples of 2^-10 below 16 in magnitude: adding 64 below keeps every logit exact
+    L = (np.round(np.clip(rng.standard_normal((4, 200)) * 3, -15, 15) * 1024) / 1024).astype(np.float32)
+    w_all, ids_all = oracle.router_topk(L, 200)
+    assert np.allclose(w_all.sum(axis=1), 1.0, rtol=1e-13)               # the full softmax sums to 1
+    assert (np.diff(w_all, axis=1) <= 0).all()                            # descending
+    assert sorted(ids_all[0].tolist()) == list(range(200))                # a permutation
+    w8, ids8 = oracle.router_topk(L, 8)
+    assert np.array_equal(ids8, ids_all[:, :8]) and np.array_equal(w8, w_all[:, :8])   # prefix of the full order
+    wr, _ = oracle.router_topk(L, 8, renormalize=True)
+    assert np.allclose(wr.sum(axis=1), 1.0, rtol=1e-13)
+    # shifting every logit by the same exactly representable amount changes nothing
+    w_s, ids_s = oracle.router_topk(L + np.float32(64.0), 8)
+    assert np.array_equal(ids_s, ids8)
+    assert np.allclose(w_s, w8, rtol=1e-12)
+    # a row with -inf entries: they get probability 0 and come last
+    Li = L[:1].copy()
+    Li[0, :100] = -np.inf
+    wi, idsi = oracle.router_topk(Li, 120)
+    assert (idsi[0, :100] >= 100).all() and (wi[0, 100:] == 0).all()
+
+
+def _topk_pins_pass(lib) -> bool:
+    """A compact subset of the top-k pins, run against a given oracle build."""
+    try:
+        w, ids = oracle.router_topk(np.full((1, 8), 0.5, np.float32), 3, lib=lib)
+        if ids.tolist() != [[0, 1, 2]] or not np.allclose(w, 1 / 8, rtol=1e-15, atol=0):
+            return False
+        rng = np.random.default_rng(33)
+        L = rng.standard_normal((3, 50)).astype(np.float32)
+        L[0, 10] = L[0, 20] = L[0].max() + 1
+        for renorm in (False, True):
+            w, ids = oracle.router_topk(L, 6, renormalize=renorm, lib=lib)
+            ref_ids = np.argsort(-L, axis=1, kind="stable")[:, :6]
+            e = np.exp(L.astype(np.float64) - L.max(axis=1, keepdims=True).astype(np.float64))
+            p = e / e.sum(axis=1, keepdims=True)
+            ref_w = np.take_along_axis(p, ref_ids, axis=1)
+            if renorm:
+                ref_w = ref_w / ref_w.sum(axis=1, keepdims=True)
+            if not np.array_equal(ids, ref_ids) or not np.allclose(w, ref_w, rtol=1e-13, atol=0):
+                return False
+        return True
+    except Exception:
+        return False
+
+
+TOPK_MUTATIONS = [
+    ("ties to the higher index", "(best < 0 || row[n] > row[best])", "(best < 0 || row[n] >= row[best])"),
+    ("smallest first", "(best < 0 || row[n] > row[best])", "(best < 0 || row[n] < row[best])"),
+    ("no renormalisation", "weights[(int64_t)m * ldwt + i] /= chosen;", "weights[(int64_t)m * ldwt + i] *= 1.0;"),
+    ("id off by one", "ids[(int64_t)m * ldid + i] = best;", "ids[(int64_t)m * ldid + i] = best + 1;"),
+    ("denominator misses the last logit", "for (int n = 0; n < N; ++n) denom += exp",
+     "for (int n = 0; n < N - 1; ++n) denom += exp"),
+]
+
+
+def test_topk_planted_mistakes_are_caught():
+    with open(oracle.SOURCE_PATH) as f:
+        src = f.read()
+    with tempfile.TemporaryDirectory() as td:
+        clean_so = os.path.join(td, "clean.so")
+        oracle.build(src=oracle.SOURCE_PATH, out=clean_so)
+        assert _topk_pins_pass(oracle.load(clean_so))
+        for name, old, new in TOPK_MUTATIONS:
+            assert src.count(old) == 1, f"mutation anchor not unique: {name}"
+            path = os.path.join(td, "mut.c")
+            with open(path, "w") as f:
+                f.write(src.replace(old, new))
+            so = os.path.join(td, f"mut_topk_{abs(hash(name))}.so")
+            oracle.build(src=path, out=so)
+            assert not _topk_pins_pass(oracle.load(so)), f"planted mistake not caught: {name}"
