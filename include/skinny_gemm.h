@@ -191,6 +191,50 @@ SKINNY_API skinny_status_t skinny_plan_for(const uint16_t *X, int ldx, const uin
 SKINNY_API skinny_status_t skinny_set_option(int option, int value);
 SKINNY_API skinny_status_t skinny_get_option(int option, int *value);
 
+/*
+ * Router epilogue: for each token m < M, the softmax of its N logits
+ * (logits[m*ldl + n], fp32) and its k largest ones.
+ *
+ *     p_n          = exp(l_n - max_j l_j) / sum_j exp(l_j - max_j l_j)
+ *     ids[m*ldid+i]     = index of the i-th largest logit (i < k), descending;
+ *                         equal logits: lower index first
+ *     weights[m*ldw+i]  = p of that expert, or with renormalize != 0 that p
+ *                         divided by the sum of the k chosen p
+ *
+ * Operation defined by: "[Perf][Feat] Add generic cuteDSL LL BF16 router
+ * (GEMM)", section "Implementation breakdown" item 4 (the MoE gate's forward
+ * consumes the router logits); the pages print no epilogue, so this is the
+ * plainest softmax / top-k one.  fp32 arithmetic (CUDA expf); the selection
+ * compares the fp32 logits exactly as stored; bit-identical run to run.
+ *
+ *   logits   device, fp32 [M, N], row stride ldl >= N, 4-byte aligned; at least
+ *            one finite logit per row (NaN logits are never chosen)
+ *   weights  device, fp32 [M, k], row stride ldw >= k; ids device, int32 [M, k],
+ *            row stride ldid >= k; 4-byte aligned; neither may overlap the
+ *            logits or each other.  Only the [M, k] entries are written.
+ *   M >= 0 (0: no-op), 1 <= N <= 8192, 0 <= k <= min(N, 64) (k = 0: no-op).
+ *
+ * Asynchronous on `stream`; with PDL on (SKINNY_OPT_PDL) it may start while
+ * the preceding kernel (the router GEMM) drains and waits for it before
+ * reading the logits.  Errors are found on the host: INVALID_VALUE (sizes,
+ * strides, NULL, overlap), UNSUPPORTED (N > 8192, k > 64, M > 65535),
+ * MISALIGNED, NO_DEVICE, LAUNCH.
+ */
+SKINNY_API skinny_status_t skinny_router_topk(const float *logits, int ldl, int M, int N, int k, int renormalize,
+                                   float *weights, int ldw, int32_t *ids, int ldid, void *stream);
+
+/*
+ * The router in one call: skinny_gemm_bf16(X, W -> logits) then
+ * skinny_router_topk(logits -> weights, ids) on the same stream.  `logits` is
+ * the caller's [M, N] fp32 buffer (row stride ldl), written by the GEMM and
+ * read by the epilogue; nothing is allocated.  Every argument of both steps is
+ * checked before anything is launched (weights / ids must not overlap X, W or
+ * the logits); the statuses are those of the two calls.
+ */
+SKINNY_API skinny_status_t skinny_router_bf16_topk(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
+                                        float *logits, int ldl, int M, int N, int K, int k, int renormalize,
+                                        float *weights, int ldwt, int32_t *ids, int ldid, void *stream);
+
 /* Synchronises `stream`, then reads and clears the current device's status
  * word: *code = 0 if no kernel reported an error since the last read, else a
  * value whose low 8 bits are a skinny_status_t (SKINNY_ERR_DEVICE_TIMEOUT)

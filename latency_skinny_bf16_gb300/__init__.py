@@ -23,7 +23,8 @@ __all__ = [
     "SkinnyError", "load_library", "library_path",
     "skinny_gemm_bf16", "skinny_gemm_bf16_bf16out", "skinny_init", "skinny_query_plan", "skinny_plan_for",
     "skinny_set_option", "skinny_get_option", "skinny_get_device_status",
-    "skinny_status_string", "skinny_version", "gemm", "options",
+    "skinny_status_string", "skinny_version", "skinny_router_topk", "skinny_router_bf16_topk",
+    "gemm", "router_topk", "options",
 ]
 
 # ---- constants mirrored from include/skinny_gemm.h
@@ -58,7 +59,7 @@ SKINNY_OPT_FORCE_STAGE_K = 10
 EXPORTED_SYMBOLS = (
     "skinny_gemm_bf16", "skinny_gemm_bf16_bf16out", "skinny_init", "skinny_query_plan", "skinny_plan_for",
     "skinny_set_option", "skinny_get_option", "skinny_get_device_status",
-    "skinny_status_string", "skinny_version",
+    "skinny_status_string", "skinny_version", "skinny_router_topk", "skinny_router_bf16_topk",
 )
 
 
@@ -94,6 +95,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.skinny_gemm_bf16.restype = i
     lib.skinny_gemm_bf16_bf16out.argtypes = [vp, i, vp, i, vp, i, i, i, i, vp]
     lib.skinny_gemm_bf16_bf16out.restype = i
+    lib.skinny_router_topk.argtypes = [vp, i, i, i, i, i, vp, i, vp, i, vp]
+    lib.skinny_router_topk.restype = i
+    lib.skinny_router_bf16_topk.argtypes = [vp, i, vp, i, vp, i, i, i, i, i, i, vp, i, vp, i, vp]
+    lib.skinny_router_bf16_topk.restype = i
     lib.skinny_init.argtypes = [i]
     lib.skinny_init.restype = i
     lib.skinny_query_plan.argtypes = [vp, i, vp, i, vp, i, i, i, i, ctypes.POINTER(_Plan)]
@@ -135,6 +140,20 @@ def skinny_gemm_bf16(X: int, ldx: int, W: int, ldw: int, Y: int, ldy: int,
                      M: int, N: int, K: int, stream: int = 0) -> int:
     """Raw C call: device pointers as ints; returns the skinny_status_t."""
     return load_library().skinny_gemm_bf16(X, ldx, W, ldw, Y, ldy, M, N, K, stream)
+
+
+def skinny_router_topk(L: int, ldl: int, M: int, N: int, k: int, renormalize: int,
+                       weights: int, ldw: int, ids: int, ldid: int, stream: int = 0) -> int:
+    """Raw C call of the router epilogue (softmax + top-k); returns the skinny_status_t."""
+    return load_library().skinny_router_topk(L, ldl, M, N, k, renormalize, weights, ldw, ids, ldid, stream)
+
+
+def skinny_router_bf16_topk(X: int, ldx: int, W: int, ldw: int, L: int, ldl: int, M: int, N: int, K: int,
+                            k: int, renormalize: int, weights: int, ldwt: int, ids: int, ldid: int,
+                            stream: int = 0) -> int:
+    """Raw C call of the whole router (GEMM into L, then softmax + top-k)."""
+    return load_library().skinny_router_bf16_topk(X, ldx, W, ldw, L, ldl, M, N, K, k, renormalize,
+                                                  weights, ldwt, ids, ldid, stream)
 
 
 def skinny_gemm_bf16_bf16out(X: int, ldx: int, W: int, ldw: int, Y: int, ldy: int,
@@ -255,3 +274,29 @@ def gemm(x, w, out=None, stream=None):
     if st != SKINNY_OK:
         raise SkinnyError(st, "skinny_gemm_bf16")
     return out
+
+
+def router_topk(logits, k, renormalize=False, weights=None, ids=None, stream=None):
+    """Softmax over each row of the CUDA fp32 ``logits [M, N]`` (unit column
+    stride) and its ``k`` largest entries: returns ``(weights fp32 [M, k],
+    ids int32 [M, k])``; see ``skinny_router_topk`` in include/skinny_gemm.h."""
+    import torch
+    if logits.dtype != torch.float32 or logits.dim() != 2 or not logits.is_cuda:
+        raise ValueError("logits must be a CUDA fp32 [M, N] tensor")
+    M, N = logits.shape
+    if N > 1 and logits.stride(1) != 1:
+        raise ValueError("logits need unit column stride")
+    if weights is None:
+        weights = torch.empty((M, k), dtype=torch.float32, device=logits.device)
+    if ids is None:
+        ids = torch.empty((M, k), dtype=torch.int32, device=logits.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(logits.device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    ldl = logits.stride(0) if M > 1 else max(N, 1)
+    st = skinny_router_topk(logits.data_ptr(), ldl, M, N, k, 1 if renormalize else 0,
+                            weights.data_ptr(), weights.stride(0) if M > 1 else max(k, 1),
+                            ids.data_ptr(), ids.stride(0) if M > 1 else max(k, 1), s)
+    if st != SKINNY_OK:
+        raise SkinnyError(st, "skinny_router_topk")
+    return weights, ids

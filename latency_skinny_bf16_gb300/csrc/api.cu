@@ -527,10 +527,73 @@ skinny_status_t run_gemm(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
         e = launch_splitk(a, plan, c);
     return e == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
 }
+
+// Host-only checks of the router epilogue's arguments; *noop when M == 0 or k == 0.
+skinny_status_t validate_topk(const float *L, int ldl, int M, int N, int k, const float *Wt, int ldwt,
+                              const int32_t *ids, int ldid, bool *noop) {
+    *noop = false;
+    if (M < 0 || N < 0 || k < 0) return SKINNY_ERR_INVALID_VALUE;
+    if (M == 0 || k == 0) { *noop = true; return SKINNY_OK; }
+    if (N < 1 || k > N) return SKINNY_ERR_INVALID_VALUE;
+    if (N > kTopkMaxN || k > kTopkMaxK || M > 65535) return SKINNY_ERR_UNSUPPORTED;
+    if (!L || !Wt || !ids || ldl < N || ldwt < k || ldid < k) return SKINNY_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(L) | reinterpret_cast<uintptr_t>(Wt) | reinterpret_cast<uintptr_t>(ids)) & 3)
+        return SKINNY_ERR_MISALIGNED;
+    const uintptr_t l0 = reinterpret_cast<uintptr_t>(L), l1 = l0 + (uintptr_t)(((int64_t)(M - 1) * ldl + N) * 4);
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(Wt), w1 = w0 + (uintptr_t)(((int64_t)(M - 1) * ldwt + k) * 4);
+    const uintptr_t i0 = reinterpret_cast<uintptr_t>(ids), i1 = i0 + (uintptr_t)(((int64_t)(M - 1) * ldid + k) * 4);
+    if (ranges_overlap(w0, w1, l0, l1) || ranges_overlap(i0, i1, l0, l1) || ranges_overlap(w0, w1, i0, i1))
+        return SKINNY_ERR_INVALID_VALUE;
+    return SKINNY_OK;
+}
+
+skinny_status_t run_topk(const float *L, int ldl, int M, int N, int k, int renormalize, float *Wt, int ldwt,
+                         int32_t *ids, int ldid, void *stream) {
+    int device = 0;
+    skinny_status_t st = current_device(&device);
+    if (st != SKINNY_OK) return st;
+    const cudaError_t e = launch_router_topk(L, ldl, M, N, k, renormalize ? 1 : 0, Wt, ldwt, ids, ldid,
+                                             static_cast<cudaStream_t>(stream), opt_pdl() != 0);
+    return e == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
+}
 }  // namespace
 }  // namespace skinny
 
 extern "C" {
+
+skinny_status_t skinny_router_topk(const float *logits, int ldl, int M, int N, int k, int renormalize,
+                                   float *weights, int ldw, int32_t *ids, int ldid, void *stream) {
+    bool noop = false;
+    const skinny_status_t st = validate_topk(logits, ldl, M, N, k, weights, ldw, ids, ldid, &noop);
+    if (st != SKINNY_OK || noop) return st;
+    return run_topk(logits, ldl, M, N, k, renormalize, weights, ldw, ids, ldid, stream);
+}
+
+skinny_status_t skinny_router_bf16_topk(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
+                                        float *logits, int ldl, int M, int N, int K, int k, int renormalize,
+                                        float *weights, int ldwt, int32_t *ids, int ldid, void *stream) {
+    // every argument of both steps is checked before anything is launched
+    bool noop_g = false, noop_t = false;
+    skinny_status_t st = validate(X, ldx, W, ldw, logits, ldl, M, N, K, &noop_g, 4);
+    if (st != SKINNY_OK) return st;
+    st = validate_topk(logits, ldl, M, N, k, weights, ldwt, ids, ldid, &noop_t);
+    if (st != SKINNY_OK) return st;
+    if (!noop_t) {
+        const uintptr_t w0 = reinterpret_cast<uintptr_t>(weights), i0 = reinterpret_cast<uintptr_t>(ids);
+        const uintptr_t w1 = w0 + (uintptr_t)(((int64_t)(M - 1) * ldwt + k) * 4);
+        const uintptr_t i1 = i0 + (uintptr_t)(((int64_t)(M - 1) * ldid + k) * 4);
+        if (K > 0) {
+            const uintptr_t x0 = reinterpret_cast<uintptr_t>(X), x1 = x0 + (uintptr_t)(((int64_t)(M - 1) * ldx + K) * 2);
+            const uintptr_t v0 = reinterpret_cast<uintptr_t>(W), v1 = v0 + (uintptr_t)(((int64_t)(N - 1) * ldw + K) * 2);
+            if (ranges_overlap(w0, w1, x0, x1) || ranges_overlap(w0, w1, v0, v1) ||
+                ranges_overlap(i0, i1, x0, x1) || ranges_overlap(i0, i1, v0, v1))
+                return SKINNY_ERR_INVALID_VALUE;
+        }
+    }
+    st = run_gemm(X, ldx, W, ldw, logits, ldl, M, N, K, stream, 0);
+    if (st != SKINNY_OK || noop_t) return st;
+    return run_topk(logits, ldl, M, N, k, renormalize, weights, ldwt, ids, ldid, stream);
+}
 
 skinny_status_t skinny_gemm_bf16(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
                                  float *Y, int ldy, int M, int N, int K, void *stream) {

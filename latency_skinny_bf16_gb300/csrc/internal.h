@@ -67,6 +67,13 @@ bool stream_supported(int M);
 cudaError_t stream_prepare();
 cudaError_t launch_stream(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
 
+// ---- router epilogue (topk.cu): softmax + top-k over each token's logits
+constexpr int kTopkMaxN = 8192;   // logits per token (shared memory: 5 bytes each)
+constexpr int kTopkMaxK = 64;
+int router_topk_smem_bytes(int N);
+cudaError_t launch_router_topk(const float *L, int64_t ldl, int M, int N, int k, int renormalize, float *weights,
+                               int64_t ldwt, int32_t *ids, int64_t ldid, cudaStream_t stream, bool pdl);
+
 // Per-CTA dynamic shared memory the dispatcher may plan for (GB300: 232448
 // bytes opt-in per block, less a margin for the kernels' static shared memory).
 constexpr int kMaxDynSmem = 227 * 1024 - 1024;

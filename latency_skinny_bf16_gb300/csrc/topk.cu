@@ -1,0 +1,136 @@
+// topk.cu -- the router epilogue: softmax over each token's expert logits and
+// its top-k experts.
+//
+// Design source: "[Perf][Feat] Add generic cuteDSL LL BF16 router (GEMM)",
+// section "Implementation breakdown" item 4 (the MoE gate's forward consumes
+// the router logits).  The pages print no epilogue, so this is the plainest
+// one: p = softmax(logits of the token), the k largest logits (equal logits:
+// lower index first), weights p of those, optionally renormalised to sum to 1.
+//
+// GB300 form.  A separate small kernel, launched right after the router GEMM
+// on the same stream (with PDL it starts while the GEMM drains and waits for
+// it in griddepcontrol.wait): the k largest entries of a token need all N of
+// its logits, which the GEMM spreads over many CTAs and clusters.  One CTA of
+// 128 threads per token keeps the row in shared memory; the max and the sum
+// of exponentials are reduced in a fixed order (per thread ascending, warp
+// butterfly, warps in order), and each of the k selections is a block-wide
+// argmax over the entries not yet taken, so results are bit-identical from
+// run to run.  expf is CUDA's own.
+#include "common.cuh"
+#include "internal.h"
+
+namespace skinny {
+namespace {
+
+constexpr int kTopkThreads = 128;
+constexpr int kTopkWarps = kTopkThreads / 32;
+
+// (v, n) is a better pick than (bv, bn): larger value, equal value lower index;
+// n < 0 marks "none yet"
+__device__ __forceinline__ bool better(float v, int n, float bv, int bn) {
+    return n >= 0 && (bn < 0 || v > bv || (v == bv && n < bn));
+}
+
+__global__ void __launch_bounds__(kTopkThreads)
+router_topk_kernel(const float *__restrict__ L, int64_t ldl, int N, int k, int renormalize,
+                   float *__restrict__ weights, int64_t ldwt, int32_t *__restrict__ ids, int64_t ldid)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    float *row = reinterpret_cast<float *>(smem);                       // [N]
+    uint8_t *taken = smem + (size_t)N * 4;                              // [N]
+    __shared__ float wv[kTopkWarps];
+    __shared__ int wn[kTopkWarps];
+    __shared__ float chosen[kTopkMaxK];
+    __shared__ float stat[2];   // max, sum of exponentials
+    const int m = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    griddep_wait();   // the logits come from the preceding kernel (the router GEMM)
+    const float *src = L + (int64_t)m * ldl;
+    float lmax = -INFINITY;
+    for (int n = tid; n < N; n += kTopkThreads) {
+        const float v = src[n];
+        row[n] = v;
+        taken[n] = 0;
+        lmax = fmaxf(lmax, v);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+    if (lane == 0) wv[warp] = lmax;
+    __syncthreads();
+    if (tid == 0) {
+        float v = wv[0];
+        for (int w = 1; w < kTopkWarps; ++w) v = fmaxf(v, wv[w]);
+        stat[0] = v;
+    }
+    __syncthreads();
+    lmax = stat[0];
+    float s = 0.f;
+    for (int n = tid; n < N; n += kTopkThreads) s += expf(row[n] - lmax);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    if (lane == 0) wv[warp] = s;
+    __syncthreads();
+    if (tid == 0) {
+        float v = wv[0];
+        for (int w = 1; w < kTopkWarps; ++w) v += wv[w];
+        stat[1] = v;
+    }
+    __syncthreads();
+    const float denom = stat[1];
+
+    for (int i = 0; i < k; ++i) {
+        float bv = -INFINITY;
+        int bn = -1;
+        for (int n = tid; n < N; n += kTopkThreads)
+            if (!taken[n] && better(row[n], n, bv, bn)) { bv = row[n]; bn = n; }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            const int on = __shfl_xor_sync(0xFFFFFFFFu, bn, o);
+            if (better(ov, on, bv, bn)) { bv = ov; bn = on; }
+        }
+        if (lane == 0) { wv[warp] = bv; wn[warp] = bn; }
+        __syncthreads();
+        if (tid == 0) {
+            float v = wv[0];
+            int n = wn[0];
+            for (int w = 1; w < kTopkWarps; ++w)
+                if (better(wv[w], wn[w], v, n)) { v = wv[w]; n = wn[w]; }
+            taken[n] = 1;
+            ids[(int64_t)m * ldid + i] = n;
+            chosen[i] = expf(row[n] - lmax) / denom;
+        }
+        __syncthreads();
+    }
+    if (tid == 0 && renormalize) {
+        float t = 0.f;
+        for (int i = 0; i < k; ++i) t += chosen[i];
+        stat[1] = t;
+    }
+    __syncthreads();
+    griddep_launch_dependents();
+    for (int i = tid; i < k; i += kTopkThreads)
+        weights[(int64_t)m * ldwt + i] = renormalize ? chosen[i] / stat[1] : chosen[i];
+}
+
+}  // namespace
+
+int router_topk_smem_bytes(int N) { return N * 5; }
+
+cudaError_t launch_router_topk(const float *L, int64_t ldl, int M, int N, int k, int renormalize, float *weights,
+                               int64_t ldwt, int32_t *ids, int64_t ldid, cudaStream_t stream, bool pdl) {
+    if (M < 1 || N < 1 || N > kTopkMaxN || k < 1 || k > N || k > kTopkMaxK) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)M, 1, 1);
+    cfg.blockDim = dim3(kTopkThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)router_topk_smem_bytes(N);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, router_topk_kernel, L, ldl, N, k, renormalize, weights, ldwt, ids, ldid);
+}
+
+}  // namespace skinny

@@ -353,3 +353,57 @@ def test_stream_forced_shapes_plan():
     with sk.options(backend=sk.SKINNY_BACKEND_STREAM, stage_k=64):
         p = plan(16, 37, 1040)
         assert p["stage_k"] == 64 and p["grid_x"] == 3
+
+
+# ---------------------------------------------------------------- router epilogue (softmax + top-k)
+D16 = 0x7F0030000000
+
+
+def topk_call(L=C16, ldl=256, M=4, N=256, k=8, renorm=0, Wt=A16, ldw=8, ids=B16, ldid=8):
+    return sk.skinny_router_topk(L, ldl, M, N, k, renorm, Wt, ldw, ids, ldid, 0)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(M=-1), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(N=-1), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(k=-1), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(M=0), sk.SKINNY_OK),
+    (dict(k=0), sk.SKINNY_OK),
+    (dict(M=0, L=0, Wt=0, ids=0), sk.SKINNY_OK),
+    (dict(k=257, ldw=300, ldid=300), sk.SKINNY_ERR_INVALID_VALUE),       # k > N
+    (dict(N=8193, ldl=8193), sk.SKINNY_ERR_UNSUPPORTED),
+    (dict(k=65, ldw=65, ldid=65), sk.SKINNY_ERR_UNSUPPORTED),
+    (dict(M=65536), sk.SKINNY_ERR_UNSUPPORTED),
+    (dict(ldl=255), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(ldw=7), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(ldid=7), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(L=0), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(Wt=0), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(ids=0), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(L=C16 + 2), sk.SKINNY_ERR_MISALIGNED),
+    (dict(Wt=A16 + 2), sk.SKINNY_ERR_MISALIGNED),
+    (dict(ids=B16 + 1), sk.SKINNY_ERR_MISALIGNED),
+    (dict(Wt=C16 + 64), sk.SKINNY_ERR_INVALID_VALUE),                     # weights overlap the logits
+    (dict(ids=C16 + 4 * 256 * 3), sk.SKINNY_ERR_INVALID_VALUE),           # ids overlap the logits
+    (dict(ids=A16 + 16), sk.SKINNY_ERR_INVALID_VALUE),                    # ids overlap the weights
+    (dict(), sk.SKINNY_ERR_NO_DEVICE),                                    # valid: needs a GPU
+])
+def test_router_topk_argument_errors_are_host_side(kw, expect):
+    assert topk_call(**kw) == expect
+
+
+def test_router_fused_checks_both_steps_before_launching():
+    def fused(**kw):
+        a = dict(X=A16, ldx=7168, W=B16, ldw=7168, L=C16, ldl=256, M=4, N=256, K=7168, k=8, renorm=1,
+                 Wt=D16, ldwt=8, ids=D16 + 4096, ldid=8)
+        a.update(kw)
+        return sk.skinny_router_bf16_topk(a["X"], a["ldx"], a["W"], a["ldw"], a["L"], a["ldl"], a["M"], a["N"],
+                                          a["K"], a["k"], a["renorm"], a["Wt"], a["ldwt"], a["ids"], a["ldid"], 0)
+    assert fused() == sk.SKINNY_ERR_NO_DEVICE
+    assert fused(M=65) == sk.SKINNY_ERR_UNSUPPORTED                   # GEMM: M > 64
+    assert fused(ldx=100) == sk.SKINNY_ERR_INVALID_VALUE              # GEMM: ldx < K
+    assert fused(k=100) == sk.SKINNY_ERR_UNSUPPORTED                  # epilogue: k > 64
+    assert fused(Wt=B16 + 64) == sk.SKINNY_ERR_INVALID_VALUE          # weights overlap W
+    assert fused(ids=A16 + 8) == sk.SKINNY_ERR_INVALID_VALUE          # ids overlap X
+    assert fused(L=B16 + 1024) == sk.SKINNY_ERR_INVALID_VALUE         # logits overlap W
+    assert fused(M=0) == sk.SKINNY_OK
