@@ -15,7 +15,9 @@ Blackwell decode optimizations", "Implementation breakdown" item 3: the bf16
 A x B^T decode projections).  This module only compiles the C file with the
 host compiler and marshals numpy arrays.
 
-It also holds the router epilogue that consumes the router logits: a
+``gemm_f32w`` is the same definition with fp32 weights (the router GEMM
+for models that keep fp32 router weights).  It also holds the router
+epilogue that consumes the router logits: a
 softmax over each token's N logits and its k largest entries
 (``router_topk``); the pages print no epilogue, so the oracle takes the
 plainest one (see ``skinny_oracle.c``).
@@ -78,6 +80,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.skinny_oracle_gemm_points.restype = None
     f32p = ctypes.POINTER(ctypes.c_float)
     u8p = ctypes.POINTER(ctypes.c_uint8)
+    lib.skinny_oracle_gemm_f32w.argtypes = [u16p, i64, f32p, i64, f64p, i64, f64p, i64,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.skinny_oracle_gemm_f32w.restype = None
     lib.skinny_oracle_router_topk.argtypes = [f32p, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                               f64p, i64, i32p, i64, u8p]
     lib.skinny_oracle_router_topk.restype = None
@@ -173,6 +178,30 @@ def gemm_points(X: np.ndarray, W: np.ndarray, K: int, rows, cols,
                                   K, r.ctypes.data_as(i32p), c.ctypes.data_as(i32p), r.size,
                                   y.ctypes.data_as(f64p), a.ctypes.data_as(f64p))
     return y, a
+
+
+def gemm_f32w(X: np.ndarray, W: np.ndarray, M: int, N: int, K: int,
+              ldx: int | None = None, ldw: int | None = None, lib: ctypes.CDLL | None = None):
+    """``Y = X . W^T`` with X bf16 bit patterns ``[M, ldx]`` and W float32
+    ``[N, ldw]`` (fp32 router weights); returns ``(Y, A)`` in fp64, A the sum of
+    |x * w| per output."""
+    lib = lib or load()
+    ldx = K if ldx is None else ldx
+    ldw = K if ldw is None else ldw
+    Xf = _u16(X).reshape(-1)
+    Wf = np.ascontiguousarray(W, dtype=np.float32).reshape(-1)
+    if M and Xf.size < (M - 1) * ldx + K:
+        raise ValueError("X too small")
+    if N and Wf.size < (N - 1) * ldw + K:
+        raise ValueError("W too small")
+    Y = np.zeros((M, N), np.float64)
+    A = np.zeros((M, N), np.float64)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f32p = ctypes.POINTER(ctypes.c_float)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    lib.skinny_oracle_gemm_f32w(Xf.ctypes.data_as(u16p), ldx, Wf.ctypes.data_as(f32p), ldw,
+                                Y.ctypes.data_as(f64p), N, A.ctypes.data_as(f64p), N, M, N, K)
+    return Y, A
 
 
 def router_topk(logits: np.ndarray, k: int, renormalize: bool = False, lib: ctypes.CDLL | None = None):

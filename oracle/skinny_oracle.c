@@ -139,3 +139,34 @@ void skinny_oracle_router_topk(const float *L, int64_t ldl, int M, int N, int k,
             for (int i = 0; i < k; ++i) weights[(int64_t)m * ldwt + i] /= chosen;
     }
 }
+
+/* fp32 router weights ("GLM-5.2 Blackwell decode optimizations": the router
+ * GEMM keeps fp32 weights for the model family that needs them, FP32 router
+ * GEMM shape support): the same definition with W in fp32,
+ *
+ *     Y[m][n] = sum_k  float(X[m][k]) * W[n][k]        X bf16, W fp32
+ *
+ * Each product of an 8-bit and a 24-bit significand is exact in fp64; the
+ * products are added in ascending k in fp64.  A (may be NULL) receives
+ * sum_k |x * w|. */
+void skinny_oracle_gemm_f32w(const uint16_t *X, int64_t ldx,
+                             const float *W, int64_t ldw,
+                             double *Y, int64_t ldy,
+                             double *A, int64_t lda,
+                             int M, int N, int K)
+{
+    for (int i = 0; i < M; ++i) {
+        const uint16_t *xr = X + (int64_t)i * ldx;
+        for (int j = 0; j < N; ++j) {
+            const float *wr = W + (int64_t)j * ldw;
+            double acc = 0.0, acc_abs = 0.0;
+            for (int kk = 0; kk < K; ++kk) {
+                const double t = skinny_oracle_bf16_to_f64(xr[kk]) * (double)wr[kk];
+                acc += t;
+                acc_abs += fabs(t);
+            }
+            Y[(int64_t)i * ldy + j] = acc;
+            if (A) A[(int64_t)i * lda + j] = acc_abs;
+        }
+    }
+}

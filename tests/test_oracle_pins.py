@@ -519,3 +519,97 @@ def test_topk_planted_mistakes_are_caught():
             so = os.path.join(td, f"mut_topk_{abs(hash(name))}.so")
             oracle.build(src=path, out=so)
             assert not _topk_pins_pass(oracle.load(so)), f"planted mistake not caught: {name}"
+
+
+# ---------------------------------------------------------------- fp32 router weights
+
+def _f32_bits_to_float(bits):
+    return np.asarray(bits, np.uint32).view(np.float32)
+
+
+def test_f32w_equals_bf16_oracle_on_bf16_exact_weights():
+    """fp32 weights that are exactly bf16 values give the bf16 oracle's result, bit for bit."""
+    for seed, (M, N, K) in enumerate([(1, 7, 33), (4, 16, 257), (16, 3, 1000)]):
+        X, W = si.make_inputs(si.Case("fw", M=M, N=N, K=K, seed=2000 + seed, outliers=True))
+        Wf = _f32_bits_to_float(W.astype(np.uint32) << 16).reshape(N, K)
+        Y32, A32 = oracle.gemm_f32w(X, Wf, M, N, K)
+        Y16, A16 = oracle.gemm(X, W, M, N, K)
+        assert np.array_equal(Y32, Y16) and np.array_equal(A32, A16)
+
+
+def _exact_f32w(X, Wf, M, N, K):
+    xs = [Fraction(oracle.bf16_to_f64(int(b))) for b in X.reshape(-1)]
+    ws = [Fraction(float(v)) for v in Wf.reshape(-1)]
+    return [[sum(xs[m * K + k] * ws[n * K + k] for k in range(K)) for n in range(N)] for m in range(M)]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_f32w_bruteforce_within_fp64_bound(seed):
+    """Full-precision fp32 weights (24-bit significands): the fp64 sum is within
+    K * 2^-53 * sum|x w| of the exact rational sum."""
+    rng = np.random.default_rng(2100 + seed)
+    M, N, K = 2, 3, 29
+    X = si._to_bf16_bits(__import__("torch").from_numpy(rng.standard_normal((M, K)).astype(np.float32)))
+    Wf = (rng.standard_normal((N, K)) * np.exp(rng.uniform(-8, 8, (N, K)))).astype(np.float32)
+    Y, A = oracle.gemm_f32w(X, Wf, M, N, K)
+    exact = _exact_f32w(X, Wf, M, N, K)
+    for m in range(M):
+        for n in range(N):
+            assert abs(Fraction(Y[m, n]) - exact[m][n]) <= Fraction(K) * Fraction(2) ** -53 * Fraction(A[m, n])
+    # and the weights really carry more than bf16 precision
+    assert np.any(Wf.view(np.uint32) & 0xFFFF)
+
+
+def test_f32w_strides_and_gaps():
+    X, W = si.make_inputs(si.Case("fws", M=3, N=5, K=40, seed=2200))
+    Wf = np.random.default_rng(1).standard_normal((5, 40)).astype(np.float32)
+    ldx, ldw = 43, 41
+    Xs = si.embed_rows(X, ldx)
+    Ws = np.zeros(5 * ldw, np.float32)
+    Ws.reshape(5, ldw)[:, :40] = Wf
+    Ys, _ = oracle.gemm_f32w(Xs, Ws, 3, 5, 40, ldx=ldx, ldw=ldw)
+    Yc, _ = oracle.gemm_f32w(X, Wf, 3, 5, 40)
+    assert np.array_equal(Ys, Yc)
+
+
+def _f32w_pins_pass(lib) -> bool:
+    try:
+        rng = np.random.default_rng(2300)
+        M, N, K = 2, 3, 17
+        X = si._to_bf16_bits(__import__("torch").from_numpy(rng.standard_normal((M, K)).astype(np.float32)))
+        Wf = rng.standard_normal((N, K)).astype(np.float32)
+        Y, A = oracle.gemm_f32w(X, Wf, M, N, K, lib=lib)
+        exact = _exact_f32w(X, Wf, M, N, K)
+        for m in range(M):
+            for n in range(N):
+                if abs(Fraction(Y[m, n]) - exact[m][n]) > Fraction(K) * Fraction(2) ** -53 * Fraction(A[m, n]):
+                    return False
+        return True
+    except Exception:
+        return False
+
+
+def test_f32w_planted_mistakes_are_caught():
+    muts = [
+        ("weights truncated to bf16", "const double t = skinny_oracle_bf16_to_f64(xr[kk]) * (double)wr[kk];",
+         "float wt = wr[kk]; uint32_t wb; memcpy(&wb, &wt, 4); wb &= 0xFFFF0000u; memcpy(&wt, &wb, 4);\n"
+         "                const double t = skinny_oracle_bf16_to_f64(xr[kk]) * (double)wt;"),
+        ("transposed W index", "const float *wr = W + (int64_t)j * ldw;", "const float *wr = W + (int64_t)j;"),
+        ("fp32 product", "const double t = skinny_oracle_bf16_to_f64(xr[kk]) * (double)wr[kk];",
+         "const double t = (double)((float)skinny_oracle_bf16_to_f64(xr[kk]) * wr[kk]);"),
+        ("drop last k", "for (int kk = 0; kk < K; ++kk) {", "for (int kk = 0; kk < K - 1; ++kk) {"),
+    ]
+    with open(oracle.SOURCE_PATH) as f:
+        src = f.read()
+    with tempfile.TemporaryDirectory() as td:
+        clean_so = os.path.join(td, "clean.so")
+        oracle.build(src=oracle.SOURCE_PATH, out=clean_so)
+        assert _f32w_pins_pass(oracle.load(clean_so))
+        for name, old, new in muts:
+            assert src.count(old) == 1, f"mutation anchor not unique: {name}"
+            path = os.path.join(td, "mut.c")
+            with open(path, "w") as f:
+                f.write(src.replace(old, new))
+            so = os.path.join(td, f"mut_f32w_{abs(hash(name))}.so")
+            oracle.build(src=path, out=so)
+            assert not _f32w_pins_pass(oracle.load(so)), f"planted mistake not caught: {name}"
