@@ -192,6 +192,28 @@ SKINNY_API skinny_status_t skinny_set_option(int option, int value);
 SKINNY_API skinny_status_t skinny_get_option(int option, int *value);
 
 /*
+ * fp32 router weights: Y = X . W^T with X bf16 [M, K] and W fp32 [N, K]
+ * (ldw in fp32 elements), fp32 multiply-add (each fmaf rounds once), fp32 Y.
+ * For models that keep fp32 router weights ("GLM-5.2 Blackwell decode
+ * optimizations", the linked "FP32 router GEMM shape support and tuning" and
+ * "Preserve FP32 router weights" changes), and the review note on the first
+ * page that fp32 weights must not reach the bf16 kernel: they have their own
+ * entry point.  The dot-product kernel only: M = 1..16 (else UNSUPPORTED),
+ * any K, W 4-byte aligned (loads of 4, 2 or 1 fp32 as the W pointer and ldw
+ * allow), W traffic 4NK bytes.  Other arguments, errors, PDL and graph
+ * capture as skinny_gemm_bf16.
+ */
+SKINNY_API skinny_status_t skinny_gemm_bf16_f32w(const uint16_t *X, int ldx, const float *W, int ldw,
+                                      float *Y, int ldy, int M, int N, int K, void *stream);
+
+/* The launch skinny_gemm_bf16_f32w would make, as a pure function of the
+ * arguments and an SM count (no CUDA call).  M == 0, N == 0 or K == 0 give a
+ * zeroed plan (nothing or only a zero fill is launched). */
+SKINNY_API skinny_status_t skinny_plan_for_f32w(const uint16_t *X, int ldx, const float *W, int ldw,
+                                     const float *Y, int ldy, int M, int N, int K, int num_sms,
+                                     skinny_plan_t *plan);
+
+/*
  * Router epilogue: for each token m < M, the softmax of its N logits
  * (logits[m*ldl + n], fp32) and its k largest ones.
  *

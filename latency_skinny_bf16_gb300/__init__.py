@@ -24,7 +24,7 @@ __all__ = [
     "skinny_gemm_bf16", "skinny_gemm_bf16_bf16out", "skinny_init", "skinny_query_plan", "skinny_plan_for",
     "skinny_set_option", "skinny_get_option", "skinny_get_device_status",
     "skinny_status_string", "skinny_version", "skinny_router_topk", "skinny_router_bf16_topk",
-    "gemm", "router_topk", "options",
+    "skinny_gemm_bf16_f32w", "skinny_plan_for_f32w", "gemm", "router_topk", "options",
 ]
 
 # ---- constants mirrored from include/skinny_gemm.h
@@ -60,6 +60,7 @@ EXPORTED_SYMBOLS = (
     "skinny_gemm_bf16", "skinny_gemm_bf16_bf16out", "skinny_init", "skinny_query_plan", "skinny_plan_for",
     "skinny_set_option", "skinny_get_option", "skinny_get_device_status",
     "skinny_status_string", "skinny_version", "skinny_router_topk", "skinny_router_bf16_topk",
+    "skinny_gemm_bf16_f32w", "skinny_plan_for_f32w",
 )
 
 
@@ -95,6 +96,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.skinny_gemm_bf16.restype = i
     lib.skinny_gemm_bf16_bf16out.argtypes = [vp, i, vp, i, vp, i, i, i, i, vp]
     lib.skinny_gemm_bf16_bf16out.restype = i
+    lib.skinny_gemm_bf16_f32w.argtypes = [vp, i, vp, i, vp, i, i, i, i, vp]
+    lib.skinny_gemm_bf16_f32w.restype = i
+    lib.skinny_plan_for_f32w.argtypes = [vp, i, vp, i, vp, i, i, i, i, i, ctypes.POINTER(_Plan)]
+    lib.skinny_plan_for_f32w.restype = i
     lib.skinny_router_topk.argtypes = [vp, i, i, i, i, i, vp, i, vp, i, vp]
     lib.skinny_router_topk.restype = i
     lib.skinny_router_bf16_topk.argtypes = [vp, i, vp, i, vp, i, i, i, i, i, i, vp, i, vp, i, vp]
@@ -140,6 +145,21 @@ def skinny_gemm_bf16(X: int, ldx: int, W: int, ldw: int, Y: int, ldy: int,
                      M: int, N: int, K: int, stream: int = 0) -> int:
     """Raw C call: device pointers as ints; returns the skinny_status_t."""
     return load_library().skinny_gemm_bf16(X, ldx, W, ldw, Y, ldy, M, N, K, stream)
+
+
+def skinny_gemm_bf16_f32w(X: int, ldx: int, W: int, ldw: int, Y: int, ldy: int,
+                          M: int, N: int, K: int, stream: int = 0) -> int:
+    """Raw C call with fp32 weights (ldw in fp32 elements); returns the skinny_status_t."""
+    return load_library().skinny_gemm_bf16_f32w(X, ldx, W, ldw, Y, ldy, M, N, K, stream)
+
+
+def skinny_plan_for_f32w(X: int, ldx: int, W: int, ldw: int, Y: int, ldy: int,
+                         M: int, N: int, K: int, num_sms: int) -> dict:
+    p = _Plan()
+    st = load_library().skinny_plan_for_f32w(X, ldx, W, ldw, Y, ldy, M, N, K, num_sms, ctypes.byref(p))
+    if st != SKINNY_OK:
+        raise SkinnyError(st, "skinny_plan_for_f32w")
+    return p.as_dict()
 
 
 def skinny_router_topk(L: int, ldl: int, M: int, N: int, k: int, renormalize: int,
@@ -247,8 +267,8 @@ def gemm(x, w, out=None, stream=None):
     (unit stride along K), out fp32 or bf16 [M, N] (any row stride >= N, unit
     column stride; bf16 is the fp32 result rounded to nearest-even).  Runs on ``stream`` (default: torch's current stream)."""
     import torch
-    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
-        raise TypeError("x and w must be bfloat16")
+    if x.dtype != torch.bfloat16 or w.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("x must be bfloat16 and w bfloat16 or float32")
     if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
         raise ValueError(f"shape mismatch: x {tuple(x.shape)}, w {tuple(w.shape)}")
     if not (x.is_cuda and w.is_cuda):
@@ -269,7 +289,12 @@ def gemm(x, w, out=None, stream=None):
     ldx = x.stride(0) if M > 1 else max(K, 1)
     ldw = w.stride(0) if N > 1 else max(K, 1)
     ldy = out.stride(0) if M > 1 else max(N, 1)
-    call = skinny_gemm_bf16 if out.dtype == torch.float32 else skinny_gemm_bf16_bf16out
+    if w.dtype == torch.float32:
+        if out.dtype != torch.float32:
+            raise TypeError("fp32 weights give an fp32 output")
+        call = skinny_gemm_bf16_f32w
+    else:
+        call = skinny_gemm_bf16 if out.dtype == torch.float32 else skinny_gemm_bf16_bf16out
     st = call(x.data_ptr(), ldx, w.data_ptr(), ldw, out.data_ptr(), ldy, M, N, K, s)
     if st != SKINNY_OK:
         raise SkinnyError(st, "skinny_gemm_bf16")

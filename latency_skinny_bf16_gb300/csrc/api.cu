@@ -81,7 +81,7 @@ skinny_status_t init_device_current(DeviceState &d, int device) {
         return SKINNY_ERR_NO_DEVICE;
     if (major != 10 || minor != 3) return SKINNY_ERR_NO_DEVICE;   // built for sm_103a only
     if (dotprod_prepare() != cudaSuccess || dotmma_prepare() != cudaSuccess || splitk_prepare() != cudaSuccess ||
-        stream_prepare() != cudaSuccess)
+        stream_prepare() != cudaSuccess || dotprod_f32w_prepare() != cudaSuccess)
         return SKINNY_ERR_LAUNCH;
     void *sym = nullptr;
     if (cudaGetSymbolAddress(&sym, g_status_word) != cudaSuccess) return SKINNY_ERR_LAUNCH;
@@ -114,8 +114,8 @@ bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { re
 
 // Host-only validation; no CUDA call.  *noop is set when there is nothing to launch.
 // y_bytes: size of one Y element (4 for fp32, 2 for bf16).
-skinny_status_t validate(const uint16_t *X, int ldx, const uint16_t *W, int ldw, const void *Y, int ldy,
-                         int M, int N, int K, bool *noop, int y_bytes = 4) {
+skinny_status_t validate(const uint16_t *X, int ldx, const void *W, int ldw, const void *Y, int ldy,
+                         int M, int N, int K, bool *noop, int y_bytes = 4, int w_bytes = 2) {
     *noop = false;
     if (M < 0 || N < 0 || K < 0) return SKINNY_ERR_INVALID_VALUE;
     if (M > SKINNY_MAX_M) return SKINNY_ERR_UNSUPPORTED;
@@ -124,13 +124,14 @@ skinny_status_t validate(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
     if (reinterpret_cast<uintptr_t>(Y) & (uintptr_t)(y_bytes - 1)) return SKINNY_ERR_MISALIGNED;
     if (K == 0) return SKINNY_OK;
     if (X == nullptr || W == nullptr || ldx < K || ldw < K) return SKINNY_ERR_INVALID_VALUE;
-    if ((reinterpret_cast<uintptr_t>(X) & 1) || (reinterpret_cast<uintptr_t>(W) & 1)) return SKINNY_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(X) & 1) || (reinterpret_cast<uintptr_t>(W) & (uintptr_t)(w_bytes - 1)))
+        return SKINNY_ERR_MISALIGNED;
     const uintptr_t y0 = reinterpret_cast<uintptr_t>(Y);
     const uintptr_t y1 = y0 + (uintptr_t)(((int64_t)(M - 1) * ldy + N) * y_bytes);
     const uintptr_t x0 = reinterpret_cast<uintptr_t>(X);
     const uintptr_t x1 = x0 + (uintptr_t)(((int64_t)(M - 1) * ldx + K) * 2);
     const uintptr_t w0 = reinterpret_cast<uintptr_t>(W);
-    const uintptr_t w1 = w0 + (uintptr_t)(((int64_t)(N - 1) * ldw + K) * 2);
+    const uintptr_t w1 = w0 + (uintptr_t)(((int64_t)(N - 1) * ldw + K) * w_bytes);
     if (ranges_overlap(y0, y1, x0, x1) || ranges_overlap(y0, y1, w0, w1)) return SKINNY_ERR_INVALID_VALUE;
     return SKINNY_OK;
 }
@@ -528,6 +529,40 @@ skinny_status_t run_gemm(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
     return e == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
 }
 
+// fp32 weights: the dot-product kernel only (FMA), W loads as wide as the W
+// pointer and ldw allow (4 / 2 / 1 fp32), BN rows per CTA as in the bf16 rule.
+bool plan_f32w(const float *W, int ldw, int M, int N, int K, int num_sms, skinny_plan_t *p) {
+    std::memset(p, 0, sizeof(*p));
+    const uintptr_t w = reinterpret_cast<uintptr_t>(W);
+    const int vec = ((w & 15) == 0 && ldw % 4 == 0) ? 4 : ((w & 7) == 0 && ldw % 2 == 0) ? 2 : 1;
+    int bn = 1;
+    if (vec == 4) {
+        bn = pow2_floor(N / (2 * num_sms) > 0 ? N / (2 * num_sms) : 1);
+        if (bn > 4) bn = 4;
+    }
+    if (!dotprod_f32w_supported(M, vec, bn)) return false;
+    const int k8 = (K + 7) & ~7;
+    int kc = (kDotXBudget / (2 * M)) & ~7;
+    if (kc >= k8) {
+        kc = k8;
+    } else {
+        kc = (kc / (8 * kDotThreads)) * (8 * kDotThreads);
+        if (kc < 8 * kDotThreads) kc = 8 * kDotThreads;
+    }
+    p->backend = SKINNY_BACKEND_DOTPROD;
+    p->consumer = SKINNY_CONSUMER_FMA;
+    p->vec_elems = vec;
+    p->block_n = bn;
+    p->split_k = 1;
+    p->k_chunk = kc;
+    p->grid_x = (N + bn - 1) / bn;
+    p->grid_y = 1;
+    p->threads = kDotThreads;
+    p->smem_bytes = dotprod_f32w_smem_bytes(M, bn, kc);
+    p->pdl = opt_pdl();
+    return p->smem_bytes <= kMaxDynSmem;
+}
+
 // Host-only checks of the router epilogue's arguments; *noop when M == 0 or k == 0.
 skinny_status_t validate_topk(const float *L, int ldl, int M, int N, int k, const float *Wt, int ldwt,
                               const int32_t *ids, int ldid, bool *noop) {
@@ -560,6 +595,42 @@ skinny_status_t run_topk(const float *L, int ldl, int M, int N, int k, int renor
 }  // namespace skinny
 
 extern "C" {
+
+skinny_status_t skinny_gemm_bf16_f32w(const uint16_t *X, int ldx, const float *W, int ldw,
+                                      float *Y, int ldy, int M, int N, int K, void *stream) {
+    bool noop = false;
+    skinny_status_t st = validate(X, ldx, W, ldw, Y, ldy, M, N, K, &noop, 4, 4);
+    if (st != SKINNY_OK || noop) return st;
+    if (M > kMaxMSmall) return SKINNY_ERR_UNSUPPORTED;
+    int device = 0;
+    st = current_device(&device);
+    if (st != SKINNY_OK) return st;
+    DeviceState &d = g_dev[device];
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        const int64_t total = (int64_t)M * N;
+        int blocks = (int)((total + 255) / 256);
+        if (blocks > 4 * d.num_sms) blocks = 4 * d.num_sms;
+        zero_fill_kernel<<<blocks, 256, 0, s>>>(Y, ldy, M, N, 0);
+        return cudaPeekAtLastError() == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
+    }
+    skinny_plan_t plan;
+    if (!plan_f32w(W, ldw, M, N, K, d.num_sms, &plan)) return SKINNY_ERR_UNSUPPORTED;
+    LaunchCtx c{s, plan.pdl != 0, d.status_word, (uint64_t)g_opt_wait_us.load() * 1000ull};
+    const cudaError_t e = launch_dotprod_f32w(X, ldx, W, ldw, Y, ldy, M, N, K, plan, c);
+    return e == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
+}
+
+skinny_status_t skinny_plan_for_f32w(const uint16_t *X, int ldx, const float *W, int ldw, const float *Y, int ldy,
+                                     int M, int N, int K, int num_sms, skinny_plan_t *plan) {
+    if (!plan || num_sms < 1) return SKINNY_ERR_INVALID_VALUE;
+    bool noop = false;
+    skinny_status_t st = validate(X, ldx, W, ldw, Y, ldy, M, N, K, &noop, 4, 4);
+    if (st != SKINNY_OK) return st;
+    if (M > kMaxMSmall) return SKINNY_ERR_UNSUPPORTED;
+    if (noop || K == 0) { std::memset(plan, 0, sizeof(*plan)); return SKINNY_OK; }
+    return plan_f32w(W, ldw, M, N, K, num_sms, plan) ? SKINNY_OK : SKINNY_ERR_UNSUPPORTED;
+}
 
 skinny_status_t skinny_router_topk(const float *logits, int ldl, int M, int N, int k, int renormalize,
                                    float *weights, int ldw, int32_t *ids, int ldid, void *stream) {

@@ -67,6 +67,13 @@ bool stream_supported(int M);
 cudaError_t stream_prepare();
 cudaError_t launch_stream(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
 
+// ---- dot-product backend for fp32 weights (dotprod_f32w.cu): vec_elems 4/2/1 fp32, block_n 1/2/4
+bool dotprod_f32w_supported(int M, int vec_elems, int block_n);
+int dotprod_f32w_smem_bytes(int M, int block_n, int k_chunk);
+cudaError_t dotprod_f32w_prepare();
+cudaError_t launch_dotprod_f32w(const uint16_t *X, int64_t ldx, const float *W, int64_t ldw, float *Y, int64_t ldy,
+                                int M, int N, int K, const skinny_plan_t &p, const LaunchCtx &c);
+
 // ---- router epilogue (topk.cu): softmax + top-k over each token's logits
 constexpr int kTopkMaxN = 8192;   // logits per token (shared memory: 5 bytes each)
 constexpr int kTopkMaxK = 64;

@@ -120,6 +120,26 @@ def make_inputs(case: Case) -> tuple[np.ndarray, np.ndarray]:
     return X, W
 
 
+def make_f32_weights(case: Case) -> np.ndarray:
+    """fp32 weights ``W [N, K]`` for the fp32-router-weight path: the case's W
+    distribution drawn in fp32 and kept at full fp32 precision (no rounding to
+    bf16), from the case seed + 7919 so they differ from ``make_inputs``' W."""
+    g = torch.Generator().manual_seed(int(case.seed) + 7919)
+    shape = (case.N, case.K)
+    if case.w_dist == "normal":
+        v = torch.randn(shape, generator=g, dtype=torch.float32)
+    elif case.w_dist == "normal0.02":
+        v = torch.randn(shape, generator=g, dtype=torch.float32) * 0.02
+    elif case.w_dist == "uniform_isqrtk":
+        v = (torch.rand(shape, generator=g, dtype=torch.float32) * 2.0 - 1.0) / math.sqrt(max(case.K, 1))
+    else:
+        raise ValueError(f"unknown distribution {case.w_dist!r}")
+    if case.outliers:
+        pick = torch.rand(shape, generator=g, dtype=torch.float32) < 0.01
+        v = torch.where(pick, v * 100.0, v)
+    return v.numpy().copy()
+
+
 def embed_rows(a: np.ndarray, ld: int, fill: int = 0) -> np.ndarray:
     """Place a compact ``[R, C]`` array into a flat buffer with row stride ``ld``."""
     R, C = a.shape

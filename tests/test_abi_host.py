@@ -407,3 +407,34 @@ def test_router_fused_checks_both_steps_before_launching():
     assert fused(ids=A16 + 8) == sk.SKINNY_ERR_INVALID_VALUE          # ids overlap X
     assert fused(L=B16 + 1024) == sk.SKINNY_ERR_INVALID_VALUE         # logits overlap W
     assert fused(M=0) == sk.SKINNY_OK
+
+
+# ---------------------------------------------------------------- fp32 router weights
+def f32w_call(X=A16, ldx=64, W=B16, ldw=64, Y=C16, ldy=32, M=4, N=32, K=64):
+    return sk.skinny_gemm_bf16_f32w(X, ldx, W, ldw, Y, ldy, M, N, K, 0)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(M=-1), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(M=17), sk.SKINNY_ERR_UNSUPPORTED),       # dot-product kernel only: M <= 16
+    (dict(M=0), sk.SKINNY_OK),
+    (dict(ldw=63), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(W=B16 + 2), sk.SKINNY_ERR_MISALIGNED),    # fp32: 4-byte aligned
+    (dict(Y=B16 + 4 * 64 * 31), sk.SKINNY_ERR_INVALID_VALUE),   # Y overlaps the fp32 W (4-byte elements)
+    (dict(), sk.SKINNY_ERR_NO_DEVICE),
+])
+def test_f32w_argument_errors_are_host_side(kw, expect):
+    assert f32w_call(**kw) == expect
+
+
+def test_f32w_plan_follows_alignment():
+    def p(W=B16, ldw=None, M=4, N=256, K=7168):
+        return sk.skinny_plan_for_f32w(A16, K, W, ldw or K, C16, N, M, N, K, 152)
+    assert p()["vec_elems"] == 4 and p()["consumer"] == sk.SKINNY_CONSUMER_FMA
+    assert p(W=B16 + 8)["vec_elems"] == 2
+    assert p(W=B16 + 4)["vec_elems"] == 1
+    assert p(K=7169)["vec_elems"] == 1
+    assert p(K=7170)["vec_elems"] == 2
+    assert p(N=2048)["block_n"] == 4 and p(N=2048)["grid_x"] == 512
+    assert p(M=16, K=14336)["k_chunk"] % 1024 == 0          # X in chunks: 16 x 14336 bf16 > budget
+    assert p(M=0)["grid_x"] == 0

@@ -1,0 +1,143 @@
+"""GPU parity of the fp32-router-weight GEMM (bf16 X, fp32 W, fp32 Y) against
+the oracle, through the C ABI.
+
+Bar: |y - y_ref| <= 1e-5 * sum_k |x*w| + 1e-6 elementwise (each fmaf rounds
+once, the sums are the bf16 path's), cosine >= 0.99999, nothing written
+outside Y[:M, :N], bit-identical runs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import latency_skinny_bf16_gb300 as sk
+import oracle
+import skinny_inputs as si
+from gpu_util import CANARY, check_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _init():
+    assert sk.skinny_init(0) == sk.SKINNY_OK
+    yield
+
+
+class F32Buffers:
+    """X (bf16 bits) and fp32 W on the device, with optional strides / offsets."""
+
+    def __init__(self, case, X, Wf, ldx=None, ldw=None, ldy=None, w_offset=0):
+        self.M, self.N, self.K = case.M, case.N, case.K
+        self.ldx, self.ldw, self.ldy = ldx or case.K, ldw or case.K, ldy or case.N
+        xs = si.embed_rows(X, self.ldx) if self.M else np.zeros(1, np.uint16)
+        self.x = torch.from_numpy(xs.view(np.int16).copy()).cuda()
+        wbuf = np.zeros(max(self.N, 1) * self.ldw + w_offset + 8, np.float32)
+        if self.N and self.K:
+            wbuf[w_offset: w_offset + self.N * self.ldw].reshape(self.N, self.ldw)[:, : self.K] = Wf
+        self.w = torch.from_numpy(wbuf).cuda()
+        self.w_ptr = self.w.data_ptr() + 4 * w_offset
+        self.y = torch.full((max(self.M, 1) * self.ldy + 64,), CANARY, dtype=torch.float32, device="cuda")
+
+    def run(self, stream=0):
+        return sk.skinny_gemm_bf16_f32w(self.x.data_ptr(), self.ldx, self.w_ptr, self.ldw, self.y.data_ptr(),
+                                        self.ldy, self.M, self.N, self.K, stream)
+
+    def plan(self):
+        return sk.skinny_plan_for_f32w(self.x.data_ptr(), self.ldx, self.w_ptr, self.ldw, self.y.data_ptr(),
+                                       self.ldy, self.M, self.N, self.K, 152)
+
+    def y_mat(self):
+        torch.cuda.synchronize()
+        return self.y.cpu().numpy()[: self.M * self.ldy].reshape(self.M, self.ldy)[:, : self.N]
+
+    def canary_ok(self):
+        y = self.y.cpu().numpy()
+        body = y[: self.M * self.ldy].reshape(self.M, self.ldy)
+        return bool(np.all(body[:, self.N:] == CANARY) and np.all(y[self.M * self.ldy:] == CANARY))
+
+
+def run_check(case, **kw):
+    X, _ = si.make_inputs(case)
+    Wf = si.make_f32_weights(case)
+    b = F32Buffers(case, X, Wf, **kw)
+    yref, A = oracle.gemm_f32w(X, Wf, case.M, case.N, case.K)
+    first = None
+    for _ in range(2):
+        assert b.run() == sk.SKINNY_OK
+        y = b.y_mat().copy()
+        if first is None:
+            first = y
+            check_parity(y, yref, A, case.name)
+        else:
+            assert np.array_equal(y.view(np.uint32), first.view(np.uint32))
+    assert b.canary_ok()
+    assert sk.skinny_get_device_status() == 0
+    return b
+
+
+ROUTER = [si.Case(f"f32w_M{M}_K{K}_N{N}", M=M, N=N, K=K, seed=2400 + i)
+          for i, (M, (K, N)) in enumerate([(M, s) for s in ((7168, 256), (7168, 384), (2880, 128))
+                                           for M in (1, 2, 3, 4, 8, 12, 16)])]
+
+
+@pytest.mark.parametrize("case", ROUTER, ids=[c.name for c in ROUTER])
+def test_f32w_router_shapes(case):
+    b = run_check(case)
+    assert b.plan()["vec_elems"] == 4
+
+
+@pytest.mark.parametrize("w_offset,ldw_pad,K", [(1, 0, 1000), (2, 0, 1000), (0, 1, 999), (0, 2, 1026),
+                                                 (0, 0, 7), (0, 0, 1)])
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_f32w_alignment_and_tails(w_offset, ldw_pad, K, M):
+    case = si.Case(f"f32w_al_{M}_{w_offset}_{ldw_pad}_{K}", M=M, N=37, K=K, seed=2500 + K + M, outliers=True,
+                   w_dist="normal", ldy=37 + 3)
+    run_check(case, ldw=K + ldw_pad, w_offset=w_offset)
+
+
+def test_f32w_wide_n_and_x_chunks():
+    # N = 2112: 4 rows per CTA; M = 16 with K = 14336: X staged in chunks
+    run_check(si.Case("f32w_wide", M=4, N=2112, K=7168, seed=2600, w_dist="uniform_isqrtk"))
+    run_check(si.Case("f32w_chunks", M=16, N=96, K=14336, seed=2601, w_dist="uniform_isqrtk"))
+
+
+def test_f32w_k_zero_and_special_values():
+    case = si.Case("f32w_k0", M=3, N=10, K=0, seed=2700)
+    b = F32Buffers(case, np.zeros((3, 0), np.uint16), np.zeros((10, 0), np.float32), ldx=1, ldw=1)
+    assert b.run() == sk.SKINNY_OK
+    assert (b.y_mat() == 0).all()
+    case = si.Case("f32w_sv", M=2, N=8, K=64, seed=2701)
+    X, _ = si.make_inputs(case)
+    Wf = si.make_f32_weights(case)
+    Wf[1, 5] = np.inf
+    Wf[2, 7] = np.nan
+    Wf[3, 0] = 1.0e30                     # large but the sums stay finite in fp32
+    b = F32Buffers(case, X, Wf)
+    assert b.run() == sk.SKINNY_OK
+    yref, A = oracle.gemm_f32w(X, Wf, 2, 8, 64)
+    check_parity(b.y_mat(), yref, A, "special values")
+
+
+def test_f32w_tensor_wrapper_and_graph():
+    case = si.Case("f32w_tw", M=6, N=256, K=7168, seed=2800)
+    X, _ = si.make_inputs(case)
+    Wf = si.make_f32_weights(case)
+    x = torch.from_numpy(X.view(np.int16)).cuda().view(torch.bfloat16)
+    w = torch.from_numpy(Wf).cuda()
+    y = sk.gemm(x, w)
+    torch.cuda.synchronize()
+    yref, A = oracle.gemm_f32w(X, Wf, 6, 256, 7168)
+    check_parity(y.cpu().numpy(), yref, A, "wrapper")
+    with pytest.raises(TypeError):
+        sk.gemm(x, w, out=torch.empty(6, 256, dtype=torch.bfloat16, device="cuda"))
+    for pdl in (0, 1):
+        with sk.options(pdl=pdl):
+            s = torch.cuda.Stream()
+            out = torch.zeros(6, 256, device="cuda")
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(3):
+                    sk.gemm(x, w, out=out, stream=s)
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out.cpu().view(torch.int32), y.cpu().view(torch.int32))

@@ -71,3 +71,11 @@ def test_embed_rows():
     a = np.arange(6, dtype=np.uint16).reshape(2, 3)
     e = si.embed_rows(a, 5, fill=9)
     assert e.tolist() == [0, 1, 2, 9, 9, 3, 4, 5, 9, 9]
+
+
+def test_f32_weights_are_seeded_full_precision():
+    c = si.Case("f", M=2, N=16, K=300, seed=9)
+    a, b = si.make_f32_weights(c), si.make_f32_weights(c)
+    assert a.dtype == np.float32 and a.shape == (16, 300) and np.array_equal(a, b)
+    assert np.any(a.view(np.uint32) & 0xFFFF)          # not bf16-representable
+    assert abs(float(a.std()) - 0.02) < 0.003
