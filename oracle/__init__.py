@@ -15,7 +15,8 @@ Blackwell decode optimizations", "Implementation breakdown" item 3: the bf16
 A x B^T decode projections).  This module only compiles the C file with the
 host compiler and marshals numpy arrays.
 
-``gemm_f32w`` is the same definition with fp32 weights (the router GEMM
+``rmsnorm`` is the RMS norm of the query latent that precedes the q_b
+projection (the fused prologue).  ``gemm_f32w`` is the same definition with fp32 weights (the router GEMM
 for models that keep fp32 router weights).  It also holds the router
 epilogue that consumes the router logits: a
 softmax over each token's N logits and its k largest entries
@@ -83,6 +84,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.skinny_oracle_gemm_f32w.argtypes = [u16p, i64, f32p, i64, f64p, i64, f64p, i64,
                                             ctypes.c_int, ctypes.c_int, ctypes.c_int]
     lib.skinny_oracle_gemm_f32w.restype = None
+    lib.skinny_oracle_rmsnorm.argtypes = [u16p, i64, u16p, ctypes.c_double, ctypes.c_int, ctypes.c_int, f64p, i64]
+    lib.skinny_oracle_rmsnorm.restype = None
     lib.skinny_oracle_router_topk.argtypes = [f32p, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                               f64p, i64, i32p, i64, u8p]
     lib.skinny_oracle_router_topk.restype = None
@@ -202,6 +205,22 @@ def gemm_f32w(X: np.ndarray, W: np.ndarray, M: int, N: int, K: int,
     lib.skinny_oracle_gemm_f32w(Xf.ctypes.data_as(u16p), ldx, Wf.ctypes.data_as(f32p), ldw,
                                 Y.ctypes.data_as(f64p), N, A.ctypes.data_as(f64p), N, M, N, K)
     return Y, A
+
+
+def rmsnorm(X: np.ndarray, G: np.ndarray, eps: float, M: int, K: int, ldx: int | None = None,
+            lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Unrounded fp64 RMS norm ``x * r * g`` of the bf16 rows of X (``[M, ldx]``
+    bit patterns) with bf16 gains G ``[K]``; see ``skinny_oracle.c``."""
+    lib = lib or load()
+    ldx = K if ldx is None else ldx
+    Xf = _u16(X).reshape(-1)
+    Gf = _u16(G).reshape(-1)
+    XN = np.zeros((M, K), np.float64)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    lib.skinny_oracle_rmsnorm(Xf.ctypes.data_as(u16p), ldx, Gf.ctypes.data_as(u16p), float(eps), M, K,
+                              XN.ctypes.data_as(f64p), K)
+    return XN
 
 
 def router_topk(logits: np.ndarray, k: int, renormalize: bool = False, lib: ctypes.CDLL | None = None):

@@ -170,3 +170,31 @@ void skinny_oracle_gemm_f32w(const uint16_t *X, int64_t ldx,
         }
     }
 }
+
+/* RMS norm of the query latent before the q_b projection ("GLM-5.2 Blackwell
+ * decode optimizations", section "Implementation breakdown" item 2 and the
+ * fused_norm_rope snippet's pid == 2 branch: q_c = _rms_norm(q_c,
+ * q_rms_norm_w, eps, Q_DIM), stored to q_c_out): for each token m,
+ *
+ *     r_m   = 1 / sqrt( (1/K) sum_k x(m,k)^2 + eps )
+ *     xn(m,k) = x(m,k) * r_m * g(k)
+ *
+ * all in fp64 (x and g decoded exactly from bf16).  The value is returned
+ * unrounded in XN (the bf16 rounding of the stored q_c_out is left to the
+ * caller, which also needs to know how close each value is to a rounding
+ * boundary). */
+void skinny_oracle_rmsnorm(const uint16_t *X, int64_t ldx, const uint16_t *G, double eps,
+                           int M, int K, double *XN, int64_t ldxn)
+{
+    for (int m = 0; m < M; ++m) {
+        const uint16_t *xm = X + (int64_t)m * ldx;
+        double ss = 0.0;
+        for (int k = 0; k < K; ++k) {
+            const double v = skinny_oracle_bf16_to_f64(xm[k]);
+            ss += v * v;
+        }
+        const double r = 1.0 / sqrt(ss / (double)K + eps);
+        for (int k = 0; k < K; ++k)
+            XN[(int64_t)m * ldxn + k] = skinny_oracle_bf16_to_f64(xm[k]) * r * skinny_oracle_bf16_to_f64(G[k]);
+    }
+}

@@ -613,3 +613,81 @@ def test_f32w_planted_mistakes_are_caught():
             so = os.path.join(td, f"mut_f32w_{abs(hash(name))}.so")
             oracle.build(src=path, out=so)
             assert not _f32w_pins_pass(oracle.load(so)), f"planted mistake not caught: {name}"
+
+
+# ---------------------------------------------------------------- RMS norm prologue of the q_b projection
+
+def _bf16(vals):
+    return si._to_bf16_bits(__import__("torch").tensor(np.asarray(vals, np.float32)))
+
+
+def test_rmsnorm_closed_forms():
+    K = 16
+    ones = _bf16(np.ones(K))
+    # a row of +-2^e, unit gain, eps = 0: r = 2^-e and every output is exactly +-1
+    row = np.array([4.0, -4.0] * (K // 2), np.float32)
+    xn = oracle.rmsnorm(_bf16(row).reshape(1, K), ones, 0.0, 1, K)
+    assert xn.tolist() == [[1.0, -1.0] * (K // 2)]
+    # the gain multiplies element by element
+    g = _bf16(np.arange(1, K + 1) * 0.5)
+    xn = oracle.rmsnorm(_bf16(row).reshape(1, K), g, 0.0, 1, K)
+    assert xn.tolist() == [[(0.5 * (k + 1)) * (1 if k % 2 == 0 else -1) for k in range(K)]]
+    # a zero row stays zero for any eps > 0
+    assert not oracle.rmsnorm(_bf16(np.zeros(K)).reshape(1, K), ones, 1e-6, 1, K).any()
+    # eps: a row of ones with eps = 3 gives 1 / sqrt(1 + 3) = 1/2 everywhere
+    assert (oracle.rmsnorm(ones.reshape(1, K), ones, 3.0, 1, K) == 0.5).all()
+
+
+def test_rmsnorm_invariants():
+    rng = np.random.default_rng(41)
+    M, K = 4, 1536
+    X = _bf16(rng.standard_normal((M, K))).reshape(M, K)
+    ones = _bf16(np.ones(K))
+    xn = oracle.rmsnorm(X, ones, 0.0, M, K)
+    assert np.allclose((xn ** 2).mean(axis=1), 1.0, rtol=1e-14)         # unit RMS per row
+    # scaling a row by a power of two changes nothing (eps = 0, exact)
+    X4 = _bf16(np.asarray(X.view(np.uint16).astype(np.uint32) << 16, np.uint32).view(np.float32) * 4.0).reshape(M, K)
+    assert np.array_equal(oracle.rmsnorm(X4, ones, 0.0, M, K), xn)
+    # rows are independent, and strides are honoured
+    xs = si.embed_rows(X, K + 5)
+    assert np.array_equal(oracle.rmsnorm(xs, ones, 1e-6, M, K, ldx=K + 5), oracle.rmsnorm(X, ones, 1e-6, M, K))
+    assert np.array_equal(oracle.rmsnorm(X[2:3].copy(), ones, 1e-6, 1, K)[0], oracle.rmsnorm(X, ones, 1e-6, M, K)[2])
+
+
+def _rms_pins_pass(lib) -> bool:
+    try:
+        K = 16
+        ones = _bf16(np.ones(K))
+        row = np.array([4.0, -4.0] * (K // 2), np.float32)
+        g = _bf16(np.arange(1, K + 1) * 0.5)
+        if oracle.rmsnorm(_bf16(row).reshape(1, K), g, 0.0, 1, K, lib=lib).tolist() != \
+                [[(0.5 * (k + 1)) * (1 if k % 2 == 0 else -1) for k in range(K)]]:
+            return False
+        if not (oracle.rmsnorm(ones.reshape(1, K), ones, 3.0, 1, K, lib=lib) == 0.5).all():
+            return False
+        return True
+    except Exception:
+        return False
+
+
+def test_rmsnorm_planted_mistakes_are_caught():
+    muts = [
+        ("mean over K - 1", "sqrt(ss / (double)K + eps)", "sqrt(ss / (double)(K - 1) + eps)"),
+        ("eps dropped", "sqrt(ss / (double)K + eps)", "sqrt(ss / (double)K)"),
+        ("gain of the first element", "skinny_oracle_bf16_to_f64(G[k])", "skinny_oracle_bf16_to_f64(G[0])"),
+        ("no gain", "* r * skinny_oracle_bf16_to_f64(G[k])", "* r"),
+    ]
+    with open(oracle.SOURCE_PATH) as f:
+        src = f.read()
+    with tempfile.TemporaryDirectory() as td:
+        clean_so = os.path.join(td, "clean.so")
+        oracle.build(src=oracle.SOURCE_PATH, out=clean_so)
+        assert _rms_pins_pass(oracle.load(clean_so))
+        for name, old, new in muts:
+            assert src.count(old) == 1, f"mutation anchor not unique: {name}"
+            path = os.path.join(td, "mut.c")
+            with open(path, "w") as f:
+                f.write(src.replace(old, new))
+            so = os.path.join(td, f"mut_rms_{abs(hash(name))}.so")
+            oracle.build(src=path, out=so)
+            assert not _rms_pins_pass(oracle.load(so)), f"planted mistake not caught: {name}"
