@@ -214,6 +214,37 @@ SKINNY_API skinny_status_t skinny_plan_for_f32w(const uint16_t *X, int ldx, cons
                                      skinny_plan_t *plan);
 
 /*
+ * The q_b projection with its query RMS norm in front: for each token m < M,
+ *
+ *     r_m     = 1 / sqrt( (1/K) sum_k x(m,k)^2 + eps )          (fp32)
+ *     XN(m,k) = bf16_rn( x(m,k) * r_m * gamma(k) )               (written to XN)
+ *     Y       = XN . W^T                                          (skinny_gemm_bf16)
+ *
+ * Operation defined by: "GLM-5.2 Blackwell decode optimizations", section
+ * "Implementation breakdown" item 2 (the fused_norm_rope kernel's Q RMS norm
+ * branch, q_c = _rms_norm(q_c, q_rms_norm_w, eps, Q_DIM), stored to q_c_out)
+ * and item 3 (the q_b bf16_skinny_gemm that consumes it).
+ *
+ *   X      device, bf16 [M, K] (the query latent q_c), row stride ldx >= K, 2-byte aligned
+ *   gamma  device, bf16 [K] (the norm weight); eps >= 0, finite
+ *   XN     device, bf16 [M, K] written (q_c_out), row stride ldxn >= K; the GEMM's X, so it
+ *          obeys skinny_gemm_bf16's rules for X, and may overlap none of X, gamma, W, Y
+ *   W, Y, M (1..64), N, K, stream: as skinny_gemm_bf16 with X = XN.  K == 0 gives Y = 0 and
+ *          leaves XN untouched.
+ *
+ * Two launches on `stream`: a norm kernel (one CTA per token; fixed-order
+ * fp32 sum of squares, IEEE sqrt and division, one bf16 rounding per element;
+ * bit-identical run to run) and then the GEMM.  With PDL on, the norm kernel
+ * lets the GEMM launch at once, so the GEMM streams W while the norm runs and
+ * reads XN after waiting for it: the norm is a prologue of the GEMM's
+ * critical path, not a separate round trip.  Every argument is checked and
+ * the GEMM's plan made before anything is launched.
+ */
+SKINNY_API skinny_status_t skinny_rmsnorm_gemm_bf16(const uint16_t *X, int ldx, const uint16_t *gamma, float eps,
+                                         uint16_t *XN, int ldxn, const uint16_t *W, int ldw, float *Y, int ldy,
+                                         int M, int N, int K, void *stream);
+
+/*
  * Router epilogue: for each token m < M, the softmax of its N logits
  * (logits[m*ldl + n], fp32) and its k largest ones.
  *

@@ -24,7 +24,8 @@ __all__ = [
     "skinny_gemm_bf16", "skinny_gemm_bf16_bf16out", "skinny_init", "skinny_query_plan", "skinny_plan_for",
     "skinny_set_option", "skinny_get_option", "skinny_get_device_status",
     "skinny_status_string", "skinny_version", "skinny_router_topk", "skinny_router_bf16_topk",
-    "skinny_gemm_bf16_f32w", "skinny_plan_for_f32w", "gemm", "router_topk", "options",
+    "skinny_gemm_bf16_f32w", "skinny_plan_for_f32w", "skinny_rmsnorm_gemm_bf16", "gemm", "router_topk",
+    "rmsnorm_gemm", "options",
 ]
 
 # ---- constants mirrored from include/skinny_gemm.h
@@ -60,7 +61,7 @@ EXPORTED_SYMBOLS = (
     "skinny_gemm_bf16", "skinny_gemm_bf16_bf16out", "skinny_init", "skinny_query_plan", "skinny_plan_for",
     "skinny_set_option", "skinny_get_option", "skinny_get_device_status",
     "skinny_status_string", "skinny_version", "skinny_router_topk", "skinny_router_bf16_topk",
-    "skinny_gemm_bf16_f32w", "skinny_plan_for_f32w",
+    "skinny_gemm_bf16_f32w", "skinny_plan_for_f32w", "skinny_rmsnorm_gemm_bf16",
 )
 
 
@@ -100,6 +101,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.skinny_gemm_bf16_f32w.restype = i
     lib.skinny_plan_for_f32w.argtypes = [vp, i, vp, i, vp, i, i, i, i, i, ctypes.POINTER(_Plan)]
     lib.skinny_plan_for_f32w.restype = i
+    lib.skinny_rmsnorm_gemm_bf16.argtypes = [vp, i, vp, ctypes.c_float, vp, i, vp, i, vp, i, i, i, i, vp]
+    lib.skinny_rmsnorm_gemm_bf16.restype = i
     lib.skinny_router_topk.argtypes = [vp, i, i, i, i, i, vp, i, vp, i, vp]
     lib.skinny_router_topk.restype = i
     lib.skinny_router_bf16_topk.argtypes = [vp, i, vp, i, vp, i, i, i, i, i, i, vp, i, vp, i, vp]
@@ -160,6 +163,13 @@ def skinny_plan_for_f32w(X: int, ldx: int, W: int, ldw: int, Y: int, ldy: int,
     if st != SKINNY_OK:
         raise SkinnyError(st, "skinny_plan_for_f32w")
     return p.as_dict()
+
+
+def skinny_rmsnorm_gemm_bf16(X: int, ldx: int, gamma: int, eps: float, XN: int, ldxn: int, W: int, ldw: int,
+                             Y: int, ldy: int, M: int, N: int, K: int, stream: int = 0) -> int:
+    """Raw C call: RMS norm of X into XN, then Y = XN . W^T; returns the skinny_status_t."""
+    return load_library().skinny_rmsnorm_gemm_bf16(X, ldx, gamma, float(eps), XN, ldxn, W, ldw, Y, ldy, M, N, K,
+                                                   stream)
 
 
 def skinny_router_topk(L: int, ldl: int, M: int, N: int, k: int, renormalize: int,
@@ -325,3 +335,28 @@ def router_topk(logits, k, renormalize=False, weights=None, ids=None, stream=Non
     if st != SKINNY_OK:
         raise SkinnyError(st, "skinny_router_topk")
     return weights, ids
+
+
+def rmsnorm_gemm(x, gamma, eps, w, out=None, xn=None, stream=None):
+    """``xn = bf16(rmsnorm(x) * gamma)`` and ``out = xn . w^T`` for CUDA bf16
+    tensors x [M, K], gamma [K], w [N, K] (unit stride along K); returns
+    ``(out fp32 [M, N], xn bf16 [M, K])``; see ``skinny_rmsnorm_gemm_bf16``."""
+    import torch
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16 or gamma.dtype != torch.bfloat16:
+        raise TypeError("x, gamma and w must be bfloat16")
+    M, K = x.shape
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if xn is None:
+        xn = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = skinny_rmsnorm_gemm_bf16(x.data_ptr(), x.stride(0) if M > 1 else max(K, 1), gamma.data_ptr(), eps,
+                                  xn.data_ptr(), xn.stride(0) if M > 1 else max(K, 1),
+                                  w.data_ptr(), w.stride(0) if N > 1 else max(K, 1),
+                                  out.data_ptr(), out.stride(0) if M > 1 else max(N, 1), M, N, K, s)
+    if st != SKINNY_OK:
+        raise SkinnyError(st, "skinny_rmsnorm_gemm_bf16")
+    return out, xn

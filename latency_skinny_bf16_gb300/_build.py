@@ -20,7 +20,8 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libskinny_gemm.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
-SOURCES = ["api.cu", "dotprod.cu", "dotprod_f32w.cu", "dotmma.cu", "splitk.cu", "stream.cu", "topk.cu"]
+SOURCES = ["api.cu", "dotprod.cu", "dotprod_f32w.cu", "dotmma.cu", "splitk.cu", "stream.cu", "topk.cu",
+           "rmsnorm.cu"]
 HEADERS = ["common.cuh", "internal.h", "tuning_table.inc"]
 
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -12,6 +12,7 @@
 #include <atomic>
 #include <cstdio>
 #include <cstdlib>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <set>
@@ -630,6 +631,40 @@ skinny_status_t skinny_plan_for_f32w(const uint16_t *X, int ldx, const float *W,
     if (M > kMaxMSmall) return SKINNY_ERR_UNSUPPORTED;
     if (noop || K == 0) { std::memset(plan, 0, sizeof(*plan)); return SKINNY_OK; }
     return plan_f32w(W, ldw, M, N, K, num_sms, plan) ? SKINNY_OK : SKINNY_ERR_UNSUPPORTED;
+}
+
+skinny_status_t skinny_rmsnorm_gemm_bf16(const uint16_t *X, int ldx, const uint16_t *gamma, float eps,
+                                         uint16_t *XN, int ldxn, const uint16_t *W, int ldw, float *Y, int ldy,
+                                         int M, int N, int K, void *stream) {
+    // the GEMM's own checks, with the normalised rows as its X
+    bool noop = false;
+    skinny_status_t st = validate(XN, ldxn, W, ldw, Y, ldy, M, N, K, &noop, 4);
+    if (st != SKINNY_OK || noop) return st;
+    if (K == 0) return run_gemm(XN, ldxn, W, ldw, Y, ldy, M, N, K, stream, 0);   // Y = 0, XN untouched
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return SKINNY_ERR_INVALID_VALUE;
+    if (!X || !gamma || ldx < K) return SKINNY_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(gamma)) & 1) return SKINNY_ERR_MISALIGNED;
+    if (M > SKINNY_MAX_M) return SKINNY_ERR_UNSUPPORTED;
+    // XN is written: it may overlap none of X, gamma, W or Y
+    const uintptr_t n0 = reinterpret_cast<uintptr_t>(XN), n1 = n0 + (uintptr_t)(((int64_t)(M - 1) * ldxn + K) * 2);
+    const uintptr_t x0 = reinterpret_cast<uintptr_t>(X), x1 = x0 + (uintptr_t)(((int64_t)(M - 1) * ldx + K) * 2);
+    const uintptr_t g0 = reinterpret_cast<uintptr_t>(gamma), g1 = g0 + (uintptr_t)K * 2;
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(W), w1 = w0 + (uintptr_t)(((int64_t)(N - 1) * ldw + K) * 2);
+    const uintptr_t y0 = reinterpret_cast<uintptr_t>(Y), y1 = y0 + (uintptr_t)(((int64_t)(M - 1) * ldy + N) * 4);
+    if (ranges_overlap(n0, n1, x0, x1) || ranges_overlap(n0, n1, g0, g1) || ranges_overlap(n0, n1, w0, w1) ||
+        ranges_overlap(n0, n1, y0, y1) || ranges_overlap(y0, y1, x0, x1) || ranges_overlap(y0, y1, g0, g1))
+        return SKINNY_ERR_INVALID_VALUE;
+    // the plan must exist before anything is launched
+    int device = 0;
+    st = current_device(&device);
+    if (st != SKINNY_OK) return st;
+    skinny_plan_t plan;
+    st = make_plan(XN, ldxn, W, ldw, M, N, K, g_dev[device].num_sms, &plan);
+    if (st != SKINNY_OK) return st;
+    const cudaError_t e = launch_rmsnorm(X, ldx, gamma, eps, M, K, XN, ldxn, static_cast<cudaStream_t>(stream),
+                                         opt_pdl() != 0);
+    if (e != cudaSuccess) return SKINNY_ERR_LAUNCH;
+    return run_gemm(XN, ldxn, W, ldw, Y, ldy, M, N, K, stream, 0);
 }
 
 skinny_status_t skinny_router_topk(const float *logits, int ldl, int M, int N, int k, int renormalize,

@@ -74,6 +74,10 @@ cudaError_t dotprod_f32w_prepare();
 cudaError_t launch_dotprod_f32w(const uint16_t *X, int64_t ldx, const float *W, int64_t ldw, float *Y, int64_t ldy,
                                 int M, int N, int K, const skinny_plan_t &p, const LaunchCtx &c);
 
+// ---- query RMS norm in front of the q_b projection (rmsnorm.cu)
+cudaError_t launch_rmsnorm(const uint16_t *X, int64_t ldx, const uint16_t *G, float eps, int M, int K, uint16_t *XN,
+                           int64_t ldxn, cudaStream_t stream, bool pdl);
+
 // ---- router epilogue (topk.cu): softmax + top-k over each token's logits
 constexpr int kTopkMaxN = 8192;   // logits per token (shared memory: 5 bytes each)
 constexpr int kTopkMaxK = 64;

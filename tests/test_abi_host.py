@@ -438,3 +438,34 @@ def test_f32w_plan_follows_alignment():
     assert p(N=2048)["block_n"] == 4 and p(N=2048)["grid_x"] == 512
     assert p(M=16, K=14336)["k_chunk"] % 1024 == 0          # X in chunks: 16 x 14336 bf16 > budget
     assert p(M=0)["grid_x"] == 0
+
+
+# ---------------------------------------------------------------- RMS norm + q_b GEMM
+E16 = 0x7F0040000000
+
+
+def norm_call(X=A16, ldx=64, G=D16, eps=1e-6, XN=E16, ldxn=64, W=B16, ldw=64, Y=C16, ldy=32, M=4, N=32, K=64):
+    return sk.skinny_rmsnorm_gemm_bf16(X, ldx, G, eps, XN, ldxn, W, ldw, Y, ldy, M, N, K, 0)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(M=-1), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(M=0), sk.SKINNY_OK),
+    (dict(M=65), sk.SKINNY_ERR_UNSUPPORTED),
+    (dict(eps=-1.0), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(eps=float("inf")), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(eps=float("nan")), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(G=0), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(X=0), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(ldx=63), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(ldxn=63), sk.SKINNY_ERR_INVALID_VALUE),
+    (dict(X=A16 + 1), sk.SKINNY_ERR_MISALIGNED),
+    (dict(G=D16 + 1), sk.SKINNY_ERR_MISALIGNED),
+    (dict(XN=A16 + 64), sk.SKINNY_ERR_INVALID_VALUE),    # XN overlaps X
+    (dict(XN=D16 + 2), sk.SKINNY_ERR_INVALID_VALUE),     # XN overlaps gamma
+    (dict(XN=B16 + 64), sk.SKINNY_ERR_INVALID_VALUE),    # XN overlaps W
+    (dict(Y=A16 + 128), sk.SKINNY_ERR_INVALID_VALUE),    # Y overlaps X
+    (dict(), sk.SKINNY_ERR_NO_DEVICE),
+])
+def test_rmsnorm_gemm_argument_errors_are_host_side(kw, expect):
+    assert norm_call(**kw) == expect

@@ -1,0 +1,133 @@
+"""GPU parity of the q_b projection with its query RMS norm in front
+(skinny_rmsnorm_gemm_bf16) against the oracle.
+
+The stored XN is a bf16 rounding of x * r * g computed in fp32; the oracle
+gives that value in fp64.  Each XN element must be the nearest bf16 of the
+oracle's value, except within a relative 1e-5 of a rounding midpoint, where
+either neighbour is correct (fp32 arithmetic decides there).  Y must match the
+GEMM oracle applied to the XN the GPU produced (the standard tolerance), and
+everything is bit-identical run to run and with PDL on or off.
+"""
+import numpy as np
+import pytest
+import torch
+
+import latency_skinny_bf16_gb300 as sk
+import oracle
+import skinny_inputs as si
+from gpu_util import check_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _init():
+    assert sk.skinny_init(0) == sk.SKINNY_OK
+    yield
+
+
+def bf16_to_f64(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def check_xn(xn_bits, ref):
+    """xn_bits (bf16) against the unrounded fp64 reference values."""
+    got = bf16_to_f64(xn_bits)
+    t = torch.from_numpy(ref.astype(np.float32))
+    # nearest bf16 of the fp64 value (round to fp32 first cannot move it across a bf16 midpoint
+    # unless the value is within 2^-24 relative of it, which the allowance below covers)
+    rn = bf16_to_f64(t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    ok = got == rn
+    if not ok.all():
+        # a bf16 ulp at |v|, and the distance of v from the midpoint between got and rn
+        bad = ~ok
+        v = ref[bad]
+        mid = 0.5 * (got[bad] + rn[bad])
+        near_mid = np.abs(v - mid) <= 1e-5 * np.abs(v)
+        adjacent = np.abs(got[bad] - rn[bad]) <= np.abs(v) * 2.0 ** -7 * 1.0001
+        assert (near_mid & adjacent).all(), f"{int((~(near_mid & adjacent)).sum())} XN elements off"
+    return float((~ok).mean())
+
+
+def make_case(M, N, K, seed):
+    case = si.Case(f"qb_M{M}_N{N}_K{K}", M=M, N=N, K=K, seed=seed, w_dist="uniform_isqrtk")
+    X, W = si.make_inputs(case)
+    g = torch.Generator().manual_seed(seed + 17)
+    G = si._to_bf16_bits(1.0 + 0.1 * torch.randn(K, generator=g))
+    return case, X, W, G
+
+
+def run_norm(case, X, W, G, eps=1e-6, ldx=None, pdl=None):
+    M, N, K = case.M, case.N, case.K
+    ldx = ldx or K
+    x = torch.from_numpy(si.embed_rows(X, ldx).view(np.int16).copy()).cuda()
+    w = torch.from_numpy(W.view(np.int16)).cuda()
+    gd = torch.from_numpy(G.view(np.int16)).cuda()
+    xn = torch.zeros(M * K + 8, dtype=torch.int16, device="cuda")
+    y = torch.full((M * N + 8,), -7.0, device="cuda")
+    opts = {} if pdl is None else dict(pdl=pdl)
+    with sk.options(**opts):
+        st = sk.skinny_rmsnorm_gemm_bf16(x.data_ptr(), ldx, gd.data_ptr(), eps, xn.data_ptr(), K, w.data_ptr(), K,
+                                         y.data_ptr(), N, M, N, K, 0)
+    assert st == sk.SKINNY_OK
+    torch.cuda.synchronize()
+    xn_bits = xn.cpu().numpy()[: M * K].view(np.uint16).reshape(M, K)
+    yv = y.cpu().numpy()
+    assert (yv[M * N:] == -7.0).all()
+    return xn_bits, yv[: M * N].reshape(M, N)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 16, 32])
+def test_qb_projection_with_norm(M):
+    case, X, W, G = make_case(M, 24576, 1536, seed=3000 + M)
+    xn_bits, y = run_norm(case, X, W, G)
+    frac = check_xn(xn_bits, oracle.rmsnorm(X, G, 1e-6, M, 1536))
+    assert frac < 1e-3
+    yref, A = oracle.gemm(xn_bits, W, M, 24576, 1536)
+    check_parity(y, yref, A, case.name)
+    assert sk.skinny_get_device_status() == 0
+
+
+@pytest.mark.parametrize("backend", [dict(backend=1), dict(backend=1, consumer=2, block_n=32),
+                                     dict(backend=2, consumer=2, split_k=4), dict(backend=2, consumer=1),
+                                     dict(backend=3)])
+def test_norm_reaches_every_backend(backend):
+    """Whichever backend runs the GEMM, it reads XN only after the norm finished
+    (PDL on), and the result equals the no-PDL run bit for bit."""
+    case, X, W, G = make_case(8, 2112, 1536, seed=3100)
+    with sk.options(**backend):
+        xa, ya = run_norm(case, X, W, G, pdl=1)
+        xb, yb = run_norm(case, X, W, G, pdl=0)
+    assert np.array_equal(xa, xb) and np.array_equal(ya.view(np.uint32), yb.view(np.uint32))
+    check_xn(xa, oracle.rmsnorm(X, G, 1e-6, 8, 1536))
+    yref, A = oracle.gemm(xa, W, 8, 2112, 1536)
+    check_parity(ya, yref, A, f"norm + {backend}")
+
+
+def test_norm_strided_x_eps_and_ragged_k():
+    case, X, W, G = make_case(5, 130, 1000, seed=3200)
+    for eps in (0.0, 1e-6, 0.5):
+        xn_bits, y = run_norm(case, X, W, G, eps=eps, ldx=1003)
+        check_xn(xn_bits, oracle.rmsnorm(X, G, eps, 5, 1000))
+        yref, A = oracle.gemm(xn_bits, W, 5, 130, 1000)
+        check_parity(y, yref, A, f"eps={eps}")
+
+
+def test_norm_wrapper_and_graph():
+    case, X, W, G = make_case(4, 24576, 1536, seed=3300)
+    x = torch.from_numpy(X.view(np.int16)).cuda().view(torch.bfloat16)
+    w = torch.from_numpy(W.view(np.int16)).cuda().view(torch.bfloat16)
+    g = torch.from_numpy(G.view(np.int16)).cuda().view(torch.bfloat16)
+    y, xn = sk.rmsnorm_gemm(x, g, 1e-6, w)
+    torch.cuda.synchronize()
+    for pdl in (0, 1):
+        with sk.options(pdl=pdl):
+            s = torch.cuda.Stream()
+            y2 = torch.zeros_like(y)
+            xn2 = torch.zeros_like(xn)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s):
+                sk.rmsnorm_gemm(x, g, 1e-6, w, out=y2, xn=xn2, stream=s)
+            graph.replay()
+            torch.cuda.synchronize()
+        assert torch.equal(y2.view(torch.int32), y.view(torch.int32)) and torch.equal(xn2, xn)
