@@ -15,7 +15,9 @@
 // of exponentials are reduced in a fixed order (per thread ascending, warp
 // butterfly, warps in order), and each of the k selections is a block-wide
 // argmax over the entries not yet taken, so results are bit-identical from
-// run to run.  expf is CUDA's own.
+// run to run.  Rows of at most 1024 logits (the router's 256 / 384 experts)
+// take a warp per token instead, the row in registers and no barrier at all.
+// expf is CUDA's own.
 #include "common.cuh"
 #include "internal.h"
 
@@ -113,6 +115,76 @@ router_topk_kernel(const float *__restrict__ L, int64_t ldl, int N, int k, int r
         weights[(int64_t)m * ldwt + i] = renormalize ? chosen[i] / stat[1] : chosen[i];
 }
 
+// One warp per token for N <= 32 * VPL (VPL <= 32): lane l holds the logits
+// n = l + 32 j in registers; the max and the sum of exponentials are warp
+// butterflies over per-lane sums in ascending j, and each selection is a warp
+// argmax over the entries not yet taken (a per-lane bit mask): no barrier and
+// no shared memory.  Four tokens per CTA.
+template <int VPL>
+__global__ void __launch_bounds__(kTopkThreads)
+router_topk_warp_kernel(const float *__restrict__ L, int64_t ldl, int M, int N, int k, int renormalize,
+                        float *__restrict__ weights, int64_t ldwt, int32_t *__restrict__ ids, int64_t ldid)
+{
+    const int lane = threadIdx.x & 31;
+    const int m = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
+    griddep_wait();   // the logits come from the preceding kernel (the router GEMM)
+    if (m >= M) return;
+    const float *src = L + (int64_t)m * ldl;
+    float v[VPL];
+    float lmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+        const int n = lane + 32 * j;
+        v[j] = (n < N) ? src[n] : -INFINITY;
+        if (n < N) lmax = fmaxf(lmax, v[j]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+        if (lane + 32 * j < N) s += expf(v[j] - lmax);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    uint32_t taken = 0;
+    // lane l keeps choice l (lo) and choice 32 + l (hi); every lane sums the
+    // chosen probabilities in selection order
+    float p_lo = 0.f, p_hi = 0.f, total = 0.f;
+    int id_lo = -1, id_hi = -1;
+    for (int i = 0; i < k; ++i) {
+        float bv = -INFINITY;
+        int bn = -1, bj = -1;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+            const int n = lane + 32 * j;
+            if (n < N && !((taken >> j) & 1u) && better(v[j], n, bv, bn)) { bv = v[j]; bn = n; bj = j; }
+        }
+        float wv = bv;
+        int wn = bn;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, wv, o);
+            const int on = __shfl_xor_sync(0xFFFFFFFFu, wn, o);
+            if (better(ov, on, wv, wn)) { wv = ov; wn = on; }
+        }
+        if (wn == bn && bn >= 0) taken |= 1u << bj;   // the owner lane marks it
+        const float p = expf(wv - lmax) / s;
+        total += p;
+        if (lane == (i & 31)) {
+            if (i < 32) { p_lo = p; id_lo = wn; } else { p_hi = p; id_hi = wn; }
+        }
+    }
+    if (lane < k) {
+        ids[(int64_t)m * ldid + lane] = id_lo;
+        weights[(int64_t)m * ldwt + lane] = renormalize ? p_lo / total : p_lo;
+    }
+    if (32 + lane < k) {
+        ids[(int64_t)m * ldid + 32 + lane] = id_hi;
+        weights[(int64_t)m * ldwt + 32 + lane] = renormalize ? p_hi / total : p_hi;
+    }
+    griddep_launch_dependents();
+}
+
 }  // namespace
 
 int router_topk_smem_bytes(int N) { return N * 5; }
@@ -121,15 +193,28 @@ cudaError_t launch_router_topk(const float *L, int64_t ldl, int M, int N, int k,
                                int64_t ldwt, int32_t *ids, int64_t ldid, cudaStream_t stream, bool pdl) {
     if (M < 1 || N < 1 || N > kTopkMaxN || k < 1 || k > N || k > kTopkMaxK) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)M, 1, 1);
     cfg.blockDim = dim3(kTopkThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)router_topk_smem_bytes(N);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (N <= 1024) {
+        // a warp per token, the row in registers
+        cfg.gridDim = dim3((unsigned)((M + kTopkWarps - 1) / kTopkWarps), 1, 1);
+        cfg.dynamicSmemBytes = 0;
+        if (N <= 256)
+            return cudaLaunchKernelEx(&cfg, router_topk_warp_kernel<8>, L, ldl, M, N, k, renormalize, weights, ldwt,
+                                      ids, ldid);
+        if (N <= 512)
+            return cudaLaunchKernelEx(&cfg, router_topk_warp_kernel<16>, L, ldl, M, N, k, renormalize, weights, ldwt,
+                                      ids, ldid);
+        return cudaLaunchKernelEx(&cfg, router_topk_warp_kernel<32>, L, ldl, M, N, k, renormalize, weights, ldwt,
+                                  ids, ldid);
+    }
+    cfg.gridDim = dim3((unsigned)M, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)router_topk_smem_bytes(N);
     return cudaLaunchKernelEx(&cfg, router_topk_kernel, L, ldl, N, k, renormalize, weights, ldwt, ids, ldid);
 }
 
