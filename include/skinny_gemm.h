@@ -22,13 +22,14 @@
  * Token range.  M = 1..16 is the router tier of the first page; every
  * backend takes it.  M = 17..64 is the medium-M regime that the second page
  * (item 3) hands to a separate fused GEMM before falling back to cuBLAS; here
- * it runs on the cluster split-K backend with the mma.sync consumer only
- * (the tokens become 2 or 4 groups of 16 on the MMA's N side), so it needs
- * K % 16 == 0, 16-byte aligned W rows (W and ldw), and a per-CTA X slice
+ * it runs on the tensor cores only (the tokens become 2 or 4 groups of 16 on
+ * the MMA's N side): the tensor-core dot-product for weights of 16 MB or more
+ * with K % 32 == 0 (any K: X is staged in chunks), else the cluster split-K
+ * backend with the mma.sync consumer, which needs a per-CTA X slice
  * (M x K / split_k x 2 bytes, split_k <= 8) of at most 160 KB that fits in
- * shared memory beside the W ring: at 64 tokens K = 7168 runs, K = 14336
- * does not.  Other M > 16 shapes return
- * SKINNY_ERR_UNSUPPORTED.
+ * shared memory beside the W ring (at 64 tokens K = 7168 runs, K = 14336 does
+ * not).  Both need K % 16 == 0 and 16-byte aligned W rows (W and ldw).  Other
+ * M > 16 shapes return SKINNY_ERR_UNSUPPORTED.
  *
  * bf16 values are passed as their 16-bit patterns (uint16_t) so this header
  * needs no CUDA header.  Streams are passed as `void*` holding a cudaStream_t

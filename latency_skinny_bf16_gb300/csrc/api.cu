@@ -208,8 +208,10 @@ bool plan_dotmma(int M, int N, int K, int vec, int force_bn, int num_sms, skinny
         while (bn < 64 && (N + 2 * bn - 1) / (2 * bn) >= 2 * num_sms) bn *= 2;
     }
     if (!dotmma_supported(M, bn)) return false;
-    const int MT = M <= 8 ? 8 : 16;
-    int kc = (kMmaXBudget / (2 * MT)) & ~31;
+    const int MT = dotmma_tokens(M);
+    // 8 / 16 tokens: 64 KB of X per CTA (3 CTAs per SM); 32 / 64: 96 KB, so
+    // the chunks stay at least 768 elements long
+    int kc = ((MT >= 32 ? 96 * 1024 : kMmaXBudget) / (2 * MT)) & ~31;
     if (kc >= K) kc = K;
     if (kc < 32) kc = 32;
     p->backend = SKINNY_BACKEND_DOTPROD;
@@ -385,20 +387,28 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
     int backend = fb, consumer = fc, split = fs, bn = fbn, stages = fst, stage_k = g_opt_force_stage_k.load();
     int tuned = 0;
     const bool dotmma_ok = splitk_ok && K % 32 == 0;
-    // 17..64 tokens: only the split-K backend with the MMA consumer
+    // 17..64 tokens: tensor cores only, on the split-K backend, or on the
+    // tensor-core dot-product for large weights (>= 16 MB, K % 32 == 0)
     const bool mid_m = M > kMaxMSmall;
     if (mid_m) {
         if (!mma_ok) return SKINNY_ERR_UNSUPPORTED;
-        if ((fb != SKINNY_BACKEND_AUTO && fb != SKINNY_BACKEND_SPLITK) ||
+        if ((fb != SKINNY_BACKEND_AUTO && fb != SKINNY_BACKEND_SPLITK && fb != SKINNY_BACKEND_DOTPROD) ||
             (fc != SKINNY_CONSUMER_AUTO && fc != SKINNY_CONSUMER_MMA))
             return SKINNY_ERR_UNSUPPORTED;
-        backend = SKINNY_BACKEND_SPLITK;
         consumer = SKINNY_CONSUMER_MMA;
+        if (fb == SKINNY_BACKEND_DOTPROD && !dotmma_ok) return SKINNY_ERR_UNSUPPORTED;
+        backend = fb != SKINNY_BACKEND_AUTO ? fb
+                  : (dotmma_ok && 2.0 * N * K >= 16e6) ? SKINNY_BACKEND_DOTPROD : SKINNY_BACKEND_SPLITK;
         const TunedEntry *e = (fb == SKINNY_BACKEND_AUTO) ? lookup_tuned(M, N, K) : nullptr;
         if (e && e->backend == SKINNY_BACKEND_SPLITK && e->consumer == SKINNY_CONSUMER_MMA) {
+            backend = SKINNY_BACKEND_SPLITK;
             if (!split) split = e->split_k;
             if (!stages) stages = e->stages;
             if (!stage_k) stage_k = e->stage_k;
+            tuned = 1;
+        } else if (e && e->backend == SKINNY_BACKEND_DOTPROD && e->consumer == SKINNY_CONSUMER_MMA && dotmma_ok) {
+            backend = SKINNY_BACKEND_DOTPROD;
+            if (!bn) bn = e->block_n;
             tuned = 1;
         }
     }
@@ -434,7 +444,10 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
     bool ok;
     if (backend == SKINNY_BACKEND_DOTPROD && consumer == SKINNY_CONSUMER_MMA) {
         ok = plan_dotmma(M, N, K, vec, bn, num_sms, p);
-        if (!ok && fb == SKINNY_BACKEND_AUTO && fc == SKINNY_CONSUMER_AUTO) {
+        if (!ok && fb == SKINNY_BACKEND_AUTO && mid_m) {
+            ok = plan_splitk(M, N, K, vec, consumer, fs, fst, fgy, g_opt_force_stage_k.load(), num_sms, p);
+            tuned = 0;
+        } else if (!ok && fb == SKINNY_BACKEND_AUTO && fc == SKINNY_CONSUMER_AUTO) {
             ok = plan_dotprod(M, N, K, vec, 0, num_sms, p);
             tuned = 0;
         }

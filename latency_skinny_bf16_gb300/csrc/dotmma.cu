@@ -139,7 +139,8 @@ dotmma_kernel(const uint16_t *__restrict__ X, int64_t ldx,
                     mbar_arrive_expect_tx(xbar, (uint32_t)(M * klen * 2));
                 }
                 __syncwarp();
-                if (lane < M) bulk_copy_g2s(smem_u32(xs + lane * xrowb), X + lane * ldx + k0, (uint32_t)(klen * 2), xbar);
+                for (int r = lane; r < M; r += 32)
+                    bulk_copy_g2s(smem_u32(xs + r * xrowb), X + r * ldx + k0, (uint32_t)(klen * 2), xbar);
             }
             const uint32_t par = (uint32_t)((k0 / kc) & 1);
             if (!mbar_wait_bounded(xbar, par, budget_ns)) {
@@ -192,9 +193,14 @@ dotmma_kernel(const uint16_t *__restrict__ X, int64_t ldx,
 using MmaKernel = void (*)(const uint16_t *, int64_t, const uint16_t *, int64_t, void *, int64_t,
                            int, int, int, int, int, int *, uint64_t, int);
 
-const MmaKernel kTable[2][3] = {
+// token buckets 8 / 16 / 32 / 64 (M = 17..64: the medium-M regime on large weights)
+const MmaKernel kTable[4][3] = {
     {&dotmma_kernel<8, 1>, &dotmma_kernel<8, 2>, &dotmma_kernel<8, 4>},
-    {&dotmma_kernel<16, 1>, &dotmma_kernel<16, 2>, &dotmma_kernel<16, 4>}};
+    {&dotmma_kernel<16, 1>, &dotmma_kernel<16, 2>, &dotmma_kernel<16, 4>},
+    {&dotmma_kernel<32, 1>, &dotmma_kernel<32, 2>, &dotmma_kernel<32, 4>},
+    {&dotmma_kernel<64, 1>, &dotmma_kernel<64, 2>, &dotmma_kernel<64, 4>}};
+
+int bucket(int M) { return M <= 8 ? 0 : M <= 16 ? 1 : M <= 32 ? 2 : 3; }
 
 int rt_index(int block_n) {
     switch (block_n) { case 16: return 0; case 32: return 1; case 64: return 2; default: return -1; }
@@ -202,16 +208,18 @@ int rt_index(int block_n) {
 
 }  // namespace
 
-bool dotmma_supported(int M, int block_n) { return M >= 1 && M <= kMaxMSmall && rt_index(block_n) >= 0; }
+bool dotmma_supported(int M, int block_n) { return M >= 1 && M <= kMaxMSplitMma && rt_index(block_n) >= 0; }
+
+int dotmma_tokens(int M) { return 8 << bucket(M); }
 
 int dotmma_smem_bytes(int M, int block_n, int k_chunk) {
     (void)block_n;
-    const int MT = M <= 8 ? 8 : 16;
+    const int MT = dotmma_tokens(M);
     return MT * xrow_bytes(k_chunk) + kWarps * 16 * MT * 4;
 }
 
 cudaError_t dotmma_prepare() {
-    for (int a = 0; a < 2; ++a)
+    for (int a = 0; a < 4; ++a)
         for (int b = 0; b < 3; ++b) {
             cudaError_t e = set_max_dyn_smem(kTable[a][b]);
             if (e != cudaSuccess) return e;
@@ -221,8 +229,8 @@ cudaError_t dotmma_prepare() {
 
 cudaError_t launch_dotmma(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c) {
     const int ri = rt_index(p.block_n);
-    if (ri < 0 || a.M < 1 || a.M > kMaxMSmall || a.K % 32 != 0 || p.k_chunk % 32 != 0) return cudaErrorInvalidValue;
-    MmaKernel fn = kTable[a.M <= 8 ? 0 : 1][ri];
+    if (ri < 0 || a.M < 1 || a.M > kMaxMSplitMma || a.K % 32 != 0 || p.k_chunk % 32 != 0) return cudaErrorInvalidValue;
+    MmaKernel fn = kTable[bucket(a.M)][ri];
     const int x_vec16 = ((reinterpret_cast<uintptr_t>(a.X) & 15) == 0 && (a.ldx & 7) == 0) ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid_x, 1, 1);

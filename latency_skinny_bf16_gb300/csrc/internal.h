@@ -43,6 +43,7 @@ cudaError_t launch_dotprod(const GemmArgs &a, const skinny_plan_t &p, const Laun
 // ---- dot-product backend with mma.sync arithmetic (dotmma.cu): block_n 16/32/64
 int dotmma_smem_bytes(int M, int block_n, int k_chunk);
 bool dotmma_supported(int M, int block_n);
+int dotmma_tokens(int M);   // token bucket of the instantiation: 8, 16, 32 or 64
 cudaError_t dotmma_prepare();
 cudaError_t launch_dotmma(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
 

@@ -40,9 +40,13 @@ def token_bucket(M: int) -> int:
 def candidates(M: int, K: int, N: int = 0):
     out = []
     if M > 16:
-        # 17..64 tokens: cluster split-K with the MMA consumer is the only path
+        # 17..64 tokens: tensor cores only -- cluster split-K with the MMA
+        # consumer, or the tensor-core dot-product for large weights
         if K % 16:
             return out
+        if 2 * N * K > 16e6 and K % 32 == 0:
+            for bn in (16, 32, 64):
+                out.append(dict(backend=1, consumer=2, split_k=0, stages=0, block_n=bn, stage_k=0))
         for s in (2, 4, 6, 8):
             for bk in (0, 512):           # 0: the dispatcher's ring chunk for this shape
                 out.append(dict(backend=2, consumer=2, split_k=s, stages=0, block_n=0, stage_k=bk))

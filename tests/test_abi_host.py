@@ -195,8 +195,8 @@ def test_every_tuned_entry_is_a_supported_plan_and_is_used():
         assert 1 <= m_lo <= m_hi <= 64
         # a row never spans two kernels: 1..8 / 9..16 / 17..32 / 33..64 tokens
         assert (m_lo <= 8) == (m_hi <= 8) and (m_lo <= 16) == (m_hi <= 16) and (m_lo <= 32) == (m_hi <= 32)
-        if m_hi > 16:
-            assert (be, co) == (sk.SKINNY_BACKEND_SPLITK, sk.SKINNY_CONSUMER_MMA)
+        if m_hi > 16:   # tensor cores only: split-K MMA or the tensor-core dot-product
+            assert co == sk.SKINNY_CONSUMER_MMA and be in (sk.SKINNY_BACKEND_SPLITK, sk.SKINNY_BACKEND_DOTPROD)
         for M in range(m_lo, m_hi + 1):
             p = plan(M, N, K)
             assert p["tuned"] == 1, (K, N, M)
@@ -263,28 +263,45 @@ def test_bf16_output_two_byte_aligned_y_passes_the_checks():
 MID_M = (17, 24, 32, 33, 40, 48, 63, 64)
 
 
-def test_mid_m_takes_the_splitk_mma_path_one_tile_per_cluster():
+def test_mid_m_takes_a_tensor_core_path():
     for M in MID_M:
-        for (N, K) in ((256, 7168), (384, 7168), (2112, 7168), (1536, 4096)):
+        for (N, K) in ((256, 7168), (384, 7168), (2112, 7168), (1536, 4096), (7168, 14336)):
             p = plan(M, N, K)
-            assert (p["backend"], p["consumer"]) == (sk.SKINNY_BACKEND_SPLITK, sk.SKINNY_CONSUMER_MMA), (M, N, K)
-            assert p["block_n"] == 16 and p["smem_bytes"] <= 227 * 1024
-            assert p["split_k"] * p["k_chunk"] >= K and p["k_chunk"] % 16 == 0
-            if p["split_k"] > 1:
-                # a single partial-sum buffer: no cluster loops over two tiles
-                assert p["grid_y"] == (N + 15) // 16
+            assert p["consumer"] == sk.SKINNY_CONSUMER_MMA and p["smem_bytes"] <= 227 * 1024, (M, N, K)
+            if p["backend"] == sk.SKINNY_BACKEND_SPLITK:
+                assert p["block_n"] == 16
+                assert p["split_k"] * p["k_chunk"] >= K and p["k_chunk"] % 16 == 0
+                if p["split_k"] > 1:
+                    # a single partial-sum buffer: no cluster loops over two tiles
+                    assert p["grid_y"] == (N + 15) // 16
+            else:
+                assert p["backend"] == sk.SKINNY_BACKEND_DOTPROD and p["block_n"] in (16, 32, 64)
+                assert 2 * N * K >= 16e6 and p["k_chunk"] % 32 == 0
+    # the default rule on untuned shapes: split-K below 16 MB of W, the tensor-core dot-product above
+    assert plan(40, 320, 7168)["backend"] == sk.SKINNY_BACKEND_SPLITK
+    p = plan(40, 8192, 4096)
+    assert (p["backend"], p["consumer"]) == (sk.SKINNY_BACKEND_DOTPROD, sk.SKINNY_CONSUMER_MMA)
+    with sk.options(backend=sk.SKINNY_BACKEND_DOTPROD):
+        assert plan(20, 320, 7168)["consumer"] == sk.SKINNY_CONSUMER_MMA
 
 
 def test_mid_m_unsupported_shapes_are_refused_on_the_host():
     with pytest.raises(sk.SkinnyError) as e:
-        plan(64, 7168, 14336)                      # X slice does not fit shared memory
+        plan(64, 256, 14336)                       # split-K only (7 MB of W): the X slice does not fit
+    assert e.value.status == sk.SKINNY_ERR_UNSUPPORTED
+    p = plan(64, 7168, 14336)                      # 206 MB of W: the tensor-core dot-product, X in chunks
+    assert p["backend"] == sk.SKINNY_BACKEND_DOTPROD and p["k_chunk"] < 14336
+    with pytest.raises(sk.SkinnyError) as e:
+        with sk.options(backend=sk.SKINNY_BACKEND_DOTPROD):
+            plan(20, 256, 7184)                    # K % 32 != 0: no tensor-core dot-product
     assert e.value.status == sk.SKINNY_ERR_UNSUPPORTED
     for kw in (dict(K=7160), dict(K=7176, W=B16 + 8), dict(K=7169)):   # K % 16, W rows not 16-byte aligned
         K = kw.pop("K")
         with pytest.raises(sk.SkinnyError) as e:
             plan(20, 256, K, **kw)
         assert e.value.status == sk.SKINNY_ERR_UNSUPPORTED
-    for opts in (dict(backend=sk.SKINNY_BACKEND_DOTPROD), dict(consumer=sk.SKINNY_CONSUMER_FMA),
+    for opts in (dict(backend=sk.SKINNY_BACKEND_DOTPROD, consumer=sk.SKINNY_CONSUMER_FMA),
+                 dict(consumer=sk.SKINNY_CONSUMER_FMA),
                  dict(backend=sk.SKINNY_BACKEND_SPLITK, split_k=8, clusters=4)):
         with sk.options(**opts):
             with pytest.raises(sk.SkinnyError) as e:

@@ -166,3 +166,31 @@ def test_midm_graph_capture_chain(pdl):
     for b, e, c in zip(bufs, eager, cases):
         assert np.array_equal(b.y_mat().view(np.uint32), e.view(np.uint32)), c.name
     assert sk.skinny_get_device_status() == 0
+
+
+@pytest.mark.parametrize("bn", [16, 32, 64])
+@pytest.mark.parametrize("M", [17, 24, 33, 64])
+def test_midm_tensor_core_dotprod(M, bn):
+    """17..64 tokens on the tensor-core dot-product (the route for large
+    weights): ragged N, X staged in several chunks, strided Y."""
+    for i, (N, K) in enumerate([(130, 1536), (100, 14336), (300, 4096)]):
+        case = si.Case(f"midm_dm_M{M}_bn{bn}_{N}_{K}", M=M, N=N, K=K, seed=3400 + 10 * M + bn + i,
+                       w_dist="uniform_isqrtk", ldy=N + 3)
+        X, W = si.make_inputs(case)
+        with sk.options(backend=sk.SKINNY_BACKEND_DOTPROD, consumer=sk.SKINNY_CONSUMER_MMA, block_n=bn):
+            b = Buffers(case, X, W)
+            p = b.plan()
+            assert (p["backend"], p["consumer"], p["block_n"]) == (sk.SKINNY_BACKEND_DOTPROD,
+                                                                   sk.SKINNY_CONSUMER_MMA, bn)
+            yref, A = reference(case, X, W)
+            first = None
+            for _ in range(2):
+                assert b.run() == sk.SKINNY_OK
+                y = b.y_mat().copy()
+                if first is None:
+                    first = y
+                    check_parity(y, yref, A, case.name)
+                else:
+                    assert np.array_equal(y.view(np.uint32), first.view(np.uint32))
+            assert b.canary_ok()
+    assert sk.skinny_get_device_status() == 0
