@@ -76,9 +76,14 @@ typedef enum {
     SKINNY_BACKEND_AUTO = 0,
     SKINNY_BACKEND_DOTPROD = 1,     /* one CTA per block of output columns, whole K */
     SKINNY_BACKEND_SPLITK = 2,      /* K split over the CTAs of a thread-block cluster */
-    SKINNY_BACKEND_STREAM = 3       /* one CTA per SM, whole K per 16-row tile, K-outer: X and W
+    SKINNY_BACKEND_STREAM = 3,      /* one CTA per SM, whole K per 16-row tile, K-outer: X and W
                                        stream through one ring chunk by chunk (large weights;
                                        needs 16-byte aligned X and W rows, K % 16 == 0, M <= 16) */
+    SKINNY_BACKEND_TCGEN05 = 4      /* 128 W rows per CTA on the fifth-generation tensor cores
+                                       (tcgen05.mma, accumulator in tensor memory), W and X boxes by
+                                       tensor-map TMA, K split over a cluster of split_k CTAs
+                                       (1, 2, 4 or 8); needs 16-byte aligned X and W rows
+                                       (pointers, ldx and ldw); any K >= 1, M <= 64 */
 } skinny_backend_t;
 
 typedef enum {

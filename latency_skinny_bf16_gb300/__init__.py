@@ -42,6 +42,7 @@ SKINNY_BACKEND_AUTO = 0
 SKINNY_BACKEND_DOTPROD = 1
 SKINNY_BACKEND_SPLITK = 2
 SKINNY_BACKEND_STREAM = 3
+SKINNY_BACKEND_TCGEN05 = 4
 SKINNY_CONSUMER_AUTO = 0
 SKINNY_CONSUMER_FMA = 1
 SKINNY_CONSUMER_MMA = 2

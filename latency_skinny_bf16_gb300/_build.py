@@ -21,7 +21,7 @@ LIB_NAME = "libskinny_gemm.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
 SOURCES = ["api.cu", "dotprod.cu", "dotprod_f32w.cu", "dotmma.cu", "splitk.cu", "stream.cu", "topk.cu",
-           "rmsnorm.cu"]
+           "rmsnorm.cu", "tmem_gemm.cu"]
 HEADERS = ["common.cuh", "internal.h", "tuning_table.inc"]
 
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]

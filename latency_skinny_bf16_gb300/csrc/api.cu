@@ -82,7 +82,7 @@ skinny_status_t init_device_current(DeviceState &d, int device) {
         return SKINNY_ERR_NO_DEVICE;
     if (major != 10 || minor != 3) return SKINNY_ERR_NO_DEVICE;   // built for sm_103a only
     if (dotprod_prepare() != cudaSuccess || dotmma_prepare() != cudaSuccess || splitk_prepare() != cudaSuccess ||
-        stream_prepare() != cudaSuccess || dotprod_f32w_prepare() != cudaSuccess)
+        stream_prepare() != cudaSuccess || dotprod_f32w_prepare() != cudaSuccess || tc_prepare() != cudaSuccess)
         return SKINNY_ERR_LAUNCH;
     void *sym = nullptr;
     if (cudaGetSymbolAddress(&sym, g_status_word) != cudaSuccess) return SKINNY_ERR_LAUNCH;
@@ -369,6 +369,60 @@ bool plan_stream(int M, int N, int K, int vec, bool x_ok, int force_c, int force
     return true;
 }
 
+// Tensor-core (tcgen05) plan: 128 W rows per CTA; clusters of S CTAs along K
+// while the row tiles alone leave SMs idle; the deepest ring that lets the
+// whole grid be resident at once (up to 3 CTAs per SM share its shared memory).
+bool plan_tc(int M, int N, int K, int vec, bool x_ok, int force_s, int force_stages, int force_bk, int num_sms,
+             skinny_plan_t *p) {
+    if (vec != 8 || !x_ok || K < 1 || !tc_supported(M)) return false;
+    const int tiles = (N + 127) / 128;
+    if (tiles < 1 || tiles > 65535) return false;
+    const int bk = force_bk ? force_bk : 64;
+    if (bk < 64 || bk > kTcMaxBK || bk % 64) return false;
+    const int nk = (K + bk - 1) / bk;             // ring stages over the whole K
+    int S = force_s;
+    if (S == 0) {
+        S = 1;
+        // double while SMs stay idle and every rank still gets a non-empty slice
+        while (S < kSplitMaxCluster && tiles * S < num_sms && 2 * S <= nk &&
+               (2 * S - 1) * ((nk + 2 * S - 1) / (2 * S)) < nk)
+            S *= 2;
+    }
+    if (S < 1 || S > kSplitMaxCluster || 128 % S != 0) return false;
+    const int per_rank = (nk + S - 1) / S;        // ring stages per cluster rank (a forced S may leave
+                                                  // the last ranks empty: they add zeros)
+    int stages = force_stages;
+    if (!stages) {
+        int per_sm = (tiles * S + num_sms - 1) / num_sms;
+        if (per_sm < 1) per_sm = 1;
+        if (per_sm > 3) per_sm = 3;
+        int budget = (228 * 1024) / per_sm - 2048;
+        if (budget > kMaxDynSmem) budget = kMaxDynSmem;
+        stages = kSplitMaxStages;
+        while (stages > 1 && tc_smem_bytes(M, bk, stages, S) > budget) --stages;
+        // no deeper than the slice, but deep enough to receive the partials
+        int least = 1;
+        while (least < stages && tc_smem_bytes(M, bk, least, S) > kMaxDynSmem) ++least;
+        if (stages > per_rank) stages = per_rank > least ? per_rank : least;
+    }
+    if (stages < 1 || stages > kSplitMaxStages) return false;
+    const int smem = tc_smem_bytes(M, bk, stages, S);
+    if (smem > kMaxDynSmem) return false;
+    p->backend = SKINNY_BACKEND_TCGEN05;
+    p->consumer = SKINNY_CONSUMER_MMA;
+    p->vec_elems = 8;
+    p->block_n = 128;
+    p->split_k = S;
+    p->stages = stages;
+    p->stage_k = bk;
+    p->k_chunk = per_rank * bk;
+    p->grid_x = S;
+    p->grid_y = tiles;
+    p->threads = kTcThreads;
+    p->smem_bytes = smem;
+    return true;
+}
+
 skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw, int M, int N, int K, int num_sms,
                           skinny_plan_t *p) {
     std::memset(p, 0, sizeof(*p));
@@ -382,25 +436,36 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
     const bool mma_ok = splitk_ok && K % 16 == 0;
     const bool x_ok = (reinterpret_cast<uintptr_t>(X) & 15) == 0 && ldx % 8 == 0;
     const bool stream_ok = mma_ok && x_ok && M <= kMaxMSmall;
+    const bool tc_ok = vec == 8 && x_ok;
     const int pdl = opt_pdl();
 
     int backend = fb, consumer = fc, split = fs, bn = fbn, stages = fst, stage_k = g_opt_force_stage_k.load();
     int tuned = 0;
     const bool dotmma_ok = splitk_ok && K % 32 == 0;
-    // 17..64 tokens: tensor cores only, on the split-K backend, or on the
-    // tensor-core dot-product for large weights (>= 16 MB, K % 32 == 0)
+    // 17..64 tokens: tensor cores only, on the split-K backend, on the
+    // tensor-core dot-product for large weights (>= 16 MB, K % 32 == 0), or on
+    // the tcgen05 backend (also the only one for K % 16 != 0)
     const bool mid_m = M > kMaxMSmall;
     if (mid_m) {
-        if (!mma_ok) return SKINNY_ERR_UNSUPPORTED;
-        if ((fb != SKINNY_BACKEND_AUTO && fb != SKINNY_BACKEND_SPLITK && fb != SKINNY_BACKEND_DOTPROD) ||
+        if (!mma_ok && !tc_ok) return SKINNY_ERR_UNSUPPORTED;
+        if ((fb != SKINNY_BACKEND_AUTO && fb != SKINNY_BACKEND_SPLITK && fb != SKINNY_BACKEND_DOTPROD &&
+             fb != SKINNY_BACKEND_TCGEN05) ||
             (fc != SKINNY_CONSUMER_AUTO && fc != SKINNY_CONSUMER_MMA))
             return SKINNY_ERR_UNSUPPORTED;
         consumer = SKINNY_CONSUMER_MMA;
         if (fb == SKINNY_BACKEND_DOTPROD && !dotmma_ok) return SKINNY_ERR_UNSUPPORTED;
+        if (fb == SKINNY_BACKEND_SPLITK && !mma_ok) return SKINNY_ERR_UNSUPPORTED;
         backend = fb != SKINNY_BACKEND_AUTO ? fb
+                  : !mma_ok                               ? SKINNY_BACKEND_TCGEN05
                   : (dotmma_ok && 2.0 * N * K >= 16e6) ? SKINNY_BACKEND_DOTPROD : SKINNY_BACKEND_SPLITK;
         const TunedEntry *e = (fb == SKINNY_BACKEND_AUTO) ? lookup_tuned(M, N, K) : nullptr;
-        if (e && e->backend == SKINNY_BACKEND_SPLITK && e->consumer == SKINNY_CONSUMER_MMA) {
+        if (e && e->backend == SKINNY_BACKEND_TCGEN05 && tc_ok) {
+            backend = SKINNY_BACKEND_TCGEN05;
+            if (!split) split = e->split_k;
+            if (!stages) stages = e->stages;
+            if (!stage_k) stage_k = e->stage_k;
+            tuned = 1;
+        } else if (e && e->backend == SKINNY_BACKEND_SPLITK && e->consumer == SKINNY_CONSUMER_MMA && mma_ok) {
             backend = SKINNY_BACKEND_SPLITK;
             if (!split) split = e->split_k;
             if (!stages) stages = e->stages;
@@ -419,7 +484,8 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
                   (e->backend == SKINNY_BACKEND_DOTPROD && e->consumer == SKINNY_CONSUMER_MMA && dotmma_ok) ||
                   (e->backend == SKINNY_BACKEND_SPLITK && splitk_ok &&
                    (e->consumer != SKINNY_CONSUMER_MMA || mma_ok)) ||
-                  (e->backend == SKINNY_BACKEND_STREAM && stream_ok));
+                  (e->backend == SKINNY_BACKEND_STREAM && stream_ok) ||
+                  (e->backend == SKINNY_BACKEND_TCGEN05 && tc_ok));
         if (entry_ok) {
             backend = e->backend;
             if (consumer == SKINNY_CONSUMER_AUTO) consumer = e->consumer;
@@ -468,6 +534,11 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
             ok = plan_dotprod(M, N, K, vec, 0, num_sms, p);
             tuned = 0;
         }
+        if (!ok && fb == SKINNY_BACKEND_AUTO && mid_m && tc_ok) {
+            // 17..64 tokens whose X slice does not fit beside the split-K ring
+            ok = plan_tc(M, N, K, vec, x_ok, 0, 0, 0, num_sms, p);
+            tuned = 0;
+        }
     } else if (backend == SKINNY_BACKEND_STREAM) {
         if ((fc != SKINNY_CONSUMER_AUTO && fc != SKINNY_CONSUMER_MMA) || (bn != 0 && bn != 16))
             return SKINNY_ERR_UNSUPPORTED;
@@ -476,6 +547,21 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
             // a tuned or default streaming plan these pointers / sizes cannot use
             ok = (dotmma_ok && M >= 4 && plan_dotmma(M, N, K, vec, 0, num_sms, p)) ||
                  plan_dotprod(M, N, K, vec, 0, num_sms, p);
+            tuned = 0;
+        }
+    } else if (backend == SKINNY_BACKEND_TCGEN05) {
+        if ((fc != SKINNY_CONSUMER_AUTO && fc != SKINNY_CONSUMER_MMA) || (bn != 0 && bn != 128))
+            return SKINNY_ERR_UNSUPPORTED;
+        ok = plan_tc(M, N, K, vec, x_ok, split, stages, stage_k, num_sms, p);
+        if (!ok && fb == SKINNY_BACKEND_AUTO) {
+            // a tuned tensor-core plan these pointers / strides cannot use: the
+            // default rule of the token range
+            const bool big = dotmma_ok && 2.0 * N * K >= 16e6;
+            ok = mid_m ? ((big && plan_dotmma(M, N, K, vec, 0, num_sms, p)) ||
+                          plan_splitk(M, N, K, vec, SKINNY_CONSUMER_MMA, fs, fst, fgy, g_opt_force_stage_k.load(),
+                                      num_sms, p))
+                       : ((big && M >= 4 && plan_dotmma(M, N, K, vec, 0, num_sms, p)) ||
+                          plan_dotprod(M, N, K, vec, 0, num_sms, p));
             tuned = 0;
         }
     } else {
@@ -496,7 +582,10 @@ void log_plan(int M, int N, int K, int ldw, const skinny_plan_t &p) {
                  "[skinny] M=%d N=%d K=%d ldw=%d -> %s consumer=%d vec=%d block_n=%d split_k=%d stages=%d stage_k=%d "
                  "k_chunk=%d grid=%dx%d smem=%d pdl=%d tuned=%d\n",
                  M, N, K, ldw,
-                 p.backend == SKINNY_BACKEND_DOTPROD ? "dotprod" : p.backend == SKINNY_BACKEND_SPLITK ? "splitk" : "stream",
+                 p.backend == SKINNY_BACKEND_DOTPROD  ? "dotprod"
+                 : p.backend == SKINNY_BACKEND_SPLITK ? "splitk"
+                 : p.backend == SKINNY_BACKEND_STREAM ? "stream"
+                                                      : "tcgen05",
                  p.consumer,
                  p.vec_elems, p.block_n, p.split_k, p.stages, p.stage_k, p.k_chunk, p.grid_x, p.grid_y, p.smem_bytes,
                  p.pdl, p.tuned);
@@ -538,6 +627,8 @@ skinny_status_t run_gemm(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
         e = plan.consumer == SKINNY_CONSUMER_MMA ? launch_dotmma(a, plan, c) : launch_dotprod(a, plan, c);
     else if (plan.backend == SKINNY_BACKEND_STREAM)
         e = launch_stream(a, plan, c);
+    else if (plan.backend == SKINNY_BACKEND_TCGEN05)
+        e = launch_tc(a, plan, c);
     else
         e = launch_splitk(a, plan, c);
     return e == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
@@ -755,7 +846,7 @@ skinny_status_t skinny_set_option(int option, int value) {
             if (value != 0 && value != 1) return SKINNY_ERR_INVALID_VALUE;
             g_opt_pdl.store(value); return SKINNY_OK;
         case SKINNY_OPT_FORCE_BACKEND:
-            if (value < 0 || value > 3) return SKINNY_ERR_INVALID_VALUE;
+            if (value < 0 || value > 4) return SKINNY_ERR_INVALID_VALUE;
             g_opt_force_backend.store(value); return SKINNY_OK;
         case SKINNY_OPT_FORCE_CONSUMER:
             if (value < 0 || value > 2) return SKINNY_ERR_INVALID_VALUE;
@@ -765,7 +856,7 @@ skinny_status_t skinny_set_option(int option, int value) {
             g_opt_force_split_k.store(value); return SKINNY_OK;
         case SKINNY_OPT_FORCE_BLOCK_N:
             if (!(value == 0 || value == 1 || value == 2 || value == 4 || value == 8 || value == 16 ||
-                  value == 32 || value == 64))
+                  value == 32 || value == 64 || value == 128))
                 return SKINNY_ERR_INVALID_VALUE;
             g_opt_force_block_n.store(value); return SKINNY_OK;
         case SKINNY_OPT_FORCE_STAGES:

@@ -33,12 +33,25 @@ DEFAULT_SHAPES = ["7168x256", "7168x384", "2880x128", "4096x256", "7168x2112", "
 
 def token_bucket(M: int) -> int:
     """Kernels are instantiated per token bucket: 1..8, 9..16 (MMA tiles of 8 /
-    16 tokens), 17..32 and 33..64 (split-K MMA only)."""
+    16 tokens), 17..32 and 33..64 (tensor cores only)."""
     return 8 if M <= 8 else 16 if M <= 16 else 32 if M <= 32 else 64
+
+
+def tc_candidates(M: int, K: int, N: int):
+    """tcgen05 plans: cluster sizes along K, 1 or 2 boxes per ring stage, the
+    planner's ring depth for the grid."""
+    out = []
+    for s in (1, 2, 4, 8):
+        for bk in (64, 128):
+            out.append(dict(backend=4, consumer=0, split_k=s, stages=0, block_n=0, stage_k=bk))
+    return out
 
 
 def candidates(M: int, K: int, N: int = 0):
     out = []
+    big = 2 * N * K > 16e6
+    if M > 16 or big:
+        out += tc_candidates(M, K, N)
     if M > 16:
         # 17..64 tokens: tensor cores only -- cluster split-K with the MMA
         # consumer, or the tensor-core dot-product for large weights
@@ -56,7 +69,6 @@ def candidates(M: int, K: int, N: int = 0):
     if K % 32 == 0:
         for bn in (16, 32, 64):
             out.append(dict(backend=1, block_n=bn, consumer=2, split_k=0, stages=0, stage_k=0))
-    big = 2 * N * K > 16e6
     for cons in (1, 2):
         if cons == 2 and K % 16:
             continue

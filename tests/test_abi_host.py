@@ -161,7 +161,7 @@ def test_forced_options_and_restore():
             plan(8, 256, 7176)
 
 
-@pytest.mark.parametrize("opt,bad", [(sk.SKINNY_OPT_PDL, 2), (sk.SKINNY_OPT_FORCE_BACKEND, 4),
+@pytest.mark.parametrize("opt,bad", [(sk.SKINNY_OPT_PDL, 2), (sk.SKINNY_OPT_FORCE_BACKEND, 5),
                                      (sk.SKINNY_OPT_FORCE_SPLIT_K, 9), (sk.SKINNY_OPT_FORCE_BLOCK_N, 3),
                                      (sk.SKINNY_OPT_FORCE_STAGES, 17), (sk.SKINNY_OPT_WAIT_TIMEOUT_US, -1),
                                      (99, 0)])
@@ -286,16 +286,21 @@ def test_mid_m_takes_a_tensor_core_path():
 
 
 def test_mid_m_unsupported_shapes_are_refused_on_the_host():
-    with pytest.raises(sk.SkinnyError) as e:
-        plan(64, 256, 14336)                       # split-K only (7 MB of W): the X slice does not fit
-    assert e.value.status == sk.SKINNY_ERR_UNSUPPORTED
+    # 7 MB of W: the split-K X slice of 64 tokens does not fit; tcgen05 takes it
+    assert plan(64, 256, 14336)["backend"] == sk.SKINNY_BACKEND_TCGEN05
     p = plan(64, 7168, 14336)                      # 206 MB of W: the tensor-core dot-product, X in chunks
     assert p["backend"] == sk.SKINNY_BACKEND_DOTPROD and p["k_chunk"] < 14336
     with pytest.raises(sk.SkinnyError) as e:
         with sk.options(backend=sk.SKINNY_BACKEND_DOTPROD):
             plan(20, 256, 7184)                    # K % 32 != 0: no tensor-core dot-product
     assert e.value.status == sk.SKINNY_ERR_UNSUPPORTED
-    for kw in (dict(K=7160), dict(K=7176, W=B16 + 8), dict(K=7169)):   # K % 16, W rows not 16-byte aligned
+    # K % 16 != 0 with 16-byte aligned rows: only the tcgen05 backend
+    assert plan(20, 256, 7160)["backend"] == sk.SKINNY_BACKEND_TCGEN05
+    with pytest.raises(sk.SkinnyError) as e:
+        with sk.options(backend=sk.SKINNY_BACKEND_SPLITK):
+            plan(20, 256, 7160)
+    assert e.value.status == sk.SKINNY_ERR_UNSUPPORTED
+    for kw in (dict(K=7176, W=B16 + 8), dict(K=7169)):   # W rows / X rows not 16-byte aligned
         K = kw.pop("K")
         with pytest.raises(sk.SkinnyError) as e:
             plan(20, 256, K, **kw)

@@ -29,10 +29,15 @@ def test_merge_rows_never_crosses_the_8_token_boundary():
     assert [(l[2], l[3]) for l in lines] == [(3, 8), (12, 16)]   # M 9..11 left to the default rule
 
 
-def test_mid_m_candidates_are_splitk_mma_only():
+def test_mid_m_candidates_are_tensor_core_only():
     c = tune.candidates(17, 7168, 256)
-    assert c and all((x["backend"], x["consumer"]) == (2, 2) for x in c)
-    assert tune.candidates(40, 7176, 256) == []      # K % 16 != 0: no path for 17..64 tokens
+    assert c and all((x["backend"], x["consumer"]) in ((2, 2), (4, 0)) for x in c)
+    assert {x["backend"] for x in c} == {2, 4}
+    c = tune.candidates(40, 7176, 256)      # K % 16 != 0: only the tcgen05 backend (any K)
+    assert c and all(x["backend"] == 4 for x in c)
+    # large weights: tcgen05 plans at every M
+    assert any(x["backend"] == 4 for x in tune.candidates(1, 1536, 24576))
+    assert not any(x["backend"] == 4 for x in tune.candidates(1, 7168, 256))
     assert [tune.token_bucket(m) for m in (1, 8, 9, 16, 17, 32, 33, 64)] == [8, 8, 16, 16, 32, 32, 64, 64]
 
 
