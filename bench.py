@@ -49,11 +49,14 @@ WORKLOAD_DESC = {
     "splitk": "split-K regime: M in {5,8,12,16} x (K,N) in {(7168,256),(7168,384),(4096,256)}, 12 calls",
     "projection": "decode projections: M in {1,2,3,8,16} x (N,K) in {(2112,7168),(24576,1536),(7168,14336)}, "
                   "ldy=N+64, 15 calls",
-    "midm": "medium-M decode regime (split-K MMA): M in {17,24,32,40,64} x (K,N) in {(7168,256),(4096,384)}, "
+    "midm": "medium-M decode regime (tensor cores): M in {17,24,32,40,64} x (K,N) in {(7168,256),(4096,384)}, "
             "M in {17,32,64} x (N,K) in {(2112,7168),(24576,1536)}, M in {17,32} x (7168,14336), 18 calls",
 }
-# the device code: DRAM traffic measured by ncu stays valid while these are unchanged
-KERNEL_SOURCES = ["dotprod.cu", "dotmma.cu", "splitk.cu", "stream.cu", "common.cuh", "internal.h"]
+# the sources that define each kernel family (a committed DRAM-traffic figure
+# is used only while they are unchanged)
+KERNEL_SOURCES = {"dotprod": ["dotprod.cu"], "dotmma": ["dotmma.cu"], "splitk": ["splitk.cu"],
+                  "stream": ["stream.cu"], "tmem_gemm": ["tmem_gemm.cu"]}
+COMMON_SOURCES = ["common.cuh", "internal.h"]
 
 
 def parse_args(argv=None):
@@ -118,9 +121,9 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, no measured peak file)"
 
 
-def kernel_sources_digest() -> str:
+def kernel_sources_digest(family: str) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[family] + COMMON_SOURCES:
         with open(os.path.join(ROOT, "latency_skinny_bf16_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -137,7 +140,7 @@ def committed_traffic(family: str, workload: str):
                 if ":" in line:
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
-        if kv.get("kernel_sources_sha256_16") != kernel_sources_digest():
+        if kv.get("kernel_sources_sha256_16") != kernel_sources_digest(family):
             return None
         return float(kv["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -494,8 +497,8 @@ def main(argv=None):
     fam_time, fam_bytes, fam_n = {}, {}, {}
     per_shape = []
     for c, p, us in zip(cases, r["plans"], r["per_launch"]):
-        fam = (("dotmma" if p["consumer"] == 2 else "dotprod") if p["backend"] == 1 else
-               "splitk" if p["backend"] == 2 else "stream")
+        fam = {1: "dotmma" if p["consumer"] == 2 else "dotprod", 2: "splitk", 3: "stream",
+               4: "tmem_gemm"}[p["backend"]]
         fam_time[fam] = fam_time.get(fam, 0.0) + us
         fam_bytes[fam] = fam_bytes.get(fam, 0.0) + c.algorithmic_bytes
         fam_n[fam] = fam_n.get(fam, 0) + 1

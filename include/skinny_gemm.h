@@ -21,15 +21,14 @@
  *
  * Token range.  M = 1..16 is the router tier of the first page; every
  * backend takes it.  M = 17..64 is the medium-M regime that the second page
- * (item 3) hands to a separate fused GEMM before falling back to cuBLAS; here
- * it runs on the tensor cores only (the tokens become 2 or 4 groups of 16 on
- * the MMA's N side): the tensor-core dot-product for weights of 16 MB or more
- * with K % 32 == 0 (any K: X is staged in chunks), else the cluster split-K
- * backend with the mma.sync consumer, which needs a per-CTA X slice
- * (M x K / split_k x 2 bytes, split_k <= 8) of at most 160 KB that fits in
- * shared memory beside the W ring (at 64 tokens K = 7168 runs, K = 14336 does
- * not).  Both need K % 16 == 0 and 16-byte aligned W rows (W and ldw).  Other
- * M > 16 shapes return SKINNY_ERR_UNSUPPORTED.
+ * (item 3) hands to a separate GEMM before falling back to cuBLAS; here it
+ * runs on the tensor cores only: the tcgen05 backend (16-byte aligned X and
+ * W rows, i.e. pointers, ldx and ldw multiples of 8 elements; any K), the
+ * tensor-core dot-product (weights of 16 MB or more, K % 32 == 0, X staged in
+ * chunks), or the cluster split-K backend with the mma.sync consumer
+ * (K % 16 == 0, 16-byte aligned W rows, and a per-CTA X slice of M x K /
+ * split_k x 2 bytes, split_k <= 8, of at most 160 KB beside the W ring).
+ * M > 16 calls that none of them can take return SKINNY_ERR_UNSUPPORTED.
  *
  * bf16 values are passed as their 16-bit patterns (uint16_t) so this header
  * needs no CUDA header.  Streams are passed as `void*` holding a cudaStream_t
@@ -64,8 +63,9 @@ extern "C" {
 typedef enum {
     SKINNY_OK = 0,
     SKINNY_ERR_INVALID_VALUE = 1,   /* negative size, ld too small, NULL with work to do, Y overlaps X or W */
-    SKINNY_ERR_UNSUPPORTED = 2,     /* M > 64; M > 16 on a shape the split-K MMA path cannot
-                                       take; or a forced plan that cannot run this shape */
+    SKINNY_ERR_UNSUPPORTED = 2,     /* M > 64; M > 16 on a shape no tensor-core backend can
+                                       take (see "Token range"); or a forced plan that cannot
+                                       run this shape */
     SKINNY_ERR_MISALIGNED = 3,      /* X or W not 2-byte aligned, Y not 4-byte aligned */
     SKINNY_ERR_LAUNCH = 4,          /* the CUDA launch failed (cudaGetLastError after the launch) */
     SKINNY_ERR_DEVICE_TIMEOUT = 5,  /* a bounded wait inside a kernel gave up (see skinny_get_device_status) */
@@ -297,8 +297,9 @@ SKINNY_API skinny_status_t skinny_router_bf16_topk(const uint16_t *X, int ldx, c
 /* Synchronises `stream`, then reads and clears the current device's status
  * word: *code = 0 if no kernel reported an error since the last read, else a
  * value whose low 8 bits are a skinny_status_t (SKINNY_ERR_DEVICE_TIMEOUT)
- * and whose upper bits say which wait gave up (1 = consumer full-slot wait,
- * 2 = producer empty-slot wait, 3 = drain wait).  Test and diagnostic use. */
+ * and whose upper bits say which wait gave up (1 = consumer / MMA full-slot
+ * wait, 2 = producer empty-slot wait, 3 = drain wait, 4 = X staging wait,
+ * 5 = tcgen05 epilogue wait for the last MMA).  Test and diagnostic use. */
 SKINNY_API skinny_status_t skinny_get_device_status(void *stream, int *code);
 
 /* Static string for a status code (never NULL). */

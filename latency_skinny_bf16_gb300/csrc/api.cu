@@ -369,22 +369,25 @@ bool plan_stream(int M, int N, int K, int vec, bool x_ok, int force_c, int force
     return true;
 }
 
-// Tensor-core (tcgen05) plan: 128 W rows per CTA; clusters of S CTAs along K
-// while the row tiles alone leave SMs idle; the deepest ring that lets the
-// whole grid be resident at once (up to 3 CTAs per SM share its shared memory).
+// Tensor-core (tcgen05) plan: 128 W rows per CTA; two 64-element boxes per
+// ring stage (each W row is then read 256 bytes at a time: measured faster
+// than one box on every projection shape); clusters of S <= 4 CTAs along K
+// while the row tiles alone leave SMs idle (clusters of 8 with a full ring
+// fit only two per GPC); the deepest ring that lets the whole grid be
+// resident at once (up to 3 CTAs per SM share its shared memory).
 bool plan_tc(int M, int N, int K, int vec, bool x_ok, int force_s, int force_stages, int force_bk, int num_sms,
              skinny_plan_t *p) {
     if (vec != 8 || !x_ok || K < 1 || !tc_supported(M)) return false;
     const int tiles = (N + 127) / 128;
     if (tiles < 1 || tiles > 65535) return false;
-    const int bk = force_bk ? force_bk : 64;
+    const int bk = force_bk ? force_bk : (K > 64 ? 128 : 64);
     if (bk < 64 || bk > kTcMaxBK || bk % 64) return false;
     const int nk = (K + bk - 1) / bk;             // ring stages over the whole K
     int S = force_s;
     if (S == 0) {
         S = 1;
         // double while SMs stay idle and every rank still gets a non-empty slice
-        while (S < kSplitMaxCluster && tiles * S < num_sms && 2 * S <= nk &&
+        while (S < 4 && tiles * S < num_sms && 2 * S <= nk &&
                (2 * S - 1) * ((nk + 2 * S - 1) / (2 * S)) < nk)
             S *= 2;
     }
@@ -455,9 +458,10 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
         consumer = SKINNY_CONSUMER_MMA;
         if (fb == SKINNY_BACKEND_DOTPROD && !dotmma_ok) return SKINNY_ERR_UNSUPPORTED;
         if (fb == SKINNY_BACKEND_SPLITK && !mma_ok) return SKINNY_ERR_UNSUPPORTED;
-        backend = fb != SKINNY_BACKEND_AUTO ? fb
-                  : !mma_ok                               ? SKINNY_BACKEND_TCGEN05
-                  : (dotmma_ok && 2.0 * N * K >= 16e6) ? SKINNY_BACKEND_DOTPROD : SKINNY_BACKEND_SPLITK;
+        backend = fb != SKINNY_BACKEND_AUTO                ? fb
+                  : (!mma_ok || (tc_ok && 2.0 * N * K >= 16e6)) ? SKINNY_BACKEND_TCGEN05
+                  : (dotmma_ok && 2.0 * N * K >= 16e6)         ? SKINNY_BACKEND_DOTPROD
+                                                               : SKINNY_BACKEND_SPLITK;
         const TunedEntry *e = (fb == SKINNY_BACKEND_AUTO) ? lookup_tuned(M, N, K) : nullptr;
         if (e && e->backend == SKINNY_BACKEND_TCGEN05 && tc_ok) {
             backend = SKINNY_BACKEND_TCGEN05;
@@ -494,10 +498,10 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
             if (!stages) stages = e->stages;
             if (!stage_k) stage_k = e->stage_k;
             tuned = 1;
-        } else if (stream_ok && M >= 12 && K >= 4096 && 2.0 * N * K >= 16e6) {
-            // default rule, bandwidth-bound weights (>= 16 MB), long K and many tokens:
-            // K-outer streaming (measured ahead of the other backends only there)
-            backend = SKINNY_BACKEND_STREAM;
+        } else if (tc_ok && M >= 9 && 2.0 * N * K >= 16e6) {
+            // default rule, bandwidth-bound weights (>= 16 MB) and 9..16 tokens:
+            // tcgen05 (measured ahead of the other backends there on GB300)
+            backend = SKINNY_BACKEND_TCGEN05;
         } else if (dotmma_ok && M >= 4 && 2.0 * N * K >= 16e6) {
             // default rule, bandwidth-bound weights (>= 16 MB): tensor-core dot-product
             backend = SKINNY_BACKEND_DOTPROD;

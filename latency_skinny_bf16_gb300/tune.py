@@ -42,7 +42,7 @@ def tc_candidates(M: int, K: int, N: int):
     planner's ring depth for the grid."""
     out = []
     for s in (1, 2, 4, 8):
-        for bk in (64, 128):
+        for bk in (64, 128, 256):
             out.append(dict(backend=4, consumer=0, split_k=s, stages=0, block_n=0, stage_k=bk))
     return out
 
@@ -208,6 +208,33 @@ def plannable_range(K, N, m_lo, m_hi, c, num_sms):
     return last
 
 
+TABLE = __import__("os").path.join(__import__("os").path.dirname(__file__), "csrc", "tuning_table.inc")
+
+
+def install(lines, path=TABLE):
+    """Write table lines into the compiled-in table: every existing line of a
+    (K, N) shape that `lines` covers is dropped, the new lines take their
+    place (first match wins in the dispatcher), comments are kept."""
+    def key(line):
+        v = line.split("//", 1)[0].strip().strip("{},").split(",")
+        return (int(v[0]), int(v[1]))
+    shapes = {key(l) for l in lines}
+    with open(path) as f:
+        old = f.read().rstrip("\n").split("\n")
+    out, placed = [], False
+    for l in old:
+        if l.strip().startswith("{") and key(l) in shapes:
+            if not placed:
+                out += lines
+                placed = True
+            continue
+        out.append(l)
+    if not placed:
+        out += lines
+    with open(path, "w") as f:
+        f.write("\n".join(out) + "\n")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--shapes", default=",".join(DEFAULT_SHAPES))
@@ -215,6 +242,8 @@ def main(argv=None):
     ap.add_argument("--m-large", default="1,2,3,4,6,8,9,12,16", help="M values for shapes with W > 16 MB")
     ap.add_argument("--m-mid", default="17,24,32,33,48,64", help="M values 17..64 (split-K MMA), every shape")
     ap.add_argument("--out", default="-")
+    ap.add_argument("--install", action="store_true",
+                    help="replace the lines of the tuned shapes in csrc/tuning_table.inc with the new ones")
     ap.add_argument("--log", default=None)
     a = ap.parse_args(argv)
     def parse_m(spec):
@@ -239,6 +268,8 @@ def main(argv=None):
             if mhi >= mlo:
                 out_lines.append(f"{{{k}, {n}, {mlo}, {mhi}, {be}, {co}, {sp}, {bn}, {st}, {bk}}},  // us/call {us}")
     text = "\n".join(out_lines) + "\n"
+    if a.install:
+        install(out_lines)
     if a.out == "-":
         sys.stdout.write(text)
     else:

@@ -195,14 +195,21 @@ def test_every_tuned_entry_is_a_supported_plan_and_is_used():
         assert 1 <= m_lo <= m_hi <= 64
         # a row never spans two kernels: 1..8 / 9..16 / 17..32 / 33..64 tokens
         assert (m_lo <= 8) == (m_hi <= 8) and (m_lo <= 16) == (m_hi <= 16) and (m_lo <= 32) == (m_hi <= 32)
-        if m_hi > 16:   # tensor cores only: split-K MMA or the tensor-core dot-product
-            assert co == sk.SKINNY_CONSUMER_MMA and be in (sk.SKINNY_BACKEND_SPLITK, sk.SKINNY_BACKEND_DOTPROD)
+        if m_hi > 16:   # tensor cores only: split-K MMA, the tensor-core dot-product or tcgen05
+            assert (co == sk.SKINNY_CONSUMER_MMA and be in (sk.SKINNY_BACKEND_SPLITK, sk.SKINNY_BACKEND_DOTPROD)) \
+                or be == sk.SKINNY_BACKEND_TCGEN05
         for M in range(m_lo, m_hi + 1):
             p = plan(M, N, K)
             assert p["tuned"] == 1, (K, N, M)
             assert p["backend"] == be
             if be == sk.SKINNY_BACKEND_SPLITK:
                 assert (p["consumer"], p["split_k"]) == (co, s)
+                if st:
+                    assert p["stages"] == st
+                if bk:
+                    assert p["stage_k"] == bk
+            elif be == sk.SKINNY_BACKEND_TCGEN05:
+                assert (p["split_k"], p["block_n"], p["consumer"]) == (s, 128, sk.SKINNY_CONSUMER_MMA)
                 if st:
                     assert p["stages"] == st
                 if bk:
@@ -274,13 +281,20 @@ def test_mid_m_takes_a_tensor_core_path():
                 if p["split_k"] > 1:
                     # a single partial-sum buffer: no cluster loops over two tiles
                     assert p["grid_y"] == (N + 15) // 16
+            elif p["backend"] == sk.SKINNY_BACKEND_TCGEN05:
+                assert p["block_n"] == 128 and p["grid_y"] == (N + 127) // 128
+                assert p["split_k"] * p["k_chunk"] >= K and p["k_chunk"] % p["stage_k"] == 0
             else:
                 assert p["backend"] == sk.SKINNY_BACKEND_DOTPROD and p["block_n"] in (16, 32, 64)
                 assert 2 * N * K >= 16e6 and p["k_chunk"] % 32 == 0
-    # the default rule on untuned shapes: split-K below 16 MB of W, the tensor-core dot-product above
+    # the default rule on untuned shapes: split-K below 16 MB of W, tcgen05 above
     assert plan(40, 320, 7168)["backend"] == sk.SKINNY_BACKEND_SPLITK
     p = plan(40, 8192, 4096)
-    assert (p["backend"], p["consumer"]) == (sk.SKINNY_BACKEND_DOTPROD, sk.SKINNY_CONSUMER_MMA)
+    assert (p["backend"], p["consumer"]) == (sk.SKINNY_BACKEND_TCGEN05, sk.SKINNY_CONSUMER_MMA)
+    assert (p["split_k"], p["stage_k"], p["grid_y"]) == (4, 128, 64)   # 64 tiles x 4 >= 152 SMs
+    # 9..16 tokens on large weights take it too; fewer stay on the earlier backends
+    assert plan(12, 8192, 4096)["backend"] == sk.SKINNY_BACKEND_TCGEN05
+    assert plan(8, 8192, 3072)["backend"] == sk.SKINNY_BACKEND_DOTPROD
     with sk.options(backend=sk.SKINNY_BACKEND_DOTPROD):
         assert plan(20, 320, 7168)["consumer"] == sk.SKINNY_CONSUMER_MMA
 
@@ -288,7 +302,9 @@ def test_mid_m_takes_a_tensor_core_path():
 def test_mid_m_unsupported_shapes_are_refused_on_the_host():
     # 7 MB of W: the split-K X slice of 64 tokens does not fit; tcgen05 takes it
     assert plan(64, 256, 14336)["backend"] == sk.SKINNY_BACKEND_TCGEN05
-    p = plan(64, 7168, 14336)                      # 206 MB of W: the tensor-core dot-product, X in chunks
+    assert plan(64, 7168, 14336)["backend"] == sk.SKINNY_BACKEND_TCGEN05   # 206 MB of W, tuned
+    with sk.options(backend=sk.SKINNY_BACKEND_DOTPROD):
+        p = plan(64, 7168, 14336)                  # the tensor-core dot-product stages X in chunks
     assert p["backend"] == sk.SKINNY_BACKEND_DOTPROD and p["k_chunk"] < 14336
     with pytest.raises(sk.SkinnyError) as e:
         with sk.options(backend=sk.SKINNY_BACKEND_DOTPROD):
@@ -331,8 +347,9 @@ def test_mid_m_forced_split_sizes_plan():
 
 
 # ---------------------------------------------------------------- K-outer streaming backend
-def test_stream_default_rule_for_large_weights_with_long_k():
-    p = plan(16, 8192, 8192)                 # 128 MB of W, not tuned
+def test_stream_plan_for_large_weights_with_long_k():
+    with sk.options(backend=sk.SKINNY_BACKEND_STREAM):
+        p = plan(16, 8192, 8192)             # 128 MB of W
     assert (p["backend"], p["consumer"]) == (sk.SKINNY_BACKEND_STREAM, sk.SKINNY_CONSUMER_MMA)
     tiles = 8192 // 16
     assert p["grid_x"] == 152 and p["grid_y"] == 1 and p["split_k"] == 1

@@ -49,3 +49,17 @@ def test_merge_rows_respects_every_token_bucket():
     # a shape whose 33..64 bucket does not run ends its last line at 32
     lines = tune.merge_rows(14336, 7168, rows[:5])
     assert [(l[2], l[3]) for l in lines] == [(12, 16), (17, 32)]
+
+
+def test_install_replaces_the_lines_of_tuned_shapes(tmp_path):
+    path = tmp_path / "table.inc"
+    path.write_text("// header\n{7168, 256, 1, 2, 1, 0, 0, 1, 0, 0},  // a\n"
+                    "{1536, 24576, 1, 8, 1, 2, 0, 64, 0, 0},  // b\n{1536, 24576, 9, 16, 2, 2, 1, 0, 0, 0},  // c\n"
+                    "{7168, 384, 1, 1, 1, 0, 0, 1, 0, 0},  // d\n")
+    new = ["{1536, 24576, 1, 16, 4, 0, 1, 0, 0, 128},  // e"]
+    tune.install(new, str(path))
+    lines = path.read_text().strip().split("\n")
+    assert lines == ["// header", "{7168, 256, 1, 2, 1, 0, 0, 1, 0, 0},  // a", new[0],
+                     "{7168, 384, 1, 1, 1, 0, 0, 1, 0, 0},  // d"]
+    tune.install(["{2880, 128, 1, 3, 1, 0, 0, 2, 0, 0},  // f"], str(path))   # a new shape goes at the end
+    assert path.read_text().strip().split("\n")[-1].endswith("// f")
