@@ -126,8 +126,9 @@ typedef enum {
                                         (default: env SKINNY_LOG) */
     SKINNY_OPT_FORCE_CLUSTERS = 9,   /* split-K: 0 = dispatcher, else the number of (persistent)
                                         clusters, each looping over row tiles (tests / tuning only) */
-    SKINNY_OPT_FORCE_STAGE_K = 10    /* split-K: 0 = dispatcher, else K elements per ring stage
-                                        (64..2048, multiple of 64; tests / tuning only) */
+    SKINNY_OPT_FORCE_STAGE_K = 10    /* split-K, streaming, tcgen05: 0 = dispatcher, else K elements
+                                        per ring stage (multiple of 64; split-K and streaming
+                                        64..2048, tcgen05 64..256; tests / tuning only) */
 } skinny_option_t;
 
 /*
