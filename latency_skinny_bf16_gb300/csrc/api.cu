@@ -369,16 +369,19 @@ bool plan_stream(int M, int N, int K, int vec, bool x_ok, int force_c, int force
     return true;
 }
 
-// Tensor-core (tcgen05) plan: 128 W rows per CTA; two 64-element boxes per
+// Tensor-core (tcgen05) plan: 128 W rows per CTA (64 when forced or tuned:
+// twice the CTAs, spread more evenly over the SMs); two 64-element boxes per
 // ring stage (each W row is then read 256 bytes at a time: measured faster
 // than one box on every projection shape); clusters of S <= 4 CTAs along K
 // while the row tiles alone leave SMs idle (clusters of 8 with a full ring
 // fit only two per GPC); the deepest ring that lets the whole grid be
 // resident at once (up to 3 CTAs per SM share its shared memory).
-bool plan_tc(int M, int N, int K, int vec, bool x_ok, int force_s, int force_stages, int force_bk, int num_sms,
-             skinny_plan_t *p) {
+bool plan_tc(int M, int N, int K, int vec, bool x_ok, int force_bn, int force_s, int force_stages, int force_bk,
+             int num_sms, skinny_plan_t *p) {
     if (vec != 8 || !x_ok || K < 1 || !tc_supported(M)) return false;
-    const int tiles = (N + 127) / 128;
+    const int bn = force_bn ? force_bn : 128;    // W rows per CTA: the MMA's M (128 or 64)
+    if (bn != 128 && bn != 64) return false;
+    const int tiles = (N + bn - 1) / bn;
     if (tiles < 1 || tiles > 65535) return false;
     const int bk = force_bk ? force_bk : (K > 64 ? 128 : 64);
     if (bk < 64 || bk > kTcMaxBK || bk % 64) return false;
@@ -391,7 +394,7 @@ bool plan_tc(int M, int N, int K, int vec, bool x_ok, int force_s, int force_sta
                (2 * S - 1) * ((nk + 2 * S - 1) / (2 * S)) < nk)
             S *= 2;
     }
-    if (S < 1 || S > kSplitMaxCluster || 128 % S != 0) return false;
+    if (S < 1 || S > kSplitMaxCluster || bn % S != 0) return false;
     const int per_rank = (nk + S - 1) / S;        // ring stages per cluster rank (a forced S may leave
                                                   // the last ranks empty: they add zeros)
     int stages = force_stages;
@@ -402,19 +405,19 @@ bool plan_tc(int M, int N, int K, int vec, bool x_ok, int force_s, int force_sta
         int budget = (228 * 1024) / per_sm - 2048;
         if (budget > kMaxDynSmem) budget = kMaxDynSmem;
         stages = kSplitMaxStages;
-        while (stages > 1 && tc_smem_bytes(M, bk, stages, S) > budget) --stages;
+        while (stages > 1 && tc_smem_bytes(M, bn, bk, stages, S) > budget) --stages;
         // no deeper than the slice, but deep enough to receive the partials
         int least = 1;
-        while (least < stages && tc_smem_bytes(M, bk, least, S) > kMaxDynSmem) ++least;
+        while (least < stages && tc_smem_bytes(M, bn, bk, least, S) > kMaxDynSmem) ++least;
         if (stages > per_rank) stages = per_rank > least ? per_rank : least;
     }
     if (stages < 1 || stages > kSplitMaxStages) return false;
-    const int smem = tc_smem_bytes(M, bk, stages, S);
+    const int smem = tc_smem_bytes(M, bn, bk, stages, S);
     if (smem > kMaxDynSmem) return false;
     p->backend = SKINNY_BACKEND_TCGEN05;
     p->consumer = SKINNY_CONSUMER_MMA;
     p->vec_elems = 8;
-    p->block_n = 128;
+    p->block_n = bn;
     p->split_k = S;
     p->stages = stages;
     p->stage_k = bk;
@@ -465,6 +468,7 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
         const TunedEntry *e = (fb == SKINNY_BACKEND_AUTO) ? lookup_tuned(M, N, K) : nullptr;
         if (e && e->backend == SKINNY_BACKEND_TCGEN05 && tc_ok) {
             backend = SKINNY_BACKEND_TCGEN05;
+            if (!bn) bn = e->block_n;
             if (!split) split = e->split_k;
             if (!stages) stages = e->stages;
             if (!stage_k) stage_k = e->stage_k;
@@ -540,7 +544,7 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
         }
         if (!ok && fb == SKINNY_BACKEND_AUTO && mid_m && tc_ok) {
             // 17..64 tokens whose X slice does not fit beside the split-K ring
-            ok = plan_tc(M, N, K, vec, x_ok, 0, 0, 0, num_sms, p);
+            ok = plan_tc(M, N, K, vec, x_ok, 0, 0, 0, 0, num_sms, p);
             tuned = 0;
         }
     } else if (backend == SKINNY_BACKEND_STREAM) {
@@ -554,9 +558,9 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
             tuned = 0;
         }
     } else if (backend == SKINNY_BACKEND_TCGEN05) {
-        if ((fc != SKINNY_CONSUMER_AUTO && fc != SKINNY_CONSUMER_MMA) || (bn != 0 && bn != 128))
+        if ((fc != SKINNY_CONSUMER_AUTO && fc != SKINNY_CONSUMER_MMA) || (bn != 0 && bn != 128 && bn != 64))
             return SKINNY_ERR_UNSUPPORTED;
-        ok = plan_tc(M, N, K, vec, x_ok, split, stages, stage_k, num_sms, p);
+        ok = plan_tc(M, N, K, vec, x_ok, bn, split, stages, stage_k, num_sms, p);
         if (!ok && fb == SKINNY_BACKEND_AUTO) {
             // a tuned tensor-core plan these pointers / strides cannot use: the
             // default rule of the token range

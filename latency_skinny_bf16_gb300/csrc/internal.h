@@ -68,15 +68,15 @@ bool stream_supported(int M);
 cudaError_t stream_prepare();
 cudaError_t launch_stream(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
 
-// ---- fifth-generation tensor-core backend (tmem_gemm.cu): 128 W rows per CTA
-// (tcgen05.mma M = 128), tokens on the MMA's N side (16 / 32 / 64), W and X
-// boxes by tensor-map TMA, optional cluster split-K along K
+// ---- fifth-generation tensor-core backend (tmem_gemm.cu): block_n = 128 or 64
+// W rows per CTA (tcgen05.mma M), tokens on the MMA's N side (16 / 32 / 64),
+// W and X boxes by tensor-map TMA, optional cluster split-K along K
 constexpr int kTcThreads = 128;
 constexpr int kTcMaxBK = 256;          // K elements per ring stage: 64..256, multiple of 64
 constexpr int kTcMinSmem = 30 * 1024;  // <= 7 CTAs per SM: their tensor memory always fits
 int tc_tokens(int M);                  // MMA N of the instantiation: 16, 32 or 64
 bool tc_supported(int M);
-int tc_smem_bytes(int M, int stage_k, int stages, int split_k);
+int tc_smem_bytes(int M, int block_n, int stage_k, int stages, int split_k);
 cudaError_t tc_prepare();
 cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
 

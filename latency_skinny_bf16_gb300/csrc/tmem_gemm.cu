@@ -8,28 +8,30 @@
 // router (GEMM)", item 2 (K split over the CTAs of a thread-block cluster,
 // partial sums reduced through distributed shared memory).
 //
-// GB300 form.  A CTA owns 128 rows of W (the MMA's M side; rows past N read
-// as zeros) and, in a cluster of S CTAs along K, the K slice of its rank
-// (KS elements, a whole number of ring stages).  The tokens are the MMA's N
-// side (MT = 16, 32 or 64; rows past M read as zeros).
+// GB300 form.  A CTA owns TM = 128 or 64 rows of W (the MMA's M side; rows
+// past N read as zeros) and, in a cluster of S CTAs along K, the K slice of
+// its rank (KS elements, a whole number of ring stages).  The tokens are the
+// MMA's N side (MT = 16, 32 or 64; rows past M read as zeros).  64-row tiles
+// double the CTA count, which spreads a weight more evenly over the SMs.
 //   * Thread 0 drives the TMA engine: per ring stage it loads stage_k / 64
-//     boxes of W [128 rows x 64 K] and of X [MT rows x 64 K] through 2-D
+//     boxes of W [TM rows x 64 K] and of X [MT rows x 64 K] through 2-D
 //     tensor maps with the 128-byte swizzle (columns past K arrive as zeros),
 //     all completing on the stage's "full" mbarrier.  W is a weight, so with
 //     PDL the W boxes of the first ring pass are issued before
 //     griddepcontrol.wait; X boxes only after it.
-//   * Thread 32 issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32; M = 128,
+//   * Thread 32 issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32; M = TM,
 //     N = MT, K = 16 each; operands from shared-memory descriptors, K-major,
-//     128-byte swizzle) into an fp32 accumulator of 128 lanes x MT columns in
-//     tensor memory, frees each stage by tcgen05.commit on its "empty"
-//     mbarrier, and signals "done" with a last commit.
+//     128-byte swizzle) into an fp32 accumulator of MT columns in tensor
+//     memory (M = 128: row r in lane r; M = 64: row 16w + i in lane 32w + i,
+//     i < 16), frees each stage by tcgen05.commit on its "empty" mbarrier,
+//     and signals "done" with a last commit.
 //   * Warp 2 allocates the tensor-memory columns and frees them at the end.
-//   * Epilogue, all four warps: warp w reads lanes 32w..32w+31 (W rows) with
+//   * Epilogue, all four warps: warp w reads lanes 32w..32w+31 with
 //     tcgen05.ld 32x32b: a thread holds one output column n, its registers
-//     the tokens.  S = 1: Y is written directly (per token, a warp's 32
-//     columns are one 128-byte store).  S > 1: after one cluster barrier
+//     the tokens.  S = 1: Y is written directly (per token, a warp's columns
+//     are one contiguous store).  S > 1: after one cluster barrier
 //     (every CTA's MMAs are complete, so every ring is free) each CTA sends
-//     the partials of rows owned by rank q = row / (128 / S) into q's ring
+//     the partials of rows owned by rank q = row / (TM / S) into q's ring
 //     (slot = sending rank) with st.shared::cluster; after a second barrier
 //     each owner adds slots 0..S-1 in that order and writes Y.  The MMA order
 //     and the reduction order are fixed, so a plan's result is bit-identical
@@ -47,12 +49,13 @@
 namespace skinny {
 namespace {
 
-constexpr int kWBox = 128 * 128;                 // W box: 128 rows x 64 bf16 (128 B) = 16 KB
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 enum : int { kWaitDone = 5 };
 
+// a box is `rows` x 64 bf16 (128 bytes per row)
+__host__ __device__ constexpr int w_box_bytes(int TM) { return TM * 128; }
 __host__ __device__ constexpr int x_box_bytes(int MT) { return MT * 128; }
-__host__ __device__ constexpr int stage_bytes(int MT, int kb) { return kb * (kWBox + x_box_bytes(MT)); }
+__host__ __device__ constexpr int stage_bytes(int TM, int MT, int kb) { return kb * (w_box_bytes(TM) + x_box_bytes(MT)); }
 __host__ __device__ constexpr int tmem_cols(int MT) { return MT <= 32 ? 32 : MT; }   // a power of two >= 32
 
 // ------------------------------------------------------------------ TMA (tensor maps)
@@ -89,10 +92,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 // Instruction descriptor, kind::f16: fp32 D, bf16 A and B, both K-major,
-// N = MT (bits 17-22, N / 8), M = 128 (bits 24-28, M / 16).
-template <int MT>
-__host__ __device__ constexpr uint32_t idesc_bf16_m128() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(MT >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+// N = MT (bits 17-22, N / 8), M = TM (bits 24-28, M / 16).
+template <int MT, int TM>
+__host__ __device__ constexpr uint32_t idesc_bf16() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(MT >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
 }
 // D[tmem] (+)= A[smem] . B[smem]^T; accumulate = 0 overwrites D.
 __device__ __forceinline__ void umma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
@@ -137,11 +140,11 @@ struct TcParams {
 
 // Shared memory from the 1024-byte aligned base: the ring, then full[stages],
 // empty[stages], done (8 bytes each), then the tensor-memory address.
-__host__ __device__ inline int tc_layout_bytes(int MT, int kb, int stages) {
-    return stages * stage_bytes(MT, kb) + 8 * (2 * stages + 1) + 8;
+__host__ __device__ inline int tc_layout_bytes(int TM, int MT, int kb, int stages) {
+    return stages * stage_bytes(TM, MT, kb) + 8 * (2 * stages + 1) + 8;
 }
 
-template <int MT>
+template <int MT, int TM>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tmem_gemm_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx, const TcParams p)
 {
@@ -149,7 +152,8 @@ tmem_gemm_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant_
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;            // 128-byte swizzle atoms: 1024-byte aligned
     uint8_t *smem = smem_raw + (base - raw);
-    const int sbytes = stage_bytes(MT, p.kb);
+    constexpr int kWBox = w_box_bytes(TM);
+    const int sbytes = stage_bytes(TM, MT, p.kb);
     const int stages = p.stages;
     const uint32_t bars = base + stages * sbytes;
     auto full = [&](int s) { return bars + 8u * s; };
@@ -160,7 +164,7 @@ tmem_gemm_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = gridDim.x;
     const int rank = (S > 1) ? (int)cluster_ctarank() : 0;
-    const int n0 = blockIdx.y * 128;
+    const int n0 = blockIdx.y * TM;
     const int kbeg = rank * p.KS;
     const int kend = min(p.K, kbeg + p.KS);
     const int sk = 64 * p.kb;
@@ -222,7 +226,7 @@ tmem_gemm_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant_
         // ---- MMA issuer
         griddep_wait();
         griddep_launch_dependents();
-        constexpr uint32_t idesc = idesc_bf16_m128<MT>();
+        constexpr uint32_t idesc = idesc_bf16<MT, TM>();
         for (int i = 0; i < nsteps; ++i) {
             const int s = i % stages;
             if (!mbar_wait_bounded(full(s), (uint32_t)((i / stages) & 1), p.budget_ns)) {
@@ -268,23 +272,27 @@ tmem_gemm_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant_
 #pragma unroll
         for (int j = 0; j < MT; ++j) v[j] = 0.f;   // an empty K slice adds nothing
     }
-    const int row = 32 * warp + lane;
+    // accumulator row of this thread (M = 64: lanes 16..31 of each warp hold none)
+    const int row = (TM == 128) ? 32 * warp + lane : 16 * warp + lane;
+    const bool has_row = (TM == 128) || lane < 16;
     if (S == 1) {
         const int n = n0 + row;
-        if (n < p.N) {
+        if (has_row && n < p.N) {
 #pragma unroll
             for (int m = 0; m < MT; ++m)
                 if (m < M) store_y(p.Y, p.out_bf16, m * p.ldy + n, v[m]);
         }
     } else {
-        const int R = 128 / S;                   // rows owned by each rank
+        const int R = TM / S;                    // rows owned by each rank
         cluster_arrive_release();                // every CTA of the cluster is past its MMAs
         cluster_wait_acquire();
-        const int q = row / R, rl = row - q * R;
-        const uint32_t dst = mapa_shared(base, (uint32_t)q);
+        if (has_row) {
+            const int q = row / R, rl = row - q * R;
+            const uint32_t dst = mapa_shared(base, (uint32_t)q);
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
-            if (m < M) st_shared_cluster_f32(dst + 4u * (uint32_t)((rank * M + m) * R + rl), v[m]);
+            for (int m = 0; m < MT; ++m)
+                if (m < M) st_shared_cluster_f32(dst + 4u * (uint32_t)((rank * M + m) * R + rl), v[m]);
+        }
         cluster_arrive_release();                // every partial is in its owner's slots
         cluster_wait_acquire();
         const float *slots = reinterpret_cast<const float *>(smem);
@@ -306,7 +314,9 @@ tmem_gemm_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant_
 }
 
 using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const TcParams);
-const TcKernel kTc[3] = {&tmem_gemm_kernel<16>, &tmem_gemm_kernel<32>, &tmem_gemm_kernel<64>};
+const TcKernel kTc[3][2] = {{&tmem_gemm_kernel<16, 128>, &tmem_gemm_kernel<16, 64>},
+                            {&tmem_gemm_kernel<32, 128>, &tmem_gemm_kernel<32, 64>},
+                            {&tmem_gemm_kernel<64, 128>, &tmem_gemm_kernel<64, 64>}};
 
 int tc_index(int M) { return M <= 16 ? 0 : M <= 32 ? 1 : 2; }
 
@@ -345,12 +355,12 @@ int tc_tokens(int M) { return 16 << tc_index(M); }
 
 bool tc_supported(int M) { return M >= 1 && M <= SKINNY_MAX_M; }
 
-int tc_smem_bytes(int M, int stage_k, int stages, int split_k) {
+int tc_smem_bytes(int M, int block_n, int stage_k, int stages, int split_k) {
     const int MT = tc_tokens(M);
     const int kb = stage_k / 64;
-    int bytes = tc_layout_bytes(MT, kb, stages);
-    // S > 1: the ring also receives the partials (S slots of M x 128 / S fp32)
-    if (split_k > 1 && stages * stage_bytes(MT, kb) < 128 * M * 4) return 1 << 30;
+    int bytes = tc_layout_bytes(block_n, MT, kb, stages);
+    // S > 1: the ring also receives the partials (S slots of M x block_n / S fp32)
+    if (split_k > 1 && stages * stage_bytes(block_n, MT, kb) < block_n * M * 4) return 1 << 30;
     // at most 7 resident CTAs per SM, so their tensor memory (<= 64 columns
     // each) always fits in the SM's 512 columns and an allocation never waits
     if (bytes < kTcMinSmem - 1024) bytes = kTcMinSmem - 1024;
@@ -358,27 +368,29 @@ int tc_smem_bytes(int M, int stage_k, int stages, int split_k) {
 }
 
 cudaError_t tc_prepare() {
-    for (int i = 0; i < 3; ++i) {
-        cudaError_t e = set_max_dyn_smem(kTc[i]);
-        if (e != cudaSuccess) return e;
-    }
+    for (int i = 0; i < 3; ++i)
+        for (int j = 0; j < 2; ++j) {
+            cudaError_t e = set_max_dyn_smem(kTc[i][j]);
+            if (e != cudaSuccess) return e;
+        }
     return cudaSuccess;
 }
 
 cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCtx &c) {
     const int S = pl.split_k;
-    if (!tc_supported(a.M) || pl.block_n != 128 || S < 1 || S > kSplitMaxCluster || (128 % S) != 0 ||
+    const int TM = pl.block_n;
+    if (!tc_supported(a.M) || (TM != 128 && TM != 64) || S < 1 || S > kSplitMaxCluster || (TM % S) != 0 ||
         pl.stage_k < 64 || pl.stage_k > kTcMaxBK || pl.stage_k % 64 || pl.stages < 1 ||
         pl.stages > kSplitMaxStages || pl.k_chunk % pl.stage_k || (int64_t)pl.k_chunk * S < a.K ||
-        pl.grid_x != S || pl.grid_y != (a.N + 127) / 128 || pl.smem_bytes < kTcMinSmem ||
-        pl.smem_bytes < tc_smem_bytes(a.M, pl.stage_k, pl.stages, S))
+        pl.grid_x != S || pl.grid_y != (a.N + TM - 1) / TM || pl.smem_bytes < kTcMinSmem ||
+        pl.smem_bytes < tc_smem_bytes(a.M, TM, pl.stage_k, pl.stages, S))
         return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(a.X) & 15) || (a.ldx & 7) || (reinterpret_cast<uintptr_t>(a.W) & 15) ||
         (a.ldw & 7))
         return cudaErrorInvalidValue;
     const int idx = tc_index(a.M);
     CUtensorMap tmw, tmx;
-    if (!encode_bf16_2d(&tmw, a.W, a.K, a.N, a.ldw, 128) || !encode_bf16_2d(&tmx, a.X, a.K, a.M, a.ldx, 16 << idx))
+    if (!encode_bf16_2d(&tmw, a.W, a.K, a.N, a.ldw, TM) || !encode_bf16_2d(&tmx, a.X, a.K, a.M, a.ldx, 16 << idx))
         return cudaErrorInvalidValue;
     TcParams p;
     p.Y = a.Y;
@@ -412,7 +424,7 @@ cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCt
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, kTc[idx], tmw, tmx, p);
+    return cudaLaunchKernelEx(&cfg, kTc[idx][TM == 128 ? 0 : 1], tmw, tmx, p);
 }
 
 }  // namespace skinny

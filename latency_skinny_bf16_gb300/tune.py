@@ -38,12 +38,13 @@ def token_bucket(M: int) -> int:
 
 
 def tc_candidates(M: int, K: int, N: int):
-    """tcgen05 plans: cluster sizes along K, 1 or 2 boxes per ring stage, the
-    planner's ring depth for the grid."""
+    """tcgen05 plans: 128- or 64-row tiles, cluster sizes along K, 2 or 4 boxes
+    per ring stage (1 never won on GB300), the planner's ring depth."""
     out = []
-    for s in (1, 2, 4, 8):
-        for bk in (64, 128, 256):
-            out.append(dict(backend=4, consumer=0, split_k=s, stages=0, block_n=0, stage_k=bk))
+    for bn in (0, 64):                    # 0: the planner's 128-row tile
+        for s in (1, 2, 4, 8):
+            for bk in (128, 256):
+                out.append(dict(backend=4, consumer=0, split_k=s, stages=0, block_n=bn, stage_k=bk))
     return out
 
 

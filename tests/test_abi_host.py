@@ -209,7 +209,7 @@ def test_every_tuned_entry_is_a_supported_plan_and_is_used():
                 if bk:
                     assert p["stage_k"] == bk
             elif be == sk.SKINNY_BACKEND_TCGEN05:
-                assert (p["split_k"], p["block_n"], p["consumer"]) == (s, 128, sk.SKINNY_CONSUMER_MMA)
+                assert (p["split_k"], p["block_n"], p["consumer"]) == (s, bn or 128, sk.SKINNY_CONSUMER_MMA)
                 if st:
                     assert p["stages"] == st
                 if bk:
@@ -282,7 +282,7 @@ def test_mid_m_takes_a_tensor_core_path():
                     # a single partial-sum buffer: no cluster loops over two tiles
                     assert p["grid_y"] == (N + 15) // 16
             elif p["backend"] == sk.SKINNY_BACKEND_TCGEN05:
-                assert p["block_n"] == 128 and p["grid_y"] == (N + 127) // 128
+                assert p["block_n"] in (64, 128) and p["grid_y"] == -(-N // p["block_n"])
                 assert p["split_k"] * p["k_chunk"] >= K and p["k_chunk"] % p["stage_k"] == 0
             else:
                 assert p["backend"] == sk.SKINNY_BACKEND_DOTPROD and p["block_n"] in (16, 32, 64)
@@ -508,3 +508,15 @@ def norm_call(X=A16, ldx=64, G=D16, eps=1e-6, XN=E16, ldxn=64, W=B16, ldw=64, Y=
 ])
 def test_rmsnorm_gemm_argument_errors_are_host_side(kw, expect):
     assert norm_call(**kw) == expect
+
+
+def test_tcgen05_tile_heights():
+    for bn in (64, 128):
+        with sk.options(backend=sk.SKINNY_BACKEND_TCGEN05, block_n=bn):
+            for M, N, K in ((1, 24576, 1536), (40, 2112, 7168), (64, 100, 520)):
+                p = plan(M, N, K)
+                assert (p["backend"], p["block_n"], p["grid_y"]) == (sk.SKINNY_BACKEND_TCGEN05, bn, -(-N // bn))
+                assert p["split_k"] * p["k_chunk"] >= K and p["smem_bytes"] <= 227 * 1024
+    with sk.options(backend=sk.SKINNY_BACKEND_TCGEN05, block_n=32):
+        with pytest.raises(sk.SkinnyError):
+            plan(8, 24576, 1536)

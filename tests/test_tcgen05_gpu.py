@@ -51,14 +51,15 @@ CASES = [si.Case(f"tc_M{M}_N{N}_K{K}", M=M, N=N, K=K, seed=5000 + 37 * i + M, w_
          for i, (N, K) in enumerate(SHAPES) for M in TOKENS]
 
 
+@pytest.mark.parametrize("bn", [128, 64])
 @pytest.mark.parametrize("case", CASES, ids=_ids(CASES))
-def test_tc_default_plan(case):
+def test_tc_default_plan(case, bn):
     X, W = si.make_inputs(case)
-    with sk.options(**TC):
+    with sk.options(block_n=bn, **TC):
         b = Buffers(case, X, W)
         p = b.plan()
-        assert (p["backend"], p["block_n"]) == (sk.SKINNY_BACKEND_TCGEN05, 128)
-        assert p["grid_y"] == (case.N + 127) // 128 and p["grid_x"] == p["split_k"]
+        assert (p["backend"], p["block_n"]) == (sk.SKINNY_BACKEND_TCGEN05, bn)
+        assert p["grid_y"] == -(-case.N // bn) and p["grid_x"] == p["split_k"]
         yref, A = reference(case, X, W)
         _run_twice(b, yref, A, case.name)
     assert sk.skinny_get_device_status() == 0
@@ -76,10 +77,11 @@ VARIANT_CASES = [
 
 def _variants():
     out = []
-    for s in (1, 2, 4, 8):
-        for stages in (1, 2, 3, 6):
-            for stage_k in (64, 128, 256):
-                out.append(dict(split_k=s, stages=stages, stage_k=stage_k, **TC))
+    for bn in (128, 64):
+        for s in (1, 2, 4, 8):
+            for stages in (1, 2, 3, 6):
+                for stage_k in (64, 128, 256):
+                    out.append(dict(block_n=bn, split_k=s, stages=stages, stage_k=stage_k, **TC))
     return out
 
 
@@ -100,7 +102,8 @@ def test_tc_every_variant(case):
                 continue
             assert st == sk.SKINNY_OK, (v, sk.skinny_status_string(st))
             p = b.plan()
-            assert (p["split_k"], p["stages"], p["stage_k"]) == (v["split_k"], v["stages"], v["stage_k"])
+            assert (p["block_n"], p["split_k"], p["stages"], p["stage_k"]) == \
+                (v["block_n"], v["split_k"], v["stages"], v["stage_k"])
             check_parity(b.y_mat(), yref, A, f"{case.name} {v}")
             assert b.canary_ok(), v
             assert sk.skinny_get_device_status() == 0, v
@@ -133,14 +136,15 @@ def test_tc_needs_16_byte_rows(ldx_pad, x_off, w_off):
     assert b.plan()["backend"] != sk.SKINNY_BACKEND_TCGEN05
 
 
+@pytest.mark.parametrize("bn", [128, 64])
 @pytest.mark.parametrize("M", [1, 16, 64])
 @pytest.mark.parametrize("N,K", [(24576, 1536), (7168, 14336), (2112, 7168)])
-def test_tc_projection_shapes_sampled(M, N, K):
+def test_tc_projection_shapes_sampled(M, N, K, bn):
     """The decode projection weights at full size, in the default tcgen05 plan
-    for them; 512 output columns checked against the oracle."""
+    for them at each tile height; 512 output columns checked against the oracle."""
     case = si.Case(f"tc_proj_M{M}_{N}x{K}", M=M, N=N, K=K, seed=5400 + M + N % 97, w_dist="uniform_isqrtk")
     X, W = si.make_inputs(case)
-    with sk.options(**TC):
+    with sk.options(block_n=bn, **TC):
         b = Buffers(case, X, W)
         first = None
         for _ in range(2):
@@ -164,8 +168,8 @@ def test_tc_rows_do_not_depend_on_other_tokens():
     big = si.Case("tc_rows64", M=64, N=384, K=4096, seed=5500)
     X, W = si.make_inputs(big)
     small = si.Case("tc_rows40", M=40, N=384, K=4096, seed=5500)
-    for s in (1, 4):
-        with sk.options(split_k=s, stages=4, **TC):
+    for s, bn in ((1, 128), (4, 128), (2, 64)):
+        with sk.options(split_k=s, stages=4, block_n=bn, **TC):
             b64 = Buffers(big, X, W)
             b40 = Buffers(small, X[:40].copy(), W)
             assert b64.run() == sk.SKINNY_OK and b40.run() == sk.SKINNY_OK
@@ -220,21 +224,21 @@ def test_tc_graph_capture_chain(pdl):
     assert sk.skinny_get_device_status() == 0
 
 
-@pytest.mark.parametrize("split_k", [1, 4])
-def test_tc_timeout_path_reports_and_recovers(split_k):
+@pytest.mark.parametrize("split_k,bn", [(1, 128), (4, 128), (2, 64)])
+def test_tc_timeout_path_reports_and_recovers(split_k, bn):
     """A wait budget of 0 makes every bounded wait give up at once: the kernel
     records the error, drains the copies in flight, takes part in both cluster
     barriers, frees its tensor memory and exits; the next call is exact."""
     case = si.Case(f"tc_to{split_k}", M=16, N=256, K=8192, seed=5800 + split_k)
     X, W = si.make_inputs(case)
     assert sk.skinny_get_device_status() == 0
-    with sk.options(wait_timeout_us=0, split_k=split_k, stages=4, **TC):
+    with sk.options(wait_timeout_us=0, split_k=split_k, stages=4, block_n=bn, **TC):
         b = Buffers(case, X, W)
         assert b.run() == sk.SKINNY_OK
         code = sk.skinny_get_device_status()
     assert code & 0xFF == sk.SKINNY_ERR_DEVICE_TIMEOUT
     assert (code >> 8) in (1, 2, 5)
     assert sk.skinny_get_device_status() == 0
-    with sk.options(split_k=split_k, stages=4, **TC):
+    with sk.options(split_k=split_k, stages=4, block_n=bn, **TC):
         run_and_check(case)
     assert sk.skinny_get_device_status() == 0
