@@ -51,7 +51,7 @@ def tc_candidates(M: int, K: int, N: int):
 def candidates(M: int, K: int, N: int = 0):
     out = []
     big = 2 * N * K > 16e6
-    if M > 16 or big:
+    if M > 4 or big:
         out += tc_candidates(M, K, N)
     if M > 16:
         # 17..64 tokens: tensor cores only -- cluster split-K with the MMA

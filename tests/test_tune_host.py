@@ -6,7 +6,8 @@ tune = pytest.importorskip("latency_skinny_bf16_gb300.tune")
 
 def test_candidates_cover_both_backends_and_respect_k16():
     c = tune.candidates(8, 7168)
-    assert {x["backend"] for x in c} == {1, 2}
+    assert {x["backend"] for x in c} == {1, 2, 4}
+    assert {x["backend"] for x in tune.candidates(3, 7168)} == {1, 2}
     assert any(x["backend"] == 2 and x["consumer"] == 2 for x in c)
     c = tune.candidates(8, 7176)     # K % 16 != 0: no MMA consumer
     assert not any(x["backend"] == 2 and x["consumer"] == 2 for x in c)
@@ -37,7 +38,8 @@ def test_mid_m_candidates_are_tensor_core_only():
     assert c and all(x["backend"] == 4 for x in c)
     # large weights: tcgen05 plans at every M
     assert any(x["backend"] == 4 for x in tune.candidates(1, 1536, 24576))
-    assert not any(x["backend"] == 4 for x in tune.candidates(1, 7168, 256))
+    assert not any(x["backend"] == 4 for x in tune.candidates(4, 7168, 256))   # tiny M on small weights
+    assert any(x["backend"] == 4 for x in tune.candidates(12, 7168, 256))
     assert [tune.token_bucket(m) for m in (1, 8, 9, 16, 17, 32, 33, 64)] == [8, 8, 16, 16, 32, 32, 64, 64]
 
 
