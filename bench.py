@@ -361,6 +361,40 @@ def run_native(args):
     sk.skinny_set_option(sk.SKINNY_OPT_PDL, args.pdl)
     launches += 0  # the per-launch pass is outside the timed region
 
+    # ---- PDL chain: one CUDA graph of 64 back-to-back calls M=4, K=7168,
+    # N=256 (same X and W, so L2-warm; a Y per call), total us per replay with
+    # programmatic dependent launch on and off (outside the timed region)
+    chain = None
+    if not args.profile_mode:
+        cc = si.pdl_chain_case()
+        Xc, Wc = si.make_inputs(cc)
+        xc = torch.from_numpy(Xc.reshape(-1).view(np.int16).copy()).cuda()
+        wc = torch.from_numpy(Wc.reshape(-1).view(np.int16).copy()).cuda()
+        ycs = [torch.zeros(cc.M * cc.N, dtype=torch.float32, device="cuda") for _ in range(64)]
+        chain = {"calls": 64, "M": cc.M, "N": cc.N, "K": cc.K,
+                 "method": "one CUDA graph of the 64 calls, mean over 20 replays after 2 untimed ones"}
+        for pdl in (1, 0):
+            sk.skinny_set_option(sk.SKINNY_OPT_PDL, pdl)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for y in ycs:
+                    st = sk.skinny_gemm_bf16(xc.data_ptr(), cc.K, wc.data_ptr(), cc.K, y.data_ptr(), cc.N,
+                                             cc.M, cc.N, cc.K, sh)
+                    if st != sk.SKINNY_OK:
+                        raise sk.SkinnyError(st, cc.name)
+            with torch.cuda.stream(stream):
+                g.replay()
+                g.replay()
+                c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                c0.record(stream)
+                for _ in range(20):
+                    g.replay()
+                c1.record(stream)
+            torch.cuda.synchronize()
+            chain["us_total_pdl_on" if pdl else "us_total_pdl_off"] = round(c0.elapsed_time(c1) * 1e3 / 20, 2)
+            del g
+        sk.skinny_set_option(sk.SKINNY_OPT_PDL, args.pdl)
+
     # ---- e2e: host -> device X, the calls, device -> host Y, per step, through the C ABI
     h2d = sum(2 * c.M * c.K for c in cases)
     d2h = sum(4 * c.M * c.N for c in cases)
@@ -413,21 +447,36 @@ def run_native(args):
     return dict(cases=cases, plans=plans, elapsed=elapsed_max, units=units, launches=launches,
                 warm_us_per_call=warm_us_per_call, per_launch=per_launch, clocks=clock_summary,
                 e2e_elapsed=e2e_max, h2d=h2d, d2h=d2h, pool_mb=pool_mb, n_rep=n_rep, l2=l2,
-                step_bytes=step_bytes, world=world, rank=rank)
+                step_bytes=step_bytes, world=world, rank=rank, chain=chain)
 
 
 # ------------------------------------------------------------------ oracle timing
 
-def oracle_step_sample(cases, seconds: float, max_steps: int | None = None):
+def oracle_step_sample(cases, seconds: float, max_steps: int | None = None, threads: int = 1):
     """Time the oracle (test infrastructure) on whole steps of the workload,
-    column-sampled when one step would exceed ~`seconds`/4."""
+    column-sampled when one step would exceed ~`seconds`/4.  threads > 1 splits
+    each call's output columns into that many contiguous ranges computed
+    concurrently (the oracle's C routine runs without the interpreter lock)."""
     import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    pool = ThreadPoolExecutor(threads) if threads > 1 else None
+
+    def call(X, W, c, n):
+        if pool is None:
+            oracle.gemm(X, W[:n], c.M, n, c.K)
+            return
+        bounds = [n * t // threads for t in range(threads + 1)]
+        futs = [pool.submit(oracle.gemm, X, W[a:b], c.M, b - a, c.K)
+                for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+        for f in futs:
+            f.result()
+
     inputs = [si.make_inputs(c) for c in cases]
     full_macs = sum(c.M * c.N * c.K for c in cases)
     # probe: one call of the smallest case
     t0 = time.perf_counter()
     c0 = min(cases, key=lambda c: c.M * c.N * c.K)
-    oracle.gemm(inputs[cases.index(c0)][0], inputs[cases.index(c0)][1], c0.M, c0.N, c0.K)
+    call(inputs[cases.index(c0)][0], inputs[cases.index(c0)][1], c0, c0.N)
     rate = max(c0.M * c0.N * c0.K / max(time.perf_counter() - t0, 1e-6), 1e6)   # MAC/s
     frac = min(1.0, (seconds / 4) * rate / full_macs)
     bytes_done = 0.0
@@ -436,15 +485,18 @@ def oracle_step_sample(cases, seconds: float, max_steps: int | None = None):
     while True:
         for c, (X, W) in zip(cases, inputs):
             n = max(1, int(round(c.N * frac)))
-            oracle.gemm(X, W[:n], c.M, n, c.K)
+            call(X, W, c, n)
             bytes_done += 2 * n * c.K + 2 * c.M * c.K + 4 * c.M * n
         steps += 1
         el = time.perf_counter() - t0
         if (max_steps is not None and steps >= max_steps) or (max_steps is None and el >= seconds):
             break
+    who = "single thread" if threads == 1 else f"{threads} threads over output columns"
     sample = (f"{steps} step(s) of the whole workload, each call on the first {frac:.1%} of its N columns "
-              f"(all of M and K), single thread" if frac < 1 else
-              f"{steps} whole step(s) of the workload, single thread")
+              f"(all of M and K), {who}" if frac < 1 else
+              f"{steps} whole step(s) of the workload, {who}")
+    if pool is not None:
+        pool.shutdown()
     return bytes_done / el, el / steps, sample
 
 
@@ -519,10 +571,15 @@ def main(argv=None):
                 "avg_launch_us": round(fam_time[dom] / fam_n[dom], 3),
                 "algorithmic_bytes_per_launch": round(fam_bytes[dom] / fam_n[dom])}
 
-    cpu = None
+    cpu = cpu_threads = None
     if not (args.no_cpu_baseline or args.profile_mode):
         gbs, s_step, sample = oracle_step_sample(cases, args.cpu_seconds)
         cpu = {"value": round(gbs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample}
+        nthr = os.cpu_count() or 1
+        if nthr > 1:
+            gbs, s_step, sample = oracle_step_sample(cases, args.cpu_seconds, threads=nthr)
+            cpu_threads = {"value": round(gbs / 1e9, 4), "unit": "GB/s", "cores": nthr, "kind": "oracle",
+                           "sample": sample}
 
     e2e_gbs = r["step_bytes"] * args.steps * n / r["e2e_elapsed"] / 1e9
     line = {
@@ -540,12 +597,14 @@ def main(argv=None):
         "pct_of_roofline_step": round(value_gbs / n / peak, 4),
         "roofline": roofline,
         "cpu_baseline": cpu,
+        "cpu_baseline_threads": cpu_threads,
         "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"],
                 "us_per_call": round(r["e2e_elapsed"] / args.steps / len(cases) * 1e6, 3),
                 "note": "W resident (weights); X copied in and Y copied out every step, inside the graph"},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
+        "pdl_chain": r["chain"],
         "per_shape": per_shape,
     }
     print(json.dumps(line), flush=True)

@@ -520,3 +520,40 @@ def test_tcgen05_tile_heights():
     with sk.options(backend=sk.SKINNY_BACKEND_TCGEN05, block_n=32):
         with pytest.raises(sk.SkinnyError):
             plan(8, 24576, 1536)
+
+
+def test_tcgen05_plans_are_consistent():
+    """Every tcgen05 plan the host accepts fits what the kernel assumes: a ring
+    of whole stages in the shared memory it asks for (>= 30 KB, so at most 7
+    CTAs share an SM's tensor memory), K slices of whole stages covering K, a
+    ring large enough to receive the cluster's partials, and the grid the
+    launcher checks."""
+    import random
+    rng = random.Random(11)
+    ran = 0
+    for _ in range(600):
+        M = rng.randint(1, 64)
+        N = rng.randint(1, 30000)
+        K = 8 * rng.randint(1, 2048)
+        bn, S = rng.choice([0, 64, 128]), rng.choice([0, 1, 2, 4, 8])
+        bk, st = rng.choice([0, 64, 128, 256]), rng.choice([0, 1, 2, 3, 6])
+        with sk.options(backend=sk.SKINNY_BACKEND_TCGEN05, block_n=bn, split_k=S, stage_k=bk, stages=st):
+            try:
+                p = plan(M, N, K, X=0x100000000000, W=0x200000000000, Y=0x300000000000)   # no overlap
+            except sk.SkinnyError as e:
+                assert e.status == sk.SKINNY_ERR_UNSUPPORTED
+                continue
+        ran += 1
+        tm, s, sk_ = p["block_n"], p["split_k"], p["stage_k"]
+        assert tm in (64, 128) and (bn == 0 or tm == bn) and (S == 0 or s == S) and (bk == 0 or sk_ == bk)
+        assert (st == 0 or p["stages"] == st) and 1 <= p["stages"] <= 16
+        assert p["grid_x"] == s and p["grid_y"] == -(-N // tm) and tm % s == 0
+        assert sk_ % 64 == 0 and 64 <= sk_ <= 256
+        assert p["k_chunk"] % sk_ == 0 and s * p["k_chunk"] >= K
+        mt = 16 if M <= 16 else 32 if M <= 32 else 64
+        ring = p["stages"] * (sk_ // 64) * (tm + mt) * 128
+        assert 30 * 1024 <= p["smem_bytes"] <= 227 * 1024
+        assert ring + 8 * (2 * p["stages"] + 1) + 8 + 1024 <= p["smem_bytes"]
+        if s > 1:
+            assert ring >= tm * M * 4                  # S slots of M x (tm / S) fp32 partials
+    assert ran > 300
