@@ -242,3 +242,14 @@ def test_tc_timeout_path_reports_and_recovers(split_k, bn):
     with sk.options(split_k=split_k, stages=4, block_n=bn, **TC):
         run_and_check(case)
     assert sk.skinny_get_device_status() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(20, 300, 1000), (17, 64, 4104), (64, 256, 14336)])
+def test_tc_takes_medium_m_shapes_the_other_backends_cannot(M, N, K):
+    """Unforced: 17..64 tokens with K % 16 != 0, or 64 tokens whose split-K X
+    slice does not fit shared memory, run on tcgen05 (16-byte aligned rows)."""
+    case = si.Case(f"tc_route_M{M}_N{N}_K{K}", M=M, N=N, K=K, seed=5900 + M + K % 97, w_dist="uniform_isqrtk",
+                   ldy=N + 2)
+    b = run_and_check(case)
+    assert b.plan()["backend"] == sk.SKINNY_BACKEND_TCGEN05
+    assert sk.skinny_get_device_status() == 0
