@@ -557,3 +557,17 @@ def test_tcgen05_plans_are_consistent():
         if s > 1:
             assert ring >= tm * M * 4                  # S slots of M x (tm / S) fp32 partials
     assert ran > 300
+
+
+def test_tcgen05_refuses_rows_a_tensor_map_cannot_address():
+    """The tensor maps need 16-byte aligned row starts for X and W (base
+    pointers and strides): anything else is refused on the host when tcgen05
+    is forced, and planned on another backend when it is not."""
+    with sk.options(backend=sk.SKINNY_BACKEND_TCGEN05):
+        assert plan(16, 4096, 4096)["backend"] == sk.SKINNY_BACKEND_TCGEN05
+        for kw in (dict(X=A16 + 2), dict(W=B16 + 8), dict(ldx=4100), dict(ldw=4100)):
+            with pytest.raises(sk.SkinnyError) as e:
+                plan(16, 4096, 4096, **kw)
+            assert e.value.status == sk.SKINNY_ERR_UNSUPPORTED
+    for kw in (dict(X=A16 + 2), dict(ldx=4100)):
+        assert plan(16, 4096, 4096, **kw)["backend"] != sk.SKINNY_BACKEND_TCGEN05
