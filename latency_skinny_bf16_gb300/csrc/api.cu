@@ -25,6 +25,12 @@ namespace {
 
 // ------------------------------------------------------------------ device status word
 __device__ int g_status_word;
+__device__ int g_status_taken;   // the value the last read-and-clear took
+
+// Read and clear the status word in one atomic step, so a report that lands
+// at any moment is either returned now or kept for the next read.
+__global__ void status_take_kernel() { g_status_taken = atomicExch(&g_status_word, 0); }
+std::mutex g_status_mu;          // one reader of g_status_taken at a time
 
 // K == 0: Y is the empty sum, +0 (fp32 or bf16 bits).
 __global__ void zero_fill_kernel(void *Y, int64_t ldy, int M, int N, int out_bf16) {
@@ -140,11 +146,11 @@ skinny_status_t validate(const uint16_t *X, int ldx, const void *W, int ldw, con
 // ------------------------------------------------------------------ dispatcher
 struct TunedEntry {
     int K, N, m_lo, m_hi;
-    int backend, consumer, split_k, block_n, stages, stage_k;
+    int backend, consumer, split_k, block_n, stages, stage_k, clusters;
 };
 const TunedEntry kTuned[] = {
 #include "tuning_table.inc"
-    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0}};
+    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0}};
 
 const TunedEntry *lookup_tuned(int M, int N, int K) {
     for (const TunedEntry &e : kTuned)
@@ -369,64 +375,12 @@ bool plan_stream(int M, int N, int K, int vec, bool x_ok, int force_c, int force
     return true;
 }
 
-// Tensor-core (tcgen05) plan: 128 W rows per CTA (64 when forced or tuned:
-// twice the CTAs, spread more evenly over the SMs); two 64-element boxes per
-// ring stage (each W row is then read 256 bytes at a time: measured faster
-// than one box on every projection shape); clusters of S <= 4 CTAs along K
-// while the row tiles alone leave SMs idle (clusters of 8 with a full ring
-// fit only two per GPC); the deepest ring that lets the whole grid be
-// resident at once (up to 3 CTAs per SM share its shared memory).
+// Tensor-core (tcgen05) plan: see tc_make_plan (tmem_gemm.cu).  Rows of X and
+// W must be 16-byte aligned (tensor maps).
 bool plan_tc(int M, int N, int K, int vec, bool x_ok, int force_bn, int force_s, int force_stages, int force_bk,
-             int num_sms, skinny_plan_t *p) {
-    if (vec != 8 || !x_ok || K < 1 || !tc_supported(M)) return false;
-    const int bn = force_bn ? force_bn : 128;    // W rows per CTA: the MMA's M (128 or 64)
-    if (bn != 128 && bn != 64) return false;
-    const int tiles = (N + bn - 1) / bn;
-    if (tiles < 1 || tiles > 65535) return false;
-    const int bk = force_bk ? force_bk : (K > 64 ? 128 : 64);
-    if (bk < 64 || bk > kTcMaxBK || bk % 64) return false;
-    const int nk = (K + bk - 1) / bk;             // ring stages over the whole K
-    int S = force_s;
-    if (S == 0) {
-        S = 1;
-        // double while SMs stay idle and every rank still gets a non-empty slice
-        while (S < 4 && tiles * S < num_sms && 2 * S <= nk &&
-               (2 * S - 1) * ((nk + 2 * S - 1) / (2 * S)) < nk)
-            S *= 2;
-    }
-    if (S < 1 || S > kSplitMaxCluster || bn % S != 0) return false;
-    const int per_rank = (nk + S - 1) / S;        // ring stages per cluster rank (a forced S may leave
-                                                  // the last ranks empty: they add zeros)
-    int stages = force_stages;
-    if (!stages) {
-        int per_sm = (tiles * S + num_sms - 1) / num_sms;
-        if (per_sm < 1) per_sm = 1;
-        if (per_sm > 3) per_sm = 3;
-        int budget = (228 * 1024) / per_sm - 2048;
-        if (budget > kMaxDynSmem) budget = kMaxDynSmem;
-        stages = kSplitMaxStages;
-        while (stages > 1 && tc_smem_bytes(M, bn, bk, stages, S) > budget) --stages;
-        // no deeper than the slice, but deep enough to receive the partials
-        int least = 1;
-        while (least < stages && tc_smem_bytes(M, bn, bk, least, S) > kMaxDynSmem) ++least;
-        if (stages > per_rank) stages = per_rank > least ? per_rank : least;
-    }
-    if (stages < 1 || stages > kSplitMaxStages) return false;
-    const int smem = tc_smem_bytes(M, bn, bk, stages, S);
-    if (smem > kMaxDynSmem) return false;
-    p->backend = SKINNY_BACKEND_TCGEN05;
-    p->consumer = SKINNY_CONSUMER_MMA;
-    p->vec_elems = 8;
-    p->block_n = bn;
-    p->split_k = S;
-    p->stages = stages;
-    p->stage_k = bk;
-    p->k_chunk = per_rank * bk;
-    p->grid_x = S;
-    p->grid_y = tiles;
-    p->threads = kTcThreads;
-    p->smem_bytes = smem;
-    return true;
+             int force_c, int num_sms, skinny_plan_t *p) {
+    if (vec != 8 || !x_ok) return false;
+    return tc_make_plan(M, N, K, force_bn, force_s, force_stages, force_bk, force_c, num_sms, p);
 }
 
 skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw, int M, int N, int K, int num_sms,
@@ -446,6 +400,7 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
     const int pdl = opt_pdl();
 
     int backend = fb, consumer = fc, split = fs, bn = fbn, stages = fst, stage_k = g_opt_force_stage_k.load();
+    int clusters = fgy;
     int tuned = 0;
     const bool dotmma_ok = splitk_ok && K % 32 == 0;
     // 17..64 tokens: tensor cores only, on the split-K backend, on the
@@ -472,6 +427,7 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
             if (!split) split = e->split_k;
             if (!stages) stages = e->stages;
             if (!stage_k) stage_k = e->stage_k;
+            if (!clusters) clusters = e->clusters;
             tuned = 1;
         } else if (e && e->backend == SKINNY_BACKEND_SPLITK && e->consumer == SKINNY_CONSUMER_MMA && mma_ok) {
             backend = SKINNY_BACKEND_SPLITK;
@@ -501,6 +457,7 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
             if (!bn) bn = e->block_n;
             if (!stages) stages = e->stages;
             if (!stage_k) stage_k = e->stage_k;
+            if (!clusters) clusters = e->clusters;
             tuned = 1;
         } else if (tc_ok && M >= 9 && 2.0 * N * K >= 16e6) {
             // default rule, bandwidth-bound weights (>= 16 MB) and 9..16 tokens:
@@ -531,7 +488,7 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
     } else if (backend == SKINNY_BACKEND_SPLITK) {
         if (consumer == SKINNY_CONSUMER_AUTO) consumer = (M > 4 && mma_ok) ? SKINNY_CONSUMER_MMA : SKINNY_CONSUMER_FMA;
         if (bn != 0 && bn != 16) return SKINNY_ERR_UNSUPPORTED;
-        ok = plan_splitk(M, N, K, vec, consumer, split, stages, fgy, stage_k, num_sms, p);
+        ok = plan_splitk(M, N, K, vec, consumer, split, stages, clusters, stage_k, num_sms, p);
         if (!ok && mid_m && tuned) {
             // a tuned entry these pointers / strides cannot use: the default split-K plan
             ok = plan_splitk(M, N, K, vec, consumer, fs, fst, fgy, g_opt_force_stage_k.load(), num_sms, p);
@@ -544,13 +501,13 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
         }
         if (!ok && fb == SKINNY_BACKEND_AUTO && mid_m && tc_ok) {
             // 17..64 tokens whose X slice does not fit beside the split-K ring
-            ok = plan_tc(M, N, K, vec, x_ok, 0, 0, 0, 0, num_sms, p);
+            ok = plan_tc(M, N, K, vec, x_ok, 0, 0, 0, 0, 0, num_sms, p);
             tuned = 0;
         }
     } else if (backend == SKINNY_BACKEND_STREAM) {
         if ((fc != SKINNY_CONSUMER_AUTO && fc != SKINNY_CONSUMER_MMA) || (bn != 0 && bn != 16))
             return SKINNY_ERR_UNSUPPORTED;
-        ok = plan_stream(M, N, K, vec, x_ok, fgy, stages, stage_k, num_sms, p);
+        ok = plan_stream(M, N, K, vec, x_ok, clusters, stages, stage_k, num_sms, p);
         if (!ok && fb == SKINNY_BACKEND_AUTO) {
             // a tuned or default streaming plan these pointers / sizes cannot use
             ok = (dotmma_ok && M >= 4 && plan_dotmma(M, N, K, vec, 0, num_sms, p)) ||
@@ -560,7 +517,7 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
     } else if (backend == SKINNY_BACKEND_TCGEN05) {
         if ((fc != SKINNY_CONSUMER_AUTO && fc != SKINNY_CONSUMER_MMA) || (bn != 0 && bn != 128 && bn != 64))
             return SKINNY_ERR_UNSUPPORTED;
-        ok = plan_tc(M, N, K, vec, x_ok, bn, split, stages, stage_k, num_sms, p);
+        ok = plan_tc(M, N, K, vec, x_ok, bn, split, stages, stage_k, clusters, num_sms, p);
         if (!ok && fb == SKINNY_BACKEND_AUTO) {
             // a tuned tensor-core plan these pointers / strides cannot use: the
             // default rule of the token range
@@ -909,11 +866,14 @@ skinny_status_t skinny_get_device_status(void *stream, int *code) {
     int device = 0;
     skinny_status_t st = current_device(&device);
     if (st != SKINNY_OK) return st;
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SKINNY_ERR_LAUNCH;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> g(g_status_mu);
     int v = 0;
-    const int zero = 0;
-    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return SKINNY_ERR_LAUNCH;
-    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return SKINNY_ERR_LAUNCH;
+    status_take_kernel<<<1, 1, 0, s>>>();
+    if (cudaPeekAtLastError() != cudaSuccess ||
+        cudaMemcpyFromSymbolAsync(&v, g_status_taken, sizeof(int), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return SKINNY_ERR_LAUNCH;
     *code = v;
     return SKINNY_OK;
 }

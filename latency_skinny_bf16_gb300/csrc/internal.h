@@ -68,15 +68,26 @@ bool stream_supported(int M);
 cudaError_t stream_prepare();
 cudaError_t launch_stream(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
 
-// ---- fifth-generation tensor-core backend (tmem_gemm.cu): block_n = 128 or 64
-// W rows per CTA (tcgen05.mma M), tokens on the MMA's N side (16 / 32 / 64),
-// W and X boxes by tensor-map TMA, optional cluster split-K along K
-constexpr int kTcThreads = 128;
-constexpr int kTcMaxBK = 256;          // K elements per ring stage: 64..256, multiple of 64
-constexpr int kTcMinSmem = 30 * 1024;  // <= 7 CTAs per SM: their tensor memory always fits
+// ---- fifth-generation tensor-core backend (tmem_gemm.cu): W rows split into
+// C balanced ranges of 8-row groups (clusters of split_k CTAs along K), tiles of
+// at most 128 rows on the MMA's M side (block_n = 64 or 128), tokens on its N
+// side (16 / 32 / 64), W and X boxes by tensor-map TMA, the tensor-memory
+// accumulator drained into fp32 registers after every ring stage
+constexpr int kTcThreads = 192;        // producer warp, MMA warp, four draining warps
+constexpr int kTcMaxBK = 256;          // K elements per ring stage: 64..256, multiple of 64 (<= 16 MMAs)
+constexpr int kTcCtasPerSm = 2;        // the default grid: two CTAs per SM
+constexpr int kTcSmemBudget = 110 * 1024;   // per CTA, so two fit in an SM's 228 KB
+// Shared memory asked for at least, so the CTAs an SM can hold never need more
+// tensor memory (four accumulators of MT columns each) than its 512 columns:
+constexpr int kTcMinSmem16 = 30 * 1024;  // 16 tokens, 64 columns: <= 7 CTAs per SM
+constexpr int kTcMinSmem32 = 46 * 1024;  // 32 tokens, 128 columns: <= 4 CTAs per SM
+constexpr int kTcMinSmem64 = 77 * 1024;  // 64 tokens, 256 columns: <= 2 CTAs per SM
 int tc_tokens(int M);                  // MMA N of the instantiation: 16, 32 or 64
 bool tc_supported(int M);
-int tc_smem_bytes(int M, int block_n, int stage_k, int stages, int split_k);
+int tc_smem_bytes(int M, int N, int block_n, int stage_k, int stages, int split_k, int clusters);
+// The plan for (M, N, K); zero arguments take the default.  false if none fits.
+bool tc_make_plan(int M, int N, int K, int force_bn, int force_s, int force_stages, int force_bk, int force_c,
+                  int num_sms, skinny_plan_t *p);
 cudaError_t tc_prepare();
 cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
 

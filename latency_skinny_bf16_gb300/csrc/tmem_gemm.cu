@@ -1,45 +1,54 @@
-// tmem_gemm.cu -- the fifth-generation tensor-core backend: W and X tiles by
-// tensor-map TMA, tcgen05.mma into tensor memory.
+// tmem_gemm.cu -- the fifth-generation tensor-core backend: W and X boxes by
+// tensor-map TMA, tcgen05.mma into tensor memory, the accumulator drained into
+// fp32 registers after every ring stage.
 //
 // Design source: "GLM-5.2 Blackwell decode optimizations", section
 // "Implementation breakdown" item 3 (the decode projections qkv_a / q_b /
 // eh_proj: the skinny GEMM at small M and a separate GEMM at medium M, picked
-// per (N, K) by measured speed), and "[Perf][Feat] Add generic cuteDSL LL BF16
-// router (GEMM)", item 2 (K split over the CTAs of a thread-block cluster,
-// partial sums reduced through distributed shared memory).
+// per (N, K) by measured speed) and item 2 (programmatic dependent launch),
+// and "[Perf][Feat] Add generic cuteDSL LL BF16 router (GEMM)", item 2 (K split
+// over the CTAs of a thread-block cluster, partial sums reduced through
+// distributed shared memory).
 //
-// GB300 form.  A CTA owns TM = 128 or 64 rows of W (the MMA's M side; rows
-// past N read as zeros) and, in a cluster of S CTAs along K, the K slice of
-// its rank (KS elements, a whole number of ring stages).  The tokens are the
-// MMA's N side (MT = 16, 32 or 64; rows past M read as zeros).  64-row tiles
-// double the CTA count, which spreads a weight more evenly over the SMs.
-//   * Thread 0 drives the TMA engine: per ring stage it loads stage_k / 64
-//     boxes of W [TM rows x 64 K] and of X [MT rows x 64 K] through 2-D
-//     tensor maps with the 128-byte swizzle (columns past K arrive as zeros),
-//     all completing on the stage's "full" mbarrier.  W is a weight, so with
-//     PDL the W boxes of the first ring pass are issued before
-//     griddepcontrol.wait; X boxes only after it.
+// GB300 form.
+//   * Work split.  W's rows are cut into groups of 8.  The grid has C row
+//     ranges (clusters of S CTAs along K); range c holds the groups
+//     [c*G/C, (c+1)*G/C), so no range has more than one group more than
+//     another.  A range is walked as T tiles of at most VP rows (VP a multiple
+//     of 8, at most 128); the MMA's M side is 64 or 128 rows, and rows past a
+//     tile's last row are never stored.  The planner sizes the grid at two
+//     CTAs per SM, so the next call's CTAs (programmatic dependent launch)
+//     fill each SM as this call's CTAs leave it.
+//   * Thread 0 drives the TMA engine: per ring stage, for each 64-element
+//     K box, the tile's rows as at most five boxes of 128 / 64 / 32 / 16 / 8
+//     rows (one tensor map per height, 128-byte swizzle) and one box of the
+//     MT token rows of X (rows past M and columns past K read as zeros), all
+//     completing on the stage's "full" mbarrier.  W is a weight, so with PDL
+//     the W boxes of the first ring pass go out before griddepcontrol.wait.
 //   * Thread 32 issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32; M = TM,
-//     N = MT, K = 16 each; operands from shared-memory descriptors, K-major,
-//     128-byte swizzle) into an fp32 accumulator of MT columns in tensor
-//     memory (M = 128: row r in lane r; M = 64: row 16w + i in lane 32w + i,
-//     i < 16), frees each stage by tcgen05.commit on its "empty" mbarrier,
-//     and signals "done" with a last commit.
-//   * Warp 2 allocates the tensor-memory columns and frees them at the end.
-//   * Epilogue, all four warps: warp w reads lanes 32w..32w+31 with
-//     tcgen05.ld 32x32b: a thread holds one output column n, its registers
-//     the tokens.  S = 1: Y is written directly (per token, a warp's columns
-//     are one contiguous store).  S > 1: after one cluster barrier
-//     (every CTA's MMAs are complete, so every ring is free) each CTA sends
-//     the partials of rows owned by rank q = row / (TM / S) into q's ring
-//     (slot = sending rank) with st.shared::cluster; after a second barrier
-//     each owner adds slots 0..S-1 in that order and writes Y.  The MMA order
-//     and the reduction order are fixed, so a plan's result is bit-identical
-//     from run to run.
+//     N = MT tokens, K = 16 each) into one of four tensor-memory accumulators
+//     (MT columns each) in rotation, one per chunk of ring stages holding at
+//     most 16 MMAs: the chunk's first MMA overwrites, so no accumulator chain
+//     is longer than 16 MMAs, and the issuer runs up to four chunks ahead of
+//     the draining warps.  tcgen05.commit frees each ring stage and marks the
+//     accumulator full at the end of its chunk.
+//   * Warps 2..5 (one per lane quarter of tensor memory) wait for each
+//     accumulator, read it with tcgen05.ld, add it into fp32 registers (one
+//     output row per thread, the tokens in registers) and release it.  The
+//     tensor core's own accumulation is not round-to-nearest per add (its
+//     error is biased; measured on same-sign data), so it is kept to one
+//     chunk, and the chunk sums are added in order with rounded fp32 adds.
+//   * S = 1: each tile's rows are stored once its last stage is drained.
+//     S > 1 (one tile per CTA): after a cluster barrier every CTA sends the
+//     rows owned by rank q into q's ring (slot = sending rank) with
+//     st.shared::cluster; after a second barrier each owner adds slots
+//     0..S-1 in that order.  Every order is fixed, so a plan's result is
+//     bit-identical from run to run.
 // Every mbarrier wait is bounded; a wait that gives up records an error in
-// the device status word, the rest of the K loop is skipped, copies in flight
-// are drained (bounded), and the CTA still takes part in both cluster
-// barriers and frees its tensor memory.
+// the device status word and the CTA winds down: copies in flight and issued
+// MMAs are waited for (bounded), a CTA whose accumulator was not drained sends
+// no partials, both cluster barriers are still passed, and tensor memory is
+// freed only once every issued MMA is known to be complete.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -50,13 +59,15 @@ namespace skinny {
 namespace {
 
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
-enum : int { kWaitDone = 5 };
+enum : int { kWaitAcc = 5, kWaitAccEmpty = 6 };
+constexpr int kWMaps = 5;                      // W box heights 128, 64, 32, 16, 8 rows
+constexpr int kAccWarp0 = 2;                   // warps 2..5 drain the accumulators
 
-// a box is `rows` x 64 bf16 (128 bytes per row)
-__host__ __device__ constexpr int w_box_bytes(int TM) { return TM * 128; }
-__host__ __device__ constexpr int x_box_bytes(int MT) { return MT * 128; }
-__host__ __device__ constexpr int stage_bytes(int TM, int MT, int kb) { return kb * (w_box_bytes(TM) + x_box_bytes(MT)); }
-__host__ __device__ constexpr int tmem_cols(int MT) { return MT <= 32 ? 32 : MT; }   // a power of two >= 32
+constexpr int kNAcc = 4;                       // tensor-memory accumulators in rotation
+__host__ __device__ constexpr int tmem_cols(int MT) { return kNAcc * MT; }   // 64 / 128 / 256 columns
+// Ring stages per accumulator chunk: at most 16 MMAs (4 per 64-element box)
+// accumulate in tensor memory before the chunk is drained into registers.
+__host__ __device__ inline int tc_chunk_stages(int kb) { return kb >= 4 ? 1 : 4 / kb; }
 
 // ------------------------------------------------------------------ TMA (tensor maps)
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
@@ -110,21 +121,31 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar)
                  : "memory");
 }
-// 16 consecutive fp32 columns of this thread's lane, waited for in the same
-// statement so no use of the registers can be scheduled before the wait.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
-    uint32_t r[16];
+// 16 consecutive fp32 columns of this thread's lane (not yet waited for).
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
+// Wait for this thread's tcgen05.ld; the registers are passed through the
+// statement so no use of them can be scheduled above the wait.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15])
+                 :
+                 : "memory");
+}
+
+struct TcMaps {
+    CUtensorMap w[kWMaps];   // box heights 128, 64, 32, 16, 8 rows (64 K elements each)
+    CUtensorMap x;           // box MT rows x 64 K elements
+};
 
 struct TcParams {
     void *Y;
@@ -133,187 +154,283 @@ struct TcParams {
     int KS;          // K elements per cluster rank, a multiple of 64 * kb
     int kb;          // 64-element boxes per ring stage
     int stages;
+    int G, C;        // 8-row groups of W, row ranges
+    int vg;          // groups per tile (VP = 8 * vg rows)
     int *status;
     uint64_t budget_ns;
     int out_bf16;
 };
 
-// Shared memory from the 1024-byte aligned base: the ring, then full[stages],
-// empty[stages], done (8 bytes each), then the tensor-memory address.
-__host__ __device__ inline int tc_layout_bytes(int TM, int MT, int kb, int stages) {
-    return stages * stage_bytes(TM, MT, kb) + 8 * (2 * stages + 1) + 8;
+// Shared-memory layout from the 1024-byte aligned base: the ring (per stage:
+// kb W regions of VP rows x 128 bytes, then kb X regions of MT rows x 128
+// bytes), a pad the MMA may read past the last W region (rows VP..TM-1 of the
+// last tile are never stored), then the mbarriers, the tensor-memory address
+// and the failure flag.
+__host__ __device__ inline int tc_stage_bytes(int VP, int MT, int kb) { return kb * (VP + MT) * 128; }
+__host__ __device__ inline int tc_pad_bytes(int VP, int MT, int kb, int TM) {
+    const int over = (TM - VP) * 128 - kb * MT * 128;
+    return over > 0 ? over : 0;
+}
+__host__ __device__ inline int tc_layout_bytes(int VP, int MT, int kb, int stages, int TM) {
+    return stages * tc_stage_bytes(VP, MT, kb) + tc_pad_bytes(VP, MT, kb, TM) + 8 * (2 * stages + 2 * kNAcc + 1) + 16;
 }
 
 template <int MT, int TM>
-__global__ void __launch_bounds__(kTcThreads, 1)
-tmem_gemm_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx, const TcParams p)
+__global__ void __launch_bounds__(kTcThreads, 2)
+tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
 {
+    // the next call may start as soon as every CTA of this one is resident:
+    // its W streaming fills the SMs this call leaves
+    griddep_launch_dependents();
+
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;            // 128-byte swizzle atoms: 1024-byte aligned
     uint8_t *smem = smem_raw + (base - raw);
-    constexpr int kWBox = w_box_bytes(TM);
-    const int sbytes = stage_bytes(TM, MT, p.kb);
-    const int stages = p.stages;
-    const uint32_t bars = base + stages * sbytes;
+    const int kb = p.kb, stages = p.stages;
+    const int VP = 8 * p.vg;
+    const int sbytes = tc_stage_bytes(VP, MT, kb);
+    const uint32_t bars = base + stages * sbytes + tc_pad_bytes(VP, MT, kb, TM);
     auto full = [&](int s) { return bars + 8u * s; };
     auto empty = [&](int s) { return bars + 8u * (stages + s); };
-    const uint32_t done = bars + 16u * stages;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + stages * sbytes + 8 * (2 * stages + 1));
+    auto accf = [&](int b) { return bars + 8u * (2 * stages + b); };
+    auto acce = [&](int b) { return bars + 8u * (2 * stages + kNAcc + b); };
+    const uint32_t done = bars + 8u * (2 * stages + 2 * kNAcc);
+    uint8_t *tail = smem + stages * sbytes + tc_pad_bytes(VP, MT, kb, TM) + 8 * (2 * stages + 2 * kNAcc + 1);
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(tail);
+    volatile int *fail = reinterpret_cast<volatile int *>(tail + 4);    // an accumulator was not drained
+    volatile int *mma_ok = reinterpret_cast<volatile int *>(tail + 8);  // every issued MMA completed
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = gridDim.x;
     const int rank = (S > 1) ? (int)cluster_ctarank() : 0;
-    const int n0 = blockIdx.y * TM;
+    // this CTA's rows [r0, r1) and K slice [kbeg, kend)
+    const int c = blockIdx.y;
+    const int g0 = (int)(((int64_t)c * p.G) / p.C), g1 = (int)(((int64_t)(c + 1) * p.G) / p.C);
+    const int r0 = 8 * g0, r1 = 8 * g1;
+    const int ntiles = (g1 - g0 + p.vg - 1) / p.vg;
     const int kbeg = rank * p.KS;
     const int kend = min(p.K, kbeg + p.KS);
-    const int sk = 64 * p.kb;
-    const int nsteps = kend > kbeg ? (kend - kbeg + sk - 1) / sk : 0;
+    const int sk = 64 * kb;
+    const int nk = kend > kbeg ? (kend - kbeg + sk - 1) / sk : 0;   // ring stages per tile
+    const int total = ntiles * nk;
+    const int cs = tc_chunk_stages(kb);                             // stages per accumulator chunk
+    const int nchunk = (nk + cs - 1) / cs;                          // chunks per tile
 
     if (tid == 0) {
+        for (int i = 0; i < kWMaps; ++i) prefetch_tensormap(&maps.w[i]);
+        prefetch_tensormap(&maps.x);
         for (int s = 0; s < stages; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
         }
+        for (int b = 0; b < kNAcc; ++b) {
+            mbar_init(accf(b), 1);
+            mbar_init(acce(b), 4);            // lane 0 of each draining warp
+        }
         mbar_init(done, 1);
+        *fail = 0;
+        *mma_ok = 0;
         fence_mbarrier_init_cluster();
     }
-    if (warp == 2) tmem_alloc(smem_u32(tmem_slot), tmem_cols(MT));
-    tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
 
-    if (tid == 0) {
-        // ---- TMA producer (the other lanes of warp 0 wait for it at __syncwarp)
-        prefetch_tensormap(&tmw);
-        prefetch_tensormap(&tmx);
-        const uint32_t tx = (uint32_t)sbytes;
-        auto w_boxes = [&](int i, int s) {
-            for (int b = 0; b < p.kb; ++b)
-                tma_load_2d(base + s * sbytes + b * kWBox, &tmw, kbeg + (i * p.kb + b) * 64, n0, full(s));
-        };
-        auto x_boxes = [&](int i, int s) {
-            for (int b = 0; b < p.kb; ++b)
-                tma_load_2d(base + s * sbytes + p.kb * kWBox + b * x_box_bytes(MT), &tmx,
-                            kbeg + (i * p.kb + b) * 64, 0, full(s));
-        };
-        const int pre = min(nsteps, stages);
-        for (int i = 0; i < pre; ++i) {
-            mbar_arrive_expect_tx(full(i), tx);
-            w_boxes(i, i);                       // the weight: before the PDL wait
-        }
-        griddep_wait();
-        griddep_launch_dependents();
-        for (int i = 0; i < pre; ++i) x_boxes(i, i);
-        int issued = pre;
-        for (int i = pre; i < nsteps; ++i) {
-            const int s = i % stages;
-            if (!mbar_wait_bounded(empty(s), (uint32_t)((i / stages - 1) & 1), p.budget_ns)) {
-                report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitProducerEmpty);
-                break;
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- TMA producer
+            auto tile_rows = [&](int t) { return min(VP, r1 - (r0 + t * VP)); };
+            auto issue = [&](int i, int s, bool w_part, bool x_part) {
+                const int t = i / nk, ks = i - t * nk;
+                const int rows = tile_rows(t), row0 = r0 + t * VP;
+                const uint32_t st = base + s * sbytes;
+                for (int b = 0; b < kb; ++b) {
+                    const int k0 = kbeg + (ks * kb + b) * 64;
+                    if (w_part) {
+                        int off = 0;
+#pragma unroll
+                        for (int h = 0; h < kWMaps; ++h) {
+                            const int height = 128 >> h;
+                            if (rows - off >= height) {
+                                tma_load_2d(st + b * VP * 128 + off * 128, &maps.w[h], k0, row0 + off, full(s));
+                                off += height;
+                            }
+                        }
+                    }
+                    if (x_part) tma_load_2d(st + kb * VP * 128 + b * MT * 128, &maps.x, k0, 0, full(s));
+                }
+            };
+            auto stage_tx = [&](int i) { return (uint32_t)(kb * (tile_rows(i / nk) + MT) * 128); };
+            const int pre = min(total, stages);
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(full(i), stage_tx(i));
+                issue(i, i, true, false);          // the weight: before the PDL wait
             }
-            mbar_arrive_expect_tx(full(s), tx);
-            w_boxes(i, s);
-            x_boxes(i, s);
-            issued = i + 1;
+            griddep_wait();
+            for (int i = 0; i < pre; ++i) issue(i, i, false, true);
+            int issued = pre;
+            for (int i = pre; i < total; ++i) {
+                const int s = i % stages;
+                if (!mbar_wait_bounded(empty(s), (uint32_t)((i / stages - 1) & 1), p.budget_ns)) {
+                    report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitProducerEmpty);
+                    break;
+                }
+                mbar_arrive_expect_tx(full(s), stage_tx(i));
+                issue(i, s, true, true);
+                issued = i + 1;
+            }
+            // every copy issued has landed before the ring is reused or the CTA exits
+            for (int i = max(0, issued - stages); i < issued; ++i)
+                if (!mbar_wait_bounded(full(i % stages), (uint32_t)((i / stages) & 1), kDrainNs))
+                    report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitDrain);
         }
-        // every copy issued has landed before the ring is reused or the CTA exits
-        for (int i = max(0, issued - stages); i < issued; ++i)
-            if (!mbar_wait_bounded(full(i % stages), (uint32_t)((i / stages) & 1), kDrainNs))
-                report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitDrain);
-    } else if (tid == 32) {
-        // ---- MMA issuer
-        griddep_wait();
-        griddep_launch_dependents();
-        constexpr uint32_t idesc = idesc_bf16<MT, TM>();
-        for (int i = 0; i < nsteps; ++i) {
-            const int s = i % stages;
-            if (!mbar_wait_bounded(full(s), (uint32_t)((i / stages) & 1), p.budget_ns)) {
-                report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitConsumerFull);
+        __syncwarp();
+    } else if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), tmem_cols(MT));
+        tc_fence_before();
+        named_bar_sync(1, kTcThreads - 32);        // warps 1..5: the tensor-memory address is published
+        tc_fence_after();
+        const uint32_t tmem = *tmem_slot;
+        if (lane == 0) {
+            // ---- MMA issuer (its bounded waits start once the preceding kernel is done)
+            griddep_wait();
+            constexpr uint32_t idesc = idesc_bf16<MT, TM>();
+            for (int i = 0; i < total; ++i) {
+                const int s = i % stages;
+                const int t = i / nk, ks = i - t * nk;
+                const int g = t * nchunk + ks / cs;                 // accumulator chunk
+                const int b = g % kNAcc;
+                const bool first = (ks % cs) == 0, last = (ks % cs) == cs - 1 || ks == nk - 1;
+                if (first && g >= kNAcc &&
+                    !mbar_wait_bounded(acce(b), (uint32_t)((g / kNAcc - 1) & 1), p.budget_ns)) {
+                    report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitAccEmpty);
+                    break;
+                }
+                if (!mbar_wait_bounded(full(s), (uint32_t)((i / stages) & 1), p.budget_ns)) {
+                    report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitConsumerFull);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t wst = base + s * sbytes;
+                const uint32_t xst = wst + kb * VP * 128;
+                for (int cb = 0; cb < kb; ++cb)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        umma_bf16(tmem + (uint32_t)(b * MT), sw128_desc(wst + cb * VP * 128 + 32 * j),
+                                  sw128_desc(xst + cb * MT * 128 + 32 * j), idesc,
+                                  (first && (cb | j) == 0) ? 0u : 1u);
+                umma_commit(empty(s));               // the stage is free once these MMAs have read it
+                if (last) umma_commit(accf(b));      // the chunk's sum is complete
+            }
+            umma_commit(done);                       // tracks every MMA issued, also after a give-up
+            if (mbar_wait_bounded(done, 0, kDrainNs)) *mma_ok = 1;
+            else report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitDrain);
+        }
+        __syncwarp();
+    } else {
+        // ---- accumulator warps: lane quarter q of tensor memory
+        named_bar_sync(1, kTcThreads - 32);
+        tc_fence_after();
+        const uint32_t tmem = *tmem_slot;
+        griddep_wait();                          // Y may be read or written by the preceding kernel
+        const int q = warp & 3;
+        // accumulator row of this thread (M = 64: lanes 16..31 of each quarter hold none)
+        const int row = (TM == 128) ? 32 * q + lane : 16 * q + lane;
+        const bool has_row = (TM == 128) || lane < 16;
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+        const int M = p.M;
+        float acc[MT];
+#pragma unroll
+        for (int j = 0; j < MT; ++j) acc[j] = 0.f;
+        bool ok = true;
+        for (int g = 0; g < ntiles * nchunk; ++g) {
+            const int b = g % kNAcc;
+            bool got = true;
+            if (lane == 0) got = mbar_wait_bounded(accf(b), (uint32_t)((g / kNAcc) & 1), p.budget_ns);
+            got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+            if (!got) {
+                if (lane == 0) report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitAcc);
+                ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t wst = base + s * sbytes;
-            const uint32_t xst = wst + p.kb * kWBox;
-            for (int b = 0; b < p.kb; ++b)
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    umma_bf16(tmem, sw128_desc(wst + b * kWBox + 32 * j), sw128_desc(xst + b * x_box_bytes(MT) + 32 * j),
-                              idesc, (i | b | j) != 0 ? 1u : 0u);
-            umma_commit(empty(s));               // the stage is free once these MMAs have read it
+            for (int cc = 0; cc < MT / 16; ++cc) {
+                if (16 * cc < M) {                // warp-uniform
+                    uint32_t r[16];
+                    tmem_ld16_nowait(lane_base + (uint32_t)(b * MT + 16 * cc), r);
+                    tmem_ld_wait(r);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[16 * cc + j] += __uint_as_float(r[j]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce(b));
+            if (S == 1 && (g % nchunk) == nchunk - 1) {
+                // the tile's last chunk: store its rows
+                const int t = g / nchunk;
+                const int rows = min(VP, r1 - (r0 + t * VP));
+                const int n = r0 + t * VP + row;
+                if (has_row && row < rows && n < p.N) {
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+                        if (m < M) store_y(p.Y, p.out_bf16, m * p.ldy + n, acc[m]);
+                }
+#pragma unroll
+                for (int j = 0; j < MT; ++j) acc[j] = 0.f;
+            }
         }
-        umma_commit(done);                       // also when the loop gave up: tracks what was issued
-    } else {
-        griddep_wait();                          // Y may be read or written by the preceding kernel
-        griddep_launch_dependents();
-    }
-    __syncwarp();
-
-    // ---- epilogue: accumulator rows 32*warp + lane, columns = tokens
-    if (!mbar_wait_bounded(done, 0, p.budget_ns)) {
-        if (lane == 0) report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitDone);
-        if (!mbar_wait_bounded(done, 0, kDrainNs) && lane == 0)
-            report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitDrain);
-    }
-    tc_fence_after();
-    const int M = p.M;
-    float v[MT];
+        if (!ok) *fail = 1;
+        // S > 1: one tile per CTA (the planner guarantees it); `acc` holds this
+        // rank's partial sum (zeros for an empty K slice) until the reduction
+        __syncthreads();                          // A: producer drained, MMAs complete
+        if (S > 1) {
+            cluster_arrive_release();             // B1: every CTA's ring is free
+            cluster_wait_acquire();
+            const int RQ = (VP + S - 1) / S;
+            const int rows = min(VP, r1 - r0);
+            if (has_row && row < rows && !*fail && *mma_ok) {
+                const int qo = row / RQ, rl = row - qo * RQ;
+                const uint32_t dst = mapa_shared(base, (uint32_t)qo);
 #pragma unroll
-    for (int c = 0; c < MT / 16; ++c) {
-        if (16 * c < M && nsteps > 0) {          // warp-uniform
-            tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + 16 * c, v + 16 * c);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[16 * c + j] = 0.f;
+                for (int m = 0; m < MT; ++m)
+                    if (m < M) st_shared_cluster_f32(dst + 4u * (uint32_t)((rank * M + m) * RQ + rl), acc[m]);
+            }
+            cluster_arrive_release();             // B2: every partial is in its owner's slots
+            cluster_wait_acquire();
+            const float *slots = reinterpret_cast<const float *>(smem);
+            const int mine = max(0, min(RQ, rows - rank * RQ));
+            for (int e = tid - kAccWarp0 * 32; e < M * mine; e += 4 * 32) {
+                const int m = e / mine, r = e - m * mine;
+                const int n = r0 + rank * RQ + r;
+                float a = slots[m * RQ + r];
+                for (int src = 1; src < S; ++src) a += slots[(src * M + m) * RQ + r];
+                if (n < p.N) store_y(p.Y, p.out_bf16, m * p.ldy + n, a);
+            }
         }
-    }
-    if (nsteps == 0) {
-#pragma unroll
-        for (int j = 0; j < MT; ++j) v[j] = 0.f;   // an empty K slice adds nothing
-    }
-    // accumulator row of this thread (M = 64: lanes 16..31 of each warp hold none)
-    const int row = (TM == 128) ? 32 * warp + lane : 16 * warp + lane;
-    const bool has_row = (TM == 128) || lane < 16;
-    if (S == 1) {
-        const int n = n0 + row;
-        if (has_row && n < p.N) {
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-                if (m < M) store_y(p.Y, p.out_bf16, m * p.ldy + n, v[m]);
-        }
-    } else {
-        const int R = TM / S;                    // rows owned by each rank
-        cluster_arrive_release();                // every CTA of the cluster is past its MMAs
-        cluster_wait_acquire();
-        if (has_row) {
-            const int q = row / R, rl = row - q * R;
-            const uint32_t dst = mapa_shared(base, (uint32_t)q);
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-                if (m < M) st_shared_cluster_f32(dst + 4u * (uint32_t)((rank * M + m) * R + rl), v[m]);
-        }
-        cluster_arrive_release();                // every partial is in its owner's slots
-        cluster_wait_acquire();
-        const float *slots = reinterpret_cast<const float *>(smem);
-        for (int i = tid; i < M * R; i += kTcThreads) {
-            const int m = i / R, r = i - m * R;
-            const int n = n0 + rank * R + r;
-            float acc = slots[m * R + r];
-            for (int src = 1; src < S; ++src) acc += slots[(src * M + m) * R + r];
-            if (n < p.N) store_y(p.Y, p.out_bf16, m * p.ldy + n, acc);
-        }
+        tc_fence_before();
+        __syncthreads();                          // C: tensor memory no longer read
+        return;
     }
 
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 2) {
+    // ---- producer and MMA warps: the same barriers as the draining warps
+    __syncthreads();                              // A
+    if (S > 1) {
+        cluster_arrive_release();                 // B1
+        cluster_wait_acquire();
+        cluster_arrive_release();                 // B2
+        cluster_wait_acquire();
+    }
+    __syncthreads();                              // C
+    if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, tmem_cols(MT));
+        if (*mma_ok) tmem_dealloc(*tmem_slot, tmem_cols(MT));
+        // else: an issued MMA may still write this tensor memory; it stays
+        // allocated until the CTA exits rather than being handed to another CTA
     }
 }
 
-using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const TcParams);
+using TcKernel = void (*)(const TcMaps, const TcParams);
 const TcKernel kTc[3][2] = {{&tmem_gemm_kernel<16, 128>, &tmem_gemm_kernel<16, 64>},
                             {&tmem_gemm_kernel<32, 128>, &tmem_gemm_kernel<32, 64>},
                             {&tmem_gemm_kernel<64, 128>, &tmem_gemm_kernel<64, 64>}};
@@ -349,22 +466,105 @@ bool encode_bf16_2d(CUtensorMap *map, const void *ptr, int cols, int rows, int64
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row split of a plan: groups per tile (vg) for C ranges of G groups, tiles
+// of at most `max_vg` groups, as even as the ranges allow.
+int tc_groups_per_tile(int G, int C, int max_vg) {
+    const int gmax = (G + C - 1) / C;
+    const int T = (gmax + max_vg - 1) / max_vg;
+    return (gmax + T - 1) / T;
+}
+
 }  // namespace
 
 int tc_tokens(int M) { return 16 << tc_index(M); }
 
 bool tc_supported(int M) { return M >= 1 && M <= SKINNY_MAX_M; }
 
-int tc_smem_bytes(int M, int block_n, int stage_k, int stages, int split_k) {
+int tc_smem_bytes(int M, int N, int block_n, int stage_k, int stages, int split_k, int clusters) {
     const int MT = tc_tokens(M);
     const int kb = stage_k / 64;
-    int bytes = tc_layout_bytes(block_n, MT, kb, stages);
-    // S > 1: the ring also receives the partials (S slots of M x block_n / S fp32)
-    if (split_k > 1 && stages * stage_bytes(block_n, MT, kb) < block_n * M * 4) return 1 << 30;
-    // at most 7 resident CTAs per SM, so their tensor memory (<= 64 columns
-    // each) always fits in the SM's 512 columns and an allocation never waits
-    if (bytes < kTcMinSmem - 1024) bytes = kTcMinSmem - 1024;
+    const int G = (N + 7) / 8;
+    const int vg = tc_groups_per_tile(G, clusters, block_n / 8);
+    const int VP = 8 * vg;
+    int bytes = tc_layout_bytes(VP, MT, kb, stages, block_n);
+    // S > 1: the ring also receives the partials (S slots of M x ceil(VP / S) fp32)
+    if (split_k > 1 && stages * tc_stage_bytes(VP, MT, kb) < split_k * M * ((VP + split_k - 1) / split_k) * 4)
+        return 1 << 30;
+    // cap the CTAs an SM can hold, so their tensor memory (four accumulators
+    // of MT columns each) always fits in the SM's 512 columns
+    const int min_smem = (MT == 64) ? kTcMinSmem64 : (MT == 32) ? kTcMinSmem32 : kTcMinSmem16;
+    if (bytes < min_smem - 1024) bytes = min_smem - 1024;
     return bytes + 1024;                         // slack for the 1024-byte alignment
+}
+
+bool tc_make_plan(int M, int N, int K, int force_bn, int force_s, int force_stages, int force_bk, int force_c,
+                  int num_sms, skinny_plan_t *p) {
+    if (!tc_supported(M) || N < 1 || K < 1 || num_sms < 1) return false;
+    if (force_bn && force_bn != 128 && force_bn != 64) return false;
+    const int G = (N + 7) / 8;
+    const int slots = kTcCtasPerSm * num_sms;
+    const int bk = force_bk ? force_bk : (K > 64 ? 128 : 64);
+    if (bk < 64 || bk > kTcMaxBK || bk % 64) return false;
+    const int nk_all = (K + bk - 1) / bk;         // ring stages over the whole K
+    // S: split K over a cluster while the tiles the CTA slots would get are
+    // thinner than 48 rows (the MMA reads all TM rows of a tile from shared
+    // memory, and a ring stage should carry enough W to cover its round trip),
+    // each rank keeping at least two stages of K
+    int S = force_s;
+    if (S == 0) {
+        S = 1;
+        while (S < kSplitMaxCluster && nk_all >= 4 * S) {
+            int c = slots / S;
+            if (c > G) c = G;
+            if (8 * tc_groups_per_tile(G, c < 1 ? 1 : c, 16) >= 48) break;
+            S *= 2;
+        }
+    }
+    if (S < 1 || S > kSplitMaxCluster || (S & (S - 1))) return false;
+    const int max_vg_default = (force_bn == 64) ? 8 : 16;
+    int C = force_c;
+    if (C == 0) {
+        C = slots / S;
+        if (C > G) C = G;
+        if (S > 1 && (G + C - 1) / C > max_vg_default) C = (G + max_vg_default - 1) / max_vg_default;
+        if (C < 1) C = 1;
+    }
+    if (C < 1 || C > 65535 || C > G) return false;
+    const int vg = tc_groups_per_tile(G, C, max_vg_default);
+    const int VP = 8 * vg;
+    if (S > 1 && (G + C - 1) / C > vg) return false;   // S > 1: one tile per CTA
+    const int bn = force_bn ? force_bn : (VP <= 64 ? 64 : 128);
+    if (VP > bn) return false;
+    const int per_rank = (nk_all + S - 1) / S;    // ring stages per cluster rank (a forced S may leave
+                                                  // the last ranks empty: they add zeros)
+    const int ntiles_max = ((G + C - 1) / C + vg - 1) / vg;
+    int stages = force_stages;
+    if (!stages) {
+        const int budget = kTcSmemBudget;
+        stages = kSplitMaxStages;
+        while (stages > 1 && tc_smem_bytes(M, N, bn, bk, stages, S, C) > budget) --stages;
+        // no deeper than the CTA's stages, but deep enough to receive the partials
+        int least = 1;
+        while (least < stages && tc_smem_bytes(M, N, bn, bk, least, S, C) > kMaxDynSmem) ++least;
+        const int work = per_rank * ntiles_max;
+        if (stages > work) stages = work > least ? work : least;
+    }
+    if (stages < 1 || stages > kSplitMaxStages) return false;
+    const int smem = tc_smem_bytes(M, N, bn, bk, stages, S, C);
+    if (smem > kMaxDynSmem) return false;
+    p->backend = SKINNY_BACKEND_TCGEN05;
+    p->consumer = SKINNY_CONSUMER_MMA;
+    p->vec_elems = 8;
+    p->block_n = bn;
+    p->split_k = S;
+    p->stages = stages;
+    p->stage_k = bk;
+    p->k_chunk = per_rank * bk;
+    p->grid_x = S;
+    p->grid_y = C;
+    p->threads = kTcThreads;
+    p->smem_bytes = smem;
+    return true;
 }
 
 cudaError_t tc_prepare() {
@@ -379,19 +579,25 @@ cudaError_t tc_prepare() {
 cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCtx &c) {
     const int S = pl.split_k;
     const int TM = pl.block_n;
-    if (!tc_supported(a.M) || (TM != 128 && TM != 64) || S < 1 || S > kSplitMaxCluster || (TM % S) != 0 ||
+    const int C = pl.grid_y;
+    const int G = (a.N + 7) / 8;
+    if (!tc_supported(a.M) || (TM != 128 && TM != 64) || S < 1 || S > kSplitMaxCluster || (S & (S - 1)) ||
         pl.stage_k < 64 || pl.stage_k > kTcMaxBK || pl.stage_k % 64 || pl.stages < 1 ||
-        pl.stages > kSplitMaxStages || pl.k_chunk % pl.stage_k || (int64_t)pl.k_chunk * S < a.K ||
-        pl.grid_x != S || pl.grid_y != (a.N + TM - 1) / TM || pl.smem_bytes < kTcMinSmem ||
-        pl.smem_bytes < tc_smem_bytes(a.M, TM, pl.stage_k, pl.stages, S))
+        pl.stages > kSplitMaxStages || pl.k_chunk % pl.stage_k || (int64_t)pl.k_chunk * S < a.K || pl.grid_x != S ||
+        C < 1 || C > G || C > 65535 || pl.threads != kTcThreads)
+        return cudaErrorInvalidValue;
+    const int vg = tc_groups_per_tile(G, C, TM / 8);
+    if (8 * vg > TM || (S > 1 && (G + C - 1) / C > vg) ||
+        pl.smem_bytes < tc_smem_bytes(a.M, a.N, TM, pl.stage_k, pl.stages, S, C) || pl.smem_bytes > kMaxDynSmem)
         return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(a.X) & 15) || (a.ldx & 7) || (reinterpret_cast<uintptr_t>(a.W) & 15) ||
         (a.ldw & 7))
         return cudaErrorInvalidValue;
     const int idx = tc_index(a.M);
-    CUtensorMap tmw, tmx;
-    if (!encode_bf16_2d(&tmw, a.W, a.K, a.N, a.ldw, TM) || !encode_bf16_2d(&tmx, a.X, a.K, a.M, a.ldx, 16 << idx))
-        return cudaErrorInvalidValue;
+    TcMaps maps;
+    for (int h = 0; h < kWMaps; ++h)
+        if (!encode_bf16_2d(&maps.w[h], a.W, a.K, a.N, a.ldw, 128 >> h)) return cudaErrorInvalidValue;
+    if (!encode_bf16_2d(&maps.x, a.X, a.K, a.M, a.ldx, 16 << idx)) return cudaErrorInvalidValue;
     TcParams p;
     p.Y = a.Y;
     p.ldy = a.ldy;
@@ -401,12 +607,15 @@ cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCt
     p.KS = pl.k_chunk;
     p.kb = pl.stage_k / 64;
     p.stages = pl.stages;
+    p.G = G;
+    p.C = C;
+    p.vg = vg;
     p.status = c.status;
     p.budget_ns = c.budget_ns;
     p.out_bf16 = a.out_bf16;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(S, pl.grid_y, 1);
+    cfg.gridDim = dim3(S, C, 1);
     cfg.blockDim = dim3(kTcThreads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem_bytes;
     cfg.stream = c.stream;
@@ -424,7 +633,7 @@ cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCt
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, kTc[idx][TM == 128 ? 0 : 1], tmw, tmx, p);
+    return cudaLaunchKernelEx(&cfg, kTc[idx][TM == 128 ? 0 : 1], maps, p);
 }
 
 }  // namespace skinny

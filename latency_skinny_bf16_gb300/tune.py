@@ -37,22 +37,32 @@ def token_bucket(M: int) -> int:
     return 8 if M <= 8 else 16 if M <= 16 else 32 if M <= 32 else 64
 
 
-def tc_candidates(M: int, K: int, N: int):
-    """tcgen05 plans: 128- or 64-row tiles, cluster sizes along K, 2 or 4 boxes
-    per ring stage (1 never won on GB300), the planner's ring depth."""
+def tc_candidates(M: int, K: int, N: int, num_sms: int = 152):
+    """tcgen05 plans: cluster sizes S along K; for each, the planner's own
+    number of row ranges and the range counts that give tiles of about 32 to
+    128 rows (W rows come in groups of 8), at most three CTAs per SM; 2 or 4
+    boxes per ring stage; the planner's tile height and ring depth."""
     out = []
-    for bn in (0, 64):                    # 0: the planner's 128-row tile
-        for s in (1, 2, 4, 8):
+    G = -(-max(N, 1) // 8)
+    for s in (1, 2, 4, 8):
+        if K < 2 * s * 128:
+            continue
+        counts = {0}
+        for groups in (4, 6, 8, 12, 16):
+            c = -(-G // groups)
+            if c * s <= 3 * num_sms:
+                counts.add(c)
+        for c in sorted(counts):
             for bk in (128, 256):
-                out.append(dict(backend=4, consumer=0, split_k=s, stages=0, block_n=bn, stage_k=bk))
+                out.append(dict(backend=4, consumer=0, split_k=s, stages=0, block_n=0, stage_k=bk, clusters=c))
     return out
 
 
-def candidates(M: int, K: int, N: int = 0):
+def candidates(M: int, K: int, N: int = 0, num_sms: int = 152):
     out = []
     big = 2 * N * K > 16e6
     if M > 4 or big:
-        out += tc_candidates(M, K, N)
+        out += tc_candidates(M, K, N, num_sms)
     if M > 16:
         # 17..64 tokens: tensor cores only -- cluster split-K with the MMA
         # consumer, or the tensor-core dot-product for large weights
@@ -187,7 +197,7 @@ def merge_rows(K, N, rows, m_max=64):
         else:
             m_hi = min(m_max, b)
         lines.append((K, N, rows[i][0], m_hi, c["backend"], c["consumer"], c["split_k"], c["block_n"],
-                      c["stages"], c.get("stage_k", 0), [round(r[2], 2) for r in rows[i:j + 1]]))
+                      c["stages"], c.get("stage_k", 0), c.get("clusters", 0), [round(r[2], 2) for r in rows[i:j + 1]]))
         i = j + 1
     return lines
 
@@ -197,7 +207,8 @@ def plannable_range(K, N, m_lo, m_hi, c, num_sms):
     every M in m_lo..m_hi' (a plan measured at one M may not fit a larger M
     of the same line, e.g. its X slice); M past it keep the default rule."""
     x, w, y = 0x7F0000000000, 0x7F0010000000, 0x7F0020000000   # 16-byte aligned, never dereferenced
-    opts = {k: v for k, v in c.items() if k in ("backend", "consumer", "split_k", "block_n", "stages", "stage_k")}
+    opts = {k: v for k, v in c.items()
+            if k in ("backend", "consumer", "split_k", "block_n", "stages", "stage_k", "clusters")}
     last = m_lo - 1
     for M in range(m_lo, m_hi + 1):
         with sk.options(**opts):
@@ -263,11 +274,12 @@ def main(argv=None):
         K, N = (int(v) for v in shp.lower().split("x"))
         rows = tune_shape(K, N, (m_large if 2 * N * K > 16e6 else m_small) + m_mid, l2, None, log)
         num_sms = torch.cuda.get_device_properties(0).multi_processor_count
-        for (k, n, mlo, mhi, be, co, sp, bn, st, bk, us) in merge_rows(K, N, rows):
-            c = dict(backend=be, consumer=co, split_k=sp, block_n=bn, stages=st, stage_k=bk)
+        for (k, n, mlo, mhi, be, co, sp, bn, st, bk, cl, us) in merge_rows(K, N, rows):
+            c = dict(backend=be, consumer=co, split_k=sp, block_n=bn, stages=st, stage_k=bk, clusters=cl)
             mhi = plannable_range(K, N, mlo, mhi, c, num_sms)
             if mhi >= mlo:
-                out_lines.append(f"{{{k}, {n}, {mlo}, {mhi}, {be}, {co}, {sp}, {bn}, {st}, {bk}}},  // us/call {us}")
+                out_lines.append(f"{{{k}, {n}, {mlo}, {mhi}, {be}, {co}, {sp}, {bn}, {st}, {bk}, {cl}}},  "
+                                 f"// us/call {us}")
     text = "\n".join(out_lines) + "\n"
     if a.install:
         install(out_lines)

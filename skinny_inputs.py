@@ -30,6 +30,9 @@ qkv_a / q_b / eh_proj style projection shapes):
                      ldy in [N, N+67], X and W ~N(0,1) with 1% x100 outliers;
                      case parameters from master seed 4.
 * ``pdl_chain``      64 back-to-back calls M=4, K=7168, N=256 (seed 5).
+* same-sign operands (``abs_normal``: |N(0,1)|, ``abs_uniform_isqrtk``:
+  U(0, 1/sqrt(K))) for the accumulation tests: every product is positive,
+  so rounding errors of a long fp32 sum cannot cancel.
 * ``midm``           the medium-M decode regime, 17..64 tokens:
                      M in {17,24,32,40,64} x (K,N) in {(7168,256),(4096,384)}
                      (router distributions, seeds 401..410), then
@@ -58,8 +61,9 @@ class Case:
     N: int
     K: int
     seed: int
-    x_dist: str = "normal"          # "normal" -> N(0,1)
-    w_dist: str = "normal0.02"      # "normal0.02", "uniform_isqrtk", "normal"
+    x_dist: str = "normal"          # "normal" -> N(0,1); "abs_normal" -> |N(0,1)|
+    w_dist: str = "normal0.02"      # "normal0.02", "uniform_isqrtk", "normal", "abs_normal",
+                                    # "abs_uniform_isqrtk" (U(0, 1/sqrt(K)))
     outliers: bool = False          # 1% of entries x100 (both X and W)
     ldx: int | None = None
     ldw: int | None = None
@@ -101,6 +105,10 @@ def _draw(shape: tuple[int, int], dist: str, K: int, outliers: bool,
     elif dist == "uniform_isqrtk":
         bound = 1.0 / math.sqrt(max(K, 1))
         v = (torch.rand(shape, generator=g, dtype=torch.float32) * 2.0 - 1.0) * bound
+    elif dist == "abs_normal":
+        v = torch.randn(shape, generator=g, dtype=torch.float32).abs()
+    elif dist == "abs_uniform_isqrtk":
+        v = torch.rand(shape, generator=g, dtype=torch.float32) / math.sqrt(max(K, 1))
     else:
         raise ValueError(f"unknown distribution {dist!r}")
     if outliers:

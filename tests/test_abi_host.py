@@ -12,6 +12,7 @@ import re
 import pytest
 
 import latency_skinny_bf16_gb300 as sk
+from plan_checks import check_tc_geometry
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 A16 = 0x7F0000000000        # fake, 16-byte aligned "device" addresses: never dereferenced
@@ -191,7 +192,7 @@ def _table_entries():
 
 
 def test_every_tuned_entry_is_a_supported_plan_and_is_used():
-    for K, N, m_lo, m_hi, be, co, s, bn, st, bk in _table_entries():
+    for K, N, m_lo, m_hi, be, co, s, bn, st, bk, cl in _table_entries():
         assert 1 <= m_lo <= m_hi <= 64
         # a row never spans two kernels: 1..8 / 9..16 / 17..32 / 33..64 tokens
         assert (m_lo <= 8) == (m_hi <= 8) and (m_lo <= 16) == (m_hi <= 16) and (m_lo <= 32) == (m_hi <= 32)
@@ -209,7 +210,9 @@ def test_every_tuned_entry_is_a_supported_plan_and_is_used():
                 if bk:
                     assert p["stage_k"] == bk
             elif be == sk.SKINNY_BACKEND_TCGEN05:
-                assert (p["split_k"], p["block_n"], p["consumer"]) == (s, bn or 128, sk.SKINNY_CONSUMER_MMA)
+                assert (p["split_k"], p["consumer"]) == (s, sk.SKINNY_CONSUMER_MMA)
+                assert (bn == 0 or p["block_n"] == bn) and (cl == 0 or p["grid_y"] == cl)
+                check_tc_geometry(p, M, N, K)
                 if st:
                     assert p["stages"] == st
                 if bk:
@@ -282,8 +285,7 @@ def test_mid_m_takes_a_tensor_core_path():
                     # a single partial-sum buffer: no cluster loops over two tiles
                     assert p["grid_y"] == (N + 15) // 16
             elif p["backend"] == sk.SKINNY_BACKEND_TCGEN05:
-                assert p["block_n"] in (64, 128) and p["grid_y"] == -(-N // p["block_n"])
-                assert p["split_k"] * p["k_chunk"] >= K and p["k_chunk"] % p["stage_k"] == 0
+                check_tc_geometry(p, M, N, K)
             else:
                 assert p["backend"] == sk.SKINNY_BACKEND_DOTPROD and p["block_n"] in (16, 32, 64)
                 assert 2 * N * K >= 16e6 and p["k_chunk"] % 32 == 0
@@ -291,7 +293,10 @@ def test_mid_m_takes_a_tensor_core_path():
     assert plan(40, 320, 7168)["backend"] == sk.SKINNY_BACKEND_SPLITK
     p = plan(40, 8192, 4096)
     assert (p["backend"], p["consumer"]) == (sk.SKINNY_BACKEND_TCGEN05, sk.SKINNY_CONSUMER_MMA)
-    assert (p["split_k"], p["stage_k"], p["grid_y"]) == (4, 128, 64)   # 64 tiles x 4 >= 152 SMs
+    # 1024 row groups: 304 ranges would give tiles of 32 rows, so K is split in
+    # two (clusters of 2, 152 ranges of 6-7 groups: tiles of 56 rows)
+    assert (p["split_k"], p["stage_k"], p["grid_y"], p["block_n"]) == (2, 128, 152, 64)
+    check_tc_geometry(p, 40, 8192, 4096)
     # 9..16 tokens on large weights take it too; fewer stay on the earlier backends
     assert plan(12, 8192, 4096)["backend"] == sk.SKINNY_BACKEND_TCGEN05
     assert plan(8, 8192, 3072)["backend"] == sk.SKINNY_BACKEND_DOTPROD
@@ -515,8 +520,8 @@ def test_tcgen05_tile_heights():
         with sk.options(backend=sk.SKINNY_BACKEND_TCGEN05, block_n=bn):
             for M, N, K in ((1, 24576, 1536), (40, 2112, 7168), (64, 100, 520)):
                 p = plan(M, N, K)
-                assert (p["backend"], p["block_n"], p["grid_y"]) == (sk.SKINNY_BACKEND_TCGEN05, bn, -(-N // bn))
-                assert p["split_k"] * p["k_chunk"] >= K and p["smem_bytes"] <= 227 * 1024
+                assert (p["backend"], p["block_n"]) == (sk.SKINNY_BACKEND_TCGEN05, bn)
+                check_tc_geometry(p, M, N, K)
     with sk.options(backend=sk.SKINNY_BACKEND_TCGEN05, block_n=32):
         with pytest.raises(sk.SkinnyError):
             plan(8, 24576, 1536)
@@ -547,15 +552,7 @@ def test_tcgen05_plans_are_consistent():
         tm, s, sk_ = p["block_n"], p["split_k"], p["stage_k"]
         assert tm in (64, 128) and (bn == 0 or tm == bn) and (S == 0 or s == S) and (bk == 0 or sk_ == bk)
         assert (st == 0 or p["stages"] == st) and 1 <= p["stages"] <= 16
-        assert p["grid_x"] == s and p["grid_y"] == -(-N // tm) and tm % s == 0
-        assert sk_ % 64 == 0 and 64 <= sk_ <= 256
-        assert p["k_chunk"] % sk_ == 0 and s * p["k_chunk"] >= K
-        mt = 16 if M <= 16 else 32 if M <= 32 else 64
-        ring = p["stages"] * (sk_ // 64) * (tm + mt) * 128
-        assert 30 * 1024 <= p["smem_bytes"] <= 227 * 1024
-        assert ring + 8 * (2 * p["stages"] + 1) + 8 + 1024 <= p["smem_bytes"]
-        if s > 1:
-            assert ring >= tm * M * 4                  # S slots of M x (tm / S) fp32 partials
+        check_tc_geometry(p, M, N, K)
     assert ran > 300
 
 

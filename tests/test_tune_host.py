@@ -20,7 +20,17 @@ def test_merge_rows_merges_consecutive_equal_winners():
     lines = tune.merge_rows(7168, 256, rows)
     # a gap (M=6 not tuned) goes to the line before it; the last line ends with its token bucket
     assert [(l[2], l[3], l[4]) for l in lines] == [(1, 1, 1), (2, 4, 2), (5, 6, 1), (7, 8, 2)]
-    assert lines[1][10] == [3.5, 3.6, 3.7]
+    assert lines[1][10] == 0 and lines[1][11] == [3.5, 3.6, 3.7]     # clusters: the planner's own
+
+
+def test_tc_candidates_span_cluster_sizes_and_tile_heights():
+    c = tune.tc_candidates(16, 7168, 2112, num_sms=152)
+    assert {x["split_k"] for x in c} == {1, 2, 4, 8}
+    assert all(x["backend"] == 4 and x["stage_k"] in (128, 256) for x in c)
+    # row-range counts: the planner's (0) and those giving 4..16 groups of 8 rows per tile
+    assert {x["clusters"] for x in c if x["split_k"] == 8} == {0, 17, 22, 33, 44}   # 66 x 8 > 3 per SM
+    assert all(x["clusters"] * x["split_k"] <= 3 * 152 for x in c)
+    assert {x["split_k"] for x in tune.tc_candidates(16, 512, 256)} == {1, 2}   # K < 2 * S * 128 refused
 
 
 def test_merge_rows_never_crosses_the_8_token_boundary():
