@@ -257,7 +257,10 @@ SKINNY_API skinny_status_t skinny_rmsnorm_gemm_bf16(const uint16_t *X, int ldx, 
  *
  *     p_n          = exp(l_n - max_j l_j) / sum_j exp(l_j - max_j l_j)
  *     ids[m*ldid+i]     = index of the i-th largest logit (i < k), descending;
- *                         equal logits: lower index first
+ *                         equal logits: lower index first; a NaN logit ranks
+ *                         below every other value (-inf included), NaNs among
+ *                         themselves by index, so the k ids are always
+ *                         distinct indices in [0, N)
  *     weights[m*ldw+i]  = p of that expert, or with renormalize != 0 that p
  *                         divided by the sum of the k chosen p
  *
@@ -267,8 +270,10 @@ SKINNY_API skinny_status_t skinny_rmsnorm_gemm_bf16(const uint16_t *X, int ldx, 
  * plainest softmax / top-k one.  fp32 arithmetic (CUDA expf); the selection
  * compares the fp32 logits exactly as stored; bit-identical run to run.
  *
- *   logits   device, fp32 [M, N], row stride ldl >= N, 4-byte aligned; at least
- *            one finite logit per row (NaN logits are never chosen)
+ *   logits   device, fp32 [M, N], row stride ldl >= N, 4-byte aligned.  The
+ *            softmax is IEEE arithmetic: a NaN or +inf logit makes its token's
+ *            sum of exponentials NaN, so every weight of that token is NaN
+ *            (its ids stay as above)
  *   weights  device, fp32 [M, k], row stride ldw >= k; ids device, int32 [M, k],
  *            row stride ldid >= k; 4-byte aligned; neither may overlap the
  *            logits or each other.  Only the [M, k] entries are written.
@@ -295,12 +300,17 @@ SKINNY_API skinny_status_t skinny_router_bf16_topk(const uint16_t *X, int ldx, c
                                         float *logits, int ldl, int M, int N, int K, int k, int renormalize,
                                         float *weights, int ldwt, int32_t *ids, int ldid, void *stream);
 
-/* Synchronises `stream`, then reads and clears the current device's status
- * word: *code = 0 if no kernel reported an error since the last read, else a
- * value whose low 8 bits are a skinny_status_t (SKINNY_ERR_DEVICE_TIMEOUT)
- * and whose upper bits say which wait gave up (1 = consumer / MMA full-slot
- * wait, 2 = producer empty-slot wait, 3 = drain wait, 4 = X staging wait,
- * 5 = tcgen05 epilogue wait for the last MMA).  Test and diagnostic use. */
+/* Reads and clears the current device's status word once the work queued on
+ * `stream` before the call has finished: a one-thread kernel on `stream`
+ * swaps the word with 0 atomically, and the call waits for `stream`.  *code =
+ * 0 if no kernel reported an error since the last read, else the first error
+ * reported since then: low 8 bits a skinny_status_t (SKINNY_ERR_DEVICE_TIMEOUT),
+ * upper bits the wait that gave up (1 = consumer / MMA full-slot wait,
+ * 2 = producer empty-slot wait, 3 = drain wait, 4 = X staging wait,
+ * 5 = tcgen05 accumulator-full wait, 6 = tcgen05 accumulator-free wait).  The
+ * word is shared by every stream of the device: a report made by a kernel on
+ * another stream is returned by this read or kept for the next one, never
+ * lost.  Test and diagnostic use. */
 SKINNY_API skinny_status_t skinny_get_device_status(void *stream, int *code);
 
 /* Static string for a status code (never NULL). */

@@ -27,10 +27,17 @@ namespace {
 constexpr int kTopkThreads = 128;
 constexpr int kTopkWarps = kTopkThreads / 32;
 
-// (v, n) is a better pick than (bv, bn): larger value, equal value lower index;
-// n < 0 marks "none yet"
+// (v, n) is a better pick than (bv, bn): the larger logit; a NaN ranks below
+// every other value (-inf included); equal logits, or two NaNs, the lower
+// index.  n < 0 marks "none yet".  Every row thus has a total order, so the k
+// ids are distinct valid indices whatever the logits hold.
 __device__ __forceinline__ bool better(float v, int n, float bv, int bn) {
-    return n >= 0 && (bn < 0 || v > bv || (v == bv && n < bn));
+    if (n < 0) return false;
+    if (bn < 0) return true;
+    const bool vnan = isnan(v), bnan = isnan(bv);
+    if (vnan != bnan) return bnan;
+    if (!vnan && v != bv) return v > bv;
+    return n < bn;
 }
 
 __global__ void __launch_bounds__(kTopkThreads)

@@ -105,22 +105,36 @@ void skinny_oracle_gemm_points(const uint16_t *X, int64_t ldx,
  *
  *   p_n = exp(l_n - l_max) / sum_j exp(l_j - l_max)          (fp64)
  *   ids  = the k indices of the largest logits, in descending order of the
- *          logit as given (float32), equal logits by ascending index
+ *          logit as given (float32), equal logits by ascending index; a NaN
+ *          logit ranks below every other value (-inf included), and NaNs
+ *          among themselves by ascending index
  *   weights[i] = p_{ids[i]}, or with renormalize != 0
  *   weights[i] = p_{ids[i]} / sum_{i'<k} p_{ids[i']}
  *
- * Selection is made on the float32 logits exactly as given (the same values
- * the GPU kernel compares), by k passes of "largest not yet chosen" over the
- * row.  Rows must hold at least one finite logit; 1 <= k <= N. */
+ * l_max is the largest logit that is not NaN (-inf when there is none).  The
+ * arithmetic is IEEE: a NaN or +inf logit makes the sum NaN, so every weight
+ * of that token is NaN, while its ids stay well defined (the pages say nothing
+ * on non-finite logits; this is the plain IEEE reading).  Selection is made on
+ * the float32 logits exactly as given (the same values the GPU kernel
+ * compares), by k passes of "highest-ranked not yet chosen" over the row;
+ * 1 <= k <= N. */
+static int topk_ranks_above(float v, int n, float b, int nb)
+{
+    const int vnan = isnan(v), bnan = isnan(b);
+    if (vnan != bnan) return bnan;
+    if (!vnan && v != b) return v > b;
+    return n < nb;
+}
+
 void skinny_oracle_router_topk(const float *L, int64_t ldl, int M, int N, int k, int renormalize,
                                double *weights, int64_t ldwt, int32_t *ids, int64_t ldid,
                                unsigned char *taken /* N bytes of scratch */)
 {
     for (int m = 0; m < M; ++m) {
         const float *row = L + (int64_t)m * ldl;
-        float lmax = row[0];
-        for (int n = 1; n < N; ++n)
-            if (row[n] > lmax) lmax = row[n];
+        float lmax = -INFINITY;
+        for (int n = 0; n < N; ++n)
+            if (!isnan(row[n]) && row[n] > lmax) lmax = row[n];
         double denom = 0.0;
         for (int n = 0; n < N; ++n) denom += exp((double)row[n] - (double)lmax);
         memset(taken, 0, (size_t)N);
@@ -128,7 +142,7 @@ void skinny_oracle_router_topk(const float *L, int64_t ldl, int M, int N, int k,
         for (int i = 0; i < k; ++i) {
             int best = -1;
             for (int n = 0; n < N; ++n)
-                if (!taken[n] && (best < 0 || row[n] > row[best])) best = n;
+                if (!taken[n] && (best < 0 || topk_ranks_above(row[n], n, row[best], best))) best = n;
             taken[best] = 1;
             ids[(int64_t)m * ldid + i] = best;
             const double pv = exp((double)row[best] - (double)lmax) / denom;

@@ -470,6 +470,27 @@ def test_topk_invariants():
     assert (idsi[0, :100] >= 100).all() and (wi[0, 100:] == 0).all()
 
 
+def test_topk_nan_logits_rank_last_and_make_the_weights_nan():
+    """Hand-worked rows.  A NaN logit ranks below every value (-inf included)
+    and NaNs among themselves by index; the softmax is IEEE arithmetic, so a
+    NaN (or +inf) logit makes every weight of its row NaN; a row without them
+    keeps its closed-form softmax."""
+    nan, inf = np.nan, np.inf
+    L = np.array([[nan, 1.0, -inf, 2.0, nan, 0.5],    # NaN first and mid-row
+                  [0.0, 3.0, -1.0, -inf, 2.0, 1.0],   # plain row
+                  [1.0, inf, 0.0, -1.0, 2.0, 0.0],    # +inf
+                  [nan, nan, nan, nan, nan, nan]], np.float32)
+    w, ids = oracle.router_topk(L, 6)
+    assert ids.tolist() == [[3, 1, 5, 2, 0, 4], [1, 4, 5, 0, 2, 3], [1, 4, 0, 2, 5, 3], [0, 1, 2, 3, 4, 5]]
+    assert np.isnan(w[0]).all() and np.isnan(w[2]).all() and np.isnan(w[3]).all()
+    denom = math.exp(-3) + 1 + math.exp(-4) + math.exp(-1) + math.exp(-2)
+    expect = [1 / denom, math.exp(-1) / denom, math.exp(-2) / denom, math.exp(-3) / denom,
+              math.exp(-4) / denom, 0.0]
+    assert np.allclose(w[1], expect, rtol=1e-14, atol=0)
+    w2, ids2 = oracle.router_topk(L[:1], 2, renormalize=True)
+    assert ids2.tolist() == [[3, 1]] and np.isnan(w2).all()
+
+
 def _topk_pins_pass(lib) -> bool:
     """A compact subset of the top-k pins, run against a given oracle build."""
     try:
@@ -489,14 +510,20 @@ def _topk_pins_pass(lib) -> bool:
                 ref_w = ref_w / ref_w.sum(axis=1, keepdims=True)
             if not np.array_equal(ids, ref_ids) or not np.allclose(w, ref_w, rtol=1e-13, atol=0):
                 return False
+        nan = np.nan
+        w, ids = oracle.router_topk(np.array([[nan, 1.0, -np.inf, 2.0, nan]], np.float32), 5, lib=lib)
+        if ids.tolist() != [[3, 1, 2, 0, 4]] or not np.isnan(w).all():
+            return False
         return True
     except Exception:
         return False
 
 
 TOPK_MUTATIONS = [
-    ("ties to the higher index", "(best < 0 || row[n] > row[best])", "(best < 0 || row[n] >= row[best])"),
-    ("smallest first", "(best < 0 || row[n] > row[best])", "(best < 0 || row[n] < row[best])"),
+    ("ties to the higher index", "    return n < nb;", "    return n > nb;"),
+    ("smallest first", "if (!vnan && v != b) return v > b;", "if (!vnan && v != b) return v < b;"),
+    ("NaN ranked first", "if (vnan != bnan) return bnan;", "if (vnan != bnan) return vnan;"),
+    ("NaN left to the comparison", "if (vnan != bnan) return bnan;", "if (0) return bnan;"),
     ("no renormalisation", "weights[(int64_t)m * ldwt + i] /= chosen;", "weights[(int64_t)m * ldwt + i] *= 1.0;"),
     ("id off by one", "ids[(int64_t)m * ldid + i] = best;", "ids[(int64_t)m * ldid + i] = best + 1;"),
     ("denominator misses the last logit", "for (int n = 0; n < N; ++n) denom += exp",

@@ -29,8 +29,10 @@ def _init():
 def check_topk(L: np.ndarray, k: int, renorm: bool, w: np.ndarray, ids: np.ndarray, what=""):
     w_ref, ids_ref = oracle.router_topk(L, k, renormalize=renorm)
     assert np.array_equal(ids, ids_ref), f"{what}: ids differ"
-    err = np.abs(w.astype(np.float64) - w_ref)
-    bound = W_RTOL * np.abs(w_ref) + W_ATOL
+    nan_ref = np.isnan(w_ref)
+    assert np.array_equal(np.isnan(w), nan_ref), f"{what}: NaN pattern of the weights differs"
+    err = np.abs(w.astype(np.float64)[~nan_ref] - w_ref[~nan_ref])
+    bound = W_RTOL * np.abs(w_ref[~nan_ref]) + W_ATOL
     assert (err <= bound).all(), f"{what}: weights off by {err.max():.3e}"
 
 
@@ -70,6 +72,31 @@ def test_topk_special_rows(kind):
         w, ids = sk.router_topk(torch.from_numpy(L).cuda(), k, renormalize=renorm)
         torch.cuda.synchronize()
         check_topk(L, k, renorm, w.cpu().numpy(), ids.cpu().numpy(), kind)
+
+
+@pytest.mark.parametrize("N", [256, 384, 1000, 2048])
+def test_topk_nan_logits(N):
+    """NaN logits (at index 0, mid-row, several, a whole row, next to +inf):
+    they rank below every other logit, NaNs by index, and the IEEE softmax
+    makes every weight of such a row NaN; the ids match the oracle exactly
+    and rows without NaN are unaffected.  Both the warp-per-token kernel
+    (N <= 1024) and the CTA-per-token kernel run."""
+    M, k = 6, 8
+    L = logits_case(M, N, seed=4000 + N)
+    L[0, 0] = np.nan                                  # first entry
+    L[1, N // 2] = np.nan                             # mid-row
+    L[2, [1, 5, 9, N - 1]] = np.nan                   # several
+    L[3, :] = np.nan                                  # a whole row: ids 0..k-1
+    L[4, 3] = np.inf                                  # +inf: inf - inf is NaN
+    # row 5 keeps plain values
+    for renorm in (False, True):
+        w, ids = sk.router_topk(torch.from_numpy(L).cuda(), k, renormalize=renorm)
+        torch.cuda.synchronize()
+        w, ids = w.cpu().numpy(), ids.cpu().numpy()
+        check_topk(L, k, renorm, w, ids, f"NaN rows N{N}")
+        assert ids[3].tolist() == list(range(k))
+        assert np.isnan(w[:5]).all() and np.isfinite(w[5]).all()
+        assert all(len(set(r.tolist())) == k and r.min() >= 0 and r.max() < N for r in ids)
 
 
 def test_topk_strided_outputs_and_bit_identity():
