@@ -6,9 +6,11 @@
 // q_c_out), whose result is the X of the q_b bf16_skinny_gemm (item 3).
 //
 // GB300 form.  One CTA of 128 threads per token: the sum of squares in fp32
-// (per thread ascending k, warp butterfly, warps in order: a fixed order, so
-// the result is bit-identical run to run), r = 1 / sqrtf(mean + eps) (IEEE
-// square root and division), then xn = bf16_rn(x * r * g) written to the
+// (thread j takes the 8-element chunks j, j + 128, ... in ascending k, then a
+// warp butterfly and the warps in order: a fixed order, so the result is
+// bit-identical run to run, and the same order the fused tcgen05 prologue
+// uses), r = 1 / sqrtf(mean + eps) (IEEE square root and division), then
+// xn = bf16_rn(x * r * g) written to the
 // caller's buffer, which the q_b GEMM launched right behind it reads as X.
 // With PDL the kernel lets its dependent launch at once, so the GEMM streams
 // its weights while the norm runs and reads xn after griddepcontrol.wait.
@@ -30,10 +32,29 @@ rmsnorm_kernel(const uint16_t *__restrict__ X, int64_t ldx, const uint16_t *__re
     griddep_launch_dependents();   // the GEMM behind may start streaming its weights now
     griddep_wait();                // X comes from the preceding kernel
     const uint16_t *xm = X + (int64_t)m * ldx;
+    const bool vec = (reinterpret_cast<uintptr_t>(xm) & 15) == 0;
+    const int chunks = (K + 7) / 8;
+    // thread j: the squares of its 8-element chunks c = j, j + 128, ... in
+    // ascending k (one fused multiply-add each); the order does not depend on
+    // how the chunk is loaded
     float ss = 0.f;
-    for (int k = tid; k < K; k += kNormThreads) {
-        const float v = bf16_one(ldg_u16(xm + k));
-        ss = fmaf(v, v, ss);
+    for (int c = tid; c < chunks; c += kNormThreads) {
+        const int k0 = 8 * c;
+        if (vec && k0 + 8 <= K) {
+            const uint4 q = ldg_v4(xm + k0);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
+                ss = fmaf(a, a, ss);
+                ss = fmaf(b, b, ss);
+            }
+        } else {
+            for (int k = k0; k < min(K, k0 + 8); ++k) {
+                const float v = bf16_one(ldg_u16(xm + k));
+                ss = fmaf(v, v, ss);
+            }
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);

@@ -3,11 +3,14 @@
 
 The stored XN is a bf16 rounding of x * r * g computed in fp32; the oracle
 gives that value in fp64.  Each XN element must be the nearest bf16 of the
-oracle's value, except within a relative 1e-5 of a rounding midpoint, where
-either neighbour is correct (fp32 arithmetic decides there).  Y must match the
-GEMM oracle applied to the XN the GPU produced (the standard tolerance), and
-everything is bit-identical run to run and with PDL on or off.
+oracle's value, except where the fp32 computation may land on the other side
+of a rounding midpoint: within the relative distance `xn_allowance(K)` of it,
+derived below from the kernel's arithmetic, either neighbour is correct.  Y
+must match the GEMM oracle applied to the XN the GPU produced (the standard
+tolerance), and everything is bit-identical run to run and with PDL on or off.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -30,20 +33,51 @@ def bf16_to_f64(bits):
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def check_xn(xn_bits, ref):
-    """xn_bits (bf16) against the unrounded fp64 reference values."""
+U = 2.0 ** -24          # fp32 unit roundoff
+
+
+def xn_allowance(K: int) -> float:
+    """Relative error bound of the fp32 value x * r * g before its rounding to bf16.
+
+    The norm kernel sums the K squares of a token with 128 threads: thread j
+    adds, in order, the squares of the elements of its 8-element chunks
+    c = j, j + 128, ... (one fused multiply-add each; a bf16 square is exact in
+    fp32), then a 5-level warp butterfly and the 4 warps in order.  The longest
+    chain of rounded adds is L = 8 * ceil(K / 1024) + 5 + 3, and every term is
+    non-negative, so the sum t' = t (1 + a) with |a| <= gamma_L = L u / (1 - L u).
+    Then, to first order in u:
+      q = t' / K (one rounding), + eps (eps itself rounded to fp32, one
+      rounding of the add):                       gamma_L + 2u
+      s = sqrt(.) halves that and rounds once:    gamma_L / 2 + 2u
+      r = 1 / s:                                  gamma_L / 2 + 3u
+      (x * r) * g, two roundings:                 gamma_L / 2 + 5u
+    The factor 1.001 covers the second-order terms (products of two or more
+    of the u-sized errors, below 1e-12 here)."""
+    L = 8 * math.ceil(K / 1024) + 8
+    gamma = L * U / (1 - L * U)
+    return 1.001 * (gamma / 2 + 5 * U)
+
+
+def bf16_rne(v: np.ndarray) -> np.ndarray:
+    """Nearest bf16 (ties to even) of float64 values, rounded once (no fp32
+    step): v = m * 2^e with 0.5 <= |m| < 1, and bf16 keeps 8 significant bits."""
+    m, e = np.frexp(v)
+    return np.ldexp(np.round(m * 256.0) / 256.0, e)   # np.round: ties to even
+
+
+def check_xn(xn_bits, ref, K):
+    """xn_bits (bf16) against the unrounded fp64 reference values: the nearest
+    bf16, or its neighbour when the reference lies within xn_allowance(K)
+    (relative) of the midpoint between them."""
     got = bf16_to_f64(xn_bits)
-    t = torch.from_numpy(ref.astype(np.float32))
-    # nearest bf16 of the fp64 value (round to fp32 first cannot move it across a bf16 midpoint
-    # unless the value is within 2^-24 relative of it, which the allowance below covers)
-    rn = bf16_to_f64(t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    rn = bf16_rne(ref)
     ok = got == rn
     if not ok.all():
-        # a bf16 ulp at |v|, and the distance of v from the midpoint between got and rn
         bad = ~ok
         v = ref[bad]
         mid = 0.5 * (got[bad] + rn[bad])
-        near_mid = np.abs(v - mid) <= 1e-5 * np.abs(v)
+        near_mid = np.abs(v - mid) <= xn_allowance(K) * np.abs(v)
+        # got is the other neighbour: one bf16 step (2^-7 of the binade) away
         adjacent = np.abs(got[bad] - rn[bad]) <= np.abs(v) * 2.0 ** -7 * 1.0001
         assert (near_mid & adjacent).all(), f"{int((~(near_mid & adjacent)).sum())} XN elements off"
     return float((~ok).mean())
@@ -81,7 +115,7 @@ def run_norm(case, X, W, G, eps=1e-6, ldx=None, pdl=None):
 def test_qb_projection_with_norm(M):
     case, X, W, G = make_case(M, 24576, 1536, seed=3000 + M)
     xn_bits, y = run_norm(case, X, W, G)
-    frac = check_xn(xn_bits, oracle.rmsnorm(X, G, 1e-6, M, 1536))
+    frac = check_xn(xn_bits, oracle.rmsnorm(X, G, 1e-6, M, 1536), 1536)
     assert frac < 1e-3
     yref, A = oracle.gemm(xn_bits, W, M, 24576, 1536)
     check_parity(y, yref, A, case.name)
@@ -99,7 +133,7 @@ def test_norm_reaches_every_backend(backend):
         xa, ya = run_norm(case, X, W, G, pdl=1)
         xb, yb = run_norm(case, X, W, G, pdl=0)
     assert np.array_equal(xa, xb) and np.array_equal(ya.view(np.uint32), yb.view(np.uint32))
-    check_xn(xa, oracle.rmsnorm(X, G, 1e-6, 8, 1536))
+    check_xn(xa, oracle.rmsnorm(X, G, 1e-6, 8, 1536), 1536)
     yref, A = oracle.gemm(xa, W, 8, 2112, 1536)
     check_parity(ya, yref, A, f"norm + {backend}")
 
@@ -108,7 +142,7 @@ def test_norm_strided_x_eps_and_ragged_k():
     case, X, W, G = make_case(5, 130, 1000, seed=3200)
     for eps in (0.0, 1e-6, 0.5):
         xn_bits, y = run_norm(case, X, W, G, eps=eps, ldx=1003)
-        check_xn(xn_bits, oracle.rmsnorm(X, G, eps, 5, 1000))
+        check_xn(xn_bits, oracle.rmsnorm(X, G, eps, 5, 1000), 1000)
         yref, A = oracle.gemm(xn_bits, W, 5, 130, 1000)
         check_parity(y, yref, A, f"eps={eps}")
 
