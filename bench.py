@@ -2,8 +2,12 @@
 """Benchmark of the GB300 skinny BF16 GEMM (Y[M,N] = X[M,K] . W[N,K]^T, fp32 out).
 
 One *step* is one pass of the whole hot path over one batch of the workload:
-every call of the workload (default ``dotprod``: M in {1,2,3,4} x (K,N) in
-{(7168,256),(7168,384),(2880,128)}, 12 calls), each through the C ABI.
+every call of the workload, each through the C ABI.  The default workload is
+the decode projections (M in {1,2,3,8,16} x (N,K) in {(2112,7168),
+(24576,1536),(7168,14336)}, ldy = N+64, 15 calls: 30-206 MB weights, where the
+bandwidth roofline applies).  The router workloads (M=1 K=7168 N=256; the
+dot-product regime M 1-4; the split-K regime M 5-16) are timed the same way
+in the same run and reported under ``per_config``.
 
 Timing rules followed here:
 * W is a weight resident in HBM; every step reads a different replica of the
@@ -13,8 +17,10 @@ Timing rules followed here:
   (as a decode step is); W untimed warm-up steps, then exactly K timed steps
   bracketed by a barrier and cuda synchronize, timed with CUDA events on the
   launching stream; the max over ranks is reported.
-* per-launch durations for the roofline come from CUDA-event pairs around each
-  call in a second pass over the same rotating replicas.
+* per-launch durations for the roofline: for each call shape, a CUDA graph of
+  back-to-back launches over rotating W copies (L2-cold), PDL off, CUDA events
+  around whole replays; cross-checked by a flush kernel (a write of 2x the L2
+  size) before each isolated call, with a CUDA-event pair around the call alone.
 * clocks are sampled with nvidia-smi while the GPU is under load.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
@@ -65,7 +71,8 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
-    p.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="dotprod")
+    p.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="projection")
+    p.add_argument("--no-per-config", action="store_true", help="skip the router workloads' figures")
     p.add_argument("--pdl", type=int, choices=[0, 1], default=1)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget (s)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -241,6 +248,163 @@ def launch_step(sk, cases, rep, stream_handle, counter=None):
             counter[0] += 1
 
 
+class Workload:
+    """A workload's device replicas (together > 2x L2, so every call reads its W
+    from HBM), its plans, and one CUDA graph per replica of one whole step."""
+
+    def __init__(self, sk, torch, cases, l2, stream):
+        self.cases = cases
+        self.host_inputs = [si.make_inputs(c) for c in cases]
+        self.step_bytes = sum(c.algorithmic_bytes for c in cases)
+        self.step_w_bytes = sum(2 * c.N * c.K for c in cases)
+        self.n_rep = max(1, math.ceil(2 * l2 / self.step_w_bytes))
+        self.reps = [Replica(cases, self.host_inputs, torch)]
+        for _ in range(self.n_rep - 1):
+            self.reps.append(Replica(cases, self.host_inputs, torch, src=self.reps[0]))
+        self.pool_mb = self.n_rep * self.step_w_bytes / 1e6
+        self.plans = [sk.skinny_query_plan(x.data_ptr(), c.lx, w.data_ptr(), c.lw, y.data_ptr(), c.ly, c.M, c.N, c.K)
+                      for c, x, w, y in zip(cases, self.reps[0].x, self.reps[0].w, self.reps[0].y)]
+        sh = stream.cuda_stream
+        with torch.cuda.stream(stream):        # eager warm-up: first launches, module load
+            for r in self.reps:
+                launch_step(sk, cases, r, sh)
+        torch.cuda.synchronize()
+        self.graphs = []
+        for r in self.reps:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                launch_step(sk, cases, r, sh)
+            self.graphs.append(g)
+        torch.cuda.synchronize()
+
+    def replay(self, i):
+        self.graphs[i % self.n_rep].replay()
+
+
+def time_steps(torch, stream, wl, steps, warmup, soak_s=0.0, use_barrier=True):
+    """Exactly `steps` graph replays (rotating replicas) after `warmup` untimed
+    ones, bracketed by a barrier and a synchronize; seconds."""
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            wl.replay(i)
+        t_end = time.time() + soak_s          # keep the GPU loaded so the clock samples see it
+        i = 0
+        while time.time() < t_end:
+            for _ in range(50):
+                wl.replay(i)
+                i += 1
+            stream.synchronize()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if use_barrier:
+        barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(steps):
+            wl.replay(i)
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    if use_barrier:
+        barrier()
+    return ev0.elapsed_time(ev1) / 1e3
+
+
+def time_warm(torch, stream, wl, steps):
+    """L2-warm: the same replica every step; us per call."""
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            wl.graphs[0].replay()
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0.record(stream)
+        for _ in range(steps):
+            wl.graphs[0].replay()
+        w1.record(stream)
+    torch.cuda.synchronize()
+    return w0.elapsed_time(w1) * 1e3 / (steps * len(wl.cases))
+
+
+def time_isolated(sk, torch, stream, wl, l2, iters):
+    """Per call shape: a CUDA graph of back-to-back launches over enough copies
+    of that shape's W to exceed 2x L2 (L2-cold), PDL off, CUDA events around
+    whole replays; us per launch."""
+    out = []
+    sh = stream.cuda_stream
+    with sk.options(pdl=0):
+        for j, c in enumerate(wl.cases):
+            n_j = max(8, math.ceil(2 * l2 / (2 * c.N * c.K)))
+            ws = [wl.reps[i % wl.n_rep].w[j] if i < wl.n_rep else wl.reps[0].w[j].clone() for i in range(n_j)]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i, w in enumerate(ws):
+                    r = wl.reps[i % wl.n_rep]
+                    st = sk.skinny_gemm_bf16(r.x[j].data_ptr(), c.lx, w.data_ptr(), c.lw, r.y[j].data_ptr(),
+                                             c.ly, c.M, c.N, c.K, sh)
+                    if st != sk.SKINNY_OK:
+                        raise sk.SkinnyError(st, c.name)
+            with torch.cuda.stream(stream):
+                g.replay()
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                for _ in range(iters):
+                    g.replay()
+                b_.record(stream)
+            torch.cuda.synchronize()
+            out.append(a_.elapsed_time(b_) * 1e3 / (iters * n_j))
+            del g, ws
+    return out
+
+
+def time_flushed(sk, torch, stream, wl, l2, samples):
+    """Cross-check of the L2-cold figures: before each call a flush kernel
+    writes a buffer of 2x the L2 size (outside the event pair), then a CUDA
+    event pair brackets the call alone; PDL off.  (median, p10, p90) us per
+    call shape."""
+    flush = torch.empty(max(1, 2 * l2 // 4), dtype=torch.float32, device="cuda")
+    sh = stream.cuda_stream
+    out = []
+    with sk.options(pdl=0):
+        for j, c in enumerate(wl.cases):
+            r = wl.reps[0]
+            evs = []
+            with torch.cuda.stream(stream):
+                for s in range(samples + 2):
+                    flush.fill_(float(s))
+                    a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a_.record(stream)
+                    st = sk.skinny_gemm_bf16(r.x[j].data_ptr(), c.lx, r.w[j].data_ptr(), c.lw, r.y[j].data_ptr(),
+                                             c.ly, c.M, c.N, c.K, sh)
+                    b_.record(stream)
+                    if st != sk.SKINNY_OK:
+                        raise sk.SkinnyError(st, c.name)
+                    if s >= 2:
+                        evs.append((a_, b_))
+            torch.cuda.synchronize()
+            t = sorted(a_.elapsed_time(b_) * 1e3 for a_, b_ in evs)
+            out.append((statistics.median(t), t[len(t) // 10], t[(9 * len(t)) // 10]))
+    del flush
+    return out
+
+
+def family_of(plan):
+    return {1: "dotmma" if plan["consumer"] == 2 else "dotprod", 2: "splitk", 3: "stream",
+            4: "tmem_gemm"}[plan["backend"]]
+
+
+def shape_rows(wl, iso, peak, flushed=None):
+    rows = []
+    for j, (c, p, us) in enumerate(zip(wl.cases, wl.plans, iso)):
+        row = {"M": c.M, "N": c.N, "K": c.K, "kernel": family_of(p), "consumer": p["consumer"],
+               "split_k": p["split_k"], "block_n": p["block_n"], "grid": [p["grid_x"], p["grid_y"]],
+               "us_per_launch": round(us, 3), "gbs": round(c.algorithmic_bytes / us / 1e3, 1),
+               "frac_of_peak": round(c.algorithmic_bytes / us / 1e3 / peak, 4)}
+        if flushed is not None:
+            med, p10, p90 = flushed[j]
+            row["flush_us"] = {"median": round(med, 3), "p10": round(p10, 3), "p90": round(p90, 3)}
+        rows.append(row)
+    return rows
+
+
 def run_native(args):
     import torch
     import torch.distributed as dist
@@ -254,112 +418,47 @@ def run_native(args):
     if st != sk.SKINNY_OK:
         raise sk.SkinnyError(st, "skinny_init")
     sk.skinny_set_option(sk.SKINNY_OPT_PDL, args.pdl)
-
-    cases = select_cases(args)
-    host_inputs = [si.make_inputs(c) for c in cases]
-    step_bytes = sum(c.algorithmic_bytes for c in cases)
-    step_w_bytes = sum(2 * c.N * c.K for c in cases)
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
-    n_rep = max(1, math.ceil(2 * l2 / step_w_bytes))
-    reps = [Replica(cases, host_inputs, torch)]
-    for _ in range(n_rep - 1):
-        reps.append(Replica(cases, host_inputs, torch, src=reps[0]))
-    pool_mb = n_rep * step_w_bytes / 1e6
-    plans = []
-    for c, x, w, y in zip(cases, reps[0].x, reps[0].w, reps[0].y):
-        p = sk.skinny_query_plan(x.data_ptr(), c.lx, w.data_ptr(), c.lw, y.data_ptr(), c.ly, c.M, c.N, c.K)
-        plans.append(p)
-
     stream = torch.cuda.Stream()
     sh = stream.cuda_stream
-    # eager warm-up (first launches, module load), then capture one graph per replica
-    with torch.cuda.stream(stream):
-        for r in reps:
-            launch_step(sk, cases, r, sh)
-    torch.cuda.synchronize()
-    graphs = []
-    for r in reps:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            launch_step(sk, cases, r, sh)
-        graphs.append(g)
-    torch.cuda.synchronize()
+    peak, _ = hbm_peak()
+
+    cases = select_cases(args)
+    wl = Workload(sk, torch, cases, l2, stream)
 
     clocks = ClockSampler(local) if not (args.no_clocks or args.profile_mode) else None
     if clocks:
         clocks.start()
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            graphs[i % n_rep].replay()
-        # keep the GPU loaded ~1.5 s so the clock samples see it under load
-        t_end = time.time() + (1.5 if clocks else 0.0)
-        i = 0
-        while time.time() < t_end:
-            for _ in range(50):
-                graphs[i % n_rep].replay()
-                i += 1
-            stream.synchronize()
-    torch.cuda.synchronize()
-
     # ---- timed region: exactly `steps` graph replays, L2-cold (rotating replicas)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for i in range(args.steps):
-            graphs[i % n_rep].replay()
-        ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    elapsed = ev0.elapsed_time(ev1) / 1e3
+    elapsed = time_steps(torch, stream, wl, args.steps, args.warmup, soak_s=1.5 if clocks else 0.0)
     clock_summary = clocks.stop() if clocks else None
     launches = args.steps * len(cases)
+    warm_us_per_call = time_warm(torch, stream, wl, 3 if args.profile_mode else max(50, min(args.steps, 2000)))
+    per_launch = time_isolated(sk, torch, stream, wl, l2, 2 if args.profile_mode else 10)
+    flushed = None if args.profile_mode else time_flushed(sk, torch, stream, wl, l2, 100)
 
-    # ---- L2-warm: same replica every step
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            graphs[0].replay()
-        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        warm_steps = 3 if args.profile_mode else max(50, min(args.steps, 2000))
-        w0.record(stream)
-        for _ in range(warm_steps):
-            graphs[0].replay()
-        w1.record(stream)
-    torch.cuda.synchronize()
-    warm_us_per_call = w0.elapsed_time(w1) * 1e3 / (warm_steps * len(cases))
-
-    # ---- per-launch durations: for each call shape, a CUDA graph of n_rep
-    # back-to-back launches over the rotating W replicas (L2-cold), PDL off so
-    # launches do not overlap; CUDA events around whole replays (the event
-    # clock is too coarse for a single few-microsecond launch).
-    per_launch = []
-    sk.skinny_set_option(sk.SKINNY_OPT_PDL, 0)
-    iters = 2 if args.profile_mode else 10
-    for j, c in enumerate(cases):
-        # enough copies of this call's W alone to exceed 2x L2
-        n_j = max(8, math.ceil(2 * l2 / (2 * c.N * c.K)))
-        ws = [reps[i % n_rep].w[j] if i < n_rep else reps[0].w[j].clone() for i in range(n_j)]
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i, w in enumerate(ws):
-                r = reps[i % n_rep]
-                st = sk.skinny_gemm_bf16(r.x[j].data_ptr(), c.lx, w.data_ptr(), c.lw, r.y[j].data_ptr(),
-                                         c.ly, c.M, c.N, c.K, sh)
-                if st != sk.SKINNY_OK:
-                    raise sk.SkinnyError(st, c.name)
-        with torch.cuda.stream(stream):
-            g.replay()
-            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a_.record(stream)
-            for _ in range(iters):
-                g.replay()
-            b_.record(stream)
-        torch.cuda.synchronize()
-        per_launch.append(a_.elapsed_time(b_) * 1e3 / (iters * n_j))   # us
-        del g, ws
-    sk.skinny_set_option(sk.SKINNY_OPT_PDL, args.pdl)
-    launches += 0  # the per-launch pass is outside the timed region
+    # ---- the router workloads, timed the same way (outside the headline's timed region)
+    per_config = None
+    if not (args.profile_mode or args.no_per_config):
+        per_config = {}
+        for name, tag in (("router_small", "c0"), ("dotprod", "c1"), ("splitk", "c2")):
+            if name == args.workload:
+                continue
+            wc = Workload(sk, torch, si.workload(name), l2, stream)
+            k = min(args.steps, 1000)
+            el = time_steps(torch, stream, wc, k, max(3, min(args.warmup, 20)), use_barrier=False)
+            iso = time_isolated(sk, torch, stream, wc, l2, 10)
+            per_config[tag] = {
+                "workload": WORKLOAD_DESC[name], "calls_per_step": len(wc.cases), "steps": k,
+                "us_per_call": round(el / k / len(wc.cases) * 1e6, 3),
+                "gbs": round(wc.step_bytes * k / el / 1e9, 1),
+                "us_per_call_l2_warm": round(time_warm(torch, stream, wc, 200), 3),
+                "l2": f"cold: {wc.n_rep} rotating replicas ({wc.pool_mb:.0f} MB)",
+                "isolated_us_max": round(max(iso), 3),
+                "per_shape": shape_rows(wc, iso, peak),
+            }
+            del wc
+            torch.cuda.synchronize()
 
     # ---- PDL chain: one CUDA graph of 64 back-to-back calls M=4, K=7168,
     # N=256 (same X and W, so L2-warm; a Y per call), total us per replay with
@@ -374,14 +473,14 @@ def run_native(args):
         chain = {"calls": 64, "M": cc.M, "N": cc.N, "K": cc.K,
                  "method": "one CUDA graph of the 64 calls, mean over 20 replays after 2 untimed ones"}
         for pdl in (1, 0):
-            sk.skinny_set_option(sk.SKINNY_OPT_PDL, pdl)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for y in ycs:
-                    st = sk.skinny_gemm_bf16(xc.data_ptr(), cc.K, wc.data_ptr(), cc.K, y.data_ptr(), cc.N,
-                                             cc.M, cc.N, cc.K, sh)
-                    if st != sk.SKINNY_OK:
-                        raise sk.SkinnyError(st, cc.name)
+            with sk.options(pdl=pdl):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for y in ycs:
+                        st = sk.skinny_gemm_bf16(xc.data_ptr(), cc.K, wc.data_ptr(), cc.K, y.data_ptr(), cc.N,
+                                                 cc.M, cc.N, cc.K, sh)
+                        if st != sk.SKINNY_OK:
+                            raise sk.SkinnyError(st, cc.name)
             with torch.cuda.stream(stream):
                 g.replay()
                 g.replay()
@@ -393,7 +492,6 @@ def run_native(args):
             torch.cuda.synchronize()
             chain["us_total_pdl_on" if pdl else "us_total_pdl_off"] = round(c0.elapsed_time(c1) * 1e3 / 20, 2)
             del g
-        sk.skinny_set_option(sk.SKINNY_OPT_PDL, args.pdl)
 
     # ---- e2e: host -> device X, the calls, device -> host Y, per step, through the C ABI
     h2d = sum(2 * c.M * c.K for c in cases)
@@ -401,14 +499,14 @@ def run_native(args):
     x_host = torch.empty(h2d // 2, dtype=torch.int16).pin_memory()
     y_host = torch.empty(sum(c.M * c.ly for c in cases), dtype=torch.float32).pin_memory()
     off = 0
-    for c, (X, _) in zip(cases, host_inputs):
+    for c, (X, _) in zip(cases, wl.host_inputs):
         x_host[off:off + c.M * c.K] = torch.from_numpy(X.reshape(-1).view(np.int16).copy())
         off += c.M * c.K
     x_dev = torch.empty_like(x_host, device="cuda")
     # zeros like the replicas' Y, so the never-written gaps of a strided Y compare equal
     y_dev = torch.zeros(y_host.numel(), dtype=torch.float32, device="cuda")
     e2e_graphs = []
-    for r in reps:
+    for r in wl.reps:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             x_dev.copy_(x_host, non_blocking=True)
@@ -424,30 +522,29 @@ def run_native(args):
         e2e_graphs.append(g)
     with torch.cuda.stream(stream):
         for i in range(max(3, args.warmup)):
-            e2e_graphs[i % n_rep].replay()
+            e2e_graphs[i % wl.n_rep].replay()
     torch.cuda.synchronize()
     barrier()
-    t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for i in range(args.steps):
-            e2e_graphs[i % n_rep].replay()
+            e2e_graphs[i % wl.n_rep].replay()
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_elapsed = e0.elapsed_time(e1) / 1e3
     barrier()
     # correctness spot check of the e2e output against the device-only path
-    ref_y = torch.cat([y.view(-1) for y in reps[(args.steps - 1) % n_rep].y]).cpu()
+    ref_y = torch.cat([y.view(-1) for y in wl.reps[(args.steps - 1) % wl.n_rep].y]).cpu()
     if not torch.equal(ref_y, y_host):
         raise RuntimeError("e2e output differs from the device-resident output")
 
-    elapsed_max, units = aggregate(elapsed, float(step_bytes * args.steps))
+    elapsed_max, units = aggregate(elapsed, float(wl.step_bytes * args.steps))
     e2e_max, _ = aggregate(e2e_elapsed, 0.0)
-    return dict(cases=cases, plans=plans, elapsed=elapsed_max, units=units, launches=launches,
-                warm_us_per_call=warm_us_per_call, per_launch=per_launch, clocks=clock_summary,
-                e2e_elapsed=e2e_max, h2d=h2d, d2h=d2h, pool_mb=pool_mb, n_rep=n_rep, l2=l2,
-                step_bytes=step_bytes, world=world, rank=rank, chain=chain)
+    return dict(cases=cases, wl=wl, elapsed=elapsed_max, units=units, launches=launches,
+                warm_us_per_call=warm_us_per_call, per_launch=per_launch, flushed=flushed, clocks=clock_summary,
+                e2e_elapsed=e2e_max, h2d=h2d, d2h=d2h, l2=l2, world=world, rank=rank, chain=chain,
+                per_config=per_config, peak=peak)
 
 
 # ------------------------------------------------------------------ oracle timing
@@ -519,8 +616,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s_per_step * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "us_per_call": round(us_per_call, 2),
-        "config": {"workload": WORKLOAD_DESC[args.workload], "calls_per_step": len(cases),
-                   "parallelism": "single host thread"},
+        "config": line_config(args, len(cases)),
+        "method": {"parallelism": "single host thread"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -530,6 +627,62 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ main
 
+L2_NOTE = "cold: every call reads its W from DRAM (rotating W replicas larger than 2x the L2 size)"
+
+
+def line_config(args, ncalls):
+    """The config object, identical in both arms."""
+    return {"workload": WORKLOAD_DESC[args.workload], "calls_per_step": ncalls, "l2": L2_NOTE}
+
+
+def roofline_of(wl, per_launch, peak, peak_src, workload):
+    """The dominant kernel family (largest total isolated-launch time) of the
+    workload: its algorithmic bytes per launch over its mean launch time."""
+    fam_time, fam_bytes, fam_n = {}, {}, {}
+    for c, p, us in zip(wl.cases, wl.plans, per_launch):
+        fam = family_of(p)
+        fam_time[fam] = fam_time.get(fam, 0.0) + us
+        fam_bytes[fam] = fam_bytes.get(fam, 0.0) + c.algorithmic_bytes
+        fam_n[fam] = fam_n.get(fam, 0) + 1
+    dom = max(fam_time, key=fam_time.get)
+    achieved = fam_bytes[dom] / (fam_time[dom] * 1e-6) / 1e9
+    return {"bound": "hbm", "kernel": f"{dom}_kernel", "achieved": round(achieved, 1),
+            "peak": round(peak, 1), "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "peak_source": peak_src,
+            "traffic": committed_traffic(dom, workload),
+            "time_share": round(fam_time[dom] / sum(fam_time.values()), 3),
+            "launches_per_step": fam_n[dom],
+            "method": "per call shape: CUDA graph of back-to-back launches over rotating W copies (L2-cold), "
+                      "PDL off, CUDA events around the replays; achieved = the family's algorithmic bytes "
+                      "(2NK + 2MK + 4MN per launch) over its launch time",
+            "avg_launch_us": round(fam_time[dom] / fam_n[dom], 3),
+            "algorithmic_bytes_per_launch": round(fam_bytes[dom] / fam_n[dom])}
+
+
+def cpu_baselines(args, cases, per_config):
+    """The oracle (single host thread, and split over all host threads) on
+    bounded samples of the headline workload; single-thread ms per call for
+    every router config too."""
+    gbs, s_step, sample = oracle_step_sample(cases, args.cpu_seconds)
+    cpu = {"value": round(gbs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+           "ms_per_call": round(s_step / len(cases) * 1e3, 3)}
+    cpu_threads = None
+    nthr = os.cpu_count() or 1
+    if nthr > 1:
+        gbs, s_step, sample = oracle_step_sample(cases, args.cpu_seconds, threads=nthr)
+        cpu_threads = {"value": round(gbs / 1e9, 4), "unit": "GB/s", "cores": nthr, "kind": "oracle",
+                       "sample": sample, "ms_per_call": round(s_step / len(cases) * 1e3, 3)}
+    for tag, name in (("c0", "router_small"), ("c1", "dotprod"), ("c2", "splitk")):
+        if per_config is None or tag not in per_config:
+            continue
+        cc = si.workload(name)
+        gbs, s_step, sample = oracle_step_sample(cc, max(1.0, args.cpu_seconds / 4))
+        per_config[tag]["cpu_baseline"] = {"value": round(gbs / 1e9, 4), "unit": "GB/s", "cores": 1,
+                                           "kind": "oracle", "sample": sample,
+                                           "ms_per_call": round(s_step / len(cc) * 1e3, 3)}
+    return cpu, cpu_threads
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -538,57 +691,27 @@ def main(argv=None):
     r = run_native(args)
     if r["rank"] != 0:
         return 0
-    cases = r["cases"]
+    wl = r["wl"]
+    cases = wl.cases
     n = r["world"]
     step_s = r["elapsed"] / args.steps
     value_gbs = r["units"] / r["elapsed"] / 1e9
     us_per_call = step_s / len(cases) * 1e6
     peak, peak_src = hbm_peak()
-
-    # dominant kernel family by total per-launch time
-    fam_time, fam_bytes, fam_n = {}, {}, {}
-    per_shape = []
-    for c, p, us in zip(cases, r["plans"], r["per_launch"]):
-        fam = {1: "dotmma" if p["consumer"] == 2 else "dotprod", 2: "splitk", 3: "stream",
-               4: "tmem_gemm"}[p["backend"]]
-        fam_time[fam] = fam_time.get(fam, 0.0) + us
-        fam_bytes[fam] = fam_bytes.get(fam, 0.0) + c.algorithmic_bytes
-        fam_n[fam] = fam_n.get(fam, 0) + 1
-        per_shape.append({"M": c.M, "N": c.N, "K": c.K, "kernel": fam, "consumer": p["consumer"],
-                          "split_k": p["split_k"], "block_n": p["block_n"], "grid": [p["grid_x"], p["grid_y"]],
-                          "us_per_launch": round(us, 3), "gbs": round(c.algorithmic_bytes / us / 1e3, 1),
-                          "frac_of_peak": round(c.algorithmic_bytes / us / 1e3 / peak, 4)})
-    dom = max(fam_time, key=fam_time.get)
-    total_t = sum(fam_time.values())
-    achieved = fam_bytes[dom] / (fam_time[dom] * 1e-6) / 1e9
-    traffic = committed_traffic(dom, args.workload)
-    roofline = {"bound": "hbm", "kernel": f"skinny_{dom}_kernel", "achieved": round(achieved, 1),
-                "peak": round(peak, 1), "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "peak_source": peak_src,
-                "traffic": traffic, "time_share": round(fam_time[dom] / total_t, 3),
-                "method": "per call shape: CUDA graph of back-to-back launches over rotating W copies (L2-cold), "
-                          "PDL off, CUDA events around the replays",
-                "avg_launch_us": round(fam_time[dom] / fam_n[dom], 3),
-                "algorithmic_bytes_per_launch": round(fam_bytes[dom] / fam_n[dom])}
+    roofline = roofline_of(wl, r["per_launch"], peak, peak_src, args.workload)
 
     cpu = cpu_threads = None
     if not (args.no_cpu_baseline or args.profile_mode):
-        gbs, s_step, sample = oracle_step_sample(cases, args.cpu_seconds)
-        cpu = {"value": round(gbs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample}
-        nthr = os.cpu_count() or 1
-        if nthr > 1:
-            gbs, s_step, sample = oracle_step_sample(cases, args.cpu_seconds, threads=nthr)
-            cpu_threads = {"value": round(gbs / 1e9, 4), "unit": "GB/s", "cores": nthr, "kind": "oracle",
-                           "sample": sample}
+        cpu, cpu_threads = cpu_baselines(args, cases, r["per_config"])
 
-    e2e_gbs = r["step_bytes"] * args.steps * n / r["e2e_elapsed"] / 1e9
+    e2e_gbs = wl.step_bytes * args.steps * n / r["e2e_elapsed"] / 1e9
     line = {
         "metric": METRIC, "value": round(value_gbs, 2), "unit": "GB/s", "n_gpus": n,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC[args.workload], "calls_per_step": len(cases),
-                   "l2": f"cold: {r['n_rep']} rotating replicas of every W ({r['pool_mb']:.0f} MB > 2x L2 "
+        "config": line_config(args, len(cases)),
+        "method": {"l2": f"{wl.n_rep} rotating replicas of every W ({wl.pool_mb:.0f} MB > 2x L2 "
                          f"{r['l2'] / 1e6:.0f} MB)",
                    "graph": "each step replayed from a CUDA graph of the C-ABI calls",
                    "pdl": args.pdl, "parallelism": f"replicas x{n}" if n > 1 else "single GPU"},
@@ -605,7 +728,11 @@ def main(argv=None):
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
         "pdl_chain": r["chain"],
-        "per_shape": per_shape,
+        "per_shape": shape_rows(wl, r["per_launch"], peak, r["flushed"]),
+        "flush_method": None if r["flushed"] is None else
+        "per call shape: 100 isolated calls, each after a flush kernel writing 2x L2 (outside the event pair), "
+        "a CUDA-event pair around the call alone, PDL off; median / p10 / p90",
+        "per_config": r["per_config"],
     }
     print(json.dumps(line), flush=True)
     return 0
