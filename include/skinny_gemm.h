@@ -7,8 +7,15 @@
  * [experts, hidden] matrix or a decode projection's [out, in] matrix), both
  * row-major with row strides ldx / ldw in elements; Y is [M, N] fp32, row
  * stride ldy >= N (strided output, the gaps n >= N are never written).
- * Products and sums are fp32 (fused multiply-add, round to nearest); the
- * output is fp32.
+ * Accumulation is fp32.  The CUDA-core kernels round every multiply-add to
+ * nearest (fused multiply-add).  The tensor-core kernels sum short chains
+ * inside the tensor core, whose fp32 accumulation is not rounded to nearest
+ * per add (measured biased on same-sign data), so those chains are bounded
+ * (at most 4 k16 steps per mma.sync register sum, at most 16 MMAs of K = 16
+ * per tcgen05 tensor-memory accumulator) and the chain sums are added with
+ * round-to-nearest fp32 adds.  Every kernel keeps |y - y_exact| within
+ * 1e-5 * sum_k |x * w| + 1e-6, same-sign operands at K = 14336 included.
+ * The output is fp32.
  *
  * Operation defined by: "[Perf][Feat] Add generic cuteDSL LL BF16 router
  * (GEMM)" (vllm PR #42562 report), section "Implementation breakdown"
@@ -79,11 +86,13 @@ typedef enum {
     SKINNY_BACKEND_STREAM = 3,      /* one CTA per SM, whole K per 16-row tile, K-outer: X and W
                                        stream through one ring chunk by chunk (large weights;
                                        needs 16-byte aligned X and W rows, K % 16 == 0, M <= 16) */
-    SKINNY_BACKEND_TCGEN05 = 4      /* 128 W rows per CTA on the fifth-generation tensor cores
-                                       (tcgen05.mma, accumulator in tensor memory), W and X boxes by
-                                       tensor-map TMA, K split over a cluster of split_k CTAs
-                                       (1, 2, 4 or 8); needs 16-byte aligned X and W rows
-                                       (pointers, ldx and ldw); any K >= 1, M <= 64 */
+    SKINNY_BACKEND_TCGEN05 = 4      /* the fifth-generation tensor cores (tcgen05.mma into tensor
+                                       memory, drained into fp32 registers every <= 16 MMAs): W rows
+                                       in grid_y balanced ranges of 8-row groups, tiles of up to
+                                       block_n = 64 / 128 rows, K split over a cluster of split_k
+                                       CTAs (1, 2, 4 or 8), W and X boxes by tensor-map TMA; needs
+                                       16-byte aligned X and W rows (pointers, ldx and ldw);
+                                       any K >= 1, M <= 64 */
 } skinny_backend_t;
 
 typedef enum {
@@ -98,14 +107,18 @@ typedef struct {
     int backend;       /* skinny_backend_t actually used */
     int consumer;      /* skinny_consumer_t actually used (FMA or MMA, for either backend) */
     int vec_elems;     /* W load width in bf16 elements: 8 (128-bit), 4, 2 or 1 */
-    int block_n;       /* output columns (rows of W) per CTA tile */
+    int block_n;       /* output columns (rows of W) per CTA tile; tcgen05: the MMA's M (64 or 128),
+                          the tile holding up to that many rows */
     int split_k;       /* CTAs per cluster along K (1 = no cluster) */
-    int stages;        /* shared-memory ring depth (split-K) */
-    int stage_k;       /* split-K: K elements of each W row per ring stage (64..2048, multiple of 64) */
+    int stages;        /* shared-memory ring depth (split-K, streaming, tcgen05) */
+    int stage_k;       /* K elements of each W row per ring stage (split-K and streaming 64..2048,
+                          tcgen05 64..256; multiple of 64) */
     int k_chunk;       /* dot-product: K elements of X staged in shared memory at a time;
-                          split-K: K elements per CTA (the cluster rank's slice) */
-    int grid_x;        /* grid dimensions launched; split-K: grid_x = split_k CTAs per cluster, */
-    int grid_y;        /* grid_y = clusters, each looping over 16-row tiles tile = y, y + grid_y, ... */
+                          split-K, tcgen05: K elements per CTA (the cluster rank's slice) */
+    int grid_x;        /* grid dimensions launched; split-K, tcgen05: grid_x = split_k CTAs per cluster, */
+    int grid_y;        /* split-K: grid_y clusters, each looping over 16-row tiles y, y + grid_y, ...;
+                          tcgen05: grid_y row ranges (clusters), range c holding the 8-row groups
+                          [c * G / grid_y, (c + 1) * G / grid_y), G = ceil(N / 8) */
     int threads;       /* threads per CTA */
     int smem_bytes;    /* dynamic shared memory per CTA */
     int pdl;           /* 1 if launched with programmatic dependent launch */
@@ -124,11 +137,14 @@ typedef enum {
                                         which exercises the timeout path without any real hang */
     SKINNY_OPT_LOG = 8,              /* 1: print the plan chosen for each new call shape to stderr
                                         (default: env SKINNY_LOG) */
-    SKINNY_OPT_FORCE_CLUSTERS = 9,   /* split-K: 0 = dispatcher, else the number of (persistent)
-                                        clusters, each looping over row tiles (tests / tuning only) */
-    SKINNY_OPT_FORCE_STAGE_K = 10    /* split-K, streaming, tcgen05: 0 = dispatcher, else K elements
+    SKINNY_OPT_FORCE_CLUSTERS = 9,   /* 0 = dispatcher; split-K: the number of (persistent) clusters,
+                                        each looping over row tiles; tcgen05: the number of row
+                                        ranges (grid_y) (tests / tuning only) */
+    SKINNY_OPT_FORCE_STAGE_K = 10,   /* split-K, streaming, tcgen05: 0 = dispatcher, else K elements
                                         per ring stage (multiple of 64; split-K and streaming
                                         64..2048, tcgen05 64..256; tests / tuning only) */
+    SKINNY_OPT_FUSE_NORM = 11        /* 1 (default): skinny_rmsnorm_gemm_bf16 runs the norm inside the
+                                        tcgen05 GEMM when its plan allows; 0: always two launches */
 } skinny_option_t;
 
 /*
@@ -239,13 +255,18 @@ SKINNY_API skinny_status_t skinny_plan_for_f32w(const uint16_t *X, int ldx, cons
  *   W, Y, M (1..64), N, K, stream: as skinny_gemm_bf16 with X = XN.  K == 0 gives Y = 0 and
  *          leaves XN untouched.
  *
- * Two launches on `stream`: a norm kernel (one CTA per token; fixed-order
- * fp32 sum of squares, IEEE sqrt and division, one bf16 rounding per element;
- * bit-identical run to run) and then the GEMM.  With PDL on, the norm kernel
- * lets the GEMM launch at once, so the GEMM streams W while the norm runs and
- * reads XN after waiting for it: the norm is a prologue of the GEMM's
- * critical path, not a separate round trip.  Every argument is checked and
- * the GEMM's plan made before anything is launched.
+ * One launch when the GEMM's plan is tcgen05 and M <= 16 (and the option
+ * SKINNY_OPT_FUSE_NORM is on): every CTA of the GEMM computes the r_m of all
+ * tokens from X itself (the sum of squares in the same fixed order as the
+ * norm kernel below, so the same bits), normalises the X of its own K slice
+ * into shared memory and streams W meanwhile; the CTAs of the first row range
+ * also store XN.  Otherwise two launches on `stream`: a norm kernel (one CTA
+ * per token; fixed-order fp32 sum of squares, IEEE sqrt and division, one
+ * bf16 rounding per element) and then the GEMM, with PDL letting the GEMM
+ * stream W while the norm runs.  Either way bit-identical run to run, and the
+ * fused and the two-launch forms give the same XN and, under the same plan,
+ * the same Y.  Every argument is checked and the plan made before anything is
+ * launched.
  */
 SKINNY_API skinny_status_t skinny_rmsnorm_gemm_bf16(const uint16_t *X, int ldx, const uint16_t *gamma, float eps,
                                          uint16_t *XN, int ldxn, const uint16_t *W, int ldw, float *Y, int ldy,

@@ -1,8 +1,14 @@
 """GB300-native low-latency skinny BF16 GEMM, ``Y[M,N] = X[M,K] . W[N,K]^T``.
 
-bf16 inputs, fp32 multiply-add, fp32 (or bf16) output, M = 1..16 (decode-sized)
-on every kernel and M = 17..64 on the cluster split-K tensor-core kernel, as
-used for the MoE router logits and the small-batch decode projections.
+bf16 inputs, fp32 accumulation, fp32 (or bf16) output, as used for the MoE
+router logits and the small-batch decode projections.  M = 1..16 (decode
+sized) runs on every kernel; M = 17..64 runs on the tensor cores only: the
+tcgen05 kernel (tensor-memory accumulator, W by tensor-map TMA; any K, 16-byte
+aligned rows), the tensor-core dot-product and the cluster split-K kernel's
+mma.sync consumer, chosen per shape by the measured tuning table.  The
+router's softmax / top-k epilogue, fp32 router weights and the query RMS norm
+in front of the q_b projection (fused into the tcgen05 GEMM for M <= 16) have
+entry points of their own.
 
 This module is a thin ctypes binding over ``libskinny_gemm.so`` (the C ABI in
 ``include/skinny_gemm.h``): the functions below carry the C names and only
@@ -57,6 +63,7 @@ SKINNY_OPT_WAIT_TIMEOUT_US = 7
 SKINNY_OPT_LOG = 8
 SKINNY_OPT_FORCE_CLUSTERS = 9
 SKINNY_OPT_FORCE_STAGE_K = 10
+SKINNY_OPT_FUSE_NORM = 11
 
 EXPORTED_SYMBOLS = (
     "skinny_gemm_bf16", "skinny_gemm_bf16_bf16out", "skinny_init", "skinny_query_plan", "skinny_plan_for",
@@ -254,7 +261,8 @@ class options:
                  "consumer": SKINNY_OPT_FORCE_CONSUMER, "split_k": SKINNY_OPT_FORCE_SPLIT_K,
                  "block_n": SKINNY_OPT_FORCE_BLOCK_N, "stages": SKINNY_OPT_FORCE_STAGES,
                  "wait_timeout_us": SKINNY_OPT_WAIT_TIMEOUT_US, "log": SKINNY_OPT_LOG,
-                 "clusters": SKINNY_OPT_FORCE_CLUSTERS, "stage_k": SKINNY_OPT_FORCE_STAGE_K}
+                 "clusters": SKINNY_OPT_FORCE_CLUSTERS, "stage_k": SKINNY_OPT_FORCE_STAGE_K,
+                 "fuse_norm": SKINNY_OPT_FUSE_NORM}
         self._set = [(names[k], int(v)) for k, v in kw.items()]
         self._old = []
 

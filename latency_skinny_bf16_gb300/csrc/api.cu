@@ -54,6 +54,7 @@ std::atomic<int> g_opt_wait_us{500000};
 std::atomic<int> g_opt_force_grid_y{0};
 std::atomic<int> g_opt_force_stage_k{0};
 std::atomic<int> g_opt_log{-1};
+std::atomic<int> g_opt_fuse_norm{1};
 
 int env_flag(const char *name) {
     const char *v = std::getenv(name);
@@ -727,9 +728,20 @@ skinny_status_t skinny_rmsnorm_gemm_bf16(const uint16_t *X, int ldx, const uint1
     int device = 0;
     st = current_device(&device);
     if (st != SKINNY_OK) return st;
+    DeviceState &d = g_dev[device];
     skinny_plan_t plan;
-    st = make_plan(XN, ldxn, W, ldw, M, N, K, g_dev[device].num_sms, &plan);
+    st = make_plan(XN, ldxn, W, ldw, M, N, K, d.num_sms, &plan);
     if (st != SKINNY_OK) return st;
+    skinny_plan_t fused;
+    if (g_opt_fuse_norm.load() && tc_make_norm_plan(M, N, K, plan, &fused)) {
+        // one launch: the norm runs inside every CTA of the tcgen05 GEMM
+        if (opt_log()) log_plan(M, N, K, ldw, fused);
+        GemmArgs a{XN, ldxn, W, ldw, Y, ldy, M, N, K, 0};
+        LaunchCtx c{static_cast<cudaStream_t>(stream), plan.pdl != 0, d.status_word,
+                    (uint64_t)g_opt_wait_us.load() * 1000ull};
+        const TcNormArgs na{X, ldx, gamma, eps, XN, ldxn};
+        return launch_tc(a, fused, c, &na) == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
+    }
     const cudaError_t e = launch_rmsnorm(X, ldx, gamma, eps, M, K, XN, ldxn, static_cast<cudaStream_t>(stream),
                                          opt_pdl() != 0);
     if (e != cudaSuccess) return SKINNY_ERR_LAUNCH;
@@ -839,6 +851,9 @@ skinny_status_t skinny_set_option(int option, int value) {
         case SKINNY_OPT_FORCE_STAGE_K:
             if (value < 0 || value > kSplitMaxBK || value % 64) return SKINNY_ERR_INVALID_VALUE;
             g_opt_force_stage_k.store(value); return SKINNY_OK;
+        case SKINNY_OPT_FUSE_NORM:
+            if (value != 0 && value != 1) return SKINNY_ERR_INVALID_VALUE;
+            g_opt_fuse_norm.store(value); return SKINNY_OK;
         default:
             return SKINNY_ERR_INVALID_VALUE;
     }
@@ -857,6 +872,7 @@ skinny_status_t skinny_get_option(int option, int *value) {
         case SKINNY_OPT_LOG: *value = opt_log(); return SKINNY_OK;
         case SKINNY_OPT_FORCE_CLUSTERS: *value = g_opt_force_grid_y.load(); return SKINNY_OK;
         case SKINNY_OPT_FORCE_STAGE_K: *value = g_opt_force_stage_k.load(); return SKINNY_OK;
+        case SKINNY_OPT_FUSE_NORM: *value = g_opt_fuse_norm.load(); return SKINNY_OK;
         default: return SKINNY_ERR_INVALID_VALUE;
     }
 }

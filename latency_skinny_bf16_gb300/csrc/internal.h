@@ -77,19 +77,31 @@ constexpr int kTcThreads = 192;        // producer warp, MMA warp, four draining
 constexpr int kTcMaxBK = 256;          // K elements per ring stage: 64..256, multiple of 64 (<= 16 MMAs)
 constexpr int kTcCtasPerSm = 2;        // the default grid: two CTAs per SM
 constexpr int kTcSmemBudget = 110 * 1024;   // per CTA, so two fit in an SM's 228 KB
-// Shared memory asked for at least, so the CTAs an SM can hold never need more
-// tensor memory (four accumulators of MT columns each) than its 512 columns:
-constexpr int kTcMinSmem16 = 30 * 1024;  // 16 tokens, 64 columns: <= 7 CTAs per SM
-constexpr int kTcMinSmem32 = 46 * 1024;  // 32 tokens, 128 columns: <= 4 CTAs per SM
-constexpr int kTcMinSmem64 = 77 * 1024;  // 64 tokens, 256 columns: <= 2 CTAs per SM
+// Shared memory asked for at least, so an SM holds at most two CTAs and their
+// tensor memory (256 columns each) never exceeds its 512 columns
+constexpr int kTcMinSmem = 77 * 1024;
 int tc_tokens(int M);                  // MMA N of the instantiation: 16, 32 or 64
 bool tc_supported(int M);
-int tc_smem_bytes(int M, int N, int block_n, int stage_k, int stages, int split_k, int clusters);
+int tc_smem_bytes(int M, int N, int K, int block_n, int stage_k, int stages, int split_k, int clusters, bool norm);
 // The plan for (M, N, K); zero arguments take the default.  false if none fits.
 bool tc_make_plan(int M, int N, int K, int force_bn, int force_s, int force_stages, int force_bk, int force_c,
                   int num_sms, skinny_plan_t *p);
+// The fused query RMS norm in front of the GEMM (X = rms_norm(xr) * gamma,
+// also stored to xn): the tcgen05 plan `gemm` with the ring shortened so the
+// rank's whole K slice of X fits beside it.  Up to kTcNormMaxM tokens.
+constexpr int kTcNormMaxM = 16;
+struct TcNormArgs {
+    const uint16_t *xr;
+    int64_t ldxr;
+    const uint16_t *gamma;
+    float eps;
+    uint16_t *xn;
+    int64_t ldxn;
+};
+bool tc_make_norm_plan(int M, int N, int K, const skinny_plan_t &gemm, skinny_plan_t *p);
 cudaError_t tc_prepare();
-cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
+cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c,
+                      const TcNormArgs *norm = nullptr);
 
 // ---- dot-product backend for fp32 weights (dotprod_f32w.cu): vec_elems 4/2/1 fp32, block_n 1/2/4
 bool dotprod_f32w_supported(int M, int vec_elems, int block_n);

@@ -26,14 +26,17 @@
 //     completing on the stage's "full" mbarrier.  W is a weight, so with PDL
 //     the W boxes of the first ring pass go out before griddepcontrol.wait.
 //   * Thread 32 issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32; M = TM,
-//     N = MT tokens, K = 16 each) into one of four tensor-memory accumulators
-//     (MT columns each) in rotation, one per chunk of ring stages holding at
-//     most 16 MMAs: the chunk's first MMA overwrites, so no accumulator chain
-//     is longer than 16 MMAs, and the issuer runs up to four chunks ahead of
-//     the draining warps.  tcgen05.commit frees each ring stage and marks the
-//     accumulator full at the end of its chunk.
+//     N = MT tokens, K = 16 each) into one of four sets of tensor-memory
+//     accumulators in rotation, one set per chunk of ring stages holding at
+//     most 16 MMAs.  A set holds P = 64 / MT accumulators of MT columns and
+//     the chunk's MMAs go to them in turn (consecutive MMAs are independent,
+//     so the tensor core pipelines them); each accumulator's first MMA of the
+//     chunk overwrites, so no chain is longer than 16 MMAs, and the issuer
+//     runs up to four chunks ahead of the draining warps.  tcgen05.commit
+//     frees each ring stage and marks the set full at the end of its chunk.
 //   * Warps 2..5 (one per lane quarter of tensor memory) wait for each
-//     accumulator, read it with tcgen05.ld, add it into fp32 registers (one
+//     set, read its P accumulators with tcgen05.ld, add them in order into
+//     fp32 registers (one
 //     output row per thread, the tokens in registers) and release it.  The
 //     tensor core's own accumulation is not round-to-nearest per add (its
 //     error is biased; measured on same-sign data), so it is kept to one
@@ -63,8 +66,13 @@ enum : int { kWaitAcc = 5, kWaitAccEmpty = 6 };
 constexpr int kWMaps = 5;                      // W box heights 128, 64, 32, 16, 8 rows
 constexpr int kAccWarp0 = 2;                   // warps 2..5 drain the accumulators
 
-constexpr int kNAcc = 4;                       // tensor-memory accumulators in rotation
-__host__ __device__ constexpr int tmem_cols(int MT) { return kNAcc * MT; }   // 64 / 128 / 256 columns
+constexpr int kNAcc = 4;                       // accumulator sets in rotation, one per chunk
+// Each set holds P = 64 / MT accumulators of MT columns: the MMAs of a chunk
+// go to them in turn, so consecutive MMAs do not wait on each other's result
+// (a dependent chain of small MMAs runs at the tensor core's latency, not its
+// rate).  kNAcc x P x MT = 256 columns for every token bucket.
+__host__ __device__ constexpr int tc_par(int MT) { return 64 / MT; }
+__host__ __device__ constexpr int tmem_cols(int MT) { return kNAcc * tc_par(MT) * MT; }
 // Ring stages per accumulator chunk: at most 16 MMAs (4 per 64-element box)
 // accumulate in tensor memory before the chunk is drained into registers.
 __host__ __device__ inline int tc_chunk_stages(int kb) { return kb >= 4 ? 1 : 4 / kb; }
@@ -159,23 +167,155 @@ struct TcParams {
     int *status;
     uint64_t budget_ns;
     int out_bf16;
+    // fused query RMS norm (NORM instantiations only): X = xn = rms_norm(xr) * gamma
+    const uint16_t *xr;
+    int64_t ldxr;
+    const uint16_t *gamma;
+    float eps;
+    uint16_t *xn;    // written by the CTAs of row range 0 (each its K slice)
+    int64_t ldxn;
 };
 
 // Shared-memory layout from the 1024-byte aligned base: the ring (per stage:
 // kb W regions of VP rows x 128 bytes, then kb X regions of MT rows x 128
-// bytes), a pad the MMA may read past the last W region (rows VP..TM-1 of the
-// last tile are never stored), then the mbarriers, the tensor-memory address
-// and the failure flag.
-__host__ __device__ inline int tc_stage_bytes(int VP, int MT, int kb) { return kb * (VP + MT) * 128; }
-__host__ __device__ inline int tc_pad_bytes(int VP, int MT, int kb, int TM) {
-    const int over = (TM - VP) * 128 - kb * MT * 128;
+// bytes, or no X regions when X is resident), the resident X (fused norm: nxb
+// boxes of MT rows x 128 bytes, the rank's whole K slice), a pad the MMA may
+// read past the last W region (rows VP..TM-1 of a tile are never stored), then
+// the mbarriers, the tensor-memory address, two flags and the norm's scratch.
+constexpr int kTcTailBytes = 16 + 4 * 16 + 4 * 4 * 16;
+__host__ __device__ inline int tc_stage_bytes(int VP, int MT, int kb, int nxb) {
+    return kb * (VP + (nxb ? 0 : MT)) * 128;
+}
+__host__ __device__ inline int tc_pad_bytes(int VP, int MT, int kb, int TM, int nxb) {
+    const int over = (TM - VP) * 128 - (nxb ? nxb : kb) * MT * 128;
     return over > 0 ? over : 0;
 }
-__host__ __device__ inline int tc_layout_bytes(int VP, int MT, int kb, int stages, int TM) {
-    return stages * tc_stage_bytes(VP, MT, kb) + tc_pad_bytes(VP, MT, kb, TM) + 8 * (2 * stages + 2 * kNAcc + 1) + 16;
+__host__ __device__ inline int tc_layout_bytes(int VP, int MT, int kb, int stages, int TM, int nxb) {
+    return stages * tc_stage_bytes(VP, MT, kb, nxb) + nxb * MT * 128 + tc_pad_bytes(VP, MT, kb, TM, nxb) +
+           8 * (2 * stages + 2 * kNAcc + 2) + kTcTailBytes;
 }
 
-template <int MT, int TM>
+__device__ __forceinline__ uint4 lds128(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts128(void *p, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" :: "r"(smem_u32(p)), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// 8 bf16 of a row starting at k0 (zeros past K), read through L2 (.cg: the
+// row may have just been written by the preceding kernel).
+__device__ __forceinline__ uint4 load_chunk_cg(const uint16_t *row, int k0, int K) {
+    if ((reinterpret_cast<uintptr_t>(row + k0) & 15) == 0 && k0 + 8 <= K) return ldg_v4(row + k0);
+    uint32_t w[4] = {0, 0, 0, 0};
+    for (int e = 0; e < 8; ++e)
+        if (k0 + e < K) w[e >> 1] |= (uint32_t)ldg_u16(row + k0 + e) << (16 * (e & 1));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+// 8 bf16 gains from k0 (zeros past K), read-only path.
+__device__ __forceinline__ uint4 load_gamma(const uint16_t *g, int k0, int K) {
+    if ((reinterpret_cast<uintptr_t>(g + k0) & 15) == 0 && k0 + 8 <= K) return ldg_stream_v4(g + k0);
+    uint32_t w[4] = {0, 0, 0, 0};
+    for (int e = 0; e < 8; ++e)
+        if (k0 + e < K) w[e >> 1] |= (uint32_t)ldg_stream_u16(g + k0 + e) << (16 * (e & 1));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Fused query RMS norm, run by the four draining warps (jt = 0..127, wq = warp
+// 0..3 among them) before any MMA: r_m = 1 / sqrtf(sum_k x^2 / K + eps) for
+// every token, in the exact order of the standalone norm kernel (thread jt
+// takes the 8-element chunks jt, jt + 128, ... of the whole row, one fused
+// multiply-add per element, then a warp butterfly and the warps in order), so
+// both give the same bits; the chunks of this rank's K slice are kept in the
+// resident X and then replaced by bf16_rn((x * r_m) * g_k) in the swizzled
+// layout the MMA reads.  Rows >= M and columns >= K hold zeros.  The CTAs of
+// row range 0 also store the normalised rows of their slice to xn.
+template <int MT>
+__device__ __forceinline__ void norm_prologue(const TcParams &p, uint8_t *xres, float *rstat, float *part,
+                                              int kbeg, int kend, int nxb, bool write_xn, int jt, int wq,
+                                              int lane) {
+    const int K = p.K, M = p.M;
+    const int chunks = (K + 7) / 8;
+    float ss[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) ss[m] = 0.f;
+    for (int c = jt; c < chunks; c += 128) {
+        const int k0 = 8 * c;
+        uint4 q[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            q[m] = (m < M) ? load_chunk_cg(p.xr + (int64_t)m * p.ldxr, k0, K) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const uint32_t w[4] = {q[m].x, q[m].y, q[m].z, q[m].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
+                ss[m] = fmaf(a, a, ss[m]);        // zeros past K add exactly nothing
+                ss[m] = fmaf(b, b, ss[m]);
+            }
+        }
+        if (k0 >= kbeg && k0 < kend) {
+            const int off = k0 - kbeg, box = off >> 6, ch = (off >> 3) & 7;
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (m < M) sts128(xres + box * MT * 128 + m * 128 + ((ch ^ (m & 7)) << 4), q[m]);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss[m] += __shfl_xor_sync(0xFFFFFFFFu, ss[m], o);
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) part[wq * MT + m] = ss[m];
+    }
+    named_bar_sync(2, 128);
+    if (jt < M) {
+        float t = part[jt];
+        for (int w = 1; w < 4; ++w) t += part[w * MT + jt];
+        rstat[jt] = 1.0f / sqrtf(t / (float)K + p.eps);
+    }
+    named_bar_sync(2, 128);
+    for (int idx = jt; idx < MT * nxb * 8; idx += 128) {
+        const int m = idx % MT, rest = idx / MT, ch = rest & 7, box = rest >> 3;
+        const int k0 = kbeg + box * 64 + ch * 8;
+        uint8_t *addr = xres + box * MT * 128 + m * 128 + ((ch ^ (m & 7)) << 4);
+        uint4 out = make_uint4(0, 0, 0, 0);
+        if (m < M && k0 < kend) {
+            const uint4 raw = lds128(addr);
+            const uint4 gq = load_gamma(p.gamma, k0, K);
+            const float r = rstat[m];
+            const uint32_t xw[4] = {raw.x, raw.y, raw.z, raw.w}, gw[4] = {gq.x, gq.y, gq.z, gq.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t lo = f32_to_bf16_rn(bf16_lo(xw[e]) * r * bf16_lo(gw[e]));
+                const uint32_t hi = f32_to_bf16_rn(bf16_hi(xw[e]) * r * bf16_hi(gw[e]));
+                o[e] = lo | (hi << 16);
+            }
+            out = make_uint4(o[0], o[1], o[2], o[3]);
+            if (write_xn) {
+                uint16_t *dst = p.xn + (int64_t)m * p.ldxn + k0;
+                if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0 && k0 + 8 <= K) {
+                    *reinterpret_cast<uint4 *>(dst) = out;
+                } else {
+                    for (int e = 0; e < 8 && k0 + e < K; ++e)
+                        dst[e] = (uint16_t)(o[e >> 1] >> (16 * (e & 1)));
+                }
+            }
+        }
+        sts128(addr, out);
+    }
+    fence_proxy_async_smem();                    // generic-proxy writes, read next by the MMAs
+    named_bar_sync(2, 128);
+}
+
+template <int MT, int TM, bool NORM>
 __global__ void __launch_bounds__(kTcThreads, 2)
 tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
 {
@@ -189,17 +329,22 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
     uint8_t *smem = smem_raw + (base - raw);
     const int kb = p.kb, stages = p.stages;
     const int VP = 8 * p.vg;
-    const int sbytes = tc_stage_bytes(VP, MT, kb);
-    const uint32_t bars = base + stages * sbytes + tc_pad_bytes(VP, MT, kb, TM);
+    const int nxb = NORM ? p.KS / 64 : 0;                    // resident X boxes (fused norm)
+    const int sbytes = tc_stage_bytes(VP, MT, kb, nxb);
+    const uint32_t xres = base + stages * sbytes;
+    const uint32_t bars = xres + nxb * MT * 128 + tc_pad_bytes(VP, MT, kb, TM, nxb);
     auto full = [&](int s) { return bars + 8u * s; };
     auto empty = [&](int s) { return bars + 8u * (stages + s); };
     auto accf = [&](int b) { return bars + 8u * (2 * stages + b); };
     auto acce = [&](int b) { return bars + 8u * (2 * stages + kNAcc + b); };
     const uint32_t done = bars + 8u * (2 * stages + 2 * kNAcc);
-    uint8_t *tail = smem + stages * sbytes + tc_pad_bytes(VP, MT, kb, TM) + 8 * (2 * stages + 2 * kNAcc + 1);
+    const uint32_t xready = bars + 8u * (2 * stages + 2 * kNAcc + 1);   // fused norm: X is in place
+    uint8_t *tail = smem + (bars - base) + 8 * (2 * stages + 2 * kNAcc + 2);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(tail);
     volatile int *fail = reinterpret_cast<volatile int *>(tail + 4);    // an accumulator was not drained
     volatile int *mma_ok = reinterpret_cast<volatile int *>(tail + 8);  // every issued MMA completed
+    float *rstat = reinterpret_cast<float *>(tail + 16);               // fused norm: r per token
+    float *npart = reinterpret_cast<float *>(tail + 16 + 4 * 16);      // fused norm: warp partial sums
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = gridDim.x;
@@ -229,6 +374,7 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
             mbar_init(acce(b), 4);            // lane 0 of each draining warp
         }
         mbar_init(done, 1);
+        mbar_init(xready, 1);
         *fail = 0;
         *mma_ok = 0;
         fence_mbarrier_init_cluster();
@@ -259,14 +405,15 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
                     if (x_part) tma_load_2d(st + kb * VP * 128 + b * MT * 128, &maps.x, k0, 0, full(s));
                 }
             };
-            auto stage_tx = [&](int i) { return (uint32_t)(kb * (tile_rows(i / nk) + MT) * 128); };
+            auto stage_tx = [&](int i) { return (uint32_t)(kb * (tile_rows(i / nk) + (NORM ? 0 : MT)) * 128); };
             const int pre = min(total, stages);
             for (int i = 0; i < pre; ++i) {
                 mbar_arrive_expect_tx(full(i), stage_tx(i));
                 issue(i, i, true, false);          // the weight: before the PDL wait
             }
             griddep_wait();
-            for (int i = 0; i < pre; ++i) issue(i, i, false, true);
+            if (!NORM)
+                for (int i = 0; i < pre; ++i) issue(i, i, false, true);
             int issued = pre;
             for (int i = pre; i < total; ++i) {
                 const int s = i % stages;
@@ -275,7 +422,7 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
                     break;
                 }
                 mbar_arrive_expect_tx(full(s), stage_tx(i));
-                issue(i, s, true, true);
+                issue(i, s, true, !NORM);
                 issued = i + 1;
             }
             // every copy issued has landed before the ring is reused or the CTA exits
@@ -294,7 +441,12 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
             // ---- MMA issuer (its bounded waits start once the preceding kernel is done)
             griddep_wait();
             constexpr uint32_t idesc = idesc_bf16<MT, TM>();
-            for (int i = 0; i < total; ++i) {
+            bool go = true;
+            if (NORM && !mbar_wait_bounded(xready, 0, p.budget_ns)) {
+                report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitX);
+                go = false;
+            }
+            for (int i = 0; go && i < total; ++i) {
                 const int s = i % stages;
                 const int t = i / nk, ks = i - t * nk;
                 const int g = t * nchunk + ks / cs;                 // accumulator chunk
@@ -311,13 +463,16 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
                 }
                 tc_fence_after();
                 const uint32_t wst = base + s * sbytes;
-                const uint32_t xst = wst + kb * VP * 128;
+                const uint32_t xst = NORM ? xres + ks * kb * MT * 128 : wst + kb * VP * 128;
+                constexpr int P = tc_par(MT);
+                const int q0 = (ks % cs) * 4 * kb;           // MMAs of this chunk issued so far
                 for (int cb = 0; cb < kb; ++cb)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        umma_bf16(tmem + (uint32_t)(b * MT), sw128_desc(wst + cb * VP * 128 + 32 * j),
-                                  sw128_desc(xst + cb * MT * 128 + 32 * j), idesc,
-                                  (first && (cb | j) == 0) ? 0u : 1u);
+                    for (int j = 0; j < 4; ++j) {
+                        const int q = q0 + 4 * cb + j;        // the chunk's first P MMAs overwrite
+                        umma_bf16(tmem + (uint32_t)((b * P + q % P) * MT), sw128_desc(wst + cb * VP * 128 + 32 * j),
+                                  sw128_desc(xst + cb * MT * 128 + 32 * j), idesc, q < P ? 0u : 1u);
+                    }
                 umma_commit(empty(s));               // the stage is free once these MMAs have read it
                 if (last) umma_commit(accf(b));      // the chunk's sum is complete
             }
@@ -332,6 +487,10 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
         tc_fence_after();
         const uint32_t tmem = *tmem_slot;
         griddep_wait();                          // Y may be read or written by the preceding kernel
+        if (NORM)
+            norm_prologue<MT>(p, smem + (xres - base), rstat, npart, kbeg, kend, nxb, blockIdx.y == 0, tid - 64,
+                              warp - kAccWarp0, lane);
+        if (NORM && tid == 64) mbar_arrive(xready);
         const int q = warp & 3;
         // accumulator row of this thread (M = 64: lanes 16..31 of each quarter hold none)
         const int row = (TM == 128) ? 32 * q + lane : 16 * q + lane;
@@ -353,14 +512,19 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
                 break;
             }
             tc_fence_after();
+            // the chunk's P partial sums, added in a fixed order
+            constexpr int P = tc_par(MT);
 #pragma unroll
-            for (int cc = 0; cc < MT / 16; ++cc) {
-                if (16 * cc < M) {                // warp-uniform
-                    uint32_t r[16];
-                    tmem_ld16_nowait(lane_base + (uint32_t)(b * MT + 16 * cc), r);
-                    tmem_ld_wait(r);
+            for (int pp = 0; pp < P; ++pp) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc[16 * cc + j] += __uint_as_float(r[j]);
+                for (int cc = 0; cc < MT / 16; ++cc) {
+                    if (16 * cc < M) {            // warp-uniform
+                        uint32_t r[16];
+                        tmem_ld16_nowait(lane_base + (uint32_t)((b * P + pp) * MT + 16 * cc), r);
+                        tmem_ld_wait(r);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[16 * cc + j] += __uint_as_float(r[j]);
+                    }
                 }
             }
             tc_fence_before();
@@ -431,9 +595,11 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
 }
 
 using TcKernel = void (*)(const TcMaps, const TcParams);
-const TcKernel kTc[3][2] = {{&tmem_gemm_kernel<16, 128>, &tmem_gemm_kernel<16, 64>},
-                            {&tmem_gemm_kernel<32, 128>, &tmem_gemm_kernel<32, 64>},
-                            {&tmem_gemm_kernel<64, 128>, &tmem_gemm_kernel<64, 64>}};
+const TcKernel kTc[3][2] = {{&tmem_gemm_kernel<16, 128, false>, &tmem_gemm_kernel<16, 64, false>},
+                            {&tmem_gemm_kernel<32, 128, false>, &tmem_gemm_kernel<32, 64, false>},
+                            {&tmem_gemm_kernel<64, 128, false>, &tmem_gemm_kernel<64, 64, false>}};
+// the fused query RMS norm: up to 16 tokens
+const TcKernel kTcNorm[2] = {&tmem_gemm_kernel<16, 128, true>, &tmem_gemm_kernel<16, 64, true>};
 
 int tc_index(int M) { return M <= 16 ? 0 : M <= 32 ? 1 : 2; }
 
@@ -480,19 +646,23 @@ int tc_tokens(int M) { return 16 << tc_index(M); }
 
 bool tc_supported(int M) { return M >= 1 && M <= SKINNY_MAX_M; }
 
-int tc_smem_bytes(int M, int N, int block_n, int stage_k, int stages, int split_k, int clusters) {
+int tc_smem_bytes(int M, int N, int K, int block_n, int stage_k, int stages, int split_k, int clusters,
+                  bool norm) {
     const int MT = tc_tokens(M);
     const int kb = stage_k / 64;
     const int G = (N + 7) / 8;
     const int vg = tc_groups_per_tile(G, clusters, block_n / 8);
     const int VP = 8 * vg;
-    int bytes = tc_layout_bytes(VP, MT, kb, stages, block_n);
+    // fused norm: the rank's whole K slice of X stays in shared memory
+    const int per_rank = ((K + stage_k - 1) / stage_k + split_k - 1) / split_k;
+    const int nxb = norm ? per_rank * kb : 0;
+    int bytes = tc_layout_bytes(VP, MT, kb, stages, block_n, nxb);
     // S > 1: the ring also receives the partials (S slots of M x ceil(VP / S) fp32)
-    if (split_k > 1 && stages * tc_stage_bytes(VP, MT, kb) < split_k * M * ((VP + split_k - 1) / split_k) * 4)
+    if (split_k > 1 && stages * tc_stage_bytes(VP, MT, kb, nxb) < split_k * M * ((VP + split_k - 1) / split_k) * 4)
         return 1 << 30;
-    // cap the CTAs an SM can hold, so their tensor memory (four accumulators
-    // of MT columns each) always fits in the SM's 512 columns
-    const int min_smem = (MT == 64) ? kTcMinSmem64 : (MT == 32) ? kTcMinSmem32 : kTcMinSmem16;
+    // cap the CTAs an SM can hold (two), so their tensor memory (256 columns
+    // each) always fits in the SM's 512 columns
+    const int min_smem = kTcMinSmem;
     if (bytes < min_smem - 1024) bytes = min_smem - 1024;
     return bytes + 1024;                         // slack for the 1024-byte alignment
 }
@@ -506,17 +676,21 @@ bool tc_make_plan(int M, int N, int K, int force_bn, int force_s, int force_stag
     const int bk = force_bk ? force_bk : (K > 64 ? 128 : 64);
     if (bk < 64 || bk > kTcMaxBK || bk % 64) return false;
     const int nk_all = (K + bk - 1) / bk;         // ring stages over the whole K
-    // S: split K over a cluster while the tiles the CTA slots would get are
-    // thinner than 48 rows (the MMA reads all TM rows of a tile from shared
-    // memory, and a ring stage should carry enough W to cover its round trip),
-    // each rank keeping at least two stages of K
+    // Rows per MMA: the tensor core issues a small MMA (N = 16..64 tokens, K =
+    // 16) in about 45 ns per SM whatever its M, so a tile must carry at least
+    // 64 useful W rows (2 KB of W per MMA) to keep up with HBM.  Clusters:
+    // at two CTAs per SM, GB300 keeps only about 97% / 95% of the slots
+    // resident for clusters of 4 / 8 (the GPCs' SM counts), so a split grid
+    // is held to 90% of the slots (one wave).
+    auto cap = [&](int s_) { return s_ == 1 ? slots : (slots * 9) / (10 * s_); };
+    auto vp_of = [&](int c_) { return 8 * tc_groups_per_tile(G, c_ < 1 ? 1 : c_, 16); };
     int S = force_s;
     if (S == 0) {
         S = 1;
         while (S < kSplitMaxCluster && nk_all >= 4 * S) {
-            int c = slots / S;
+            int c = cap(S);
             if (c > G) c = G;
-            if (8 * tc_groups_per_tile(G, c < 1 ? 1 : c, 16) >= 48) break;
+            if (vp_of(c) >= 64) break;
             S *= 2;
         }
     }
@@ -524,8 +698,10 @@ bool tc_make_plan(int M, int N, int K, int force_bn, int force_s, int force_stag
     const int max_vg_default = (force_bn == 64) ? 8 : 16;
     int C = force_c;
     if (C == 0) {
-        C = slots / S;
+        C = cap(S);
         if (C > G) C = G;
+        // tiles of at least 64 rows where the rows allow it
+        if (vp_of(C) < 64 && G >= 8) C = (G + 7) / 8;
         if (S > 1 && (G + C - 1) / C > max_vg_default) C = (G + max_vg_default - 1) / max_vg_default;
         if (C < 1) C = 1;
     }
@@ -542,15 +718,15 @@ bool tc_make_plan(int M, int N, int K, int force_bn, int force_s, int force_stag
     if (!stages) {
         const int budget = kTcSmemBudget;
         stages = kSplitMaxStages;
-        while (stages > 1 && tc_smem_bytes(M, N, bn, bk, stages, S, C) > budget) --stages;
+        while (stages > 1 && tc_smem_bytes(M, N, K, bn, bk, stages, S, C, false) > budget) --stages;
         // no deeper than the CTA's stages, but deep enough to receive the partials
         int least = 1;
-        while (least < stages && tc_smem_bytes(M, N, bn, bk, least, S, C) > kMaxDynSmem) ++least;
+        while (least < stages && tc_smem_bytes(M, N, K, bn, bk, least, S, C, false) > kMaxDynSmem) ++least;
         const int work = per_rank * ntiles_max;
         if (stages > work) stages = work > least ? work : least;
     }
     if (stages < 1 || stages > kSplitMaxStages) return false;
-    const int smem = tc_smem_bytes(M, N, bn, bk, stages, S, C);
+    const int smem = tc_smem_bytes(M, N, K, bn, bk, stages, S, C, false);
     if (smem > kMaxDynSmem) return false;
     p->backend = SKINNY_BACKEND_TCGEN05;
     p->consumer = SKINNY_CONSUMER_MMA;
@@ -567,16 +743,36 @@ bool tc_make_plan(int M, int N, int K, int force_bn, int force_s, int force_stag
     return true;
 }
 
+bool tc_make_norm_plan(int M, int N, int K, const skinny_plan_t &gemm, skinny_plan_t *p) {
+    if (gemm.backend != SKINNY_BACKEND_TCGEN05 || M < 1 || M > kTcNormMaxM) return false;
+    *p = gemm;
+    // the same split, tiles and stage length (so the same sums in the same
+    // order); the ring as deep as the budget leaves beside the resident X
+    int stages = gemm.stages;
+    while (stages > 1 && tc_smem_bytes(M, N, K, gemm.block_n, gemm.stage_k, stages, gemm.split_k, gemm.grid_y,
+                                       true) > kTcSmemBudget)
+        --stages;
+    const int smem = tc_smem_bytes(M, N, K, gemm.block_n, gemm.stage_k, stages, gemm.split_k, gemm.grid_y, true);
+    if (smem > kMaxDynSmem) return false;
+    p->stages = stages;
+    p->smem_bytes = smem;
+    return true;
+}
+
 cudaError_t tc_prepare() {
     for (int i = 0; i < 3; ++i)
         for (int j = 0; j < 2; ++j) {
             cudaError_t e = set_max_dyn_smem(kTc[i][j]);
             if (e != cudaSuccess) return e;
         }
+    for (int j = 0; j < 2; ++j) {
+        cudaError_t e = set_max_dyn_smem(kTcNorm[j]);
+        if (e != cudaSuccess) return e;
+    }
     return cudaSuccess;
 }
 
-cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCtx &c) {
+cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCtx &c, const TcNormArgs *norm) {
     const int S = pl.split_k;
     const int TM = pl.block_n;
     const int C = pl.grid_y;
@@ -588,7 +784,10 @@ cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCt
         return cudaErrorInvalidValue;
     const int vg = tc_groups_per_tile(G, C, TM / 8);
     if (8 * vg > TM || (S > 1 && (G + C - 1) / C > vg) ||
-        pl.smem_bytes < tc_smem_bytes(a.M, a.N, TM, pl.stage_k, pl.stages, S, C) || pl.smem_bytes > kMaxDynSmem)
+        pl.smem_bytes < tc_smem_bytes(a.M, a.N, a.K, TM, pl.stage_k, pl.stages, S, C, norm != nullptr) ||
+        pl.smem_bytes > kMaxDynSmem)
+        return cudaErrorInvalidValue;
+    if (norm && (a.M > kTcNormMaxM || !norm->xr || !norm->gamma || !norm->xn || a.out_bf16))
         return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(a.X) & 15) || (a.ldx & 7) || (reinterpret_cast<uintptr_t>(a.W) & 15) ||
         (a.ldw & 7))
@@ -613,6 +812,12 @@ cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCt
     p.status = c.status;
     p.budget_ns = c.budget_ns;
     p.out_bf16 = a.out_bf16;
+    p.xr = norm ? norm->xr : nullptr;
+    p.ldxr = norm ? norm->ldxr : 0;
+    p.gamma = norm ? norm->gamma : nullptr;
+    p.eps = norm ? norm->eps : 0.f;
+    p.xn = norm ? norm->xn : nullptr;
+    p.ldxn = norm ? norm->ldxn : 0;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, C, 1);
@@ -633,7 +838,7 @@ cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCt
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, kTc[idx][TM == 128 ? 0 : 1], maps, p);
+    return cudaLaunchKernelEx(&cfg, norm ? kTcNorm[TM == 128 ? 0 : 1] : kTc[idx][TM == 128 ? 0 : 1], maps, p);
 }
 
 }  // namespace skinny

@@ -28,11 +28,10 @@ def check_tc_geometry(p, M, N, K):
     assert p["k_chunk"] % bk == 0 and s * p["k_chunk"] >= K      # trailing ranks may be empty (they add 0)
     mt = 16 if M <= 16 else 32 if M <= 32 else 64
     ring = p["stages"] * (bk // 64) * (8 * vg + mt) * 128
-    # four tensor-memory accumulators of mt columns: the shared memory asked for
-    # caps the CTAs per SM so that their columns fit in 512
-    min_kb = {16: 30, 32: 46, 64: 77}[mt]
-    assert min_kb * 1024 <= p["smem_bytes"] <= 227 * 1024
-    assert (228 * 1024 // p["smem_bytes"]) * 4 * mt <= 512
+    # 256 tensor-memory columns per CTA (four sets of 64 / mt accumulators of mt
+    # columns): the shared memory asked for caps the CTAs per SM at two
+    assert 77 * 1024 <= p["smem_bytes"] <= 227 * 1024
+    assert (228 * 1024 // p["smem_bytes"]) * 256 <= 512
     assert ring + 8 * (2 * p["stages"] + 9) + 16 + 1024 <= p["smem_bytes"]
     if s > 1:
         assert ring >= s * M * (-(-8 * vg // s)) * 4            # S slots of M x ceil(VP / S) fp32

@@ -294,8 +294,9 @@ def test_mid_m_takes_a_tensor_core_path():
     p = plan(40, 8192, 4096)
     assert (p["backend"], p["consumer"]) == (sk.SKINNY_BACKEND_TCGEN05, sk.SKINNY_CONSUMER_MMA)
     # 1024 row groups: 304 ranges would give tiles of 32 rows, so K is split in
-    # two (clusters of 2, 152 ranges of 6-7 groups: tiles of 56 rows)
-    assert (p["split_k"], p["stage_k"], p["grid_y"], p["block_n"]) == (2, 128, 152, 64)
+    # two; clusters of 2 fill 90% of the slots (136 ranges of 7-8 groups: tiles
+    # of 64 rows, at least 2 KB of W per MMA)
+    assert (p["split_k"], p["stage_k"], p["grid_y"], p["block_n"]) == (2, 128, 136, 64)
     check_tc_geometry(p, 40, 8192, 4096)
     # 9..16 tokens on large weights take it too; fewer stay on the earlier backends
     assert plan(12, 8192, 4096)["backend"] == sk.SKINNY_BACKEND_TCGEN05

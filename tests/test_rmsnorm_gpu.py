@@ -165,3 +165,84 @@ def test_norm_wrapper_and_graph():
             graph.replay()
             torch.cuda.synchronize()
         assert torch.equal(y2.view(torch.int32), y.view(torch.int32)) and torch.equal(xn2, xn)
+
+
+# ---------------------------------------------------------------- the fused form (one launch)
+
+FUSED_CASES = [
+    # (M, N, K, tcgen05 plan options)
+    (1, 24576, 1536, {}),
+    (3, 24576, 1536, {}),
+    (8, 2112, 1536, {}),
+    (16, 24576, 1536, {}),
+    (16, 2112, 1536, dict(split_k=2)),
+    (12, 300, 1536, dict(split_k=4, stage_k=64)),
+    (7, 1000, 1000, {}),                       # K % 64 != 0: the last box is part zeros
+    (16, 520, 520, dict(split_k=2, stage_k=128)),
+]
+
+
+@pytest.mark.parametrize("M,N,K,opts", FUSED_CASES, ids=[f"M{m}_N{n}_K{k}_{o}" for m, n, k, o in FUSED_CASES])
+def test_fused_norm_equals_two_launches(M, N, K, opts):
+    """The norm inside the tcgen05 GEMM (one launch) gives the same XN bits as
+    the norm kernel, and, under the same plan, the same Y bits as the norm
+    kernel followed by the GEMM; both match the oracle."""
+    case, X, W, G = make_case(M, N, K, seed=3400 + M + N % 97 + K)
+    with sk.options(backend=sk.SKINNY_BACKEND_TCGEN05, **opts):
+        with sk.options(fuse_norm=1):
+            xf, yf = run_norm(case, X, W, G)
+        with sk.options(fuse_norm=0):
+            xs, ys = run_norm(case, X, W, G)
+    assert np.array_equal(xf, xs), "XN differs between the fused and the two-launch forms"
+    assert np.array_equal(yf.view(np.uint32), ys.view(np.uint32)), "Y differs between the two forms"
+    check_xn(xf, oracle.rmsnorm(X, G, 1e-6, M, K), K)
+    cols = np.arange(N) if N <= 2112 else np.sort(np.random.default_rng(M).choice(N, 1024, replace=False))
+    yref, A = oracle.gemm(xf, np.ascontiguousarray(W[cols]), M, len(cols), K)
+    check_parity(yf[:, cols], yref, A, f"fused M{M} N{N} K{K}")
+    assert sk.skinny_get_device_status() == 0
+
+
+def test_fused_norm_strided_and_misaligned_x_and_eps():
+    """X rows that are not 16-byte aligned (scalar loads) and several eps: the
+    fused form still equals the two-launch form."""
+    case, X, W, G = make_case(5, 640, 1000, seed=3500)
+    for eps in (0.0, 1e-6, 0.5):
+        with sk.options(backend=sk.SKINNY_BACKEND_TCGEN05):
+            with sk.options(fuse_norm=1):
+                xf, yf = run_norm(case, X, W, G, eps=eps, ldx=1003)
+            with sk.options(fuse_norm=0):
+                xs, ys = run_norm(case, X, W, G, eps=eps, ldx=1003)
+        assert np.array_equal(xf, xs) and np.array_equal(yf.view(np.uint32), ys.view(np.uint32)), eps
+        check_xn(xf, oracle.rmsnorm(X, G, eps, 5, 1000), 1000)
+
+
+@pytest.mark.parametrize("pdl", [0, 1])
+def test_fused_norm_in_a_graph_chain(pdl):
+    """Two fused calls back to back in a CUDA graph (the second reads nothing
+    the first writes), replayed: the same bits as eager calls."""
+    cases = [make_case(16, 24576, 1536, seed=3600), make_case(4, 2112, 1536, seed=3601)]
+    with sk.options(pdl=pdl):
+        eager = [run_norm(*c) for c in cases]
+        tens = []
+        for case, X, W, G in cases:
+            M, N, K = case.M, case.N, case.K
+            tens.append(dict(x=torch.from_numpy(X.view(np.int16).copy()).cuda(),
+                             w=torch.from_numpy(W.view(np.int16)).cuda(),
+                             g=torch.from_numpy(G.view(np.int16)).cuda(),
+                             xn=torch.zeros(M * K, dtype=torch.int16, device="cuda"),
+                             y=torch.zeros(M * N, device="cuda"), M=M, N=N, K=K))
+        s = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            for t in tens:
+                st = sk.skinny_rmsnorm_gemm_bf16(t["x"].data_ptr(), t["K"], t["g"].data_ptr(), 1e-6,
+                                                 t["xn"].data_ptr(), t["K"], t["w"].data_ptr(), t["K"],
+                                                 t["y"].data_ptr(), t["N"], t["M"], t["N"], t["K"], s.cuda_stream)
+                assert st == sk.SKINNY_OK
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+    for t, (xe, ye) in zip(tens, eager):
+        assert np.array_equal(t["xn"].cpu().numpy().view(np.uint16).reshape(xe.shape), xe)
+        assert np.array_equal(t["y"].cpu().numpy().reshape(ye.shape).view(np.uint32), ye.view(np.uint32))
+    assert sk.skinny_get_device_status() == 0
