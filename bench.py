@@ -357,10 +357,12 @@ def time_isolated(sk, torch, stream, wl, l2, iters):
 
 def time_flushed(sk, torch, stream, wl, l2, samples):
     """Cross-check of the L2-cold figures: before each call a flush kernel
-    writes a buffer of 2x the L2 size (outside the event pair), then a CUDA
-    event pair brackets the call alone; PDL off.  (median, p10, p90) us per
-    call shape."""
-    flush = torch.empty(max(1, 2 * l2 // 4), dtype=torch.float32, device="cuda")
+    reads a buffer of 2x the L2 size (outside the event pair; a read leaves
+    clean lines, where a write would leave dirty ones whose write-back the
+    timed call would pay), then a CUDA event pair brackets the call alone;
+    PDL off.  (median, p10, p90) us per call shape."""
+    flush = torch.ones(max(1, 2 * l2 // 4), dtype=torch.float32, device="cuda")
+    sink = torch.empty(1, dtype=torch.float32, device="cuda")
     sh = stream.cuda_stream
     out = []
     with sk.options(pdl=0):
@@ -369,7 +371,7 @@ def time_flushed(sk, torch, stream, wl, l2, samples):
             evs = []
             with torch.cuda.stream(stream):
                 for s in range(samples + 2):
-                    flush.fill_(float(s))
+                    torch.sum(flush, dim=0, keepdim=True, out=sink)
                     a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     a_.record(stream)
                     st = sk.skinny_gemm_bf16(r.x[j].data_ptr(), c.lx, r.w[j].data_ptr(), c.lw, r.y[j].data_ptr(),
@@ -730,7 +732,7 @@ def main(argv=None):
         "pdl_chain": r["chain"],
         "per_shape": shape_rows(wl, r["per_launch"], peak, r["flushed"]),
         "flush_method": None if r["flushed"] is None else
-        "per call shape: 100 isolated calls, each after a flush kernel writing 2x L2 (outside the event pair), "
+        "per call shape: 100 isolated calls, each after a flush kernel reading 2x L2 (outside the event pair), "
         "a CUDA-event pair around the call alone, PDL off; median / p10 / p90",
         "per_config": r["per_config"],
     }

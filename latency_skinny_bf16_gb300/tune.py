@@ -39,18 +39,20 @@ def token_bucket(M: int) -> int:
 
 def tc_candidates(M: int, K: int, N: int, num_sms: int = 152):
     """tcgen05 plans: cluster sizes S along K; for each, the planner's own
-    number of row ranges and the range counts that give tiles of about 32 to
-    128 rows (W rows come in groups of 8), at most three CTAs per SM; 2 or 4
-    boxes per ring stage; the planner's tile height and ring depth."""
+    number of row ranges and the range counts that give tiles of about 48 to
+    128 rows (W rows come in groups of 8) in one wave of two CTAs per SM; 2 or
+    4 boxes per ring stage; the planner's tile height and ring depth."""
     out = []
     G = -(-max(N, 1) // 8)
     for s in (1, 2, 4, 8):
         if K < 2 * s * 128:
             continue
+        # one wave at two CTAs per SM (clusters: 90% of the slots, as the planner)
+        limit = 2 * num_sms if s == 1 else (2 * num_sms * 9) // (10 * s)
         counts = {0}
-        for groups in (4, 6, 8, 12, 16):
+        for groups in (6, 8, 12, 16):
             c = -(-G // groups)
-            if c * s <= 3 * num_sms:
+            if c <= limit:
                 counts.add(c)
         for c in sorted(counts):
             for bk in (128, 256):
@@ -225,24 +227,31 @@ TABLE = __import__("os").path.join(__import__("os").path.dirname(__file__), "csr
 
 def install(lines, path=TABLE):
     """Write table lines into the compiled-in table: every existing line of a
-    (K, N) shape that `lines` covers is dropped, the new lines take their
-    place (first match wins in the dispatcher), comments are kept."""
-    def key(line):
-        v = line.split("//", 1)[0].strip().strip("{},").split(",")
-        return (int(v[0]), int(v[1]))
-    shapes = {key(l) for l in lines}
+    tuned (K, N) shape whose M range meets a new line's M range is dropped,
+    the new lines take the place of the first dropped one (first match wins in
+    the dispatcher), other lines and comments are kept."""
+    def parse(line):
+        v = [int(x) for x in line.split("//", 1)[0].strip().strip("{},").split(",")]
+        return (v[0], v[1]), v[2], v[3]
+    new = {}
+    for l in lines:
+        key, lo, hi = parse(l)
+        new.setdefault(key, []).append((lo, hi))
     with open(path) as f:
         old = f.read().rstrip("\n").split("\n")
-    out, placed = [], False
+    out, placed = [], set()
     for l in old:
-        if l.strip().startswith("{") and key(l) in shapes:
-            if not placed:
-                out += lines
-                placed = True
-            continue
+        if l.strip().startswith("{"):
+            key, lo, hi = parse(l)
+            if key in new and any(lo <= b and a <= hi for a, b in new[key]):
+                if key not in placed:
+                    out += [x for x in lines if parse(x)[0] == key]
+                    placed.add(key)
+                continue
         out.append(l)
-    if not placed:
-        out += lines
+    for key in new:
+        if key not in placed:
+            out += [x for x in lines if parse(x)[0] == key]
     with open(path, "w") as f:
         f.write("\n".join(out) + "\n")
 

@@ -27,9 +27,10 @@ def test_tc_candidates_span_cluster_sizes_and_tile_heights():
     c = tune.tc_candidates(16, 7168, 2112, num_sms=152)
     assert {x["split_k"] for x in c} == {1, 2, 4, 8}
     assert all(x["backend"] == 4 and x["stage_k"] in (128, 256) for x in c)
-    # row-range counts: the planner's (0) and those giving 4..16 groups of 8 rows per tile
-    assert {x["clusters"] for x in c if x["split_k"] == 8} == {0, 17, 22, 33, 44}   # 66 x 8 > 3 per SM
-    assert all(x["clusters"] * x["split_k"] <= 3 * 152 for x in c)
+    # row-range counts: the planner's (0) and those giving 6..16 groups of 8 rows per tile
+    # that fit one wave (clusters of 8: 34 at most)
+    assert {x["clusters"] for x in c if x["split_k"] == 8} == {0, 17, 22, 33}
+    assert all(x["clusters"] * x["split_k"] <= 2 * 152 for x in c)
     assert {x["split_k"] for x in tune.tc_candidates(16, 512, 256)} == {1, 2}   # K < 2 * S * 128 refused
 
 
@@ -75,3 +76,13 @@ def test_install_replaces_the_lines_of_tuned_shapes(tmp_path):
                      "{7168, 384, 1, 1, 1, 0, 0, 1, 0, 0},  // d"]
     tune.install(["{2880, 128, 1, 3, 1, 0, 0, 2, 0, 0},  // f"], str(path))   # a new shape goes at the end
     assert path.read_text().strip().split("\n")[-1].endswith("// f")
+    # a shape tuned over part of its M range keeps its lines outside that range:
+    # the new line meets no old one, so it goes at the end
+    tune.install(["{7168, 256, 17, 32, 4, 0, 8, 0, 0, 128, 34},  // g"], str(path))
+    lines = path.read_text().strip().split("\n")
+    assert "{7168, 256, 1, 2, 1, 0, 0, 1, 0, 0},  // a" in lines and lines[-1].endswith("// g")
+    # re-tuning M = 2..32 drops every line it meets: 1..2 and 17..32
+    tune.install(["{7168, 256, 2, 32, 2, 2, 4, 0, 0, 0, 0},  // h"], str(path))
+    lines = path.read_text().strip().split("\n")
+    assert not any(l.endswith("// a") or l.endswith("// g") for l in lines)
+    assert sum(l.endswith("// h") for l in lines) == 1
