@@ -126,7 +126,10 @@ typedef struct {
 } skinny_plan_t;
 
 typedef enum {
-    SKINNY_OPT_PDL = 1,              /* 0/1: programmatic dependent launch (default: env SKINNY_PDL, else 0) */
+    SKINNY_OPT_PDL = 1,              /* programmatic dependent launch: 0 off; 1 on for calls whose weight
+                                        is under 16 MB (larger, bandwidth-bound calls run without it:
+                                        measured faster on GB300); 2 on for every call (default: env
+                                        SKINNY_PDL = 1 or 2, else 0) */
     SKINNY_OPT_FORCE_BACKEND = 2,    /* skinny_backend_t; AUTO = dispatcher (tests / tuning only) */
     SKINNY_OPT_FORCE_CONSUMER = 3,   /* skinny_consumer_t for split-K; AUTO = dispatcher */
     SKINNY_OPT_FORCE_SPLIT_K = 4,    /* 0 = dispatcher, 1..8 = cluster size */
@@ -255,12 +258,13 @@ SKINNY_API skinny_status_t skinny_plan_for_f32w(const uint16_t *X, int ldx, cons
  *   W, Y, M (1..64), N, K, stream: as skinny_gemm_bf16 with X = XN.  K == 0 gives Y = 0 and
  *          leaves XN untouched.
  *
- * One launch when the GEMM's plan is tcgen05 and M <= 16 (and the option
- * SKINNY_OPT_FUSE_NORM is on): every CTA of the GEMM computes the r_m of all
- * tokens from X itself (the sum of squares in the same fixed order as the
- * norm kernel below, so the same bits), normalises the X of its own K slice
- * into shared memory and streams W meanwhile; the CTAs of the first row range
- * also store XN.  Otherwise two launches on `stream`: a norm kernel (one CTA
+ * One launch when the GEMM's plan is tcgen05 without a K split, M <= 16,
+ * X's rows are 16-byte aligned (pointer and ldx) and the option
+ * SKINNY_OPT_FUSE_NORM is on: every CTA of the GEMM loads the raw rows of X
+ * by TMA into shared memory, computes the r_m of all tokens (the sum of
+ * squares in the same fixed order as the norm kernel below, so the same
+ * bits), normalises X in place and streams W meanwhile; the CTAs of the first
+ * row range also store XN.  Otherwise two launches on `stream`: a norm kernel (one CTA
  * per token; fixed-order fp32 sum of squares, IEEE sqrt and division, one
  * bf16 rounding per element) and then the GEMM, with PDL letting the GEMM
  * stream W while the norm runs.  Either way bit-identical run to run, and the

@@ -62,8 +62,23 @@ int env_flag(const char *name) {
 }
 int opt_pdl() {
     int v = g_opt_pdl.load();
-    if (v < 0) { v = env_flag("SKINNY_PDL"); g_opt_pdl.store(v); }
+    if (v < 0) {
+        const char *e = std::getenv("SKINNY_PDL");
+        v = (e && std::strcmp(e, "2") == 0) ? 2 : env_flag("SKINNY_PDL");
+        g_opt_pdl.store(v);
+    }
     return v;
+}
+// Programmatic dependent launch for a call moving `w_bytes` of weight.  Mode 1
+// keeps it to calls under kPdlMaxWBytes: measured on GB300, a launch of a
+// bandwidth-bound call started early lands its CTAs on whichever SMs free up
+// first, unevenly, and a decode step of the projection weights ran 10% slower
+// with PDL than without; latency-bound calls (the router, the epilogue, the
+// norm) gain from it (a chain of 64 router calls: 176 against 293 us).
+constexpr double kPdlMaxWBytes = 16e6;
+int pdl_for(double w_bytes) {
+    const int v = opt_pdl();
+    return (v == 2 || (v == 1 && w_bytes < kPdlMaxWBytes)) ? 1 : 0;
 }
 int opt_log() {
     int v = g_opt_log.load();
@@ -398,7 +413,7 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
     const bool x_ok = (reinterpret_cast<uintptr_t>(X) & 15) == 0 && ldx % 8 == 0;
     const bool stream_ok = mma_ok && x_ok && M <= kMaxMSmall;
     const bool tc_ok = vec == 8 && x_ok;
-    const int pdl = opt_pdl();
+    const int pdl = pdl_for(2.0 * N * K);
 
     int backend = fb, consumer = fc, split = fs, bn = fbn, stages = fst, stage_k = g_opt_force_stage_k.load();
     int clusters = fgy;
@@ -630,7 +645,7 @@ bool plan_f32w(const float *W, int ldw, int M, int N, int K, int num_sms, skinny
     p->grid_y = 1;
     p->threads = kDotThreads;
     p->smem_bytes = dotprod_f32w_smem_bytes(M, bn, kc);
-    p->pdl = opt_pdl();
+    p->pdl = pdl_for(4.0 * N * K);
     return p->smem_bytes <= kMaxDynSmem;
 }
 
@@ -733,7 +748,8 @@ skinny_status_t skinny_rmsnorm_gemm_bf16(const uint16_t *X, int ldx, const uint1
     st = make_plan(XN, ldxn, W, ldw, M, N, K, d.num_sms, &plan);
     if (st != SKINNY_OK) return st;
     skinny_plan_t fused;
-    if (g_opt_fuse_norm.load() && tc_make_norm_plan(M, N, K, plan, &fused)) {
+    const bool x_rows_16 = (reinterpret_cast<uintptr_t>(X) & 15) == 0 && ldx % 8 == 0;   // the raw rows by TMA
+    if (g_opt_fuse_norm.load() && x_rows_16 && tc_make_norm_plan(M, N, K, plan, &fused)) {
         // one launch: the norm runs inside every CTA of the tcgen05 GEMM
         if (opt_log()) log_plan(M, N, K, ldw, fused);
         GemmArgs a{XN, ldxn, W, ldw, Y, ldy, M, N, K, 0};
@@ -820,7 +836,7 @@ skinny_status_t skinny_plan_for(const uint16_t *X, int ldx, const uint16_t *W, i
 skinny_status_t skinny_set_option(int option, int value) {
     switch (option) {
         case SKINNY_OPT_PDL:
-            if (value != 0 && value != 1) return SKINNY_ERR_INVALID_VALUE;
+            if (value < 0 || value > 2) return SKINNY_ERR_INVALID_VALUE;
             g_opt_pdl.store(value); return SKINNY_OK;
         case SKINNY_OPT_FORCE_BACKEND:
             if (value < 0 || value > 4) return SKINNY_ERR_INVALID_VALUE;

@@ -88,6 +88,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar) : "memory");
 }
+// Box at (0, c1 = row, c2 = 64-element K box) of a 3-D view [K/64][rows][64].
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c1, int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(c1), "r"(c2), "r"(bar) : "memory");
+}
 
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -153,6 +159,12 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
 struct TcMaps {
     CUtensorMap w[kWMaps];   // box heights 128, 64, 32, 16, 8 rows (64 K elements each)
     CUtensorMap x;           // box MT rows x 64 K elements
+    // K % 64 == 0: a whole ring stage in one copy.  3-D views of W / X as
+    // [K/64 boxes][rows][64 elements] (the box index strides 128 bytes), with
+    // boxes of kb x (VP or VP - 8 rows) x 64 and kb x MT x 64; they land as
+    // kb consecutive swizzled regions, the layout of a stage.
+    CUtensorMap w3[2];
+    CUtensorMap x3;
 };
 
 struct TcParams {
@@ -167,6 +179,7 @@ struct TcParams {
     int *status;
     uint64_t budget_ns;
     int out_bf16;
+    int stage3d;     // 1: K % 64 == 0, whole stages by the 3-D maps (tiles of VP or VP - 8 rows)
     // fused query RMS norm (NORM instantiations only): X = xn = rms_norm(xr) * gamma
     const uint16_t *xr;
     int64_t ldxr;
@@ -192,7 +205,16 @@ __host__ __device__ inline int tc_pad_bytes(int VP, int MT, int kb, int TM, int 
 }
 __host__ __device__ inline int tc_layout_bytes(int VP, int MT, int kb, int stages, int TM, int nxb) {
     return stages * tc_stage_bytes(VP, MT, kb, nxb) + nxb * MT * 128 + tc_pad_bytes(VP, MT, kb, TM, nxb) +
-           8 * (2 * stages + 2 * kNAcc + 2) + kTcTailBytes;
+           8 * (2 * stages + 2 * kNAcc + 3) + kTcTailBytes;
+}
+
+// The 3-D W map a tile of `rows` rows uses: 0 for VP rows, 1 for VP - 8, -1
+// when whole-stage copies are off or the height is neither.
+__host__ __device__ inline int tc_w3_map(int stage3d, int rows, int VP) {
+    if (!stage3d) return -1;
+    if (rows == VP) return 0;
+    if (rows == VP - 8 && VP > 8) return 1;
+    return -1;
 }
 
 __device__ __forceinline__ uint4 lds128(const void *p) {
@@ -224,45 +246,38 @@ __device__ __forceinline__ uint4 load_gamma(const uint16_t *g, int k0, int K) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Fused query RMS norm, run by the four draining warps (jt = 0..127, wq = warp
-// 0..3 among them) before any MMA: r_m = 1 / sqrtf(sum_k x^2 / K + eps) for
-// every token, in the exact order of the standalone norm kernel (thread jt
-// takes the 8-element chunks jt, jt + 128, ... of the whole row, one fused
-// multiply-add per element, then a warp butterfly and the warps in order), so
-// both give the same bits; the chunks of this rank's K slice are kept in the
-// resident X and then replaced by bf16_rn((x * r_m) * g_k) in the swizzled
-// layout the MMA reads.  Rows >= M and columns >= K hold zeros.  The CTAs of
-// row range 0 also store the normalised rows of their slice to xn.
+// Fused query RMS norm (one-rank plans: the resident X holds whole rows), run
+// by the four draining warps (jt = 0..127, wq = warp 0..3 among them) once the
+// raw rows have landed by TMA in the resident X, before any MMA: r_m =
+// 1 / sqrtf(sum_k x^2 / K + eps) for every token, in the exact order of the
+// standalone norm kernel (thread jt takes the 8-element chunks jt, jt + 128,
+// ... of the row, one fused multiply-add per element, then a warp butterfly
+// and the warps in order), so both give the same bits; then every element is
+// replaced in place by bf16_rn((x * r_m) * g_k) in the swizzled layout the MMA
+// reads.  Rows >= M and columns >= K hold zeros.  The CTAs of row range 0
+// also store the normalised rows to xn.
 template <int MT>
 __device__ __forceinline__ void norm_prologue(const TcParams &p, uint8_t *xres, float *rstat, float *part,
-                                              int kbeg, int kend, int nxb, bool write_xn, int jt, int wq,
-                                              int lane) {
+                                              int nxb, bool write_xn, int jt, int wq, int lane) {
     const int K = p.K, M = p.M;
     const int chunks = (K + 7) / 8;
     float ss[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) ss[m] = 0.f;
     for (int c = jt; c < chunks; c += 128) {
-        const int k0 = 8 * c;
-        uint4 q[MT];
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-            q[m] = (m < M) ? load_chunk_cg(p.xr + (int64_t)m * p.ldxr, k0, K) : make_uint4(0, 0, 0, 0);
+        const int box = c >> 3, ch = c & 7;
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            const uint32_t w[4] = {q[m].x, q[m].y, q[m].z, q[m].w};
+            if (m < M) {
+                const uint4 q = lds128(xres + box * MT * 128 + m * 128 + ((ch ^ (m & 7)) << 4));
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
-                ss[m] = fmaf(a, a, ss[m]);        // zeros past K add exactly nothing
-                ss[m] = fmaf(b, b, ss[m]);
+                for (int e = 0; e < 4; ++e) {
+                    const float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
+                    ss[m] = fmaf(a, a, ss[m]);    // zeros past K add exactly nothing
+                    ss[m] = fmaf(b, b, ss[m]);
+                }
             }
-        }
-        if (k0 >= kbeg && k0 < kend) {
-            const int off = k0 - kbeg, box = off >> 6, ch = (off >> 3) & 7;
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-                if (m < M) sts128(xres + box * MT * 128 + m * 128 + ((ch ^ (m & 7)) << 4), q[m]);
         }
     }
 #pragma unroll
@@ -281,35 +296,41 @@ __device__ __forceinline__ void norm_prologue(const TcParams &p, uint8_t *xres, 
         rstat[jt] = 1.0f / sqrtf(t / (float)K + p.eps);
     }
     named_bar_sync(2, 128);
-    for (int idx = jt; idx < MT * nxb * 8; idx += 128) {
-        const int m = idx % MT, rest = idx / MT, ch = rest & 7, box = rest >> 3;
-        const int k0 = kbeg + box * 64 + ch * 8;
-        uint8_t *addr = xres + box * MT * 128 + m * 128 + ((ch ^ (m & 7)) << 4);
-        uint4 out = make_uint4(0, 0, 0, 0);
-        if (m < M && k0 < kend) {
-            const uint4 raw = lds128(addr);
-            const uint4 gq = load_gamma(p.gamma, k0, K);
-            const float r = rstat[m];
-            const uint32_t xw[4] = {raw.x, raw.y, raw.z, raw.w}, gw[4] = {gq.x, gq.y, gq.z, gq.w};
-            uint32_t o[4];
+    // one 8-element chunk per step, its gains loaded once for all tokens
+    for (int cc = jt; cc < nxb * 8; cc += 128) {
+        const int box = cc >> 3, ch = cc & 7;
+        const int k0 = 8 * cc;
+        const bool live = k0 < K;
+        const uint4 gq = live ? load_gamma(p.gamma, k0, K) : make_uint4(0, 0, 0, 0);
+        const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t lo = f32_to_bf16_rn(bf16_lo(xw[e]) * r * bf16_lo(gw[e]));
-                const uint32_t hi = f32_to_bf16_rn(bf16_hi(xw[e]) * r * bf16_hi(gw[e]));
-                o[e] = lo | (hi << 16);
-            }
-            out = make_uint4(o[0], o[1], o[2], o[3]);
-            if (write_xn) {
-                uint16_t *dst = p.xn + (int64_t)m * p.ldxn + k0;
-                if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0 && k0 + 8 <= K) {
-                    *reinterpret_cast<uint4 *>(dst) = out;
-                } else {
-                    for (int e = 0; e < 8 && k0 + e < K; ++e)
-                        dst[e] = (uint16_t)(o[e >> 1] >> (16 * (e & 1)));
+        for (int m = 0; m < MT; ++m) {
+            uint8_t *addr = xres + box * MT * 128 + m * 128 + ((ch ^ (m & 7)) << 4);
+            uint4 out = make_uint4(0, 0, 0, 0);
+            if (m < M && live) {
+                const uint4 raw = lds128(addr);
+                const float r = rstat[m];
+                const uint32_t xw[4] = {raw.x, raw.y, raw.z, raw.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t lo = f32_to_bf16_rn(bf16_lo(xw[e]) * r * bf16_lo(gw[e]));
+                    const uint32_t hi = f32_to_bf16_rn(bf16_hi(xw[e]) * r * bf16_hi(gw[e]));
+                    o[e] = lo | (hi << 16);
+                }
+                out = make_uint4(o[0], o[1], o[2], o[3]);
+                if (write_xn) {
+                    uint16_t *dst = p.xn + (int64_t)m * p.ldxn + k0;
+                    if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0 && k0 + 8 <= K) {
+                        *reinterpret_cast<uint4 *>(dst) = out;
+                    } else {
+                        for (int e = 0; e < 8 && k0 + e < K; ++e)
+                            dst[e] = (uint16_t)(o[e >> 1] >> (16 * (e & 1)));
+                    }
                 }
             }
+            sts128(addr, out);
         }
-        sts128(addr, out);
     }
     fence_proxy_async_smem();                    // generic-proxy writes, read next by the MMAs
     named_bar_sync(2, 128);
@@ -339,7 +360,8 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
     auto acce = [&](int b) { return bars + 8u * (2 * stages + kNAcc + b); };
     const uint32_t done = bars + 8u * (2 * stages + 2 * kNAcc);
     const uint32_t xready = bars + 8u * (2 * stages + 2 * kNAcc + 1);   // fused norm: X is in place
-    uint8_t *tail = smem + (bars - base) + 8 * (2 * stages + 2 * kNAcc + 2);
+    const uint32_t xraw = bars + 8u * (2 * stages + 2 * kNAcc + 2);     // fused norm: raw X has landed
+    uint8_t *tail = smem + (bars - base) + 8 * (2 * stages + 2 * kNAcc + 3);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(tail);
     volatile int *fail = reinterpret_cast<volatile int *>(tail + 4);    // an accumulator was not drained
     volatile int *mma_ok = reinterpret_cast<volatile int *>(tail + 8);  // every issued MMA completed
@@ -365,6 +387,11 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
     if (tid == 0) {
         for (int i = 0; i < kWMaps; ++i) prefetch_tensormap(&maps.w[i]);
         prefetch_tensormap(&maps.x);
+        if (p.stage3d) {
+            prefetch_tensormap(&maps.w3[0]);
+            prefetch_tensormap(&maps.w3[1]);
+            prefetch_tensormap(&maps.x3);
+        }
         for (int s = 0; s < stages; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
@@ -375,6 +402,7 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
         }
         mbar_init(done, 1);
         mbar_init(xready, 1);
+        mbar_init(xraw, 1);
         *fail = 0;
         *mma_ok = 0;
         fence_mbarrier_init_cluster();
@@ -389,6 +417,34 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
                 const int t = i / nk, ks = i - t * nk;
                 const int rows = tile_rows(t), row0 = r0 + t * VP;
                 const uint32_t st = base + s * sbytes;
+                const int w3 = tc_w3_map(p.stage3d, rows, VP);
+                if (w3 >= 0 || (p.stage3d && !NORM)) {
+                    const int kbox = (kbeg >> 6) + ks * kb;
+                    if (w_part) {
+                        if (w3 >= 0) {
+                            tma_load_3d(st, &maps.w3[w3], row0, kbox, full(s));
+                        } else {
+                            // an odd tile height: per-box copies, regions VP rows apart
+                            for (int b = 0; b < kb; ++b) {
+                                int off = 0;
+#pragma unroll
+                                for (int h = 0; h < kWMaps; ++h) {
+                                    const int height = 128 >> h;
+                                    if (rows - off >= height) {
+                                        tma_load_2d(st + b * VP * 128 + off * 128, &maps.w[h], kbeg + (ks * kb + b) * 64,
+                                                    row0 + off, full(s));
+                                        off += height;
+                                    }
+                                }
+                            }
+                        }
+                    }
+                    if (x_part && p.stage3d) tma_load_3d(st + kb * VP * 128, &maps.x3, 0, kbox, full(s));
+                    else if (x_part)
+                        for (int b = 0; b < kb; ++b)
+                            tma_load_2d(st + kb * VP * 128 + b * MT * 128, &maps.x, kbeg + (ks * kb + b) * 64, 0, full(s));
+                    return;
+                }
                 for (int b = 0; b < kb; ++b) {
                     const int k0 = kbeg + (ks * kb + b) * 64;
                     if (w_part) {
@@ -414,6 +470,11 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
             griddep_wait();
             if (!NORM)
                 for (int i = 0; i < pre; ++i) issue(i, i, false, true);
+            if (NORM) {
+                // the raw rows of X (all K: the fused norm runs on one-rank plans), swizzled as the MMA reads them
+                mbar_arrive_expect_tx(xraw, (uint32_t)(nxb * MT * 128));
+                for (int b = 0; b < nxb; ++b) tma_load_2d(xres + b * MT * 128, &maps.x, b * 64, 0, xraw);
+            }
             int issued = pre;
             for (int i = pre; i < total; ++i) {
                 const int s = i % stages;
@@ -464,13 +525,15 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
                 tc_fence_after();
                 const uint32_t wst = base + s * sbytes;
                 const uint32_t xst = NORM ? xres + ks * kb * MT * 128 : wst + kb * VP * 128;
+                // a whole-stage 3-D copy packs the kb W regions at the tile's own height
+                const int wrows = tc_w3_map(p.stage3d, min(VP, r1 - (r0 + t * VP)), VP) == 1 ? VP - 8 : VP;
                 constexpr int P = tc_par(MT);
                 const int q0 = (ks % cs) * 4 * kb;           // MMAs of this chunk issued so far
                 for (int cb = 0; cb < kb; ++cb)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int q = q0 + 4 * cb + j;        // the chunk's first P MMAs overwrite
-                        umma_bf16(tmem + (uint32_t)((b * P + q % P) * MT), sw128_desc(wst + cb * VP * 128 + 32 * j),
+                        umma_bf16(tmem + (uint32_t)((b * P + q % P) * MT), sw128_desc(wst + cb * wrows * 128 + 32 * j),
                                   sw128_desc(xst + cb * MT * 128 + 32 * j), idesc, q < P ? 0u : 1u);
                     }
                 umma_commit(empty(s));               // the stage is free once these MMAs have read it
@@ -487,9 +550,15 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
         tc_fence_after();
         const uint32_t tmem = *tmem_slot;
         griddep_wait();                          // Y may be read or written by the preceding kernel
-        if (NORM)
-            norm_prologue<MT>(p, smem + (xres - base), rstat, npart, kbeg, kend, nxb, blockIdx.y == 0, tid - 64,
+        bool xok = true;
+        if (NORM) {
+            if (lane == 0) xok = mbar_wait_bounded(xraw, 0, p.budget_ns);
+            xok = __shfl_sync(0xffffffffu, xok ? 1 : 0, 0) != 0;
+            if (!xok && lane == 0) report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitX);
+            // every warp takes part in the barriers inside, whatever its wait gave
+            norm_prologue<MT>(p, smem + (xres - base), rstat, npart, nxb, blockIdx.y == 0, tid - 64,
                               warp - kAccWarp0, lane);
+        }
         if (NORM && tid == 64) mbar_arrive(xready);
         const int q = warp & 3;
         // accumulator row of this thread (M = 64: lanes 16..31 of each quarter hold none)
@@ -632,6 +701,21 @@ bool encode_bf16_2d(CUtensorMap *map, const void *ptr, int cols, int rows, int64
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 3-D view [ncols / 64][rows][64] of a bf16 [rows, ncols] matrix (ld in
+// elements; ncols a multiple of 64), boxes of kb x box_rows x 64, 128-byte
+// swizzle, zeros outside (box index or row past the end).
+bool encode_bf16_3d(CUtensorMap *map, const void *ptr, int ncols, int rows, int64_t ld, int box_rows, int kb) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || ncols % 64) return false;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(ncols / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)kb};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Row split of a plan: groups per tile (vg) for C ranges of G groups, tiles
 // of at most `max_vg` groups, as even as the ranges allow.
 int tc_groups_per_tile(int G, int C, int max_vg) {
@@ -667,45 +751,70 @@ int tc_smem_bytes(int M, int N, int K, int block_n, int stage_k, int stages, int
     return bytes + 1024;                         // slack for the 1024-byte alignment
 }
 
+// Default grid: a small cost model of what bounds the kernel, measured on GB300.
+// Each candidate (cluster size S, row ranges C) is scored by its most loaded
+// SM: the W bytes its CTAs stream (CTAs are placed evenly, so an SM holds
+// ceil(CTAs / SMs) of them) over the smaller of the SM's share of HBM (about
+// 45 GB/s) and the MMA issue rate (a small MMA about every 45 ns per SM,
+// carrying 32 bytes of W per useful tile row).  Clustered grids are held to
+// the clusters GB300 keeps resident at once (clusters of 4 and 8 do not fill
+// every GPC) and pay about a microsecond for their reduction.  Two CTAs per
+// SM only: one CTA with a ring twice as deep streams slower (a CTA's copies
+// land one stage at a time, about 0.85 us apart, whatever the depth), so
+// one-per-SM grids are left to explicit grid sizes.
+namespace {
+struct TcGrid { int per_sm, S, C; double cost; };
+TcGrid tc_default_grid(int G, int K, int bk, int num_sms, int force_s, int max_vg) {
+    TcGrid best{0, 0, 0, 1e30};
+    const int nk_all = (K + bk - 1) / bk;
+    for (int per_sm = kTcCtasPerSm; per_sm >= kTcCtasPerSm; --per_sm) {
+        const int slots = per_sm * num_sms;
+        for (int S = 1; S <= kSplitMaxCluster; S *= 2) {
+            if (force_s && S != force_s) continue;
+            if (!force_s && S > 1 && nk_all < 2 * S) break;   // each rank keeps two stages of K
+            // clusters resident at once (cudaOccupancyMaxActiveClusters on GB300):
+            // pairs fill every slot; fours about 95%; eights 95% at two CTAs per
+            // SM but 79% at one
+            const int pct = S <= 2 ? 100 : (S == 4 || per_sm >= 2) ? 90 : 75;
+            const int cap = (slots * pct) / (100 * S);
+            int C = cap < G ? cap : G;
+            if (S > 1 && (G + C - 1) / C > max_vg) continue;   // one tile per CTA
+            if (C < 1) continue;
+            const int gmax = (G + C - 1) / C;
+            const int vg = tc_groups_per_tile(G, C, max_vg);
+            const int ks = ((nk_all + S - 1) / S) * bk;
+            const int kk = ks < K ? ks : K;
+            const double cta_bytes = 8.0 * gmax * kk * 2.0;
+            const int per_sm_ctas = (C * S + num_sms - 1) / num_sms;
+            const double bw_hbm = 45e9, bw_mma = 32.0 * 8 * vg / 45e-9;
+            const double cost = per_sm_ctas * cta_bytes / (bw_mma < bw_hbm ? bw_mma : bw_hbm) + (S > 1 ? 1e-6 : 0.0);
+            if (cost < best.cost * 0.98) best = {per_sm, S, C, cost};
+        }
+    }
+    return best;
+}
+}  // namespace
+
 bool tc_make_plan(int M, int N, int K, int force_bn, int force_s, int force_stages, int force_bk, int force_c,
                   int num_sms, skinny_plan_t *p) {
     if (!tc_supported(M) || N < 1 || K < 1 || num_sms < 1) return false;
     if (force_bn && force_bn != 128 && force_bn != 64) return false;
     const int G = (N + 7) / 8;
-    const int slots = kTcCtasPerSm * num_sms;
     const int bk = force_bk ? force_bk : (K > 64 ? 128 : 64);
     if (bk < 64 || bk > kTcMaxBK || bk % 64) return false;
     const int nk_all = (K + bk - 1) / bk;         // ring stages over the whole K
-    // Rows per MMA: the tensor core issues a small MMA (N = 16..64 tokens, K =
-    // 16) in about 45 ns per SM whatever its M, so a tile must carry at least
-    // 64 useful W rows (2 KB of W per MMA) to keep up with HBM.  Clusters:
-    // at two CTAs per SM, GB300 keeps only about 97% / 95% of the slots
-    // resident for clusters of 4 / 8 (the GPCs' SM counts), so a split grid
-    // is held to 90% of the slots (one wave).
-    auto cap = [&](int s_) { return s_ == 1 ? slots : (slots * 9) / (10 * s_); };
-    auto vp_of = [&](int c_) { return 8 * tc_groups_per_tile(G, c_ < 1 ? 1 : c_, 16); };
-    int S = force_s;
-    if (S == 0) {
-        S = 1;
-        while (S < kSplitMaxCluster && nk_all >= 4 * S) {
-            int c = cap(S);
-            if (c > G) c = G;
-            if (vp_of(c) >= 64) break;
-            S *= 2;
-        }
+    const int max_vg_default = (force_bn == 64) ? 8 : 16;
+    int S = force_s, C = force_c, per_sm = kTcCtasPerSm;
+    if (S == 0 || C == 0) {
+        const TcGrid g = tc_default_grid(G, K, bk, num_sms, S, max_vg_default);
+        if (g.S == 0) return false;
+        if (S == 0) S = g.S;
+        if (C == 0) C = g.C;
+        per_sm = g.per_sm;
     }
     if (S < 1 || S > kSplitMaxCluster || (S & (S - 1))) return false;
-    const int max_vg_default = (force_bn == 64) ? 8 : 16;
-    int C = force_c;
-    if (C == 0) {
-        C = cap(S);
-        if (C > G) C = G;
-        // tiles of at least 64 rows where the rows allow it
-        if (vp_of(C) < 64 && G >= 8) C = (G + 7) / 8;
-        if (S > 1 && (G + C - 1) / C > max_vg_default) C = (G + max_vg_default - 1) / max_vg_default;
-        if (C < 1) C = 1;
-    }
     if (C < 1 || C > 65535 || C > G) return false;
+    if (force_s && force_c) per_sm = (int64_t)C * S <= num_sms ? 1 : kTcCtasPerSm;   // a forced grid's residency
     const int vg = tc_groups_per_tile(G, C, max_vg_default);
     const int VP = 8 * vg;
     if (S > 1 && (G + C - 1) / C > vg) return false;   // S > 1: one tile per CTA
@@ -716,7 +825,8 @@ bool tc_make_plan(int M, int N, int K, int force_bn, int force_s, int force_stag
     const int ntiles_max = ((G + C - 1) / C + vg - 1) / vg;
     int stages = force_stages;
     if (!stages) {
-        const int budget = kTcSmemBudget;
+        // two CTAs per SM: the ring within 110 KB; one: within the whole SM
+        const int budget = per_sm >= 2 ? kTcSmemBudget : kMaxDynSmem;
         stages = kSplitMaxStages;
         while (stages > 1 && tc_smem_bytes(M, N, K, bn, bk, stages, S, C, false) > budget) --stages;
         // no deeper than the CTA's stages, but deep enough to receive the partials
@@ -744,13 +854,17 @@ bool tc_make_plan(int M, int N, int K, int force_bn, int force_s, int force_stag
 }
 
 bool tc_make_norm_plan(int M, int N, int K, const skinny_plan_t &gemm, skinny_plan_t *p) {
-    if (gemm.backend != SKINNY_BACKEND_TCGEN05 || M < 1 || M > kTcNormMaxM) return false;
+    // one rank per range: the resident X then holds whole rows, so the raw rows
+    // arrive by TMA once and the sum of squares reads them from shared memory
+    if (gemm.backend != SKINNY_BACKEND_TCGEN05 || gemm.split_k != 1 || M < 1 || M > kTcNormMaxM) return false;
     *p = gemm;
     // the same split, tiles and stage length (so the same sums in the same
-    // order); the ring as deep as the budget leaves beside the resident X
-    int stages = gemm.stages;
+    // order) and the same CTAs per SM; the ring as deep as that budget leaves
+    // beside the resident X (one CTA per SM when the GEMM plan has one)
+    const int budget = gemm.smem_bytes > kTcSmemBudget + 2048 ? kMaxDynSmem : kTcSmemBudget;
+    int stages = kSplitMaxStages;
     while (stages > 1 && tc_smem_bytes(M, N, K, gemm.block_n, gemm.stage_k, stages, gemm.split_k, gemm.grid_y,
-                                       true) > kTcSmemBudget)
+                                       true) > budget)
         --stages;
     const int smem = tc_smem_bytes(M, N, K, gemm.block_n, gemm.stage_k, stages, gemm.split_k, gemm.grid_y, true);
     if (smem > kMaxDynSmem) return false;
@@ -787,7 +901,7 @@ cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCt
         pl.smem_bytes < tc_smem_bytes(a.M, a.N, a.K, TM, pl.stage_k, pl.stages, S, C, norm != nullptr) ||
         pl.smem_bytes > kMaxDynSmem)
         return cudaErrorInvalidValue;
-    if (norm && (a.M > kTcNormMaxM || !norm->xr || !norm->gamma || !norm->xn || a.out_bf16))
+    if (norm && (a.M > kTcNormMaxM || S != 1 || !norm->xr || !norm->gamma || !norm->xn || a.out_bf16))
         return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(a.X) & 15) || (a.ldx & 7) || (reinterpret_cast<uintptr_t>(a.W) & 15) ||
         (a.ldw & 7))
@@ -796,8 +910,21 @@ cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCt
     TcMaps maps;
     for (int h = 0; h < kWMaps; ++h)
         if (!encode_bf16_2d(&maps.w[h], a.W, a.K, a.N, a.ldw, 128 >> h)) return cudaErrorInvalidValue;
-    if (!encode_bf16_2d(&maps.x, a.X, a.K, a.M, a.ldx, 16 << idx)) return cudaErrorInvalidValue;
+    // the fused norm's X map reads the raw rows; otherwise X itself
+    if (norm && ((reinterpret_cast<uintptr_t>(norm->xr) & 15) || (norm->ldxr & 7))) return cudaErrorInvalidValue;
+    if (!encode_bf16_2d(&maps.x, norm ? norm->xr : a.X, a.K, a.M, norm ? norm->ldxr : a.ldx, 16 << idx))
+        return cudaErrorInvalidValue;
+    // whole-stage copies when K is a whole number of 64-element boxes (a 3-D
+    // view would otherwise read past the end of a row) and the maps encode
+    const int VP = 8 * vg, kb = pl.stage_k / 64;
+    int stage3d = (a.K % 64 == 0) ? 1 : 0;
+    if (stage3d) {
+        stage3d = encode_bf16_3d(&maps.w3[0], a.W, a.K, a.N, a.ldw, VP, kb) &&
+                  encode_bf16_3d(&maps.w3[1], a.W, a.K, a.N, a.ldw, VP > 8 ? VP - 8 : 8, kb) &&
+                  encode_bf16_3d(&maps.x3, norm ? norm->xr : a.X, a.K, a.M, norm ? norm->ldxr : a.ldx, 16 << idx, kb);
+    }
     TcParams p;
+    p.stage3d = stage3d;
     p.Y = a.Y;
     p.ldy = a.ldy;
     p.M = a.M;

@@ -162,7 +162,7 @@ def test_forced_options_and_restore():
             plan(8, 256, 7176)
 
 
-@pytest.mark.parametrize("opt,bad", [(sk.SKINNY_OPT_PDL, 2), (sk.SKINNY_OPT_FORCE_BACKEND, 5),
+@pytest.mark.parametrize("opt,bad", [(sk.SKINNY_OPT_PDL, 3), (sk.SKINNY_OPT_FORCE_BACKEND, 5),
                                      (sk.SKINNY_OPT_FORCE_SPLIT_K, 9), (sk.SKINNY_OPT_FORCE_BLOCK_N, 3),
                                      (sk.SKINNY_OPT_FORCE_STAGES, 17), (sk.SKINNY_OPT_WAIT_TIMEOUT_US, -1),
                                      (99, 0)])
@@ -293,10 +293,10 @@ def test_mid_m_takes_a_tensor_core_path():
     assert plan(40, 320, 7168)["backend"] == sk.SKINNY_BACKEND_SPLITK
     p = plan(40, 8192, 4096)
     assert (p["backend"], p["consumer"]) == (sk.SKINNY_BACKEND_TCGEN05, sk.SKINNY_CONSUMER_MMA)
-    # 1024 row groups: 304 ranges would give tiles of 32 rows, so K is split in
-    # two; clusters of 2 fill 90% of the slots (136 ranges of 7-8 groups: tiles
-    # of 64 rows, at least 2 KB of W per MMA)
-    assert (p["split_k"], p["stage_k"], p["grid_y"], p["block_n"]) == (2, 128, 136, 64)
+    # 1024 row groups: one range per CTA slot would give tiles of 32 rows (too
+    # few W bytes per MMA); the cost model takes clusters of 2 (152 ranges of
+    # 6-7 groups: tiles of up to 56 rows, two CTAs on every SM)
+    assert (p["split_k"], p["stage_k"], p["grid_y"], p["block_n"]) == (2, 128, 152, 64)
     check_tc_geometry(p, 40, 8192, 4096)
     # 9..16 tokens on large weights take it too; fewer stay on the earlier backends
     assert plan(12, 8192, 4096)["backend"] == sk.SKINNY_BACKEND_TCGEN05
@@ -569,3 +569,15 @@ def test_tcgen05_refuses_rows_a_tensor_map_cannot_address():
             assert e.value.status == sk.SKINNY_ERR_UNSUPPORTED
     for kw in (dict(X=A16 + 2), dict(ldx=4100)):
         assert plan(16, 4096, 4096, **kw)["backend"] != sk.SKINNY_BACKEND_TCGEN05
+
+
+def test_pdl_applies_to_latency_bound_calls():
+    """PDL mode 1 puts the attribute only on calls under 16 MB of weight; mode 2
+    on every call; 0 on none."""
+    with sk.options(pdl=1):
+        assert plan(4, 256, 7168)["pdl"] == 1                 # the router: 3.7 MB
+        assert plan(4, 24576, 1536)["pdl"] == 0               # a 75 MB projection
+    with sk.options(pdl=2):
+        assert plan(4, 24576, 1536)["pdl"] == 1
+    with sk.options(pdl=0):
+        assert plan(4, 256, 7168)["pdl"] == 0

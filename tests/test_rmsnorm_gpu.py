@@ -175,10 +175,11 @@ FUSED_CASES = [
     (3, 24576, 1536, {}),
     (8, 2112, 1536, {}),
     (16, 24576, 1536, {}),
-    (16, 2112, 1536, dict(split_k=2)),
-    (12, 300, 1536, dict(split_k=4, stage_k=64)),
+    (16, 2112, 1536, dict(split_k=1, clusters=33)),
+    (12, 300, 1536, dict(split_k=1, stage_k=64)),
     (7, 1000, 1000, {}),                       # K % 64 != 0: the last box is part zeros
-    (16, 520, 520, dict(split_k=2, stage_k=128)),
+    (16, 520, 520, dict(split_k=1, stage_k=128)),
+    (16, 2112, 1536, dict(split_k=2)),         # K split over a cluster: the two-launch form
 ]
 
 
@@ -203,15 +204,15 @@ def test_fused_norm_equals_two_launches(M, N, K, opts):
 
 
 def test_fused_norm_strided_and_misaligned_x_and_eps():
-    """X rows that are not 16-byte aligned (scalar loads) and several eps: the
-    fused form still equals the two-launch form."""
+    """Strided X rows (16-byte aligned: the fused form; not aligned: the
+    two-launch form) and several eps: both forms give the same bits."""
     case, X, W, G = make_case(5, 640, 1000, seed=3500)
-    for eps in (0.0, 1e-6, 0.5):
+    for eps, ldx in ((0.0, 1008), (1e-6, 1003), (0.5, 1016)):
         with sk.options(backend=sk.SKINNY_BACKEND_TCGEN05):
             with sk.options(fuse_norm=1):
-                xf, yf = run_norm(case, X, W, G, eps=eps, ldx=1003)
+                xf, yf = run_norm(case, X, W, G, eps=eps, ldx=ldx)
             with sk.options(fuse_norm=0):
-                xs, ys = run_norm(case, X, W, G, eps=eps, ldx=1003)
+                xs, ys = run_norm(case, X, W, G, eps=eps, ldx=ldx)
         assert np.array_equal(xf, xs) and np.array_equal(yf.view(np.uint32), ys.view(np.uint32)), eps
         check_xn(xf, oracle.rmsnorm(X, G, eps, 5, 1000), 1000)
 
