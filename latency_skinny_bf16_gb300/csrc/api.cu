@@ -220,34 +220,40 @@ bool plan_dotprod(int M, int N, int K, int vec, int force_bn, int num_sms, skinn
     return p->smem_bytes <= kMaxDynSmem;
 }
 
-// Dot-product layout with mma.sync arithmetic: block_n = 16 * row tiles.
-bool plan_dotmma(int M, int N, int K, int vec, int force_bn, int num_sms, skinny_plan_t *p) {
+// Dot-product layout with mma.sync arithmetic: block_n = 16 * row tiles;
+// split_k > 1 cuts K over the CTAs of a cluster (grid split_k x blocks).
+bool plan_dotmma(int M, int N, int K, int vec, int force_bn, int force_s, int num_sms, skinny_plan_t *p) {
     if (vec != 8 || K % 32 != 0 || K < 32) return false;
+    const int S = force_s > 0 ? force_s : 1;
+    if (!dotmma_split_ok(M, K, S)) return false;
     int bn = force_bn;
     if (bn == 0) {
         // enough CTAs for every SM, fewer X re-reads when N is large
         bn = 16;
-        while (bn < 64 && (N + 2 * bn - 1) / (2 * bn) >= 2 * num_sms) bn *= 2;
+        while (bn < 64 && (int64_t)S * ((N + 2 * bn - 1) / (2 * bn)) >= 2 * num_sms) bn *= 2;
     }
     if (!dotmma_supported(M, bn)) return false;
     const int MT = dotmma_tokens(M);
+    const int KS = S > 1 ? dotmma_k_slice(K, S) : K;
     // 8 / 16 tokens: 64 KB of X per CTA (3 CTAs per SM); 32 / 64: 96 KB, so
     // the chunks stay at least 768 elements long
     int kc = ((MT >= 32 ? 96 * 1024 : kMmaXBudget) / (2 * MT)) & ~31;
-    if (kc >= K) kc = K;
+    if (kc >= KS) kc = KS;
     if (kc < 32) kc = 32;
+    const int blocks = (N + bn - 1) / bn;
     p->backend = SKINNY_BACKEND_DOTPROD;
     p->consumer = SKINNY_CONSUMER_MMA;
     p->vec_elems = 8;
     p->block_n = bn;
-    p->split_k = 1;
+    p->split_k = S;
     p->stages = 0;
     p->stage_k = 0;
     p->k_chunk = kc;
-    p->grid_x = (N + bn - 1) / bn;
-    p->grid_y = 1;
+    p->grid_x = S > 1 ? S : blocks;
+    p->grid_y = S > 1 ? blocks : 1;
+    if (p->grid_y > 65535) return false;
     p->threads = kDotThreads;
-    p->smem_bytes = dotmma_smem_bytes(M, bn, kc);
+    p->smem_bytes = dotmma_smem_bytes(M, bn, kc, S);
     return p->smem_bytes <= kMaxDynSmem;
 }
 
@@ -454,6 +460,7 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
         } else if (e && e->backend == SKINNY_BACKEND_DOTPROD && e->consumer == SKINNY_CONSUMER_MMA && dotmma_ok) {
             backend = SKINNY_BACKEND_DOTPROD;
             if (!bn) bn = e->block_n;
+            if (!split) split = e->split_k;
             tuned = 1;
         }
     }
@@ -490,7 +497,12 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
     }
     bool ok;
     if (backend == SKINNY_BACKEND_DOTPROD && consumer == SKINNY_CONSUMER_MMA) {
-        ok = plan_dotmma(M, N, K, vec, bn, num_sms, p);
+        ok = plan_dotmma(M, N, K, vec, bn, split, num_sms, p);
+        if (!ok && tuned && fs == 0 && fbn == 0) {
+            // a tuned split these sizes cannot take: the one-CTA-per-block plan
+            ok = plan_dotmma(M, N, K, vec, 0, 0, num_sms, p);
+            tuned = 0;
+        }
         if (!ok && fb == SKINNY_BACKEND_AUTO && mid_m) {
             ok = plan_splitk(M, N, K, vec, consumer, fs, fst, fgy, g_opt_force_stage_k.load(), num_sms, p);
             tuned = 0;
@@ -526,7 +538,7 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
         ok = plan_stream(M, N, K, vec, x_ok, clusters, stages, stage_k, num_sms, p);
         if (!ok && fb == SKINNY_BACKEND_AUTO) {
             // a tuned or default streaming plan these pointers / sizes cannot use
-            ok = (dotmma_ok && M >= 4 && plan_dotmma(M, N, K, vec, 0, num_sms, p)) ||
+            ok = (dotmma_ok && M >= 4 && plan_dotmma(M, N, K, vec, 0, 0, num_sms, p)) ||
                  plan_dotprod(M, N, K, vec, 0, num_sms, p);
             tuned = 0;
         }
@@ -538,10 +550,10 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
             // a tuned tensor-core plan these pointers / strides cannot use: the
             // default rule of the token range
             const bool big = dotmma_ok && 2.0 * N * K >= 16e6;
-            ok = mid_m ? ((big && plan_dotmma(M, N, K, vec, 0, num_sms, p)) ||
+            ok = mid_m ? ((big && plan_dotmma(M, N, K, vec, 0, 0, num_sms, p)) ||
                           plan_splitk(M, N, K, vec, SKINNY_CONSUMER_MMA, fs, fst, fgy, g_opt_force_stage_k.load(),
                                       num_sms, p))
-                       : ((big && M >= 4 && plan_dotmma(M, N, K, vec, 0, num_sms, p)) ||
+                       : ((big && M >= 4 && plan_dotmma(M, N, K, vec, 0, 0, num_sms, p)) ||
                           plan_dotprod(M, N, K, vec, 0, num_sms, p));
             tuned = 0;
         }

@@ -23,6 +23,18 @@
 // rounded add.  The parts of a tile are added in a fixed order in shared
 // memory, so a plan's result is bit-identical from run to run.
 //
+// Cluster split of K (up to 16 tokens).  On small weights (the router shapes)
+// the CTAs of one column block are too few to keep HBM busy, so K is cut
+// into S slices of KS elements (a multiple of 32) taken by the S CTAs of a
+// thread-block cluster (grid S x blocks).  Each CTA sums its slice as above;
+// its partial of output (column c of the block, token m) goes by
+// st.shared::cluster into slot `rank` of CTA c % S, and after one
+// barrier.cluster arrive.release / wait.acquire that owner adds slots
+// 0..S-1 in order and writes Y: still bit-identical from run to run.  W
+// moves by plain 128-bit loads, every one of a CTA's loads in flight at once,
+// so a slice costs one DRAM round trip however short it is (the bulk-copy
+// ring of the split-K backend pays an issue cost per W row and stage).
+//
 // X sits in shared memory with a row stride of 64 (mod 128) bytes, so the
 // 128-bit reads of a quarter-warp (two rows x four 16-byte pieces) hit eight
 // different bank groups.  X rows that are 16-byte aligned arrive by bulk async
@@ -42,6 +54,21 @@ constexpr int kU = 4;   // 32-element K steps per warp per batch
 
 __host__ __device__ inline int xrow_bytes(int kc) { return ((kc * 2 + 127) & ~127) + 64; }
 
+}  // namespace
+
+// K elements per cluster rank: ceil(K / S) rounded up to a whole 32-element step.
+__host__ __device__ int dotmma_k_slice(int K, int S) { return ((K + S - 1) / S + 31) / 32 * 32; }
+
+// A split is usable when every rank gets some K and the partial slots stay small
+// (up to 16 tokens, clusters of up to 8).
+bool dotmma_split_ok(int M, int K, int S) {
+    if (S == 1) return true;
+    if (S < 1 || S > kSplitMaxCluster || M > 16) return false;
+    return (int64_t)(S - 1) * dotmma_k_slice(K, S) < K;
+}
+
+namespace {
+
 __device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
 
 template <int MT, int RT>
@@ -49,7 +76,7 @@ __global__ void __launch_bounds__(kDotThreads)
 dotmma_kernel(const uint16_t *__restrict__ X, int64_t ldx,
               const uint16_t *__restrict__ W, int64_t ldw,
               void *__restrict__ Y, int64_t ldy,
-              int M, int N, int K, int kc, int x_vec16, int *status, uint64_t budget_ns, int out_bf16)
+              int M, int N, int K, int kc, int x_vec16, int *status, uint64_t budget_ns, int out_bf16, int S)
 {
     constexpr int P = kWarps / RT;    // K parts per row tile
     constexpr int NT = MT / 8;        // n8 token tiles
@@ -58,11 +85,18 @@ dotmma_kernel(const uint16_t *__restrict__ X, int64_t ldx,
     const int xrowb = xrow_bytes(kc);
     uint8_t *xs = smem;                                              // [MT][xrowb]
     float *red = reinterpret_cast<float *>(smem + MT * xrowb);       // [RT][P][16][MT]
+    float *slots = red + kWarps * 16 * MT;                           // S > 1: [S][RT * 16][MT]
+
+    // S > 1: grid S x blocks, this CTA takes K slice `rank` of column block `blk`
+    const int rank = (S > 1) ? (int)blockIdx.x : 0;
+    const int blk = (S > 1) ? (int)blockIdx.y : (int)blockIdx.x;
+    const int KS = (S > 1) ? dotmma_k_slice(K, S) : K;
+    const int kbeg = rank * KS, kend = min(K, kbeg + KS);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tile = warp % RT, part = warp / RT;
     const int g = lane >> 2, t = lane & 3;
-    const int n0 = (blockIdx.x * RT + tile) * 16;
+    const int n0 = (blk * RT + tile) * 16;
     // rows past N re-read row N-1; their sums are dropped
     const uint16_t *w0 = W + (int64_t)min(n0 + g, N - 1) * ldw + 8 * t;
     const uint16_t *w1 = W + (int64_t)min(n0 + g + 8, N - 1) * ldw + 8 * t;
@@ -72,6 +106,7 @@ dotmma_kernel(const uint16_t *__restrict__ X, int64_t ldx,
         fence_mbarrier_init_cluster();
     }
     __syncthreads();
+    if (S > 1) cluster_arrive_relaxed();   // phase 0: this CTA's slots may be written from now on
 
     float macc[NT][4];
 #pragma unroll
@@ -120,14 +155,14 @@ dotmma_kernel(const uint16_t *__restrict__ X, int64_t ldx,
             for (int q = 0; q < 4; ++q) macc[h][q] += d[h][q];
     };
 
-    load(A0[0], A1[0], 0, min(kc, K) / 32, 0);   // W is a weight: in flight before the PDL wait
+    load(A0[0], A1[0], kbeg, max(0, min(kc, kend - kbeg)) / 32, 0);   // W is a weight: in flight before the PDL wait
     griddep_wait();
     griddep_launch_dependents();
 
-    for (int k0 = 0; k0 < K; k0 += kc) {
-        const int klen = min(kc, K - k0);
+    for (int k0 = kbeg; k0 < kend; k0 += kc) {
+        const int klen = min(kc, kend - k0);
         const int nsteps = klen / 32;
-        if (k0 > 0) {
+        if (k0 > kbeg) {
             __syncthreads();                     // every warp is done with the previous X chunk
             load(A0[0], A1[0], k0, nsteps, 0);
         }
@@ -142,7 +177,7 @@ dotmma_kernel(const uint16_t *__restrict__ X, int64_t ldx,
                 for (int r = lane; r < M; r += 32)
                     bulk_copy_g2s(smem_u32(xs + r * xrowb), X + r * ldx + k0, (uint32_t)(klen * 2), xbar);
             }
-            const uint32_t par = (uint32_t)((k0 / kc) & 1);
+            const uint32_t par = (uint32_t)(((k0 - kbeg) / kc) & 1);
             if (!mbar_wait_bounded(xbar, par, budget_ns)) {
                 if (lane == 0) report_status(status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitX);
                 if (!mbar_wait_bounded(xbar, par, 200ull * 1000 * 1000) && lane == 0)
@@ -177,21 +212,41 @@ dotmma_kernel(const uint16_t *__restrict__ X, int64_t ldx,
             red[((tile * P + part) * 16 + row) * MT + tok] = macc[h][q];
         }
     __syncthreads();
+    if (S > 1) cluster_wait();             // phase 0: every peer has started
     for (int i = tid; i < RT * 16 * M; i += kDotThreads) {
         const int tl = i / (16 * M), rem = i - tl * 16 * M;
         const int row = rem / M, m = rem - row * M;
-        const int n = (blockIdx.x * RT + tl) * 16 + row;
+        const int n = (blk * RT + tl) * 16 + row;
         if (n < N) {
             float v = red[((tl * P + 0) * 16 + row) * MT + m];
 #pragma unroll
             for (int pp = 1; pp < P; ++pp) v += red[((tl * P + pp) * 16 + row) * MT + m];
-            store_y(Y, out_bf16, m * ldy + n, v);
+            if (S == 1) {
+                store_y(Y, out_bf16, m * ldy + n, v);
+            } else {
+                const int c = tl * 16 + row;                     // column within the block
+                const uint32_t local = smem_u32(slots + (rank * RT * 16 + c) * MT + m);
+                st_shared_cluster_f32(mapa_shared(local, (uint32_t)(c % S)), v);
+            }
+        }
+    }
+    if (S > 1) {
+        cluster_arrive_release();          // phase 1: the partials are in their owners' slots
+        cluster_wait_acquire();
+        for (int i = tid; i < RT * 16 * M; i += kDotThreads) {
+            const int c = i / M, m = i - c * M;
+            const int n = blk * RT * 16 + c;
+            if (c % S == rank && n < N) {
+                float v = slots[c * MT + m];
+                for (int r = 1; r < S; ++r) v += slots[(r * RT * 16 + c) * MT + m];
+                store_y(Y, out_bf16, m * ldy + n, v);
+            }
         }
     }
 }
 
 using MmaKernel = void (*)(const uint16_t *, int64_t, const uint16_t *, int64_t, void *, int64_t,
-                           int, int, int, int, int, int *, uint64_t, int);
+                           int, int, int, int, int, int *, uint64_t, int, int);
 
 // token buckets 8 / 16 / 32 / 64 (M = 17..64: the medium-M regime on large weights)
 const MmaKernel kTable[4][3] = {
@@ -212,10 +267,9 @@ bool dotmma_supported(int M, int block_n) { return M >= 1 && M <= kMaxMSplitMma 
 
 int dotmma_tokens(int M) { return 8 << bucket(M); }
 
-int dotmma_smem_bytes(int M, int block_n, int k_chunk) {
-    (void)block_n;
+int dotmma_smem_bytes(int M, int block_n, int k_chunk, int split_k) {
     const int MT = dotmma_tokens(M);
-    return MT * xrow_bytes(k_chunk) + kWarps * 16 * MT * 4;
+    return MT * xrow_bytes(k_chunk) + kWarps * 16 * MT * 4 + (split_k > 1 ? split_k * block_n * MT * 4 : 0);
 }
 
 cudaError_t dotmma_prepare() {
@@ -229,21 +283,37 @@ cudaError_t dotmma_prepare() {
 
 cudaError_t launch_dotmma(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c) {
     const int ri = rt_index(p.block_n);
-    if (ri < 0 || a.M < 1 || a.M > kMaxMSplitMma || a.K % 32 != 0 || p.k_chunk % 32 != 0) return cudaErrorInvalidValue;
+    const int S = p.split_k;
+    if (ri < 0 || a.M < 1 || a.M > kMaxMSplitMma || a.K % 32 != 0 || p.k_chunk % 32 != 0 || p.k_chunk < 32 ||
+        !dotmma_split_ok(a.M, a.K, S))
+        return cudaErrorInvalidValue;
+    const int blocks = (a.N + p.block_n - 1) / p.block_n;
+    if ((S == 1 && (p.grid_x != blocks || p.grid_y != 1)) || (S > 1 && (p.grid_x != S || p.grid_y != blocks)) ||
+        p.smem_bytes < dotmma_smem_bytes(a.M, p.block_n, p.k_chunk, S))
+        return cudaErrorInvalidValue;
     MmaKernel fn = kTable[bucket(a.M)][ri];
     const int x_vec16 = ((reinterpret_cast<uintptr_t>(a.X) & 15) == 0 && (a.ldx & 7) == 0) ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.grid_x, 1, 1);
+    cfg.gridDim = dim3(p.grid_x, p.grid_y, 1);
     cfg.blockDim = dim3(kDotThreads, 1, 1);
     cfg.dynamicSmemBytes = p.smem_bytes;
     cfg.stream = c.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
+    ++n;
+    if (S > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = S;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, fn, a.X, a.ldx, a.W, a.ldw, a.Y, a.ldy, a.M, a.N, a.K, p.k_chunk, x_vec16,
-                              c.status, c.budget_ns, a.out_bf16);
+                              c.status, c.budget_ns, a.out_bf16, S);
 }
 
 }  // namespace skinny

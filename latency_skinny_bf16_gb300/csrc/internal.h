@@ -41,7 +41,9 @@ cudaError_t dotprod_prepare();   // per-device kernel attributes
 cudaError_t launch_dotprod(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
 
 // ---- dot-product backend with mma.sync arithmetic (dotmma.cu): block_n 16/32/64
-int dotmma_smem_bytes(int M, int block_n, int k_chunk);
+int dotmma_smem_bytes(int M, int block_n, int k_chunk, int split_k);
+__host__ __device__ int dotmma_k_slice(int K, int S);   // K elements per cluster rank
+bool dotmma_split_ok(int M, int K, int S);              // S == 1, or a cluster split K can take
 bool dotmma_supported(int M, int block_n);
 int dotmma_tokens(int M);   // token bucket of the instantiation: 8, 16, 32 or 64
 cudaError_t dotmma_prepare();

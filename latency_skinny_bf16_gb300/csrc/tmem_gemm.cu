@@ -57,6 +57,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace skinny {
 namespace {
@@ -76,24 +77,6 @@ __host__ __device__ constexpr int tmem_cols(int MT) { return kNAcc * tc_par(MT) 
 // Ring stages per accumulator chunk: at most 16 MMAs (4 per 64-element box)
 // accumulate in tensor memory before the chunk is drained into registers.
 __host__ __device__ inline int tc_chunk_stages(int kb) { return kb >= 4 ? 1 : 4 / kb; }
-
-// ------------------------------------------------------------------ TMA (tensor maps)
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
-    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-// Box at (c0 = K element, c1 = row) of a 2-D tensor map into shared memory,
-// completing on `bar`.  c0 is a multiple of 64 (128 bytes).
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar) : "memory");
-}
-// Box at (0, c1 = row, c2 = 64-element K box) of a 3-D view [K/64][rows][64].
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c1, int c2, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(c1), "r"(c2), "r"(bar) : "memory");
-}
 
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -672,9 +655,19 @@ const TcKernel kTcNorm[2] = {&tmem_gemm_kernel<16, 128, true>, &tmem_gemm_kernel
 
 int tc_index(int M) { return M <= 16 ? 0 : M <= 32 ? 1 : 2; }
 
+// Row split of a plan: groups per tile (vg) for C ranges of G groups, tiles
+// of at most `max_vg` groups, as even as the ranges allow.
+int tc_groups_per_tile(int G, int C, int max_vg) {
+    const int gmax = (G + C - 1) / C;
+    const int T = (gmax + max_vg - 1) / max_vg;
+    return (gmax + T - 1) / T;
+}
+
+}  // namespace
+
 // The driver's tensor-map encoder, resolved once through the runtime (no link
 // against the driver library).
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *f = nullptr;
         cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
@@ -716,15 +709,6 @@ bool encode_bf16_3d(CUtensorMap *map, const void *ptr, int ncols, int rows, int6
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Row split of a plan: groups per tile (vg) for C ranges of G groups, tiles
-// of at most `max_vg` groups, as even as the ranges allow.
-int tc_groups_per_tile(int G, int C, int max_vg) {
-    const int gmax = (G + C - 1) / C;
-    const int T = (gmax + max_vg - 1) / max_vg;
-    return (gmax + T - 1) / T;
-}
-
-}  // namespace
 
 int tc_tokens(int M) { return 16 << tc_index(M); }
 

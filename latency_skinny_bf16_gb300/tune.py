@@ -82,6 +82,10 @@ def candidates(M: int, K: int, N: int = 0, num_sms: int = 152):
     if K % 32 == 0:
         for bn in (16, 32, 64):
             out.append(dict(backend=1, block_n=bn, consumer=2, split_k=0, stages=0, stage_k=0))
+        # K over a cluster of S CTAs (W by plain loads, DSMEM reduce)
+        for s in (2, 4, 8):
+            for bn in (16, 32):
+                out.append(dict(backend=1, block_n=bn, consumer=2, split_k=s, stages=0, stage_k=0))
     for cons in (1, 2):
         if cons == 2 and K % 16:
             continue

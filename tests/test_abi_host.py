@@ -581,3 +581,23 @@ def test_pdl_applies_to_latency_bound_calls():
         assert plan(4, 24576, 1536)["pdl"] == 1
     with sk.options(pdl=0):
         assert plan(4, 256, 7168)["pdl"] == 0
+
+
+def test_dotmma_cluster_split_plans():
+    """K over a cluster of S CTAs on the tensor-core dot-product: grid S x blocks, a K chunk no
+    longer than a rank's slice, slot bytes in the shared memory; refused past 16 tokens and
+    where a rank would get no K."""
+    dm = dict(backend=sk.SKINNY_BACKEND_DOTPROD, consumer=sk.SKINNY_CONSUMER_MMA)
+    for (M, N, K, S, bn) in ((16, 256, 7168, 8, 16), (12, 384, 7168, 4, 32), (5, 2112, 7168, 2, 64)):
+        with sk.options(split_k=S, block_n=bn, **dm):
+            p = plan(M, N, K)
+        ks = -(-(-(-K // S)) // 32) * 32
+        assert (p["backend"], p["consumer"], p["split_k"], p["block_n"]) == (1, 2, S, bn)
+        assert (p["grid_x"], p["grid_y"]) == (S, -(-N // bn))
+        assert p["k_chunk"] % 32 == 0 and p["k_chunk"] <= ks and (S - 1) * ks < K
+        mt = 8 if M <= 8 else 16
+        assert p["smem_bytes"] >= S * bn * mt * 4 + mt * p["k_chunk"] * 2
+    for (M, N, K, S) in ((17, 256, 7168, 2), (8, 256, 64, 8), (16, 256, 96, 4)):
+        with sk.options(split_k=S, **dm):
+            with pytest.raises(sk.SkinnyError):
+                plan(M, N, K)

@@ -42,6 +42,7 @@ VARIANTS = [
     ("tc_s4_bn128", dict(backend=TC, split_k=4, block_n=128, stage_k=128), (8, 16, 64)),
     ("tc_tuned", dict(backend=TC), (2, 16, 40)),
     ("dotmma", dict(backend=DOT, consumer=MMA), (4, 8, 16, 32, 64)),
+    ("dotmma_s4", dict(backend=DOT, consumer=MMA, split_k=4), (4, 16)),
     ("splitk_mma_s4", dict(backend=SPLIT, consumer=MMA, split_k=4), (5, 16, 32)),
     ("splitk_mma_s8", dict(backend=SPLIT, consumer=MMA, split_k=8), (8, 16, 64)),
     ("splitk_fma_s8", dict(backend=SPLIT, consumer=FMA, split_k=8), (5, 16)),

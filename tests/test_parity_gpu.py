@@ -90,6 +90,11 @@ def _variants(case):
     if case.K % 32 == 0:
         for bn in (16, 32, 64):
             out.append(dict(backend=sk.SKINNY_BACKEND_DOTPROD, consumer=sk.SKINNY_CONSUMER_MMA, block_n=bn))
+        if case.M <= 16:
+            # K over a cluster of S CTAs (refused on the host when a rank would get no K)
+            for s, bn in ((2, 16), (4, 64), (8, 16)):
+                out.append(dict(backend=sk.SKINNY_BACKEND_DOTPROD, consumer=sk.SKINNY_CONSUMER_MMA, block_n=bn,
+                                split_k=s))
     for cons in (sk.SKINNY_CONSUMER_FMA, sk.SKINNY_CONSUMER_MMA):
         if cons == sk.SKINNY_CONSUMER_MMA and case.K % 16:
             continue
@@ -144,6 +149,37 @@ def test_dotmma_shapes(M, bn):
         p = b.plan()
         assert (p["consumer"], p["block_n"]) == (sk.SKINNY_CONSUMER_MMA, bn)
         b2 = run_and_check(case, ldx=case.K + 3, x_offset=1)     # X rows not 16-byte aligned
+    assert sk.skinny_get_device_status() == 0
+
+
+@pytest.mark.parametrize("M", [1, 5, 9, 16])
+@pytest.mark.parametrize("S,bn", [(2, 16), (3, 32), (4, 16), (8, 64)])
+def test_dotmma_cluster_split(M, S, bn):
+    """K cut over a cluster of S CTAs: ragged N, K = 32 * odd (a short last slice), X strided or
+    misaligned (staged by plain loads), partials summed through DSMEM in rank order: bit-identical."""
+    case = si.Case("dms", M=M, N=16 * 9 + 7, K=32 * 45, seed=1100 + 10 * M + S)
+    with sk.options(backend=sk.SKINNY_BACKEND_DOTPROD, consumer=sk.SKINNY_CONSUMER_MMA, block_n=bn, split_k=S):
+        b = run_and_check(case, ldx=case.K + 40, ldy=case.N + 5)
+        p = b.plan()
+        assert (p["consumer"], p["block_n"], p["split_k"]) == (sk.SKINNY_CONSUMER_MMA, bn, S)
+        assert (p["grid_x"], p["grid_y"]) == (S, -(-case.N // bn))
+        first = b.y_mat().copy()
+        for _ in range(5):
+            assert b.run() == sk.SKINNY_OK
+            assert np.array_equal(b.y_mat().view(np.uint32), first.view(np.uint32))
+        run_and_check(case, ldx=case.K + 3, x_offset=1)
+    assert sk.skinny_get_device_status() == 0
+
+
+@pytest.mark.parametrize("M,N,K,S", [(16, 256, 7168, 8), (12, 384, 7168, 4), (16, 256, 4096, 8), (8, 128, 2880, 2),
+                                     (16, 2112, 7168, 2)])
+def test_dotmma_cluster_split_router_shapes(M, N, K, S):
+    """The router and projection shapes the cluster split serves, full size, against the oracle."""
+    case = si.Case(f"dmr_M{M}_N{N}_K{K}_S{S}", M=M, N=N, K=K, seed=1200 + M + S, ldy=N + 64)
+    with sk.options(backend=sk.SKINNY_BACKEND_DOTPROD, consumer=sk.SKINNY_CONSUMER_MMA, split_k=S):
+        b = run_and_check(case)
+        assert b.plan()["split_k"] == S
+        assert b.canary_ok()
     assert sk.skinny_get_device_status() == 0
 
 

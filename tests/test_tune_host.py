@@ -86,3 +86,10 @@ def test_install_replaces_the_lines_of_tuned_shapes(tmp_path):
     lines = path.read_text().strip().split("\n")
     assert not any(l.endswith("// a") or l.endswith("// g") for l in lines)
     assert sum(l.endswith("// h") for l in lines) == 1
+
+
+def test_candidates_include_cluster_split_dot_product():
+    c = tune.candidates(16, 7168, 256)
+    splits = {(x["split_k"], x["block_n"]) for x in c if x["backend"] == 1 and x["consumer"] == 2}
+    assert {(2, 16), (4, 16), (8, 32)} <= splits
+    assert not any(x["backend"] == 1 and x["split_k"] > 1 for x in tune.candidates(16, 7176, 256))   # K % 32
