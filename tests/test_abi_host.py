@@ -134,7 +134,8 @@ def test_default_rule_tensor_core_dotprod_for_large_weights():
     assert (p["backend"], p["consumer"]) == (sk.SKINNY_BACKEND_DOTPROD, sk.SKINNY_CONSUMER_MMA)
     assert p["block_n"] in (16, 32, 64) and p["grid_x"] * p["block_n"] >= 8192
     p = plan(2, 2112, 7168)
-    assert p["grid_x"] * p["block_n"] >= 2112
+    blocks = p["grid_y"] if p["split_k"] > 1 else p["grid_x"]     # a cluster split: grid split_k x blocks
+    assert blocks * p["block_n"] >= 2112
 
 
 def test_x_chunking_for_large_m_times_k():
