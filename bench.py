@@ -73,7 +73,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="projection")
     p.add_argument("--no-per-config", action="store_true", help="skip the router workloads' figures")
-    p.add_argument("--pdl", type=int, choices=[0, 1], default=1)
+    p.add_argument("--pdl", type=int, choices=[0, 1, 2], default=1)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget (s)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")

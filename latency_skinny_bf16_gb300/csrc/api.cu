@@ -80,6 +80,9 @@ int pdl_for(double w_bytes) {
     const int v = opt_pdl();
     return (v == 2 || (v == 1 && w_bytes < kPdlMaxWBytes)) ? 1 : 0;
 }
+
+// Weights of 16 MB and more: the next launch starts late (see LaunchCtx::late).
+bool late_trigger(double w_bytes) { return w_bytes >= 16e6; }
 int opt_log() {
     int v = g_opt_log.load();
     if (v < 0) { v = env_flag("SKINNY_LOG"); g_opt_log.store(v); }
@@ -614,7 +617,7 @@ skinny_status_t run_gemm(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
     if (st != SKINNY_OK) return st;
     if (opt_log()) log_plan(M, N, K, ldw, plan);
     GemmArgs a{X, ldx, W, ldw, Y, ldy, M, N, K, out_bf16};
-    LaunchCtx c{s, plan.pdl != 0, d.status_word, (uint64_t)g_opt_wait_us.load() * 1000ull};
+    LaunchCtx c{s, plan.pdl != 0, late_trigger(2.0 * N * K), d.status_word, (uint64_t)g_opt_wait_us.load() * 1000ull};
     cudaError_t e;
     if (plan.backend == SKINNY_BACKEND_DOTPROD)
         e = plan.consumer == SKINNY_CONSUMER_MMA ? launch_dotmma(a, plan, c) : launch_dotprod(a, plan, c);
@@ -714,7 +717,7 @@ skinny_status_t skinny_gemm_bf16_f32w(const uint16_t *X, int ldx, const float *W
     }
     skinny_plan_t plan;
     if (!plan_f32w(W, ldw, M, N, K, d.num_sms, &plan)) return SKINNY_ERR_UNSUPPORTED;
-    LaunchCtx c{s, plan.pdl != 0, d.status_word, (uint64_t)g_opt_wait_us.load() * 1000ull};
+    LaunchCtx c{s, plan.pdl != 0, false, d.status_word, (uint64_t)g_opt_wait_us.load() * 1000ull};
     const cudaError_t e = launch_dotprod_f32w(X, ldx, W, ldw, Y, ldy, M, N, K, plan, c);
     return e == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
 }
@@ -765,7 +768,7 @@ skinny_status_t skinny_rmsnorm_gemm_bf16(const uint16_t *X, int ldx, const uint1
         // one launch: the norm runs inside every CTA of the tcgen05 GEMM
         if (opt_log()) log_plan(M, N, K, ldw, fused);
         GemmArgs a{XN, ldxn, W, ldw, Y, ldy, M, N, K, 0};
-        LaunchCtx c{static_cast<cudaStream_t>(stream), plan.pdl != 0, d.status_word,
+        LaunchCtx c{static_cast<cudaStream_t>(stream), plan.pdl != 0, late_trigger(2.0 * N * K), d.status_word,
                     (uint64_t)g_opt_wait_us.load() * 1000ull};
         const TcNormArgs na{X, ldx, gamma, eps, XN, ldxn};
         return launch_tc(a, fused, c, &na) == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;

@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(kDotThreads)
 dotmma_kernel(const uint16_t *__restrict__ X, int64_t ldx,
               const uint16_t *__restrict__ W, int64_t ldw,
               void *__restrict__ Y, int64_t ldy,
-              int M, int N, int K, int kc, int x_vec16, int *status, uint64_t budget_ns, int out_bf16, int S)
+              int M, int N, int K, int kc, int x_vec16, int *status, uint64_t budget_ns, int out_bf16, int S,
+              int late)
 {
     constexpr int P = kWarps / RT;    // K parts per row tile
     constexpr int NT = MT / 8;        // n8 token tiles
@@ -157,7 +158,7 @@ dotmma_kernel(const uint16_t *__restrict__ X, int64_t ldx,
 
     load(A0[0], A1[0], kbeg, max(0, min(kc, kend - kbeg)) / 32, 0);   // W is a weight: in flight before the PDL wait
     griddep_wait();
-    griddep_launch_dependents();
+    if (!late) griddep_launch_dependents();
 
     for (int k0 = kbeg; k0 < kend; k0 += kc) {
         const int klen = min(kc, kend - k0);
@@ -201,6 +202,7 @@ dotmma_kernel(const uint16_t *__restrict__ X, int64_t ldx,
         }
     }
 
+    if (late) griddep_launch_dependents();   // every W load of this thread has been issued
     // ---- fragments to shared memory: thread (g, t) holds rows g, g+8 for
     // tokens 2t, 2t+1 of each n8 tile; then the P parts of a tile in order
 #pragma unroll
@@ -246,7 +248,7 @@ dotmma_kernel(const uint16_t *__restrict__ X, int64_t ldx,
 }
 
 using MmaKernel = void (*)(const uint16_t *, int64_t, const uint16_t *, int64_t, void *, int64_t,
-                           int, int, int, int, int, int *, uint64_t, int, int);
+                           int, int, int, int, int, int *, uint64_t, int, int, int);
 
 // token buckets 8 / 16 / 32 / 64 (M = 17..64: the medium-M regime on large weights)
 const MmaKernel kTable[4][3] = {
@@ -313,7 +315,7 @@ cudaError_t launch_dotmma(const GemmArgs &a, const skinny_plan_t &p, const Launc
     cfg.attrs = attr;
     cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, fn, a.X, a.ldx, a.W, a.ldw, a.Y, a.ldy, a.M, a.N, a.K, p.k_chunk, x_vec16,
-                              c.status, c.budget_ns, a.out_bf16, S);
+                              c.status, c.budget_ns, a.out_bf16, S, c.late ? 1 : 0);
 }
 
 }  // namespace skinny

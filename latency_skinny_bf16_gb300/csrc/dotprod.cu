@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kDotThreads)
 dotprod_kernel(const uint16_t *__restrict__ X, int64_t ldx,
                const uint16_t *__restrict__ W, int64_t ldw,
                void *__restrict__ Y, int64_t ldy,
-               int N, int K, int kc, int x_vec16, int *status, uint64_t budget_ns, int out_bf16)
+               int N, int K, int kc, int x_vec16, int *status, uint64_t budget_ns, int out_bf16, int late)
 {
     // Loads in flight per thread per step: U vectors of each of the BN rows.
     constexpr int U = (BN >= 8) ? 1 : 8 / BN;
@@ -171,7 +171,7 @@ dotprod_kernel(const uint16_t *__restrict__ X, int64_t ldx,
         load_batch(rawA, 0, klen0 / VW, tid);
     }
     griddep_wait();
-    griddep_launch_dependents();
+    if (!late) griddep_launch_dependents();
 
     for (int k0 = 0; k0 < K; k0 += kc) {
         const int klen = min(kc, K - k0);
@@ -256,6 +256,7 @@ dotprod_kernel(const uint16_t *__restrict__ X, int64_t ldx,
         }
     }
 
+    if (late) griddep_launch_dependents();   // every W load of this thread has been issued
     // ---- reduction: butterfly in the warp, then the 4 warps in order 0..3
 #pragma unroll
     for (int m = 0; m < MT; ++m)
@@ -287,7 +288,7 @@ dotprod_kernel(const uint16_t *__restrict__ X, int64_t ldx,
 
 // ------------------------------------------------------------------ instantiation table
 using DotKernel = void (*)(const uint16_t *, int64_t, const uint16_t *, int64_t, void *, int64_t,
-                           int, int, int, int, int *, uint64_t, int);
+                           int, int, int, int, int *, uint64_t, int, int);
 
 template <int MT, int VW, int BN> constexpr DotKernel kfn() { return &dotprod_kernel<MT, VW, BN>; }
 
@@ -347,7 +348,7 @@ cudaError_t launch_dotprod(const GemmArgs &a, const skinny_plan_t &p, const Laun
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fn, a.X, a.ldx, a.W, a.ldw, a.Y, a.ldy, a.N, a.K, p.k_chunk, x_vec16, c.status,
-                              c.budget_ns, a.out_bf16);
+                              c.budget_ns, a.out_bf16, c.late ? 1 : 0);
 }
 
 }  // namespace skinny

@@ -29,6 +29,12 @@ struct GemmArgs {
 struct LaunchCtx {
     cudaStream_t stream;
     bool pdl;            // programmatic dependent launch attribute
+    // When this kernel lets the next launch start (griddepcontrol.launch_dependents):
+    // false = at once (short calls: the next call's prologue overlaps all of this
+    // one); true = once each CTA has issued its last weight load (long,
+    // bandwidth-bound calls: the next call's CTAs fill the SMs this one leaves,
+    // and do not take bandwidth or slots from its main loop).
+    bool late;
     int *status;         // device status word (error reports from bounded waits)
     uint64_t budget_ns;  // budget of each bounded wait; 0 = give up at once (test hook)
 };

@@ -97,6 +97,7 @@ struct SplitParams {
     int *status;
     uint64_t budget_ns;
     int out_bf16;
+    int late;          // let the next launch start once every W copy is issued
 };
 
 // Bounded wait used when draining: also stops early once the producer has
@@ -212,14 +213,14 @@ splitk_kernel(const SplitParams p)
             // X must be in flight before the producer first waits on a cluster
             // phase: that phase needs the consumers, and they need X.
             if (!x_done) issue_x();
-            if (i == 0) griddep_launch_dependents();
+            if (i == 0 && !p.late) griddep_launch_dependents();
             if (S > 1) {
                 cluster_wait();             // phase i
                 cluster_arrive_relaxed();   // phase i + 1 (the producer writes no slots)
             }
         }
         if (!x_done) issue_x();
-        if (my_tiles == 0) griddep_launch_dependents();
+        if (my_tiles == 0 || p.late) griddep_launch_dependents();
         if (S > 1) cluster_wait();          // phase my_tiles
     } else {
         // ============================ consumer warps ============================
@@ -249,7 +250,7 @@ splitk_kernel(const SplitParams p)
             }
         }
         named_bar_sync(1, kSplitConsumerWarps * 32);
-        griddep_launch_dependents();
+        if (!p.late) griddep_launch_dependents();
         if (S > 1) cluster_wait();          // phase 0: every peer has started
 
         const uint32_t xs_u32 = smem_u32(xs);
@@ -514,6 +515,7 @@ cudaError_t launch_splitk(const GemmArgs &a, const skinny_plan_t &pl, const Laun
     p.status = c.status;
     p.budget_ns = c.budget_ns;
     p.out_bf16 = a.out_bf16;
+    p.late = c.late ? 1 : 0;
     SplitKernel fn = (pl.consumer == SKINNY_CONSUMER_MMA) ? kMma[mma_index(a.M)] : kFma[a.M - 1];
 
     cudaLaunchConfig_t cfg = {};

@@ -70,6 +70,7 @@ struct StreamParams {
     int *status;
     uint64_t budget_ns;
     int out_bf16;
+    int late;               // let the next launch start once every W copy is issued
 };
 
 // Bounded wait while draining: stops early once the producer has given up
@@ -153,7 +154,7 @@ stream_kernel(const StreamParams p)
         for (int e = 0; e < fill; ++e)
             if (e % per_chunk == 0) issue(e);
         if (lane == 0) *issued = fill;
-        griddep_launch_dependents();
+        if (!p.late) griddep_launch_dependents();
         for (int e = fill; e < total; ++e) {
             const int s = e % stages;
             bool ok = true;
@@ -169,6 +170,7 @@ stream_kernel(const StreamParams p)
             issue(e);
             if (lane == 0) *issued = e + 1;
         }
+        if (p.late) griddep_launch_dependents();
     } else {
         // ============================ consumer warps ============================
         griddep_wait();   // Y may still be read by the preceding kernel
@@ -332,6 +334,7 @@ cudaError_t launch_stream(const GemmArgs &a, const skinny_plan_t &pl, const Laun
     p.status = c.status;
     p.budget_ns = c.budget_ns;
     p.out_bf16 = a.out_bf16;
+    p.late = c.late ? 1 : 0;
     StreamKernel fn = kStream[a.M <= 8 ? 0 : 1];
 
     cudaLaunchConfig_t cfg = {};

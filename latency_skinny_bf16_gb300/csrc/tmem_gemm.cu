@@ -163,6 +163,7 @@ struct TcParams {
     uint64_t budget_ns;
     int out_bf16;
     int stage3d;     // 1: K % 64 == 0, whole stages by the 3-D maps (tiles of VP or VP - 8 rows)
+    int late;        // let the next launch start once the producer has issued every copy
     // fused query RMS norm (NORM instantiations only): X = xn = rms_norm(xr) * gamma
     const uint16_t *xr;
     int64_t ldxr;
@@ -323,9 +324,9 @@ template <int MT, int TM, bool NORM>
 __global__ void __launch_bounds__(kTcThreads, 2)
 tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
 {
-    // the next call may start as soon as every CTA of this one is resident:
-    // its W streaming fills the SMs this call leaves
-    griddep_launch_dependents();
+    // the next call may start as soon as every CTA of this one is resident
+    // (short calls), or once this CTA's producer has issued its last copy
+    if (!p.late) griddep_launch_dependents();
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -469,6 +470,7 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
                 issue(i, s, true, !NORM);
                 issued = i + 1;
             }
+            if (p.late) griddep_launch_dependents();
             // every copy issued has landed before the ring is reused or the CTA exits
             for (int i = max(0, issued - stages); i < issued; ++i)
                 if (!mbar_wait_bounded(full(i % stages), (uint32_t)((i / stages) & 1), kDrainNs))
@@ -909,6 +911,7 @@ cudaError_t launch_tc(const GemmArgs &a, const skinny_plan_t &pl, const LaunchCt
     }
     TcParams p;
     p.stage3d = stage3d;
+    p.late = c.late ? 1 : 0;
     p.Y = a.Y;
     p.ldy = a.ldy;
     p.M = a.M;
