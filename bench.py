@@ -61,7 +61,7 @@ WORKLOAD_DESC = {
 # the sources that define each kernel family (a committed DRAM-traffic figure
 # is used only while they are unchanged)
 KERNEL_SOURCES = {"dotprod": ["dotprod.cu"], "dotmma": ["dotmma.cu"], "splitk": ["splitk.cu"],
-                  "stream": ["stream.cu"], "tmem_gemm": ["tmem_gemm.cu"]}
+                  "stream": ["stream.cu"], "tmem_gemm": ["tmem_gemm.cu", "tma.cuh"]}
 COMMON_SOURCES = ["common.cuh", "internal.h"]
 
 
@@ -250,10 +250,13 @@ def launch_step(sk, cases, rep, stream_handle, counter=None):
 
 class Workload:
     """A workload's device replicas (together > 2x L2, so every call reads its W
-    from HBM), its plans, and one CUDA graph per replica of one whole step."""
+    from HBM), its plans, and CUDA graphs of `steps_per_graph` whole steps over
+    consecutive replicas (graph j starts at replica j * steps_per_graph), so a
+    workload of a few short calls is not timed as graph-launch overhead."""
 
-    def __init__(self, sk, torch, cases, l2, stream):
+    def __init__(self, sk, torch, cases, l2, stream, steps_per_graph=1):
         self.cases = cases
+        self.G = steps_per_graph
         self.host_inputs = [si.make_inputs(c) for c in cases]
         self.step_bytes = sum(c.algorithmic_bytes for c in cases)
         self.step_w_bytes = sum(2 * c.N * c.K for c in cases)
@@ -270,14 +273,23 @@ class Workload:
                 launch_step(sk, cases, r, sh)
         torch.cuda.synchronize()
         self.graphs = []
-        for r in self.reps:
+        for j in range(self.n_rep):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                launch_step(sk, cases, r, sh)
+                for t in range(self.G):
+                    launch_step(sk, cases, self.reps[(j * self.G + t) % self.n_rep], sh)
             self.graphs.append(g)
+        # L2-warm: the same replica every step
+        self.warm_graph = self.graphs[0]
+        if self.G > 1:
+            self.warm_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.warm_graph, stream=stream):
+                for t in range(self.G):
+                    launch_step(sk, cases, self.reps[0], sh)
         torch.cuda.synchronize()
 
     def replay(self, i):
+        """Replays graph i: steps i * G .. i * G + G - 1."""
         self.graphs[i % self.n_rep].replay()
 
 
@@ -314,14 +326,14 @@ def time_warm(torch, stream, wl, steps):
     """L2-warm: the same replica every step; us per call."""
     with torch.cuda.stream(stream):
         for _ in range(3):
-            wl.graphs[0].replay()
+            wl.warm_graph.replay()
         w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         w0.record(stream)
         for _ in range(steps):
-            wl.graphs[0].replay()
+            wl.warm_graph.replay()
         w1.record(stream)
     torch.cuda.synchronize()
-    return w0.elapsed_time(w1) * 1e3 / (steps * len(wl.cases))
+    return w0.elapsed_time(w1) * 1e3 / (steps * wl.G * len(wl.cases))
 
 
 def time_isolated(sk, torch, stream, wl, l2, iters):
@@ -446,12 +458,17 @@ def run_native(args):
         for name, tag in (("router_small", "c0"), ("dotprod", "c1"), ("splitk", "c2")):
             if name == args.workload:
                 continue
-            wc = Workload(sk, torch, si.workload(name), l2, stream)
-            k = min(args.steps, 1000)
-            el = time_steps(torch, stream, wc, k, max(3, min(args.warmup, 20)), use_barrier=False)
+            cases = si.workload(name)
+            # graphs of at least 12 calls: a one-call step is otherwise timed as graph-launch latency
+            G = max(1, -(-12 // len(cases)))
+            wc = Workload(sk, torch, cases, l2, stream, steps_per_graph=G)
+            replays = -(-min(args.steps, 1000) // G)
+            k = replays * G
+            el = time_steps(torch, stream, wc, replays, max(3, min(args.warmup, 20)), use_barrier=False)
             iso = time_isolated(sk, torch, stream, wc, l2, 10)
             per_config[tag] = {
                 "workload": WORKLOAD_DESC[name], "calls_per_step": len(wc.cases), "steps": k,
+                "steps_per_graph": G,
                 "us_per_call": round(el / k / len(wc.cases) * 1e6, 3),
                 "gbs": round(wc.step_bytes * k / el / 1e9, 1),
                 "us_per_call_l2_warm": round(time_warm(torch, stream, wc, 200), 3),

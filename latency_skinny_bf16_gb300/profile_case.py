@@ -43,6 +43,8 @@ def main(argv=None):
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--cold", action="store_true", help="distinct W copies totalling more than 2x L2")
     ap.add_argument("--pdl", type=int, default=0, choices=[0, 1])
+    ap.add_argument("--split-k", type=int, default=0, help="force the K split (0: the family's own)")
+    ap.add_argument("--block-n", type=int, default=0, help="force block_n (0: the family's own)")
     ap.add_argument("--fuse", type=int, default=1, choices=[0, 1],
                     help="rmsnorm: 1 = the norm inside the tcgen05 GEMM when the plan allows, 0 = two launches")
     a = ap.parse_args(argv)
@@ -60,7 +62,12 @@ def main(argv=None):
     y = torch.empty(M, N, device="cuda")
     s = torch.cuda.current_stream().cuda_stream
     plan = None
-    with sk.options(pdl=a.pdl, fuse_norm=a.fuse, **FAMILIES.get(a.kernel, {})):
+    forced = dict(FAMILIES.get(a.kernel, {}))
+    if a.split_k:
+        forced["split_k"] = a.split_k
+    if a.block_n:
+        forced["block_n"] = a.block_n
+    with sk.options(pdl=a.pdl, fuse_norm=a.fuse, **forced):
         for i in range(n_calls):
             w = ws[i % copies]
             if a.kernel == "topk":
