@@ -458,10 +458,10 @@ def run_native(args):
         for name, tag in (("router_small", "c0"), ("dotprod", "c1"), ("splitk", "c2")):
             if name == args.workload:
                 continue
-            cases = si.workload(name)
+            pc_cases = si.workload(name)
             # graphs of at least 12 calls: a one-call step is otherwise timed as graph-launch latency
-            G = max(1, -(-12 // len(cases)))
-            wc = Workload(sk, torch, cases, l2, stream, steps_per_graph=G)
+            G = max(1, -(-12 // len(pc_cases)))
+            wc = Workload(sk, torch, pc_cases, l2, stream, steps_per_graph=G)
             replays = -(-min(args.steps, 1000) // G)
             k = replays * G
             el = time_steps(torch, stream, wc, replays, max(3, min(args.warmup, 20)), use_barrier=False)
