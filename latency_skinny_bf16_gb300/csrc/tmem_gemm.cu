@@ -19,12 +19,15 @@
 //     tile's last row are never stored.  The planner sizes the grid at two
 //     CTAs per SM, so the next call's CTAs (programmatic dependent launch)
 //     fill each SM as this call's CTAs leave it.
-//   * Thread 0 drives the TMA engine: per ring stage, for each 64-element
-//     K box, the tile's rows as at most five boxes of 128 / 64 / 32 / 16 / 8
-//     rows (one tensor map per height, 128-byte swizzle) and one box of the
-//     MT token rows of X (rows past M and columns past K read as zeros), all
-//     completing on the stage's "full" mbarrier.  W is a weight, so with PDL
-//     the W boxes of the first ring pass go out before griddepcontrol.wait.
+//   * Thread 0 drives the TMA engine (128-byte swizzle, rows past M or N and
+//     columns past K read as zeros), every copy of a stage completing on its
+//     "full" mbarrier.  When K is a multiple of 64 a stage is one copy of W
+//     through a 3-D view [K/64][N][64] (box kb x VP rows, or VP - 8 for a
+//     range's short last tile) and one of X (box kb x MT tokens); otherwise,
+//     for each 64-element K box, the tile's rows as at most five boxes of
+//     128 / 64 / 32 / 16 / 8 rows (one tensor map per height) and one box of
+//     X.  W is a weight, so with PDL the W copies of the first ring pass go
+//     out before griddepcontrol.wait.
 //   * Thread 32 issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32; M = TM,
 //     N = MT tokens, K = 16 each) into one of four sets of tensor-memory
 //     accumulators in rotation, one set per chunk of ring stages holding at
@@ -744,38 +747,35 @@ int tc_smem_bytes(int M, int N, int K, int block_n, int stage_k, int stages, int
 // 45 GB/s) and the MMA issue rate (a small MMA about every 45 ns per SM,
 // carrying 32 bytes of W per useful tile row).  Clustered grids are held to
 // the clusters GB300 keeps resident at once (clusters of 4 and 8 do not fill
-// every GPC) and pay about a microsecond for their reduction.  Two CTAs per
-// SM only: one CTA with a ring twice as deep streams slower (a CTA's copies
-// land one stage at a time, about 0.85 us apart, whatever the depth), so
-// one-per-SM grids are left to explicit grid sizes.
+// every GPC) and pay about a microsecond for their reduction.  Every plan sizes
+// its ring for two CTAs per SM: one CTA with a ring twice as deep streams
+// slower (a CTA's copies land one stage at a time, about 0.85 us apart,
+// whatever the depth).
 namespace {
-struct TcGrid { int per_sm, S, C; double cost; };
+struct TcGrid { int S, C; double cost; };
 TcGrid tc_default_grid(int G, int K, int bk, int num_sms, int force_s, int max_vg) {
-    TcGrid best{0, 0, 0, 1e30};
+    TcGrid best{0, 0, 1e30};
     const int nk_all = (K + bk - 1) / bk;
-    for (int per_sm = kTcCtasPerSm; per_sm >= kTcCtasPerSm; --per_sm) {
-        const int slots = per_sm * num_sms;
-        for (int S = 1; S <= kSplitMaxCluster; S *= 2) {
-            if (force_s && S != force_s) continue;
-            if (!force_s && S > 1 && nk_all < 2 * S) break;   // each rank keeps two stages of K
-            // clusters resident at once (cudaOccupancyMaxActiveClusters on GB300):
-            // pairs fill every slot; fours about 95%; eights 95% at two CTAs per
-            // SM but 79% at one
-            const int pct = S <= 2 ? 100 : (S == 4 || per_sm >= 2) ? 90 : 75;
-            const int cap = (slots * pct) / (100 * S);
-            int C = cap < G ? cap : G;
-            if (S > 1 && (G + C - 1) / C > max_vg) continue;   // one tile per CTA
-            if (C < 1) continue;
-            const int gmax = (G + C - 1) / C;
-            const int vg = tc_groups_per_tile(G, C, max_vg);
-            const int ks = ((nk_all + S - 1) / S) * bk;
-            const int kk = ks < K ? ks : K;
-            const double cta_bytes = 8.0 * gmax * kk * 2.0;
-            const int per_sm_ctas = (C * S + num_sms - 1) / num_sms;
-            const double bw_hbm = 45e9, bw_mma = 32.0 * 8 * vg / 45e-9;
-            const double cost = per_sm_ctas * cta_bytes / (bw_mma < bw_hbm ? bw_mma : bw_hbm) + (S > 1 ? 1e-6 : 0.0);
-            if (cost < best.cost * 0.98) best = {per_sm, S, C, cost};
-        }
+    const int slots = kTcCtasPerSm * num_sms;
+    for (int S = 1; S <= kSplitMaxCluster; S *= 2) {
+        if (force_s && S != force_s) continue;
+        if (!force_s && S > 1 && nk_all < 2 * S) break;   // each rank keeps two stages of K
+        // clusters resident at once at two CTAs per SM (cudaOccupancyMaxActiveClusters
+        // on GB300): pairs fill every slot, fours and eights about 95%
+        const int pct = S <= 2 ? 100 : 90;
+        const int cap = (slots * pct) / (100 * S);
+        int C = cap < G ? cap : G;
+        if (S > 1 && (G + C - 1) / C > max_vg) continue;   // one tile per CTA
+        if (C < 1) continue;
+        const int gmax = (G + C - 1) / C;
+        const int vg = tc_groups_per_tile(G, C, max_vg);
+        const int ks = ((nk_all + S - 1) / S) * bk;
+        const int kk = ks < K ? ks : K;
+        const double cta_bytes = 8.0 * gmax * kk * 2.0;
+        const int per_sm_ctas = (C * S + num_sms - 1) / num_sms;
+        const double bw_hbm = 45e9, bw_mma = 32.0 * 8 * vg / 45e-9;
+        const double cost = per_sm_ctas * cta_bytes / (bw_mma < bw_hbm ? bw_mma : bw_hbm) + (S > 1 ? 1e-6 : 0.0);
+        if (cost < best.cost * 0.98) best = {S, C, cost};
     }
     return best;
 }
@@ -790,17 +790,15 @@ bool tc_make_plan(int M, int N, int K, int force_bn, int force_s, int force_stag
     if (bk < 64 || bk > kTcMaxBK || bk % 64) return false;
     const int nk_all = (K + bk - 1) / bk;         // ring stages over the whole K
     const int max_vg_default = (force_bn == 64) ? 8 : 16;
-    int S = force_s, C = force_c, per_sm = kTcCtasPerSm;
+    int S = force_s, C = force_c;
     if (S == 0 || C == 0) {
         const TcGrid g = tc_default_grid(G, K, bk, num_sms, S, max_vg_default);
         if (g.S == 0) return false;
         if (S == 0) S = g.S;
         if (C == 0) C = g.C;
-        per_sm = g.per_sm;
     }
     if (S < 1 || S > kSplitMaxCluster || (S & (S - 1))) return false;
     if (C < 1 || C > 65535 || C > G) return false;
-    if (force_s && force_c) per_sm = (int64_t)C * S <= num_sms ? 1 : kTcCtasPerSm;   // a forced grid's residency
     const int vg = tc_groups_per_tile(G, C, max_vg_default);
     const int VP = 8 * vg;
     if (S > 1 && (G + C - 1) / C > vg) return false;   // S > 1: one tile per CTA
@@ -811,10 +809,9 @@ bool tc_make_plan(int M, int N, int K, int force_bn, int force_s, int force_stag
     const int ntiles_max = ((G + C - 1) / C + vg - 1) / vg;
     int stages = force_stages;
     if (!stages) {
-        // two CTAs per SM: the ring within 110 KB; one: within the whole SM
-        const int budget = per_sm >= 2 ? kTcSmemBudget : kMaxDynSmem;
+        // two CTAs per SM: the ring within 110 KB
         stages = kSplitMaxStages;
-        while (stages > 1 && tc_smem_bytes(M, N, K, bn, bk, stages, S, C, false) > budget) --stages;
+        while (stages > 1 && tc_smem_bytes(M, N, K, bn, bk, stages, S, C, false) > kTcSmemBudget) --stages;
         // no deeper than the CTA's stages, but deep enough to receive the partials
         int least = 1;
         while (least < stages && tc_smem_bytes(M, N, K, bn, bk, least, S, C, false) > kMaxDynSmem) ++least;
@@ -846,7 +843,8 @@ bool tc_make_norm_plan(int M, int N, int K, const skinny_plan_t &gemm, skinny_pl
     *p = gemm;
     // the same split, tiles and stage length (so the same sums in the same
     // order) and the same CTAs per SM; the ring as deep as that budget leaves
-    // beside the resident X (one CTA per SM when the GEMM plan has one)
+    // beside the resident X (the whole SM only when the GEMM plan itself was
+    // forced past two CTAs' budget)
     const int budget = gemm.smem_bytes > kTcSmemBudget + 2048 ? kMaxDynSmem : kTcSmemBudget;
     int stages = kSplitMaxStages;
     while (stages > 1 && tc_smem_bytes(M, N, K, gemm.block_n, gemm.stage_k, stages, gemm.split_k, gemm.grid_y,
