@@ -338,7 +338,7 @@ bool plan_splitk(int M, int N, int K, int vec, int consumer, int force_s, int fo
         p->k_chunk = ks;
         p->grid_x = S;
         p->grid_y = C;
-        p->threads = kSplitThreads;
+        p->threads = splitk_threads(consumer, consumer == SKINNY_CONSUMER_MMA ? splitk_mma_tokens(M) : M, bk);
         p->smem_bytes = smem;
         return true;
     }

@@ -56,8 +56,22 @@ cudaError_t dotmma_prepare();
 cudaError_t launch_dotmma(const GemmArgs &a, const skinny_plan_t &p, const LaunchCtx &c);
 
 // ---- cluster split-K backend (splitk.cu)
+// Consumer warps per split-K CTA.  The FMA consumer maps 4 warps x 4 rows onto
+// the 16-row tile.  The MMA consumer splits each stage's 16-wide K steps over
+// its warps: 8 when a stage holds at least 1024 K elements and the token
+// bucket is at most 16 (measured on GB300: 5-6% faster there; shorter stages
+// lose to the larger reduction, 32 / 64 tokens to the larger partial buffers),
+// else 4.
 constexpr int kSplitConsumerWarps = 4;
-constexpr int kSplitThreads = (kSplitConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kSplitMmaWarps = 8;
+__host__ __device__ constexpr int splitk_consumer_warps(int consumer, int mt, int stage_k) {
+    return (consumer == SKINNY_CONSUMER_MMA && mt <= 16 && stage_k >= 1024) ? kSplitMmaWarps
+                                                                            : kSplitConsumerWarps;
+}
+__host__ __device__ constexpr int splitk_threads(int consumer, int mt, int stage_k) {
+    return (splitk_consumer_warps(consumer, mt, stage_k) + 1) * 32;   // + one producer warp
+}
+constexpr int kSplitThreads = (kSplitConsumerWarps + 1) * 32;
 constexpr int kSplitBK = 256;        // default K elements per ring stage (one-shot slices)
 constexpr int kSplitStreamBK = 1024; // K elements per ring stage when streaming (2 KB per W row)
 constexpr int kSplitMaxBK = 2048;

@@ -76,7 +76,7 @@ __host__ __device__ inline Layout make_layout(int MT, int M, int consumer, int s
     L.ring = off;  off += stages * kBN * ring_row_bytes(bk);
     L.xs = off;    off += L.xrows * L.xrowb;
     off = round_up(off, 16);
-    L.red = off;   off += (consumer == SKINNY_CONSUMER_MMA) ? kSplitConsumerWarps * MT * kBN * 4 : 0;
+    L.red = off;   off += (consumer == SKINNY_CONSUMER_MMA) ? splitk_consumer_warps(consumer, MT, bk) * MT * kBN * 4 : 0;
     L.slots = off; off += (S > 1) ? slot_buffers(MT) * S * MT * kBN * 4 : 0;   // alternating by tile
     off = round_up(off, 8);
     L.bars = off;  off += 2 * stages * 8 + 8;      // full[stages], empty[stages], x_full
@@ -112,10 +112,11 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, int g,
     }
 }
 
-template <int MT, int CONS>
-__global__ void __launch_bounds__(kSplitThreads)
+template <int MT, int CONS, int CW>
+__global__ void __launch_bounds__((CW + 1) * 32)
 splitk_kernel(const SplitParams p)
 {
+    // CW consumer warps; warp CW produces
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = gridDim.x;                       // CTAs per cluster along K
     const int C = gridDim.y;                       // clusters, persistent over row tiles
@@ -144,7 +145,7 @@ splitk_kernel(const SplitParams p)
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kSplitConsumerWarps);
+            mbar_init(empty0 + 8 * s, CW);
         }
         mbar_init(xfull, 1);
         *abort_flag = 0;
@@ -162,7 +163,7 @@ splitk_kernel(const SplitParams p)
     //                tokens: one buffer, and a cluster owns at most one tile).
     if (S > 1) cluster_arrive_relaxed();
 
-    if (warp == kSplitConsumerWarps) {
+    if (warp == CW) {
         // ============================ producer warp ============================
         // Streams (tile, chunk) pieces through the ring across tile boundaries.
         bool aborted = false;
@@ -237,19 +238,19 @@ splitk_kernel(const SplitParams p)
         } else if (p.x_vec16) {
             const int nv = klen >> 3;
 #pragma unroll 4
-            for (int i = tid; i < p.M * nv; i += kSplitConsumerWarps * 32) {
+            for (int i = tid; i < p.M * nv; i += CW * 32) {
                 const int m = i / nv, v = i - m * nv;
                 *reinterpret_cast<uint4 *>(xs + m * L.xrowb + v * 16) =
                     ldg_v4(p.X + m * p.ldx + kbeg + 8 * v);
             }
         } else {
 #pragma unroll 4
-            for (int i = tid; i < p.M * klen; i += kSplitConsumerWarps * 32) {
+            for (int i = tid; i < p.M * klen; i += CW * 32) {
                 const int m = i / klen, k = i - m * klen;
                 *reinterpret_cast<uint16_t *>(xs + m * L.xrowb + 2 * k) = ldg_u16(p.X + m * p.ldx + kbeg + k);
             }
         }
-        named_bar_sync(1, kSplitConsumerWarps * 32);
+        named_bar_sync(1, CW * 32);
         if (!p.late) griddep_launch_dependents();
         if (S > 1) cluster_wait();          // phase 0: every peer has started
 
@@ -347,7 +348,7 @@ splitk_kernel(const SplitParams p)
                             const int tok = (MT <= 8) ? (lane & 7) : (lane & 7) + 8 * (lane >> 4) + 16 * h2;
                             xrow[h2] = (uint32_t)((tok < p.M ? tok : 0) * L.xrowb);
                         }
-                        for (int j0 = warp; j0 < steps; j0 += 4 * kSplitConsumerWarps) {
+                        for (int j0 = warp; j0 < steps; j0 += 4 * CW) {
                             float d[NT][4];
 #pragma unroll
                             for (int h = 0; h < NT; ++h)
@@ -355,7 +356,7 @@ splitk_kernel(const SplitParams p)
                                 for (int q = 0; q < 4; ++q) d[h][q] = 0.f;
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
-                                const int j = j0 + q * kSplitConsumerWarps;
+                                const int j = j0 + q * CW;
                                 if (j < steps) {
                                     uint32_t a[4];
                                     ldmatrix_x4(a_addr0 + j * 32, a[0], a[1], a[2], a[3]);
@@ -426,22 +427,22 @@ splitk_kernel(const SplitParams p)
                         if (tok < MT) red[(warp * MT + tok) * kBN + row] = macc[h][q];
                     }
                 }
-                named_bar_sync(1, kSplitConsumerWarps * 32);
-                for (int e = tid; e < MT * kBN; e += kSplitConsumerWarps * 32) {
+                named_bar_sync(1, CW * 32);
+                for (int e = tid; e < MT * kBN; e += CW * 32) {
                     const int m = e / kBN, c = e - m * kBN;
                     float v = red[m * kBN + c];
 #pragma unroll
-                    for (int w = 1; w < kSplitConsumerWarps; ++w) v += red[(w * MT + m) * kBN + c];
+                    for (int w = 1; w < CW; ++w) v += red[(w * MT + m) * kBN + c];
                     emit(m, c, v);
                 }
-                named_bar_sync(1, kSplitConsumerWarps * 32);   // red is reused by the next tile
+                named_bar_sync(1, CW * 32);   // red is reused by the next tile
             }
 
             if (S > 1) {
                 cluster_arrive_release();   // phase i + 1: partials of tile i are in the owners' slots
                 cluster_wait_acquire();
                 const float *sl = reinterpret_cast<const float *>(smem + L.slots) + sbuf * S * MT * kBN;
-                for (int e = tid; e < MT * kBN; e += kSplitConsumerWarps * 32) {
+                for (int e = tid; e < MT * kBN; e += CW * 32) {
                     const int m = e / kBN, c = e - m * kBN;
                     if (m < p.M && c < rows && (c % S) == rank) {
                         float v = sl[(0 * MT + m) * kBN + c];
@@ -456,13 +457,16 @@ splitk_kernel(const SplitParams p)
 
 using SplitKernel = void (*)(const SplitParams);
 
-template <int MT> constexpr SplitKernel fma_k() { return &splitk_kernel<MT, SKINNY_CONSUMER_FMA>; }
+template <int MT> constexpr SplitKernel fma_k() { return &splitk_kernel<MT, SKINNY_CONSUMER_FMA, kSplitConsumerWarps>; }
 
 const SplitKernel kFma[kMaxMSmall] = {
     fma_k<1>(), fma_k<2>(), fma_k<3>(), fma_k<4>(), fma_k<5>(), fma_k<6>(), fma_k<7>(), fma_k<8>(),
     fma_k<9>(), fma_k<10>(), fma_k<11>(), fma_k<12>(), fma_k<13>(), fma_k<14>(), fma_k<15>(), fma_k<16>()};
-const SplitKernel kMma[4] = {&splitk_kernel<8, SKINNY_CONSUMER_MMA>, &splitk_kernel<16, SKINNY_CONSUMER_MMA>,
-                             &splitk_kernel<32, SKINNY_CONSUMER_MMA>, &splitk_kernel<64, SKINNY_CONSUMER_MMA>};
+constexpr int kW4 = kSplitConsumerWarps, kW8 = kSplitMmaWarps;
+const SplitKernel kMma[4] = {&splitk_kernel<8, SKINNY_CONSUMER_MMA, kW4>, &splitk_kernel<16, SKINNY_CONSUMER_MMA, kW4>,
+                             &splitk_kernel<32, SKINNY_CONSUMER_MMA, kW4>, &splitk_kernel<64, SKINNY_CONSUMER_MMA, kW4>};
+// stages of at least 1024 K elements, up to 16 tokens: 8 consumer warps
+const SplitKernel kMma8[2] = {&splitk_kernel<8, SKINNY_CONSUMER_MMA, kW8>, &splitk_kernel<16, SKINNY_CONSUMER_MMA, kW8>};
 
 int mma_index(int M) { return M <= 8 ? 0 : M <= 16 ? 1 : M <= 32 ? 2 : 3; }
 
@@ -495,6 +499,10 @@ cudaError_t splitk_prepare() {
         cudaError_t e = set_max_dyn_smem(kMma[i]);
         if (e != cudaSuccess) return e;
     }
+    for (int i = 0; i < 2; ++i) {
+        cudaError_t e = set_max_dyn_smem(kMma8[i]);
+        if (e != cudaSuccess) return e;
+    }
     return cudaSuccess;
 }
 
@@ -516,11 +524,15 @@ cudaError_t launch_splitk(const GemmArgs &a, const skinny_plan_t &pl, const Laun
     p.budget_ns = c.budget_ns;
     p.out_bf16 = a.out_bf16;
     p.late = c.late ? 1 : 0;
-    SplitKernel fn = (pl.consumer == SKINNY_CONSUMER_MMA) ? kMma[mma_index(a.M)] : kFma[a.M - 1];
+    const int cw = splitk_consumer_warps(pl.consumer, mt_for(a.M, pl.consumer), pl.stage_k);
+    if (pl.threads != (cw + 1) * 32) return cudaErrorInvalidValue;
+    SplitKernel fn = (pl.consumer != SKINNY_CONSUMER_MMA) ? kFma[a.M - 1]
+                     : (cw == kSplitMmaWarps)            ? kMma8[mma_index(a.M)]
+                                                         : kMma[mma_index(a.M)];
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.grid_x, pl.grid_y, 1);
-    cfg.blockDim = dim3(kSplitThreads, 1, 1);
+    cfg.blockDim = dim3(pl.threads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem_bytes;
     cfg.stream = c.stream;
     cudaLaunchAttribute attr[2];

@@ -183,6 +183,25 @@ def test_dotmma_cluster_split_router_shapes(M, N, K, S):
     assert sk.skinny_get_device_status() == 0
 
 
+@pytest.mark.parametrize("M,N,K,S,bk,warps", [(5, 200, 14336, 2, 2048, 8), (16, 77, 7168, 4, 1024, 8),
+                                              (9, 300, 7168, 2, 1024, 8), (16, 77, 7168, 4, 512, 4),
+                                              (8, 150, 14336, 4, 1024, 8)])
+def test_splitk_mma_consumer_warps(M, N, K, S, bk, warps):
+    """The MMA consumer splits each stage over 8 warps when stages hold >= 1024 K elements
+    (up to 16 tokens), else 4: both layouts against the oracle, bit-identical over runs."""
+    case = si.Case(f"cw_M{M}_N{N}_K{K}_S{S}_bk{bk}", M=M, N=N, K=K, seed=1400 + M + S, ldy=N + 5)
+    with sk.options(backend=sk.SKINNY_BACKEND_SPLITK, consumer=sk.SKINNY_CONSUMER_MMA, split_k=S, stage_k=bk):
+        b = run_and_check(case)
+        p = b.plan()
+        assert (p["split_k"], p["stage_k"], p["threads"]) == (S, bk, (warps + 1) * 32), p
+        first = b.y_mat().copy()
+        for _ in range(3):
+            assert b.run() == sk.SKINNY_OK
+            assert np.array_equal(b.y_mat().view(np.uint32), first.view(np.uint32))
+        assert b.canary_ok()
+    assert sk.skinny_get_device_status() == 0
+
+
 # ---------------------------------------------------------------- layouts: strides, offsets, alignment
 
 @pytest.mark.parametrize("ldx_pad,ldw_pad,w_off,x_off", [
