@@ -226,6 +226,28 @@ def plannable_range(K, N, m_lo, m_hi, c, num_sms):
     return last
 
 
+def fill_gaps(K, N, lines, num_sms):
+    """Token counts left between two lines of a shape (a winner's plan cut short
+    by plannable_range) go to the following line, as far down as its plan exists
+    (`lines`: (m_lo, m_hi, config) in M order; returns the adjusted list)."""
+    x, w, y = 0x7F0000000000, 0x7F0010000000, 0x7F0020000000
+    out = []
+    for mlo, mhi, c in lines:
+        prev_hi = out[-1][1] if out else 0
+        if out and mlo > prev_hi + 1 and token_bucket(prev_hi + 1) == token_bucket(mlo):
+            opts = {k: v for k, v in c.items()
+                    if k in ("backend", "consumer", "split_k", "block_n", "stages", "stage_k", "clusters")}
+            while mlo > prev_hi + 1:
+                with sk.options(**opts):
+                    try:
+                        sk.skinny_plan_for(x, K, w, K, y, N, mlo - 1, N, K, num_sms)
+                    except sk.SkinnyError:
+                        break
+                mlo -= 1
+        out.append((mlo, mhi, c))
+    return out
+
+
 TABLE = __import__("os").path.join(__import__("os").path.dirname(__file__), "csrc", "tuning_table.inc")
 
 
@@ -287,12 +309,15 @@ def main(argv=None):
         K, N = (int(v) for v in shp.lower().split("x"))
         rows = tune_shape(K, N, (m_large if 2 * N * K > 16e6 else m_small) + m_mid, l2, None, log)
         num_sms = torch.cuda.get_device_properties(0).multi_processor_count
+        kept = []
         for (k, n, mlo, mhi, be, co, sp, bn, st, bk, cl, us) in merge_rows(K, N, rows):
             c = dict(backend=be, consumer=co, split_k=sp, block_n=bn, stages=st, stage_k=bk, clusters=cl)
             mhi = plannable_range(K, N, mlo, mhi, c, num_sms)
             if mhi >= mlo:
-                out_lines.append(f"{{{k}, {n}, {mlo}, {mhi}, {be}, {co}, {sp}, {bn}, {st}, {bk}, {cl}}},  "
-                                 f"// us/call {us}")
+                kept.append((mlo, mhi, dict(c, us=us)))
+        for mlo, mhi, c in fill_gaps(K, N, kept, num_sms):
+            out_lines.append(f"{{{K}, {N}, {mlo}, {mhi}, {c['backend']}, {c['consumer']}, {c['split_k']}, "
+                             f"{c['block_n']}, {c['stages']}, {c['stage_k']}, {c['clusters']}}},  // us/call {c['us']}")
     text = "\n".join(out_lines) + "\n"
     if a.install:
         install(out_lines)

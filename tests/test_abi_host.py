@@ -602,3 +602,16 @@ def test_dotmma_cluster_split_plans():
         with sk.options(split_k=S, **dm):
             with pytest.raises(sk.SkinnyError):
                 plan(M, N, K)
+
+
+def test_tuned_shapes_cover_every_small_m():
+    """A shape in the tuning table has a line for every M = 1..16: a partial re-tune that
+    dropped lines would send the missing token counts to the untuned default rule."""
+    ranges = {}
+    for K, N, m_lo, m_hi, *_ in _table_entries():
+        ranges.setdefault((K, N), []).append((m_lo, m_hi))
+    for shape, rs in ranges.items():
+        covered = set()
+        for lo, hi in rs:
+            covered.update(range(lo, hi + 1))
+        assert set(range(1, 17)) <= covered, (shape, sorted(set(range(1, 17)) - covered))

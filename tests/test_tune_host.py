@@ -93,3 +93,15 @@ def test_candidates_include_cluster_split_dot_product():
     splits = {(x["split_k"], x["block_n"]) for x in c if x["backend"] == 1 and x["consumer"] == 2}
     assert {(2, 16), (4, 16), (8, 32)} <= splits
     assert not any(x["backend"] == 1 and x["split_k"] > 1 for x in tune.candidates(16, 7176, 256))   # K % 32
+
+
+def test_fill_gaps_extends_the_next_line_down():
+    sk = pytest.importorskip("latency_skinny_bf16_gb300")
+    a = dict(backend=2, consumer=2, split_k=1, block_n=0, stages=0, stage_k=1024, clusters=0)
+    b = dict(backend=2, consumer=2, split_k=2, block_n=0, stages=0, stage_k=0, clusters=0)
+    # 2112 x 7168: the first plan stops planning at M = 11 (its X slice); the second takes 11
+    out = tune.fill_gaps(7168, 2112, [(9, 10, a), (12, 15, b)], 152)
+    assert [(lo, hi) for lo, hi, _ in out] == [(9, 10), (11, 15)]
+    # no gap across a token bucket (8 -> 9): left for the default rule of the bucket
+    out = tune.fill_gaps(7168, 2112, [(2, 6, b), (9, 16, b)], 152)
+    assert [(lo, hi) for lo, hi, _ in out] == [(2, 6), (9, 16)]
