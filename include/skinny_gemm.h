@@ -146,8 +146,9 @@ typedef enum {
     SKINNY_OPT_FORCE_STAGE_K = 10,   /* split-K, streaming, tcgen05: 0 = dispatcher, else K elements
                                         per ring stage (multiple of 64; split-K and streaming
                                         64..2048, tcgen05 64..256; tests / tuning only) */
-    SKINNY_OPT_FUSE_NORM = 11        /* 1 (default): skinny_rmsnorm_gemm_bf16 runs the norm inside the
-                                        tcgen05 GEMM when its plan allows; 0: always two launches */
+    SKINNY_OPT_FUSE_NORM = 11        /* 1: skinny_rmsnorm_gemm_bf16 runs the norm inside the tcgen05
+                                        GEMM when its plan allows; 0 (default): two launches, measured
+                                        faster on GB300 (the fused form's resident X halves its ring) */
 } skinny_option_t;
 
 /*
@@ -258,9 +259,9 @@ SKINNY_API skinny_status_t skinny_plan_for_f32w(const uint16_t *X, int ldx, cons
  *   W, Y, M (1..64), N, K, stream: as skinny_gemm_bf16 with X = XN.  K == 0 gives Y = 0 and
  *          leaves XN untouched.
  *
- * One launch when the GEMM's plan is tcgen05 without a K split, M <= 16,
- * X's rows are 16-byte aligned (pointer and ldx) and the option
- * SKINNY_OPT_FUSE_NORM is on: every CTA of the GEMM loads the raw rows of X
+ * One launch when the option SKINNY_OPT_FUSE_NORM is on (off by default), the
+ * GEMM's plan is tcgen05 without a K split, M <= 16, and X's rows are 16-byte
+ * aligned (pointer and ldx): every CTA of the GEMM loads the raw rows of X
  * by TMA into shared memory, computes the r_m of all tokens (the sum of
  * squares in the same fixed order as the norm kernel below, so the same
  * bits), normalises X in place and streams W meanwhile; the CTAs of the first

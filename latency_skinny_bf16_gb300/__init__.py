@@ -7,8 +7,9 @@ tcgen05 kernel (tensor-memory accumulator, W by tensor-map TMA; any K, 16-byte
 aligned rows), the tensor-core dot-product and the cluster split-K kernel's
 mma.sync consumer, chosen per shape by the measured tuning table.  The
 router's softmax / top-k epilogue, fp32 router weights and the query RMS norm
-in front of the q_b projection (fused into the tcgen05 GEMM for M <= 16) have
-entry points of their own.
+in front of the q_b projection (a norm kernel chained to the GEMM, or, with
+the ``fuse_norm`` option, fused into the tcgen05 GEMM for M <= 16) have entry
+points of their own.
 
 This module is a thin ctypes binding over ``libskinny_gemm.so`` (the C ABI in
 ``include/skinny_gemm.h``): the functions below carry the C names and only

@@ -54,7 +54,7 @@ std::atomic<int> g_opt_wait_us{500000};
 std::atomic<int> g_opt_force_grid_y{0};
 std::atomic<int> g_opt_force_stage_k{0};
 std::atomic<int> g_opt_log{-1};
-std::atomic<int> g_opt_fuse_norm{1};
+std::atomic<int> g_opt_fuse_norm{0};   // the fused q_b norm measured slower than two launches
 
 int env_flag(const char *name) {
     const char *v = std::getenv(name);
