@@ -222,7 +222,7 @@ def test_fused_norm_in_a_graph_chain(pdl):
     """Two fused calls back to back in a CUDA graph (the second reads nothing
     the first writes), replayed: the same bits as eager calls."""
     cases = [make_case(16, 24576, 1536, seed=3600), make_case(4, 2112, 1536, seed=3601)]
-    with sk.options(pdl=pdl):
+    with sk.options(pdl=pdl, fuse_norm=1):
         eager = [run_norm(*c) for c in cases]
         tens = []
         for case, X, W, G in cases:
