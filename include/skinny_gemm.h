@@ -126,10 +126,12 @@ typedef struct {
 } skinny_plan_t;
 
 typedef enum {
-    SKINNY_OPT_PDL = 1,              /* programmatic dependent launch: 0 off; 1 on for calls whose weight
-                                        is under 16 MB (larger, bandwidth-bound calls run without it:
-                                        measured faster on GB300); 2 on for every call (default: env
-                                        SKINNY_PDL = 1 or 2, else 0) */
+    SKINNY_OPT_PDL = 1,              /* programmatic dependent launch: 0 off; 1 on for calls whose plan
+                                        stages W through shared memory (split-K, streaming, tcgen05)
+                                        and for dot-product calls whose weight is under 16 MB (a larger
+                                        dot-product call started beside a shared-memory-heavy kernel
+                                        runs with a small L1 and measured slower on GB300); 2 on for
+                                        every call (default: env SKINNY_PDL = 1 or 2, else 0) */
     SKINNY_OPT_FORCE_BACKEND = 2,    /* skinny_backend_t; AUTO = dispatcher (tests / tuning only) */
     SKINNY_OPT_FORCE_CONSUMER = 3,   /* skinny_consumer_t for split-K; AUTO = dispatcher */
     SKINNY_OPT_FORCE_SPLIT_K = 4,    /* 0 = dispatcher, 1..8 = cluster size */

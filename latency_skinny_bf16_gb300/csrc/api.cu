@@ -69,16 +69,26 @@ int opt_pdl() {
     }
     return v;
 }
-// Programmatic dependent launch for a call moving `w_bytes` of weight.  Mode 1
-// keeps it to calls under kPdlMaxWBytes: measured on GB300, a launch of a
-// bandwidth-bound call started early lands its CTAs on whichever SMs free up
-// first, unevenly, and a decode step of the projection weights ran 10% slower
-// with PDL than without; latency-bound calls (the router, the epilogue, the
-// norm) gain from it (a chain of 64 router calls: 176 against 293 us).
+// Programmatic dependent launch for a call moving `w_bytes` of weight, W
+// staged through shared memory by the copy engine (`w_by_tma`: split-K,
+// K-outer streaming, tcgen05) or loaded into registers (the dot-product
+// kernels).  Mode 1 gives it to every call of the first kind and to calls of
+// the second kind under kPdlMaxWBytes.  A load into registers passes through
+// the SM's L1, whose share of the SM's on-chip memory is what the kernels
+// resident on the SM leave of it: a dot-product CTA that starts early on an SM
+// still holding a shared-memory-heavy predecessor (split-K, tcgen05) runs with
+// that small L1, which caps its loads in flight.  Measured on GB300: the
+// 24576 x 1536 dot-product call took 14.5 us after such a predecessor without
+// PDL and about 36 us with it (the same call with the largest shared-memory
+// carveout, no PDL: 30 us), while a chain of the same call gained nothing from
+// PDL.  Calls whose W goes through shared memory do not depend on L1 and gain:
+// the decode step of the projection weights went from 317 to 306 us, chains
+// of one projection call by 0.6-2.5 us per call, a chain of 64 router calls
+// from 285 to 164 us.
 constexpr double kPdlMaxWBytes = 16e6;
-int pdl_for(double w_bytes) {
+int pdl_for(double w_bytes, bool w_by_tma) {
     const int v = opt_pdl();
-    return (v == 2 || (v == 1 && w_bytes < kPdlMaxWBytes)) ? 1 : 0;
+    return (v == 2 || (v == 1 && (w_by_tma || w_bytes < kPdlMaxWBytes))) ? 1 : 0;
 }
 
 // Weights of 16 MB and more: the next launch starts late (see LaunchCtx::late).
@@ -422,7 +432,6 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
     const bool x_ok = (reinterpret_cast<uintptr_t>(X) & 15) == 0 && ldx % 8 == 0;
     const bool stream_ok = mma_ok && x_ok && M <= kMaxMSmall;
     const bool tc_ok = vec == 8 && x_ok;
-    const int pdl = pdl_for(2.0 * N * K);
 
     int backend = fb, consumer = fc, split = fs, bn = fbn, stages = fst, stage_k = g_opt_force_stage_k.load();
     int clusters = fgy;
@@ -564,7 +573,7 @@ skinny_status_t make_plan(const uint16_t *X, int ldx, const uint16_t *W, int ldw
         return SKINNY_ERR_INVALID_VALUE;
     }
     if (!ok) return SKINNY_ERR_UNSUPPORTED;
-    p->pdl = pdl;
+    p->pdl = pdl_for(2.0 * N * K, p->backend != SKINNY_BACKEND_DOTPROD);
     p->tuned = tuned;
     return SKINNY_OK;
 }
@@ -660,7 +669,7 @@ bool plan_f32w(const float *W, int ldw, int M, int N, int K, int num_sms, skinny
     p->grid_y = 1;
     p->threads = kDotThreads;
     p->smem_bytes = dotprod_f32w_smem_bytes(M, bn, kc);
-    p->pdl = pdl_for(4.0 * N * K);
+    p->pdl = pdl_for(4.0 * N * K, false);
     return p->smem_bytes <= kMaxDynSmem;
 }
 

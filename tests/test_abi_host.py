@@ -572,16 +572,31 @@ def test_tcgen05_refuses_rows_a_tensor_map_cannot_address():
         assert plan(16, 4096, 4096, **kw)["backend"] != sk.SKINNY_BACKEND_TCGEN05
 
 
-def test_pdl_applies_to_latency_bound_calls():
-    """PDL mode 1 puts the attribute only on calls under 16 MB of weight; mode 2
-    on every call; 0 on none."""
+def test_pdl_follows_how_the_plan_moves_w():
+    """PDL mode 1 puts the attribute on every plan that stages W through shared
+    memory (split-K, streaming, tcgen05) and on dot-product plans (W loaded
+    into registers through L1) under 16 MB of weight; mode 2 on every call; 0
+    on none."""
+    dot = dict(backend=sk.SKINNY_BACKEND_DOTPROD, consumer=sk.SKINNY_CONSUMER_MMA)
     with sk.options(pdl=1):
         assert plan(4, 256, 7168)["pdl"] == 1                 # the router: 3.7 MB
-        assert plan(4, 24576, 1536)["pdl"] == 0               # a 75 MB projection
-    with sk.options(pdl=2):
+        with sk.options(**dot):
+            assert plan(4, 256, 7168)["pdl"] == 1
+            assert plan(4, 24576, 1536)["pdl"] == 0           # 75 MB into registers
+        with sk.options(backend=sk.SKINNY_BACKEND_DOTPROD, consumer=sk.SKINNY_CONSUMER_FMA):
+            assert plan(1, 24576, 1536)["pdl"] == 0
+        for backend in (sk.SKINNY_BACKEND_SPLITK, sk.SKINNY_BACKEND_TCGEN05, sk.SKINNY_BACKEND_STREAM):
+            with sk.options(backend=backend):
+                p = plan(4, 24576, 1536)
+                assert p["backend"] == backend and p["pdl"] == 1, p
+        for M in (1, 16):                                     # 206 MB: split-K / tcgen05
+            p = plan(M, 7168, 14336)
+            assert p["backend"] != sk.SKINNY_BACKEND_DOTPROD and p["pdl"] == 1, p
+    with sk.options(pdl=2, **dot):
         assert plan(4, 24576, 1536)["pdl"] == 1
     with sk.options(pdl=0):
         assert plan(4, 256, 7168)["pdl"] == 0
+        assert plan(1, 7168, 14336)["pdl"] == 0
 
 
 def test_dotmma_cluster_split_plans():
