@@ -148,9 +148,13 @@ typedef enum {
     SKINNY_OPT_FORCE_STAGE_K = 10,   /* split-K, streaming, tcgen05: 0 = dispatcher, else K elements
                                         per ring stage (multiple of 64; split-K and streaming
                                         64..2048, tcgen05 64..256; tests / tuning only) */
-    SKINNY_OPT_FUSE_NORM = 11        /* 1: skinny_rmsnorm_gemm_bf16 runs the norm inside the tcgen05
+    SKINNY_OPT_FUSE_NORM = 11,       /* 1: skinny_rmsnorm_gemm_bf16 runs the norm inside the tcgen05
                                         GEMM when its plan allows; 0 (default): two launches, measured
                                         faster on GB300 (the fused form's resident X halves its ring) */
+    SKINNY_OPT_LATE_TRIGGER = 12     /* 1: a call with 16 MB or more of weight lets a programmatically
+                                        dependent launch start only once each of its CTAs has issued
+                                        its last W load; 0 (default): at kernel entry, measured faster
+                                        on GB300 with mode 1 of SKINNY_OPT_PDL */
 } skinny_option_t;
 
 /*

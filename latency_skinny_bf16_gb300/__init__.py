@@ -65,6 +65,7 @@ SKINNY_OPT_LOG = 8
 SKINNY_OPT_FORCE_CLUSTERS = 9
 SKINNY_OPT_FORCE_STAGE_K = 10
 SKINNY_OPT_FUSE_NORM = 11
+SKINNY_OPT_LATE_TRIGGER = 12
 
 EXPORTED_SYMBOLS = (
     "skinny_gemm_bf16", "skinny_gemm_bf16_bf16out", "skinny_init", "skinny_query_plan", "skinny_plan_for",
@@ -263,7 +264,7 @@ class options:
                  "block_n": SKINNY_OPT_FORCE_BLOCK_N, "stages": SKINNY_OPT_FORCE_STAGES,
                  "wait_timeout_us": SKINNY_OPT_WAIT_TIMEOUT_US, "log": SKINNY_OPT_LOG,
                  "clusters": SKINNY_OPT_FORCE_CLUSTERS, "stage_k": SKINNY_OPT_FORCE_STAGE_K,
-                 "fuse_norm": SKINNY_OPT_FUSE_NORM}
+                 "fuse_norm": SKINNY_OPT_FUSE_NORM, "late_trigger": SKINNY_OPT_LATE_TRIGGER}
         self._set = [(names[k], int(v)) for k, v in kw.items()]
         self._old = []
 

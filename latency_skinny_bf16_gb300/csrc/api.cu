@@ -55,6 +55,7 @@ std::atomic<int> g_opt_force_grid_y{0};
 std::atomic<int> g_opt_force_stage_k{0};
 std::atomic<int> g_opt_log{-1};
 std::atomic<int> g_opt_fuse_norm{0};   // the fused q_b norm measured slower than two launches
+std::atomic<int> g_opt_late_trigger{0};
 
 int env_flag(const char *name) {
     const char *v = std::getenv(name);
@@ -91,8 +92,12 @@ int pdl_for(double w_bytes, bool w_by_tma) {
     return (v == 2 || (v == 1 && (w_by_tma || w_bytes < kPdlMaxWBytes))) ? 1 : 0;
 }
 
-// Weights of 16 MB and more: the next launch starts late (see LaunchCtx::late).
-bool late_trigger(double w_bytes) { return w_bytes >= 16e6; }
+// With SKINNY_OPT_LATE_TRIGGER, weights of 16 MB and more let the next launch
+// start late (see LaunchCtx::late).  Off by default: with PDL given to the
+// plans that stage W through shared memory only, the decode step of the
+// projection weights measured 296 us with the trigger at kernel entry against
+// 302 us with the late one on GB300.
+bool late_trigger(double w_bytes) { return g_opt_late_trigger.load() != 0 && w_bytes >= 16e6; }
 int opt_log() {
     int v = g_opt_log.load();
     if (v < 0) { v = env_flag("SKINNY_LOG"); g_opt_log.store(v); }
@@ -894,6 +899,9 @@ skinny_status_t skinny_set_option(int option, int value) {
         case SKINNY_OPT_FUSE_NORM:
             if (value != 0 && value != 1) return SKINNY_ERR_INVALID_VALUE;
             g_opt_fuse_norm.store(value); return SKINNY_OK;
+        case SKINNY_OPT_LATE_TRIGGER:
+            if (value != 0 && value != 1) return SKINNY_ERR_INVALID_VALUE;
+            g_opt_late_trigger.store(value); return SKINNY_OK;
         default:
             return SKINNY_ERR_INVALID_VALUE;
     }
@@ -913,6 +921,7 @@ skinny_status_t skinny_get_option(int option, int *value) {
         case SKINNY_OPT_FORCE_CLUSTERS: *value = g_opt_force_grid_y.load(); return SKINNY_OK;
         case SKINNY_OPT_FORCE_STAGE_K: *value = g_opt_force_stage_k.load(); return SKINNY_OK;
         case SKINNY_OPT_FUSE_NORM: *value = g_opt_fuse_norm.load(); return SKINNY_OK;
+        case SKINNY_OPT_LATE_TRIGGER: *value = g_opt_late_trigger.load(); return SKINNY_OK;
         default: return SKINNY_ERR_INVALID_VALUE;
     }
 }

@@ -166,7 +166,7 @@ def test_forced_options_and_restore():
 @pytest.mark.parametrize("opt,bad", [(sk.SKINNY_OPT_PDL, 3), (sk.SKINNY_OPT_FORCE_BACKEND, 5),
                                      (sk.SKINNY_OPT_FORCE_SPLIT_K, 9), (sk.SKINNY_OPT_FORCE_BLOCK_N, 3),
                                      (sk.SKINNY_OPT_FORCE_STAGES, 17), (sk.SKINNY_OPT_WAIT_TIMEOUT_US, -1),
-                                     (99, 0)])
+                                     (sk.SKINNY_OPT_LATE_TRIGGER, 2), (sk.SKINNY_OPT_FUSE_NORM, 2), (99, 0)])
 def test_option_values_are_checked(opt, bad):
     with pytest.raises(sk.SkinnyError):
         sk.skinny_set_option(opt, bad)

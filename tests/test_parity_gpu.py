@@ -354,6 +354,42 @@ def test_cuda_graph_capture_and_replay(pdl):
             check_parity(b.y_mat(), yref, A, "graph")
 
 
+@pytest.mark.parametrize("late", [0, 1])
+def test_large_weight_graph_chain_with_pdl(late):
+    """Calls on weights of 16 MB and more (the dot-product, split-K and tcgen05
+    plans of the 30 and 75 MB projections), captured in one CUDA graph with PDL
+    mode 1, the dependents' trigger at kernel entry (late = 0) or once each CTA
+    has issued its last W load (late = 1): the replay gives the bits of the
+    same calls run eagerly without PDL, within the parity bound."""
+    cases = [si.Case(f"lw{i}", M=M, N=N, K=K, seed=6100 + i)
+             for i, (M, N, K) in enumerate([(1, 2112, 7168), (8, 2112, 7168), (16, 2112, 7168),
+                                            (3, 24576, 1536), (16, 24576, 1536)])]
+    bufs = [Buffers(c, *si.make_inputs(c)) for c in cases]
+    s = torch.cuda.Stream()
+    with sk.options(pdl=0), torch.cuda.stream(s):
+        for b in bufs:
+            assert b.run(s.cuda_stream) == sk.SKINNY_OK
+    torch.cuda.synchronize()
+    eager = [b.y_mat().copy() for b in bufs]
+    for b in bufs:
+        b.y_dev.fill_(0.0)
+    torch.cuda.synchronize()
+    with sk.options(pdl=1, late_trigger=late):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for b in bufs:
+                assert b.run(s.cuda_stream) == sk.SKINNY_OK
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert sk.skinny_get_device_status() == 0
+    for b, e, c in zip(bufs, eager, cases):
+        assert np.array_equal(b.y_mat().view(np.uint32), e.view(np.uint32)), c.name
+        X, W = si.make_inputs(c)
+        yref, A = reference(c, X, W)
+        check_parity(e, yref, A, c.name)
+
+
 def test_timeout_path_reports_and_recovers():
     """A wait budget of 0 makes every bounded wait in the split-K kernel give
     up at once; the kernel records the error, drains its copies, takes part in
