@@ -336,13 +336,14 @@ def time_warm(torch, stream, wl, steps):
     return w0.elapsed_time(w1) * 1e3 / (steps * wl.G * len(wl.cases))
 
 
-def time_isolated(sk, torch, stream, wl, l2, iters):
+def time_isolated(sk, torch, stream, wl, l2, iters, pdl=0):
     """Per call shape: a CUDA graph of back-to-back launches over enough copies
-    of that shape's W to exceed 2x L2 (L2-cold), PDL off, CUDA events around
-    whole replays; us per launch."""
+    of that shape's W to exceed 2x L2 (L2-cold), PDL off (or in the given PDL
+    mode: the sustained rate of a chain of that call), CUDA events around whole
+    replays; us per launch."""
     out = []
     sh = stream.cuda_stream
-    with sk.options(pdl=0):
+    with sk.options(pdl=pdl):
         for j, c in enumerate(wl.cases):
             n_j = max(8, math.ceil(2 * l2 / (2 * c.N * c.K)))
             ws = [wl.reps[i % wl.n_rep].w[j] if i < wl.n_rep else wl.reps[0].w[j].clone() for i in range(n_j)]
@@ -405,13 +406,17 @@ def family_of(plan):
             4: "tmem_gemm"}[plan["backend"]]
 
 
-def shape_rows(wl, iso, peak, flushed=None):
+def shape_rows(wl, iso, peak, flushed=None, chained=None):
     rows = []
     for j, (c, p, us) in enumerate(zip(wl.cases, wl.plans, iso)):
         row = {"M": c.M, "N": c.N, "K": c.K, "kernel": family_of(p), "consumer": p["consumer"],
                "split_k": p["split_k"], "block_n": p["block_n"], "grid": [p["grid_x"], p["grid_y"]],
                "us_per_launch": round(us, 3), "gbs": round(c.algorithmic_bytes / us / 1e3, 1),
                "frac_of_peak": round(c.algorithmic_bytes / us / 1e3 / peak, 4)}
+        if chained is not None:
+            # the same chain with PDL in mode 1 (the plan's own attribute)
+            row["chained_pdl"] = {"us_per_launch": round(chained[j], 3),
+                                  "frac_of_peak": round(c.algorithmic_bytes / chained[j] / 1e3 / peak, 4)}
         if flushed is not None:
             med, p10, p90 = flushed[j]
             row["flush_us"] = {"median": round(med, 3), "p10": round(p10, 3), "p90": round(p90, 3)}
@@ -449,6 +454,7 @@ def run_native(args):
     launches = args.steps * len(cases)
     warm_us_per_call = time_warm(torch, stream, wl, 3 if args.profile_mode else max(50, min(args.steps, 2000)))
     per_launch = time_isolated(sk, torch, stream, wl, l2, 2 if args.profile_mode else 10)
+    chained = None if args.profile_mode else time_isolated(sk, torch, stream, wl, l2, 10, pdl=1)
     flushed = None if args.profile_mode else time_flushed(sk, torch, stream, wl, l2, 100)
 
     # ---- the router workloads, timed the same way (outside the headline's timed region)
@@ -561,7 +567,8 @@ def run_native(args):
     elapsed_max, units = aggregate(elapsed, float(wl.step_bytes * args.steps))
     e2e_max, _ = aggregate(e2e_elapsed, 0.0)
     return dict(cases=cases, wl=wl, elapsed=elapsed_max, units=units, launches=launches,
-                warm_us_per_call=warm_us_per_call, per_launch=per_launch, flushed=flushed, clocks=clock_summary,
+                warm_us_per_call=warm_us_per_call, per_launch=per_launch, chained=chained, flushed=flushed,
+                clocks=clock_summary,
                 e2e_elapsed=e2e_max, h2d=h2d, d2h=d2h, l2=l2, world=world, rank=rank, chain=chain,
                 per_config=per_config, peak=peak)
 
@@ -747,7 +754,7 @@ def main(argv=None):
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
         "pdl_chain": r["chain"],
-        "per_shape": shape_rows(wl, r["per_launch"], peak, r["flushed"]),
+        "per_shape": shape_rows(wl, r["per_launch"], peak, r["flushed"], r["chained"]),
         "flush_method": None if r["flushed"] is None else
         "per call shape: 100 isolated calls, each after a flush kernel reading 2x L2 (outside the event pair), "
         "a CUDA-event pair around the call alone, PDL off; median / p10 / p90",
