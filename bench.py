@@ -472,6 +472,7 @@ def run_native(args):
             k = replays * G
             el = time_steps(torch, stream, wc, replays, max(3, min(args.warmup, 20)), use_barrier=False)
             iso = time_isolated(sk, torch, stream, wc, l2, 10)
+            iso_pdl = time_isolated(sk, torch, stream, wc, l2, 10, pdl=1)
             per_config[tag] = {
                 "workload": WORKLOAD_DESC[name], "calls_per_step": len(wc.cases), "steps": k,
                 "steps_per_graph": G,
@@ -480,7 +481,8 @@ def run_native(args):
                 "us_per_call_l2_warm": round(time_warm(torch, stream, wc, 200), 3),
                 "l2": f"cold: {wc.n_rep} rotating replicas ({wc.pool_mb:.0f} MB)",
                 "isolated_us_max": round(max(iso), 3),
-                "per_shape": shape_rows(wc, iso, peak),
+                "chained_pdl_us_max": round(max(iso_pdl), 3),
+                "per_shape": shape_rows(wc, iso, peak, chained=iso_pdl),
             }
             del wc
             torch.cuda.synchronize()
