@@ -172,6 +172,18 @@ def test_option_values_are_checked(opt, bad):
         sk.skinny_set_option(opt, bad)
 
 
+def test_late_trigger_option_round_trip():
+    """SKINNY_OPT_LATE_TRIGGER is 0 by default, settable to 0 or 1, and the
+    options context restores it; it changes no plan (only when a launch lets
+    its dependents start)."""
+    assert sk.skinny_get_option(sk.SKINNY_OPT_LATE_TRIGGER) == 0
+    p0 = plan(8, 7168, 14336)
+    with sk.options(late_trigger=1):
+        assert sk.skinny_get_option(sk.SKINNY_OPT_LATE_TRIGGER) == 1
+        assert plan(8, 7168, 14336) == p0
+    assert sk.skinny_get_option(sk.SKINNY_OPT_LATE_TRIGGER) == 0
+
+
 def test_every_workload_case_has_a_plan():
     import skinny_inputs as si
     for c in si.iter_all():
