@@ -226,15 +226,25 @@ SKINNY_API skinny_status_t skinny_get_option(int option, int *value);
 
 /*
  * fp32 router weights: Y = X . W^T with X bf16 [M, K] and W fp32 [N, K]
- * (ldw in fp32 elements), fp32 multiply-add (each fmaf rounds once), fp32 Y.
- * For models that keep fp32 router weights ("GLM-5.2 Blackwell decode
- * optimizations", the linked "FP32 router GEMM shape support and tuning" and
- * "Preserve FP32 router weights" changes), and the review note on the first
- * page that fp32 weights must not reach the bf16 kernel: they have their own
- * entry point.  The dot-product kernel only: M = 1..16 (else UNSUPPORTED),
- * any K, W 4-byte aligned (loads of 4, 2 or 1 fp32 as the W pointer and ldw
- * allow), W traffic 4NK bytes.  Other arguments, errors, PDL and graph
- * capture as skinny_gemm_bf16.
+ * (ldw in fp32 elements), fp32 Y.  For models that keep fp32 router weights
+ * ("GLM-5.2 Blackwell decode optimizations", the linked "FP32 router GEMM
+ * shape support and tuning" and "Preserve FP32 router weights" changes), and
+ * the review note on the first page that fp32 weights must not reach the
+ * bf16 kernel: they have their own entry point.  M = 1..16 (else
+ * UNSUPPORTED), any K, W 4-byte aligned, W traffic 4NK bytes.  Two kernels:
+ *   - the dot-product kernel (CUDA cores): fp32 multiply-add, each fmaf
+ *     rounding once; loads of 4, 2 or 1 fp32 as the W pointer and ldw allow;
+ *   - from 6 tokens on weights of 4 MB or more, when W rows are 16-byte
+ *     aligned (W and ldw) and K % 32 == 0: the tensor-core dot-product.  Each
+ *     weight is carried as two tf32 terms (its top bits, then the rest), so
+ *     every product is within 2^-20 of x * w; sums in fp32, K over a cluster
+ *     of CTAs reduced in a fixed order.
+ * Either way |y - y_exact| stays within 1e-5 * sum_k |x w| + 1e-6 and a
+ * plan's results are bit-identical from run to run.  Non-finite weights
+ * propagate as in IEEE arithmetic.  The force options SKINNY_OPT_FORCE_CONSUMER
+ * (FMA / MMA), SKINNY_OPT_FORCE_SPLIT_K and SKINNY_OPT_FORCE_BLOCK_N (16 / 32,
+ * MMA only) apply.  Other arguments, errors, PDL and graph capture as
+ * skinny_gemm_bf16.
  */
 SKINNY_API skinny_status_t skinny_gemm_bf16_f32w(const uint16_t *X, int ldx, const float *W, int ldw,
                                       float *Y, int ldy, int M, int N, int K, void *stream);

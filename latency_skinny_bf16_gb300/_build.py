@@ -20,9 +20,9 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libskinny_gemm.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
-SOURCES = ["api.cu", "dotprod.cu", "dotprod_f32w.cu", "dotmma.cu", "splitk.cu", "stream.cu", "topk.cu",
-           "rmsnorm.cu", "tmem_gemm.cu"]
-HEADERS = ["common.cuh", "internal.h", "tuning_table.inc"]
+SOURCES = ["api.cu", "dotprod.cu", "dotprod_f32w.cu", "dotmma.cu", "dotmma_f32w.cu", "splitk.cu", "stream.cu",
+           "topk.cu", "rmsnorm.cu", "tmem_gemm.cu"]
+HEADERS = ["common.cuh", "internal.h", "tuning_table.inc", "tma.cuh", "dotmma_f32w.h"]
 
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -19,6 +19,7 @@
 #include <tuple>
 
 #include "internal.h"
+#include "dotmma_f32w.h"
 
 namespace skinny {
 namespace {
@@ -122,7 +123,8 @@ skinny_status_t init_device_current(DeviceState &d, int device) {
         return SKINNY_ERR_NO_DEVICE;
     if (major != 10 || minor != 3) return SKINNY_ERR_NO_DEVICE;   // built for sm_103a only
     if (dotprod_prepare() != cudaSuccess || dotmma_prepare() != cudaSuccess || splitk_prepare() != cudaSuccess ||
-        stream_prepare() != cudaSuccess || dotprod_f32w_prepare() != cudaSuccess || tc_prepare() != cudaSuccess)
+        stream_prepare() != cudaSuccess || dotprod_f32w_prepare() != cudaSuccess ||
+        dotmma_f32w_prepare() != cudaSuccess || tc_prepare() != cudaSuccess)
         return SKINNY_ERR_LAUNCH;
     void *sym = nullptr;
     if (cudaGetSymbolAddress(&sym, g_status_word) != cudaSuccess) return SKINNY_ERR_LAUNCH;
@@ -644,12 +646,62 @@ skinny_status_t run_gemm(const uint16_t *X, int ldx, const uint16_t *W, int ldw,
     return e == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
 }
 
-// fp32 weights: the dot-product kernel only (FMA), W loads as wide as the W
+// fp32 weights, tensor-core dot-product (two tf32 terms per weight): 16-row
+// blocks (or the forced block_n), K over a cluster of S CTAs, S the largest
+// power of two up to 8 that keeps the grid within two CTAs per SM and gives
+// every rank some K (or the forced split_k), the rank's X slice resident.
+// Measured on GB300, L2-cold chains, 7168 x 384: 7.1 us at 8 tokens, 8.7 at
+// 16 (the CUDA-core kernel 13.0 and 19.4).
+bool plan_f32w_mma(int M, int N, int K, int num_sms, int force_bn, int force_s, skinny_plan_t *p) {
+    const int bn = force_bn ? force_bn : 16;
+    if (!dotmma_f32w_supported(M, bn) || K < 32 || K % 32) return false;
+    const int blocks = (N + bn - 1) / bn;
+    int S = force_s;
+    if (!S) {
+        S = 1;
+        while (S < kSplitMaxCluster && (int64_t)blocks * S * 2 <= 2 * num_sms && dotmma_f32w_split_ok(K, S * 2))
+            S *= 2;
+        while (S < kSplitMaxCluster && dotmma_f32w_smem_bytes(M, bn, K, S) > kMaxDynSmem &&
+               dotmma_f32w_split_ok(K, S * 2))
+            S *= 2;
+    }
+    if (!dotmma_f32w_split_ok(K, S) || blocks > 65535) return false;
+    p->backend = SKINNY_BACKEND_DOTPROD;
+    p->consumer = SKINNY_CONSUMER_MMA;
+    p->vec_elems = 4;
+    p->block_n = bn;
+    p->split_k = S;
+    p->k_chunk = S > 1 ? dotmma_f32w_k_slice(K, S) : K;
+    p->grid_x = S > 1 ? S : blocks;
+    p->grid_y = S > 1 ? blocks : 1;
+    p->threads = dotmma_f32w_threads(M);
+    p->smem_bytes = dotmma_f32w_smem_bytes(M, bn, K, S);
+    p->pdl = pdl_for(4.0 * N * K, false);
+    return p->smem_bytes <= kMaxDynSmem;
+}
+
+// fp32 weights.  From kF32wMmaMinM tokens on weights of kF32wMmaMinWBytes or
+// more, when the W rows are 16-byte aligned and K % 32 == 0, the tensor-core
+// dot-product; otherwise (or with the FMA
+// consumer forced) the CUDA-core dot-product kernel, W loads as wide as the W
 // pointer and ldw allow (4 / 2 / 1 fp32), BN rows per CTA as in the bf16 rule.
+// Measured on GB300 (L2-cold chains): below 6 tokens, or on weights under
+// 4 MB (2880 x 128: 1.5 MB of fp32), the CUDA-core kernel is faster.
+constexpr int kF32wMmaMinM = 6;
+constexpr double kF32wMmaMinWBytes = 4e6;
 bool plan_f32w(const float *W, int ldw, int M, int N, int K, int num_sms, skinny_plan_t *p) {
     std::memset(p, 0, sizeof(*p));
     const uintptr_t w = reinterpret_cast<uintptr_t>(W);
     const int vec = ((w & 15) == 0 && ldw % 4 == 0) ? 4 : ((w & 7) == 0 && ldw % 2 == 0) ? 2 : 1;
+    const int fc = g_opt_force_consumer.load();
+    const bool mma_fits = vec == 4 && K >= 32 && K % 32 == 0;
+    if (fc == SKINNY_CONSUMER_MMA) {
+        return mma_fits && plan_f32w_mma(M, N, K, num_sms, g_opt_force_block_n.load(), g_opt_force_split_k.load(), p);
+    }
+    if (fc == SKINNY_CONSUMER_AUTO && mma_fits && M >= kF32wMmaMinM && 4.0 * N * K >= kF32wMmaMinWBytes &&
+        plan_f32w_mma(M, N, K, num_sms, 0, 0, p))
+        return true;
+    std::memset(p, 0, sizeof(*p));
     int bn = 1;
     if (vec == 4) {
         bn = pow2_floor(N / (2 * num_sms) > 0 ? N / (2 * num_sms) : 1);
@@ -732,7 +784,9 @@ skinny_status_t skinny_gemm_bf16_f32w(const uint16_t *X, int ldx, const float *W
     skinny_plan_t plan;
     if (!plan_f32w(W, ldw, M, N, K, d.num_sms, &plan)) return SKINNY_ERR_UNSUPPORTED;
     LaunchCtx c{s, plan.pdl != 0, false, d.status_word, (uint64_t)g_opt_wait_us.load() * 1000ull};
-    const cudaError_t e = launch_dotprod_f32w(X, ldx, W, ldw, Y, ldy, M, N, K, plan, c);
+    const cudaError_t e = plan.consumer == SKINNY_CONSUMER_MMA
+                              ? launch_dotmma_f32w(X, ldx, W, ldw, Y, ldy, M, N, K, plan, c)
+                              : launch_dotprod_f32w(X, ldx, W, ldw, Y, ldy, M, N, K, plan, c);
     return e == cudaSuccess ? SKINNY_OK : SKINNY_ERR_LAUNCH;
 }
 

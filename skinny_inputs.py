@@ -140,6 +140,10 @@ def make_f32_weights(case: Case) -> np.ndarray:
         v = torch.randn(shape, generator=g, dtype=torch.float32) * 0.02
     elif case.w_dist == "uniform_isqrtk":
         v = (torch.rand(shape, generator=g, dtype=torch.float32) * 2.0 - 1.0) / math.sqrt(max(case.K, 1))
+    elif case.w_dist == "abs_normal":
+        v = torch.randn(shape, generator=g, dtype=torch.float32).abs()
+    elif case.w_dist == "abs_uniform_isqrtk":
+        v = torch.rand(shape, generator=g, dtype=torch.float32) / math.sqrt(max(case.K, 1))
     else:
         raise ValueError(f"unknown distribution {case.w_dist!r}")
     if case.outliers:

@@ -485,17 +485,57 @@ def test_f32w_argument_errors_are_host_side(kw, expect):
     assert f32w_call(**kw) == expect
 
 
+def _p32(W=B16, ldw=None, M=4, N=256, K=7168):
+    return sk.skinny_plan_for_f32w(A16, K, W, ldw or K, C16, N, M, N, K, 152)
+
+
 def test_f32w_plan_follows_alignment():
-    def p(W=B16, ldw=None, M=4, N=256, K=7168):
-        return sk.skinny_plan_for_f32w(A16, K, W, ldw or K, C16, N, M, N, K, 152)
-    assert p()["vec_elems"] == 4 and p()["consumer"] == sk.SKINNY_CONSUMER_FMA
-    assert p(W=B16 + 8)["vec_elems"] == 2
-    assert p(W=B16 + 4)["vec_elems"] == 1
-    assert p(K=7169)["vec_elems"] == 1
-    assert p(K=7170)["vec_elems"] == 2
-    assert p(N=2048)["block_n"] == 4 and p(N=2048)["grid_x"] == 512
-    assert p(M=16, K=14336)["k_chunk"] % 1024 == 0          # X in chunks: 16 x 14336 bf16 > budget
-    assert p(M=0)["grid_x"] == 0
+    """The CUDA-core kernel below 6 tokens, on weights under 4 MB, or where the
+    tensor-core kernel cannot read W (rows not 16-byte aligned, K % 32 != 0):
+    W loads as wide as the pointer and ldw allow."""
+    FMA = sk.SKINNY_CONSUMER_FMA
+    assert _p32(M=5)["vec_elems"] == 4 and _p32(M=5)["consumer"] == FMA
+    assert _p32(M=16, N=128, K=2880)["consumer"] == FMA      # 1.5 MB of fp32 W
+    for kw, vec in ((dict(W=B16 + 8), 2), (dict(W=B16 + 4), 1), (dict(K=7169), 1), (dict(K=7170), 2),
+                    (dict(K=7172), 4)):
+        p = _p32(M=8, **kw)
+        assert (p["vec_elems"], p["consumer"]) == (vec, FMA), (kw, p)
+    assert _p32(M=2, N=2048)["block_n"] == 4 and _p32(M=2, N=2048)["grid_x"] == 512
+    with sk.options(consumer=FMA):
+        assert _p32(M=16, K=14336)["k_chunk"] % 1024 == 0    # X in chunks: 16 x 14336 bf16 > budget
+    assert _p32(M=0)["grid_x"] == 0
+
+
+def test_f32w_tensor_core_plans():
+    """From 6 tokens on weights of 4 MB or more, with 16-byte W rows and
+    K % 32 == 0 (or forced): 16-row blocks, K over
+    a cluster of S CTAs (the largest power of two up to 8 that keeps the grid
+    within two CTAs per SM and gives every rank some K), the rank's X slice
+    resident, 8 warps up to 8 tokens and 4 above; forced consumer / split /
+    block honoured; refused where the kernel cannot run."""
+    MMA = sk.SKINNY_CONSUMER_MMA
+    for (M, N, K, S, force) in ((6, 256, 7168, 8, 0), (16, 384, 7168, 8, 0), (16, 128, 2880, 8, MMA),
+                                (8, 2112, 7168, 2, 0)):
+        with sk.options(consumer=force):
+            p = _p32(M=M, N=N, K=K)
+        blocks = -(-N // 16)
+        ks = -(-(-(-K // S)) // 32) * 32
+        assert (p["consumer"], p["block_n"], p["split_k"], p["vec_elems"]) == (MMA, 16, S, 4), p
+        assert (p["grid_x"], p["grid_y"]) == ((S, blocks) if S > 1 else (blocks, 1))
+        assert p["k_chunk"] == ks and (S - 1) * ks < K
+        assert blocks * S <= 2 * 152 and p["smem_bytes"] <= 227 * 1024
+        assert p["threads"] == (256 if M <= 8 else 128)
+    with sk.options(consumer=MMA, split_k=4, block_n=32):
+        p = _p32(M=2)
+        assert (p["consumer"], p["split_k"], p["block_n"], p["grid_x"], p["grid_y"]) == (MMA, 4, 32, 4, 8)
+    with sk.options(consumer=MMA):
+        for kw in (dict(W=B16 + 8), dict(K=7170), dict(K=7172), dict(K=16)):
+            with pytest.raises(sk.SkinnyError) as e:
+                _p32(**kw)
+            assert e.value.status == sk.SKINNY_ERR_UNSUPPORTED
+        with sk.options(split_k=8):
+            with pytest.raises(sk.SkinnyError):
+                _p32(K=224)                                   # 8 slices of 32: the last rank gets none
 
 
 # ---------------------------------------------------------------- RMS norm + q_b GEMM

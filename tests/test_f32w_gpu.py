@@ -1,9 +1,13 @@
 """GPU parity of the fp32-router-weight GEMM (bf16 X, fp32 W, fp32 Y) against
 the oracle, through the C ABI.
 
-Bar: |y - y_ref| <= 1e-5 * sum_k |x*w| + 1e-6 elementwise (each fmaf rounds
-once, the sums are the bf16 path's), cosine >= 0.99999, nothing written
-outside Y[:M, :N], bit-identical runs.
+Two kernels: the CUDA-core dot-product (each fmaf rounds once) and, from 6
+tokens on weights of 4 MB or more when W rows are 16-byte aligned and
+K % 32 == 0, the tensor-core
+dot-product, which carries each fp32 weight as two tf32 terms (within 2^-20
+of the weight) through mma.sync.  Bar for both: |y - y_ref| <= 1e-5 *
+sum_k |x*w| + 1e-6 elementwise, cosine >= 0.99999, nothing written outside
+Y[:M, :N], bit-identical runs.
 """
 import numpy as np
 import pytest
@@ -15,6 +19,9 @@ import skinny_inputs as si
 from gpu_util import CANARY, check_parity
 
 pytestmark = pytest.mark.gpu
+
+MMA = sk.SKINNY_CONSUMER_MMA
+FMA = sk.SKINNY_CONSUMER_FMA
 
 
 @pytest.fixture(autouse=True, scope="module")
@@ -83,7 +90,48 @@ ROUTER = [si.Case(f"f32w_M{M}_K{K}_N{N}", M=M, N=N, K=K, seed=2400 + i)
 @pytest.mark.parametrize("case", ROUTER, ids=[c.name for c in ROUTER])
 def test_f32w_router_shapes(case):
     b = run_check(case)
-    assert b.plan()["vec_elems"] == 4
+    p = b.plan()
+    assert p["vec_elems"] == 4
+    assert p["consumer"] == (MMA if case.M >= 6 and 4 * case.N * case.K >= 4e6 else FMA), p
+
+
+@pytest.mark.parametrize("case", [c for c in ROUTER if c.M >= 8], ids=[c.name for c in ROUTER if c.M >= 8])
+def test_f32w_router_shapes_fma_forced(case):
+    """The CUDA-core kernel stays exact where the dispatcher now picks the tensor cores."""
+    with sk.options(consumer=FMA):
+        b = run_check(case)
+        assert b.plan()["consumer"] == FMA
+
+
+@pytest.mark.parametrize("S,bn", [(S, bn) for S in (1, 2, 4, 8) for bn in (16, 32)])
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_f32w_tensor_core_variants(S, bn, M):
+    """Every split of K over a cluster and both block heights, on a ragged
+    N (the last block part-filled) and K = 2880 (K slices of 384..2880)."""
+    case = si.Case(f"f32w_mma_M{M}_S{S}_bn{bn}", M=M, N=100, K=2880, seed=3000 + 10 * S + bn + M,
+                   w_dist="uniform_isqrtk", outliers=True)
+    with sk.options(consumer=MMA, split_k=S, block_n=bn):
+        b = run_check(case)
+        p = b.plan()
+    assert (p["consumer"], p["split_k"], p["block_n"]) == (MMA, S, bn)
+
+
+@pytest.mark.parametrize("K,N,M", [(7168, 256, 8), (7168, 256, 16), (14336, 96, 16)])
+def test_f32w_tensor_core_same_sign_long_k(K, N, M):
+    """All products positive (X ~ |N(0,1)|, W ~ U(0, 1/sqrt(K)) in fp32), so
+    neither the two-term split's residue nor the tensor core's rounding can
+    cancel; K up to 14336."""
+    case = si.Case(f"f32w_abs_K{K}_M{M}", M=M, N=N, K=K, seed=3100 + M, x_dist="abs_normal",
+                   w_dist="abs_uniform_isqrtk")
+    X, _ = si.make_inputs(case)
+    Wf = si.make_f32_weights(case)
+    b = F32Buffers(case, X, Wf)
+    assert b.plan()["consumer"] == MMA
+    assert b.run() == sk.SKINNY_OK
+    yref, A = oracle.gemm_f32w(X, Wf, M, N, K)
+    y = b.y_mat()
+    print(f"{case.name}: max err/A = {np.max(np.abs(y - yref) / A):.2e}")
+    check_parity(y, yref, A, case.name)
 
 
 @pytest.mark.parametrize("w_offset,ldw_pad,K", [(1, 0, 1000), (2, 0, 1000), (0, 1, 999), (0, 2, 1026),
@@ -116,6 +164,24 @@ def test_f32w_k_zero_and_special_values():
     assert b.run() == sk.SKINNY_OK
     yref, A = oracle.gemm_f32w(X, Wf, 2, 8, 64)
     check_parity(b.y_mat(), yref, A, "special values")
+    # the tensor-core kernel: non-finite weights carried whole by the first
+    # tf32 term, and finite weights near the top of the range (3.4e38, whose
+    # column of X is 0.25 so the products stay finite)
+    case = si.Case("f32w_sv_mma", M=6, N=40, K=64, seed=2702)
+    X, _ = si.make_inputs(case)
+    X[:, 9] = 0x3E80                      # bf16 0.25
+    Wf = si.make_f32_weights(case)
+    Wf[1, 5] = np.inf
+    Wf[2, 7] = -np.inf
+    Wf[3, 11] = np.nan
+    Wf[4, 0] = 1.0e30
+    Wf[6, 9] = np.float32(3.4e38)
+    Wf[7, 9] = -np.float32(3.4e38)
+    b = F32Buffers(case, X, Wf)
+    assert b.plan()["consumer"] == MMA
+    assert b.run() == sk.SKINNY_OK
+    yref, A = oracle.gemm_f32w(X, Wf, 6, 40, 64)
+    check_parity(b.y_mat(), yref, A, "special values, tensor cores")
 
 
 def test_f32w_tensor_wrapper_and_graph():
