@@ -32,12 +32,26 @@ constexpr int kTopkWarps = kTopkThreads / 32;
 // index.  n < 0 marks "none yet".  Every row thus has a total order, so the k
 // ids are distinct valid indices whatever the logits hold.
 __device__ __forceinline__ bool better(float v, int n, float bv, int bn) {
-    if (n < 0) return false;
-    if (bn < 0) return true;
-    const bool vnan = isnan(v), bnan = isnan(bv);
-    if (vnan != bnan) return bnan;
-    if (!vnan && v != bv) return v > bv;
-    return n < bn;
+    const bool vnan = v != v, bnan = bv != bv;
+    const bool gt = !vnan & (bnan | (v > bv));                  // a better value class or value
+    const bool eq = (vnan & bnan) | (!vnan & !bnan & (v == bv));
+    return (n >= 0) & ((bn < 0) | gt | (eq & (n < bn)));
+}
+
+// The same order as one 64-bit key (larger = better): the logit mapped to an
+// unsigned integer that grows with it (-0 as +0, every NaN to 0, below -inf),
+// then the complement of the index, so equal logits favour the lower index.
+// 0 itself is "none": every real candidate's key has its index bits set.
+__device__ __forceinline__ uint64_t rank_key(float v, int n) {
+    uint32_t b = (v == 0.f) ? 0u : __float_as_uint(v);
+    uint32_t o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    if (v != v) o = 0u;
+    return ((uint64_t)o << 32) | (uint32_t)~(uint32_t)n;
+}
+// The logit of a key (a NaN for the NaN class; -0 comes back as +0).
+__device__ __forceinline__ float key_value(uint64_t key) {
+    const uint32_t o = (uint32_t)(key >> 32);
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
 __global__ void __launch_bounds__(kTopkThreads)
@@ -125,8 +139,8 @@ router_topk_kernel(const float *__restrict__ L, int64_t ldl, int N, int k, int r
 // One warp per token for N <= 32 * VPL (VPL <= 32): lane l holds the logits
 // n = l + 32 j in registers; the max and the sum of exponentials are warp
 // butterflies over per-lane sums in ascending j, and each selection is a warp
-// argmax over the entries not yet taken (a per-lane bit mask): no barrier and
-// no shared memory.  Four tokens per CTA.
+// maximum of rank keys over the entries not yet taken: no barrier and no
+// shared memory.  Four tokens per CTA.
 template <int VPL>
 __global__ void __launch_bounds__(kTopkThreads)
 router_topk_warp_kernel(const float *__restrict__ L, int64_t ldl, int M, int N, int k, int renormalize,
@@ -153,29 +167,34 @@ router_topk_warp_kernel(const float *__restrict__ L, int64_t ldl, int M, int N, 
         if (lane + 32 * j < N) s += expf(v[j] - lmax);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-    uint32_t taken = 0;
+    // each selection: the largest key not yet taken, per lane over its VPL
+    // keys, then across the warp (64-bit butterfly); the owner lane marks it
+    uint64_t key[VPL];
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+        const int n = lane + 32 * j;
+        key[j] = (n < N) ? rank_key(v[j], n) : 0ull;
+    }
     // lane l keeps choice l (lo) and choice 32 + l (hi); every lane sums the
     // chosen probabilities in selection order
     float p_lo = 0.f, p_hi = 0.f, total = 0.f;
     int id_lo = -1, id_hi = -1;
     for (int i = 0; i < k; ++i) {
-        float bv = -INFINITY;
-        int bn = -1, bj = -1;
+        uint64_t best = 0;
 #pragma unroll
-        for (int j = 0; j < VPL; ++j) {
-            const int n = lane + 32 * j;
-            if (n < N && !((taken >> j) & 1u) && better(v[j], n, bv, bn)) { bv = v[j]; bn = n; bj = j; }
-        }
-        float wv = bv;
-        int wn = bn;
+        for (int j = 0; j < VPL; ++j) best = key[j] > best ? key[j] : best;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xFFFFFFFFu, wv, o);
-            const int on = __shfl_xor_sync(0xFFFFFFFFu, wn, o);
-            if (better(ov, on, wv, wn)) { wv = ov; wn = on; }
+            const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+            best = other > best ? other : best;
         }
-        if (wn == bn && bn >= 0) taken |= 1u << bj;   // the owner lane marks it
-        const float p = expf(wv - lmax) / s;
+        const int wn = (int)~(uint32_t)best;
+        if ((wn & 31) == lane) {
+#pragma unroll
+            for (int j = 0; j < VPL; ++j)
+                if (j == (wn >> 5)) key[j] = 0ull;   // taken
+        }
+        const float p = expf(key_value(best) - lmax) / s;
         total += p;
         if (lane == (i & 31)) {
             if (i < 32) { p_lo = p; id_lo = wn; } else { p_hi = p; id_hi = wn; }
