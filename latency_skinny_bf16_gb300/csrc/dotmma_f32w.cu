@@ -48,10 +48,9 @@ namespace {
 // Warps per CTA, by token bucket: 8 at 8 tokens (116 registers, two CTAs an
 // SM: with K over a cluster of 8 CTAs a router CTA holds 16 rows x 896 fp32,
 // and 8 warps x 2 batches of 2 steps put all 57 KB in flight at once), 4 at 16
-// tokens (142 registers: 8 warps would leave one CTA an SM, and 16 clusters of
+// tokens (138 registers: 8 warps would leave one CTA an SM, and 16 clusters of
 // 8 CTAs would then not all be resident at once).
 __host__ __device__ constexpr int f32w_warps(int MT) { return MT == 8 ? 8 : 4; }
-constexpr int kMaxWarpsF = 8;
 constexpr int kUF = 2;   // 32-element K steps per warp per batch
 
 __host__ __device__ inline int xrow_bytes_f(int ks) { return ((ks * 2 + 127) & ~127) + 64; }
