@@ -180,20 +180,24 @@ router_topk_warp_kernel(const float *__restrict__ L, int64_t ldl, int M, int N, 
     float p_lo = 0.f, p_hi = 0.f, total = 0.f;
     int id_lo = -1, id_hi = -1;
     for (int i = 0; i < k; ++i) {
-        uint64_t best = 0;
+        // the lane's largest key: a pairwise tree (depth log2 VPL, not VPL)
+        uint64_t t[VPL];
 #pragma unroll
-        for (int j = 0; j < VPL; ++j) best = key[j] > best ? key[j] : best;
+        for (int j = 0; j < VPL; ++j) t[j] = key[j];
+#pragma unroll
+        for (int lvl = 1; lvl < VPL; lvl *= 2)
+#pragma unroll
+            for (int j = 0; j + lvl < VPL; j += 2 * lvl) t[j] = t[j + lvl] > t[j] ? t[j + lvl] : t[j];
+        uint64_t best = t[0];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
             best = other > best ? other : best;
         }
         const int wn = (int)~(uint32_t)best;
-        if ((wn & 31) == lane) {
+        // keys are unique (the index is part of each): clear the winner's
 #pragma unroll
-            for (int j = 0; j < VPL; ++j)
-                if (j == (wn >> 5)) key[j] = 0ull;   // taken
-        }
+        for (int j = 0; j < VPL; ++j) key[j] = (key[j] == best) ? 0ull : key[j];
         const float p = expf(key_value(best) - lmax) / s;
         total += p;
         if (lane == (i & 31)) {
