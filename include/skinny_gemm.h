@@ -99,27 +99,30 @@ typedef enum {
     SKINNY_CONSUMER_AUTO = 0,
     SKINNY_CONSUMER_FMA = 1,        /* CUDA-core fp32 fused multiply-add */
     SKINNY_CONSUMER_MMA = 2         /* mma.sync m16n8k16 bf16 -> fp32, W on the MMA's M side
-                                       (split-K, or the dot-product layout with block_n 16/32/64) */
+                                       (split-K, or the dot-product layout with block_n 16/32/64);
+                                       fp32 weights: mma.sync m16n8k8 tf32 -> fp32, block_n 16/32 */
 } skinny_consumer_t;
 
 /* The launch a call would make.  Filled by skinny_query_plan / skinny_plan_for. */
 typedef struct {
     int backend;       /* skinny_backend_t actually used */
     int consumer;      /* skinny_consumer_t actually used (FMA or MMA, for either backend) */
-    int vec_elems;     /* W load width in bf16 elements: 8 (128-bit), 4, 2 or 1 */
+    int vec_elems;     /* W load width in elements: bf16 8 (128-bit), 4, 2 or 1; fp32 weights 4, 2 or 1 */
     int block_n;       /* output columns (rows of W) per CTA tile; tcgen05: the MMA's M (64 or 128),
                           the tile holding up to that many rows */
     int split_k;       /* CTAs per cluster along K (1 = no cluster) */
     int stages;        /* shared-memory ring depth (split-K, streaming, tcgen05) */
     int stage_k;       /* K elements of each W row per ring stage (split-K and streaming 64..2048,
                           tcgen05 64..256; multiple of 64) */
-    int k_chunk;       /* dot-product: K elements of X staged in shared memory at a time;
-                          split-K, tcgen05: K elements per CTA (the cluster rank's slice) */
+    int k_chunk;       /* dot-product: K elements of X staged in shared memory at a time (with a
+                          cluster split: the rank's slice); split-K, tcgen05: K elements per CTA
+                          (the cluster rank's slice) */
     int grid_x;        /* grid dimensions launched; split-K, tcgen05: grid_x = split_k CTAs per cluster, */
     int grid_y;        /* split-K: grid_y clusters, each looping over 16-row tiles y, y + grid_y, ...;
                           tcgen05: grid_y row ranges (clusters), range c holding the 8-row groups
                           [c * G / grid_y, (c + 1) * G / grid_y), G = ceil(N / 8) */
-    int threads;       /* threads per CTA */
+    int threads;       /* threads per CTA (split-K: (consumer warps + 1) x 32; fp32-weight tensor-core
+                          plans: 256 up to 8 tokens, 128 above) */
     int smem_bytes;    /* dynamic shared memory per CTA */
     int pdl;           /* 1 if launched with programmatic dependent launch */
     int tuned;         /* 1 if the plan came from the measured tuning table */
