@@ -116,6 +116,19 @@ def test_f32w_tensor_core_variants(S, bn, M):
     assert (p["consumer"], p["split_k"], p["block_n"]) == (MMA, S, bn)
 
 
+@pytest.mark.parametrize("ldx_pad", [1, 3, 8])
+@pytest.mark.parametrize("M", [6, 16])
+def test_f32w_tensor_core_x_strides(ldx_pad, M):
+    """X rows that are not 16-byte aligned (ldx = K + 1, K + 3) are staged by
+    ordinary loads instead of bulk copies; ldx = K + 8 keeps the copies.  A
+    strided Y too."""
+    case = si.Case(f"f32w_ldx_M{M}_{ldx_pad}", M=M, N=72, K=1024, seed=3200 + 10 * M + ldx_pad,
+                   w_dist="uniform_isqrtk", ldy=72 + 5)
+    with sk.options(consumer=MMA, split_k=2):
+        b = run_check(case, ldx=1024 + ldx_pad, ldy=77)
+        assert b.plan()["consumer"] == MMA
+
+
 @pytest.mark.parametrize("K,N,M", [(7168, 256, 8), (7168, 256, 16), (14336, 96, 16)])
 def test_f32w_tensor_core_same_sign_long_k(K, N, M):
     """All products positive (X ~ |N(0,1)|, W ~ U(0, 1/sqrt(K)) in fp32), so
