@@ -129,6 +129,27 @@ def test_f32w_tensor_core_x_strides(ldx_pad, M):
         assert b.plan()["consumer"] == MMA
 
 
+def test_f32w_tensor_core_timeout_path_reports_and_recovers():
+    """A wait budget of 0 makes the X-staging wait give up at once: the kernel
+    records the error, still waits (bounded) for its copies to land, takes
+    part in the cluster barriers and exits.  Nothing hangs, and the next call
+    is exact."""
+    case = si.Case("f32w_to", M=8, N=64, K=2048, seed=3300, w_dist="uniform_isqrtk")
+    X, _ = si.make_inputs(case)
+    Wf = si.make_f32_weights(case)
+    assert sk.skinny_get_device_status() == 0
+    with sk.options(consumer=MMA, split_k=2, wait_timeout_us=0):
+        b = F32Buffers(case, X, Wf)
+        assert b.plan()["consumer"] == MMA
+        assert b.run() == sk.SKINNY_OK
+        code = sk.skinny_get_device_status()
+    assert code & 0xFF == sk.SKINNY_ERR_DEVICE_TIMEOUT
+    assert (code >> 8) == 4                # the X-staging wait
+    assert sk.skinny_get_device_status() == 0
+    with sk.options(consumer=MMA, split_k=2):
+        run_check(case)
+
+
 @pytest.mark.parametrize("K,N,M", [(7168, 256, 8), (7168, 256, 16), (14336, 96, 16)])
 def test_f32w_tensor_core_same_sign_long_k(K, N, M):
     """All products positive (X ~ |N(0,1)|, W ~ U(0, 1/sqrt(K)) in fp32), so
