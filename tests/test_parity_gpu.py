@@ -426,6 +426,31 @@ def test_timeout_path_reports_and_recovers():
     assert sk.skinny_get_device_status() == 0
 
 
+@pytest.mark.parametrize("opts", [dict(backend=sk.SKINNY_BACKEND_DOTPROD, consumer=sk.SKINNY_CONSUMER_FMA),
+                                  dict(backend=sk.SKINNY_BACKEND_DOTPROD, consumer=sk.SKINNY_CONSUMER_MMA),
+                                  dict(backend=sk.SKINNY_BACKEND_DOTPROD, consumer=sk.SKINNY_CONSUMER_MMA,
+                                       split_k=4, block_n=16)],
+                         ids=["dotprod", "dotmma", "dotmma_split4"])
+def test_dot_product_timeout_path_reports_and_recovers(opts):
+    """The dot-product kernels' only wait is X staging by bulk copies: with a
+    wait budget of 0 it gives up at once and is reported, the kernel still
+    waits (bounded) for its copies before reading X, and the next call is
+    exact."""
+    case = si.Case("to_dot", M=8, N=256, K=4096, seed=701)
+    X, W = si.make_inputs(case)
+    assert sk.skinny_get_device_status() == 0
+    with sk.options(wait_timeout_us=0, **opts):
+        b = Buffers(case, X, W)
+        assert b.run() == sk.SKINNY_OK
+        code = sk.skinny_get_device_status()
+    assert code & 0xFF == sk.SKINNY_ERR_DEVICE_TIMEOUT
+    assert (code >> 8) == 4                # the X-staging wait
+    assert sk.skinny_get_device_status() == 0
+    with sk.options(**opts):
+        run_and_check(case)
+    assert sk.skinny_get_device_status() == 0
+
+
 def test_tensor_wrapper():
     case = si.Case("tw", M=5, N=300, K=2048, seed=800)
     X, W = si.make_inputs(case)
