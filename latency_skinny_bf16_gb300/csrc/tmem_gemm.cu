@@ -542,7 +542,12 @@ tmem_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
         if (NORM) {
             if (lane == 0) xok = mbar_wait_bounded(xraw, 0, p.budget_ns);
             xok = __shfl_sync(0xffffffffu, xok ? 1 : 0, 0) != 0;
-            if (!xok && lane == 0) report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitX);
+            if (!xok && lane == 0) {
+                report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitX);
+                // the raw X copy is still in flight: let it land (bounded)
+                // before the region is read, and before the CTA can exit
+                if (!mbar_wait_bounded(xraw, 0, kDrainNs)) report_status(p.status, SKINNY_ERR_DEVICE_TIMEOUT, kWaitDrain);
+            }
             // every warp takes part in the barriers inside, whatever its wait gave
             norm_prologue<MT>(p, smem + (xres - base), rstat, npart, nxb, blockIdx.y == 0, tid - 64,
                               warp - kAccWarp0, lane);

@@ -203,6 +203,26 @@ def test_fused_norm_equals_two_launches(M, N, K, opts):
     assert sk.skinny_get_device_status() == 0
 
 
+def test_fused_norm_timeout_path_reports_and_recovers():
+    """A wait budget of 0 on the fused form: its waits (raw X landed, X
+    normalised, ring stages, accumulators) give up at once and are reported;
+    the CTA still lets its copies land (bounded), passes its barriers, frees
+    tensor memory once its MMAs are done and exits.  The next call is exact."""
+    case, X, W, G = make_case(8, 640, 1536, seed=3600)
+    assert sk.skinny_get_device_status() == 0
+    with sk.options(backend=sk.SKINNY_BACKEND_TCGEN05, fuse_norm=1, wait_timeout_us=0):
+        run_norm(case, X, W, G)
+        code = sk.skinny_get_device_status()
+    assert code & 0xFF == sk.SKINNY_ERR_DEVICE_TIMEOUT
+    assert sk.skinny_get_device_status() == 0
+    with sk.options(backend=sk.SKINNY_BACKEND_TCGEN05, fuse_norm=1):
+        xf, yf = run_norm(case, X, W, G)
+    check_xn(xf, oracle.rmsnorm(X, G, 1e-6, 8, 1536), 1536)
+    yref, A = oracle.gemm(xf, W, 8, 640, 1536)
+    check_parity(yf, yref, A, "fused norm after a timeout")
+    assert sk.skinny_get_device_status() == 0
+
+
 def test_fused_norm_strided_and_misaligned_x_and_eps():
     """Strided X rows (16-byte aligned: the fused form; not aligned: the
     two-launch form) and several eps: both forms give the same bits."""
