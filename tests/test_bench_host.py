@@ -72,3 +72,26 @@ def test_reference_arm_nonzero_rank_exits_quietly():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
                         "--warmup", "0"], capture_output=True, text=True, timeout=120, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_shape_rows_carry_the_sustained_rate():
+    """Each per-shape row reports the back-to-back time without PDL and, when
+    measured, the PDL-chain time, both as µs per launch and as a fraction of
+    the peak from the same algorithmic bytes; the flush cross-check when
+    given."""
+    sys.path.insert(0, ROOT)
+    import types
+    import bench
+    import skinny_inputs as si
+    cases = si.projection_cases()[:2]
+    plans = [dict(backend=1, consumer=1, split_k=1, block_n=4, grid_x=528, grid_y=1),
+             dict(backend=4, consumer=2, split_k=8, block_n=64, grid_x=8, grid_y=33)]
+    wl = types.SimpleNamespace(cases=cases, plans=plans)
+    rows = bench.shape_rows(wl, [10.0, 20.0], 6788.3, flushed=[(12.0, 11.0, 13.0)] * 2, chained=[8.0, 16.0])
+    assert [r["kernel"] for r in rows] == ["dotprod", "tmem_gemm"]
+    for r, c, iso, ch in zip(rows, cases, (10.0, 20.0), (8.0, 16.0)):
+        assert r["us_per_launch"] == iso and r["chained_pdl"]["us_per_launch"] == ch
+        assert r["frac_of_peak"] == pytest.approx(c.algorithmic_bytes / iso / 1e3 / 6788.3, abs=1e-4)
+        assert r["chained_pdl"]["frac_of_peak"] == pytest.approx(c.algorithmic_bytes / ch / 1e3 / 6788.3, abs=1e-4)
+        assert r["flush_us"] == {"median": 12.0, "p10": 11.0, "p90": 13.0}
+    assert "chained_pdl" not in bench.shape_rows(wl, [10.0, 20.0], 6788.3)[0]
